@@ -1,0 +1,136 @@
+// KV writer (quantise + append into a device page) and ring refill kernels.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "kvs_internal.h"
+
+namespace kvs {
+namespace {
+
+// One warp per (token, kv head, 32-element block).  Encodes K as Q8_0 and V
+// as Q4_0 with IEEE fp32 steps in a fixed order, so the codes match any
+// other implementation of the same definition bit for bit:
+//   Q8_0: d = max|x| / 127, id = 1/d (0 if d == 0), code = roundf(x * id)
+//   Q4_0: m = the element of largest |x| (lowest index on ties), d = m / -8,
+//         id = 1/d (0 if d == 0), code = min(15, trunc(x * id + 8.5))
+// The KV writer of the V2 design ("SET_ROWS" with a runtime row base in the
+// PR "port adaptive KV streaming") writes encoded rows at the page's token
+// slot; here the slot is t0 + token.
+__global__ void __launch_bounds__(256) quantize_kernel(const QuantizeParams p) {
+    const int D = p.geom.D, NB = D / 32, Hk = p.geom.Hk, P = p.geom.P;
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= (int64_t)p.n * Hk * NB) return;
+    const int b = (int)(wid % NB);
+    const int g = (int)((wid / NB) % Hk);
+    const int i = (int)(wid / ((int64_t)NB * Hk));
+    const int t = p.t0 + i;
+    const int64_t src = ((int64_t)i * Hk + g) * D + b * 32 + lane;
+    uint8_t *hb = p.page + (int64_t)g * p.geom.head_bytes;
+
+    // K -> Q8_0
+    const float x = p.k[src];
+    float amax = fabsf(x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+    const int qk = (int)roundf(__fmul_rn(x, id));
+    hb[(int64_t)t * D + b * 32 + lane] = (uint8_t)(int8_t)qk;
+    if (lane == 0) reinterpret_cast<__half *>(hb + p.geom.ks_off)[(int64_t)t * NB + b] = __float2half_rn(d);
+
+    // V -> Q4_0
+    const float y = p.v[src];
+    float ay = fabsf(y);
+    int idx = lane;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ao = __shfl_xor_sync(0xffffffffu, ay, o);
+        const int io = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ao > ay || (ao == ay && io < idx)) {
+            ay = ao;
+            idx = io;
+        }
+    }
+    const float mx = __shfl_sync(0xffffffffu, y, idx);
+    const float dv = __fdiv_rn(mx, -8.0f);
+    const float idv = (dv != 0.0f) ? __fdiv_rn(1.0f, dv) : 0.0f;
+    const float u = __fadd_rn(__fmul_rn(y, idv), 8.5f);
+    int c = __float2int_rz(u);
+    c = c > 15 ? 15 : (c < 0 ? 0 : c);
+    const int chi = __shfl_down_sync(0xffffffffu, c, 16);
+    if (lane < 16) hb[p.geom.vq_off + (int64_t)(b * 16 + lane) * P + t] = (uint8_t)(c | (chi << 4));
+    if (lane == 0) reinterpret_cast<__half *>(hb + p.geom.vs_off)[(int64_t)b * P + t] = __float2half_rn(dv);
+}
+
+// Zero token slots [t0, P) of every section of every head of one page.
+__global__ void clear_tail_kernel(uint8_t *page, PageGeom g, int t0) {
+    const int64_t n = g.page_bytes;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t off = i % g.head_bytes;
+        int64_t tok;
+        if (off < g.ks_off) tok = off / g.D;
+        else if (off < g.vq_off) tok = (off - g.ks_off) / (g.D / 16);
+        else if (off < g.vs_off) tok = (off - g.vq_off) % g.P;
+        else tok = ((off - g.vs_off) / 2) % g.P;
+        if (tok >= t0) page[i] = 0;
+    }
+}
+
+__device__ __forceinline__ uint4 ld_nc_u4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// grid = (ctas per page, pages); host pages are read through their mapped
+// device address.  Four independent 16-byte loads per thread are in flight.
+__global__ void __launch_bounds__(512) fill_kernel(const __grid_constant__ FillParams p) {
+    const int pg = blockIdx.y;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.src[pg]);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.dst[pg]);
+    const int64_t n = p.page_bytes / 16;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        const uint4 a = ld_nc_u4(src + i), b = ld_nc_u4(src + i + stride);
+        const uint4 c = ld_nc_u4(src + i + 2 * stride), d = ld_nc_u4(src + i + 3 * stride);
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n; i += stride) dst[i] = ld_nc_u4(src + i);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantizeParams &p, cudaStream_t s) {
+    if (p.n <= 0) return cudaSuccess;
+    const int64_t warps = (int64_t)p.n * p.geom.Hk * (p.geom.D / 32);
+    const int64_t blocks = (warps * 32 + 255) / 256;
+    quantize_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStream_t s) {
+    if (t0 <= 0) return cudaMemsetAsync(page, 0, (size_t)g.page_bytes, s);
+    if (t0 >= g.P) return cudaSuccess;
+    clear_tail_kernel<<<152, 256, 0, s>>>(page, g, t0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill(const FillParams &p, cudaStream_t s) {
+    if (p.n <= 0) return cudaSuccess;
+    if (p.n > kMaxFillPages || p.page_bytes % 16 != 0) return cudaErrorInvalidValue;
+    // about 16 CTAs in total saturate the host link (measured); at least one per page
+    int per_page = (16 + p.n - 1) / p.n;
+    dim3 grid(per_page, p.n);
+    fill_kernel<<<grid, 512, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kvs

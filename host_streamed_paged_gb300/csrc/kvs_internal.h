@@ -1,0 +1,96 @@
+// Internal declarations shared by the kvs host runtime and its CUDA kernels.
+// Nothing here is part of the C ABI (include/kvs.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvs {
+
+// Byte layout of one page (see kvs_query_sizes in include/kvs.h).
+struct PageGeom {
+    int P;               // tokens per page
+    int Hk;              // kv heads
+    int D;               // head dim
+    int64_t head_bytes;  // P*D*13/8: one kv head's section
+    int64_t page_bytes;  // Hk*head_bytes
+    int64_t ks_off;      // K scales  fp16 [P][D/32]
+    int64_t vq_off;      // V nibbles u8  [D/2][P]
+    int64_t vs_off;      // V scales  fp16 [D/32][P]
+};
+
+inline PageGeom make_geom(int P, int Hk, int D) {
+    PageGeom g;
+    g.P = P;
+    g.Hk = Hk;
+    g.D = D;
+    g.ks_off = (int64_t)P * D;
+    g.vq_off = g.ks_off + (int64_t)P * D / 16;
+    g.vs_off = g.vq_off + (int64_t)P * D / 2;
+    g.head_bytes = g.vs_off + (int64_t)P * D / 16;
+    g.page_bytes = g.head_bytes * Hk;
+    return g;
+}
+
+// ---------------------------------------------------------------- decode
+// One work item = one (page, device slot) pair; the grid is (items, Hk).
+constexpr int kMaxItems = 256;
+
+struct DecodeParams {
+    const uint8_t *arena;  // slot 0 of the page-slot array
+    PageGeom geom;
+    const void *q;         // [R][Hq][D], fp32 or fp16
+    int q_f16;
+    float *part_o;         // [split][Hq][R][D]   split = logical page
+    float *part_ml;        // [split][Hq][R][2]   (max in log2 units, sum)
+    int R, Hq, G;
+    long long pos0;
+    float scale_log2;      // scale * log2(e)
+    int n_items;
+    uint32_t page[kMaxItems];
+    uint32_t slot[kMaxItems];
+};
+
+// Returns cudaErrorInvalidValue for an unsupported (D, rows) combination.
+cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s);
+int decode_max_mma_rows();  // G*R bound served by launch_decode
+
+// ---------------------------------------------------------------- combine
+struct CombineParams {
+    const float *part_o;
+    const float *part_ml;
+    float *out;   // [R][Hq][D]
+    float *lse;   // [R][Hq] or null
+    int R, Hq, D, P;
+    long long pos0;
+};
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
+
+// ---------------------------------------------------------------- append
+// Quantise rows [n][Hk][D] of K (Q8_0) and V (Q4_0) into one page slot,
+// token slots t0 .. t0+n-1 of that page.
+struct QuantizeParams {
+    const float *k;
+    const float *v;
+    uint8_t *page;  // device page base
+    PageGeom geom;
+    int t0, n;
+};
+cudaError_t launch_quantize(const QuantizeParams &p, cudaStream_t s);
+
+// Zero token slots [t0, P) of one device page (all sections of all heads).
+cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStream_t s);
+
+// ---------------------------------------------------------------- ring fill
+// Copy whole pages host -> device with SM loads (pinned host memory is
+// directly addressable by the GPU).  One launch per ring chunk.
+constexpr int kMaxFillPages = 64;
+struct FillParams {
+    int n;
+    int64_t page_bytes;
+    const uint8_t *src[kMaxFillPages];
+    uint8_t *dst[kMaxFillPages];
+};
+cudaError_t launch_fill(const FillParams &p, cudaStream_t s);
+
+}  // namespace kvs

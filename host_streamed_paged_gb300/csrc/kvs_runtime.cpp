@@ -1,0 +1,1170 @@
+// kvs host runtime: geometry, host history, page table, resident pool, the
+// shared transfer ring with its ready/consumed fences, the span plan and the
+// C ABI of include/kvs.h.
+//
+// Design source: "Adaptive KV Streaming for llama.cpp V2" --
+//   "KV data movement and attention": the complete history stays in host
+//     memory; the device holds resident pages plus ONE ring shared by every
+//     layer; the copy stream fills free slots for later layers while the
+//     attention stream computes; a ready fence keeps attention from reading
+//     an incomplete copy and a consumed fence keeps the copy stream from
+//     overwriting a slot still in use; physical budget = resident pages +
+//     ring slots.
+//   "Keep the stock attention order": one ordered history, resident pages
+//     and ring spans (at most two per wrap), then one final reduction.
+//   "Backend-neutral memory and streaming contracts": the span plan covers
+//     the history without gaps or overlaps.
+// and "Adaptive KV Streaming for llama.cpp", "Adaptive KV streaming":
+//   consumed ring slots are recycled immediately.
+//
+// Scheduling model.  Nonresident pages are grouped, layer by layer in the
+// order layers are announced, into chunks of up to chunk_pages pages.  Each
+// page of the global chunk sequence takes the next ring sequence number and
+// lives in slot seq % ring_slots.  A chunk's copy is enqueued only when the
+// attention of every chunk that last used its slots has been enqueued; the
+// copy waits on the newest of those chunks' consumed events (attention is
+// in order, so that implies the older ones), copies, and records its own
+// ready event.  Attention waits on ready, reads, and records consumed.  Each
+// chunk holds at least one slot, so at most ring_slots chunks are live and
+// ring_slots ready/consumed events, indexed by chunk id, suffice.
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <string.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <deque>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "kvs.h"
+#include "kvs_internal.h"
+
+using kvs::PageGeom;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+constexpr int kAttn = 0;
+constexpr int kCopy = 1;
+
+struct Chunk {
+    uint64_t id;
+    uint32_t layer;
+    uint64_t seq0;               // ring sequence number of its first page
+    std::vector<int64_t> pages;  // logical pages, ascending
+    bool filled = false;
+};
+
+struct LayerState {
+    uint64_t T = 0;                  // tokens appended
+    std::vector<uint8_t> mask;       // requested residency per page
+    std::vector<int64_t> pool_slot;  // pool slot per page or -1
+    int64_t tail_page[2] = {-1, -1};  // page held by tail slot (page % 2)
+};
+
+}  // namespace
+
+struct kvs_ctx {
+    kvs_config cfg;
+    PageGeom geom;
+    bool plan_only = false;
+    cudaStream_t attn = nullptr, copy = nullptr;
+    std::string err;
+
+    // device page slots: [0, 2L) tails, [2L, 2L + pool_n) pool, then the ring
+    int64_t n_slots = 0, pool_n = 0, ring_first = 0;
+    uint32_t ring_n = 0, chunk_pages = 1;
+    std::vector<int32_t> pool_layer;  // owner layer per pool slot (-1 free)
+    std::vector<int64_t> pool_page;
+    int64_t pool_used = 0;
+
+    int64_t max_pages = 0;
+    std::vector<LayerState> layers;
+
+    uint8_t *host = nullptr;      // host history (host address)
+    uint8_t *host_dev = nullptr;  // same bytes, device-visible address
+    bool host_registered = false;
+
+    // ring scheduler
+    uint64_t ring_seq = 0, next_chunk = 0, attended = 0;
+    std::vector<int64_t> slot_last_chunk;  // per ring slot, -1 if never used
+    std::deque<Chunk> queue;               // planned chunks, not yet attended
+    std::deque<uint32_t> announced;        // layers announced by prefetch/attend, in order
+
+    // events: [0, R) ready, [R, 2R) consumed, 2R attn mark, 2R+1 copy mark,
+    // then one publish event per tail slot
+    std::vector<cudaEvent_t> events;
+    int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0;
+
+    // timing of attention kernels
+    bool timing = false;
+    std::vector<cudaEvent_t> timer_free;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timer_pending;
+
+    // fault injection
+    uint32_t fault = KVS_FAULT_NONE;
+    uint64_t fault_nth = 0, fault_count = 0;
+
+    kvs_stats_t st;
+    std::vector<kvs_trace_op> trace;
+
+    int64_t tail_slot(uint32_t layer, int64_t page) const { return 2 * (int64_t)layer + (page & 1); }
+    int64_t pool_slot_id(int64_t i) const { return 2 * (int64_t)cfg.n_layers + i; }
+    int64_t ring_slot_id(uint64_t seq) const { return ring_first + (int64_t)(seq % ring_n); }
+    uint8_t *slot_ptr(int64_t slot) const {
+        return static_cast<uint8_t *>(cfg.arena) + slot * geom.page_bytes;
+    }
+    uint8_t *host_page(uint32_t layer, int64_t page) const {
+        return host + ((int64_t)layer * max_pages + page) * geom.page_bytes;
+    }
+    uint8_t *host_page_dev(uint32_t layer, int64_t page) const {
+        return host_dev + ((int64_t)layer * max_pages + page) * geom.page_bytes;
+    }
+    cudaStream_t stream(int s) const { return s == kAttn ? attn : copy; }
+};
+
+namespace {
+
+kvs_status fail(kvs_ctx *c, kvs_status s, const std::string &msg) {
+    if (c) c->err = msg;
+    return s;
+}
+
+kvs_status cuda_fail(kvs_ctx *c, cudaError_t e, const char *what) {
+    return fail(c, KVS_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+void log_op(kvs_ctx *c, uint32_t op, int stream, uint32_t layer, uint32_t ev, int64_t a, int64_t b,
+            int64_t cc = 0) {
+    kvs_trace_op t;
+    t.op = op;
+    t.stream = (uint32_t)stream;
+    t.layer = layer;
+    t.event = ev;
+    t.a = a;
+    t.b = b;
+    t.c = cc;
+    t.d = 0;
+    c->trace.push_back(t);
+}
+
+// ---- stream primitives (logged in plan-only mode, executed otherwise)
+
+kvs_status op_record(kvs_ctx *c, int stream, int ev) {
+    if (c->plan_only) {
+        log_op(c, KVS_OP_RECORD, stream, 0, (uint32_t)ev, 0, 0);
+        return KVS_OK;
+    }
+    cudaError_t e = cudaEventRecord(c->events[ev], c->stream(stream));
+    return e == cudaSuccess ? KVS_OK : cuda_fail(c, e, "cudaEventRecord");
+}
+
+kvs_status op_wait(kvs_ctx *c, int stream, int ev) {
+    if (c->plan_only) {
+        log_op(c, KVS_OP_WAIT, stream, 0, (uint32_t)ev, 0, 0);
+        return KVS_OK;
+    }
+    cudaError_t e = cudaStreamWaitEvent(c->stream(stream), c->events[ev], 0);
+    return e == cudaSuccess ? KVS_OK : cuda_fail(c, e, "cudaStreamWaitEvent");
+}
+
+// attention stream waits for everything enqueued so far on the copy stream
+kvs_status join_copy_into_attn(kvs_ctx *c) {
+    kvs_status s = op_record(c, kCopy, c->ev_copy_mark);
+    return s != KVS_OK ? s : op_wait(c, kAttn, c->ev_copy_mark);
+}
+
+// copy stream waits for everything enqueued so far on the attention stream
+kvs_status join_attn_into_copy(kvs_ctx *c) {
+    kvs_status s = op_record(c, kAttn, c->ev_attn_mark);
+    return s != KVS_OK ? s : op_wait(c, kCopy, c->ev_attn_mark);
+}
+
+// host pages -> device slots on the copy stream (ring fill or pool load)
+kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
+                         const std::vector<int64_t> &slots, uint32_t kind,
+                         const std::vector<uint64_t> *seqs) {
+    c->st.kernel_launches += (pages.size() + kvs::kMaxFillPages - 1) / kvs::kMaxFillPages;
+    if (c->plan_only) {
+        for (size_t i = 0; i < pages.size(); ++i)
+            log_op(c, kind, kCopy, layer, 0, pages[i], slots[i], seqs ? (int64_t)(*seqs)[i] : 0);
+        return KVS_OK;
+    }
+    for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxFillPages) {
+        kvs::FillParams fp;
+        fp.n = (int)std::min<size_t>(kvs::kMaxFillPages, pages.size() - i0);
+        fp.page_bytes = c->geom.page_bytes;
+        for (int j = 0; j < fp.n; ++j) {
+            fp.src[j] = c->host_page_dev(layer, pages[i0 + j]);
+            fp.dst[j] = c->slot_ptr(slots[i0 + j]);
+        }
+        cudaError_t e = kvs::launch_fill(fp, c->copy);
+        if (e != cudaSuccess) return cuda_fail(c, e, "ring/pool fill launch");
+    }
+    return KVS_OK;
+}
+
+kvs_status timed_begin(kvs_ctx *c, cudaEvent_t *ev) {
+    *ev = nullptr;
+    if (!c->timing || c->plan_only) return KVS_OK;
+    if (c->timer_free.empty()) {
+        cudaEvent_t e;
+        cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) return cuda_fail(c, r, "cudaEventCreate");
+        c->timer_free.push_back(e);
+    }
+    *ev = c->timer_free.back();
+    c->timer_free.pop_back();
+    cudaError_t r = cudaEventRecord(*ev, c->attn);
+    return r == cudaSuccess ? KVS_OK : cuda_fail(c, r, "cudaEventRecord");
+}
+
+kvs_status timed_end(kvs_ctx *c, cudaEvent_t start) {
+    if (!start) return KVS_OK;
+    if (c->timer_free.empty()) {
+        cudaEvent_t e;
+        cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) return cuda_fail(c, r, "cudaEventCreate");
+        c->timer_free.push_back(e);
+    }
+    cudaEvent_t stop = c->timer_free.back();
+    c->timer_free.pop_back();
+    cudaError_t r = cudaEventRecord(stop, c->attn);
+    if (r != cudaSuccess) return cuda_fail(c, r, "cudaEventRecord");
+    c->timer_pending.push_back({start, stop});
+    return KVS_OK;
+}
+
+void harvest_timers(kvs_ctx *c) {
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> keep;
+    for (auto &pr : c->timer_pending) {
+        if (cudaEventQuery(pr.second) == cudaSuccess) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess) {
+                c->st.decode_ms += ms;
+                c->st.decode_timed += 1;
+            }
+            c->timer_free.push_back(pr.first);
+            c->timer_free.push_back(pr.second);
+        } else {
+            keep.push_back(pr);
+        }
+    }
+    c->timer_pending.swap(keep);
+}
+
+// ---- events
+
+void destroy_events(kvs_ctx *c) {
+    if (!c->plan_only)
+        for (cudaEvent_t e : c->events)
+            if (e) cudaEventDestroy(e);
+    c->events.clear();
+}
+
+kvs_status create_events(kvs_ctx *c) {
+    const int R = (int)c->ring_n;
+    const int n = 2 * R + 2 + 2 * (int)c->cfg.n_layers;
+    c->ev_attn_mark = 2 * R;
+    c->ev_copy_mark = 2 * R + 1;
+    c->ev_pub0 = 2 * R + 2;
+    c->events.assign(n, nullptr);
+    if (c->plan_only) return KVS_OK;
+    for (int i = 0; i < n; ++i) {
+        cudaError_t e = cudaEventCreateWithFlags(&c->events[i], cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaEventCreate");
+    }
+    return KVS_OK;
+}
+
+// ---- placement
+
+// 1: tail slot, 2: pool, 0: host only
+int locate(const kvs_ctx *c, uint32_t layer, int64_t page, int64_t *slot) {
+    const LayerState &L = c->layers[layer];
+    if (L.tail_page[page & 1] == page) {
+        *slot = c->tail_slot(layer, page);
+        return 1;
+    }
+    if (page < (int64_t)L.pool_slot.size() && L.pool_slot[page] >= 0) {
+        *slot = L.pool_slot[page];
+        return 2;
+    }
+    *slot = -1;
+    return 0;
+}
+
+int64_t n_pages_of(const kvs_ctx *c, uint32_t layer) {
+    return (int64_t)((c->layers[layer].T + c->geom.P - 1) / c->geom.P);
+}
+
+int64_t pool_alloc(kvs_ctx *c, uint32_t layer, int64_t page) {
+    for (int64_t i = 0; i < c->pool_n; ++i) {
+        if (c->pool_layer[i] < 0) {
+            c->pool_layer[i] = (int32_t)layer;
+            c->pool_page[i] = page;
+            c->pool_used++;
+            return c->pool_slot_id(i);
+        }
+    }
+    return -1;
+}
+
+void pool_free(kvs_ctx *c, int64_t slot) {
+    const int64_t i = slot - 2 * (int64_t)c->cfg.n_layers;
+    if (i >= 0 && i < c->pool_n && c->pool_layer[i] >= 0) {
+        c->pool_layer[i] = -1;
+        c->pool_page[i] = -1;
+        c->pool_used--;
+    }
+}
+
+bool layer_has_plan(const kvs_ctx *c, uint32_t layer) {
+    return std::find(c->announced.begin(), c->announced.end(), layer) != c->announced.end();
+}
+
+// Where a page leaving its tail slot goes: 1 = resident pool, 0 = host only
+// (streamed later), 2 = host only and appended to the layer's pending plan,
+// -1 = nowhere (pending plan not last in the queue and no free pool slot).
+int evict_target(const kvs_ctx *c, uint32_t layer, int64_t page, int64_t free_pool) {
+    const LayerState &L = c->layers[layer];
+    const bool want = page < (int64_t)L.mask.size() && L.mask[page];
+    const bool planned = layer_has_plan(c, layer);
+    if (want && free_pool > 0) return 1;
+    if (!planned) return 0;
+    if (c->announced.back() == layer) return 2;
+    return free_pool > 0 ? 1 : -1;
+}
+
+// ---- ring scheduling
+
+// Plan the nonresident pages of `layer` into chunks at the end of the queue.
+void plan_layer(kvs_ctx *c, uint32_t layer) {
+    const int64_t np = n_pages_of(c, layer);
+    std::vector<int64_t> streamed;
+    for (int64_t p = 0; p < np; ++p) {
+        int64_t s;
+        if (locate(c, layer, p, &s) == 0) streamed.push_back(p);
+    }
+    for (size_t i = 0; i < streamed.size(); i += c->chunk_pages) {
+        Chunk ch;
+        ch.id = c->next_chunk++;
+        ch.layer = layer;
+        ch.seq0 = c->ring_seq;
+        const size_t n = std::min<size_t>(c->chunk_pages, streamed.size() - i);
+        ch.pages.assign(streamed.begin() + i, streamed.begin() + i + n);
+        c->ring_seq += n;
+        c->queue.push_back(std::move(ch));
+    }
+    c->announced.push_back(layer);
+}
+
+bool fill_possible(const kvs_ctx *c, const Chunk &ch) {
+    for (size_t i = 0; i < ch.pages.size(); ++i) {
+        const int64_t prev = c->slot_last_chunk[(ch.seq0 + i) % c->ring_n];
+        if (prev >= 0 && (uint64_t)prev >= c->attended) return false;
+    }
+    return true;
+}
+
+kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
+    if (c->fault == KVS_FAULT_FILL_ENQUEUE && c->fault_nth) {
+        if (++c->fault_count == c->fault_nth)
+            return fail(c, KVS_ERR_INJECTED, "injected fault: ring refill enqueue");
+    }
+    int64_t newest = -1;
+    for (size_t i = 0; i < ch.pages.size(); ++i)
+        newest = std::max(newest, c->slot_last_chunk[(ch.seq0 + i) % c->ring_n]);
+    kvs_status s;
+    if (newest >= 0) {
+        s = op_wait(c, kCopy, (int)c->ring_n + (int)(newest % c->ring_n));
+        if (s != KVS_OK) return s;
+    }
+    std::vector<int64_t> slots(ch.pages.size());
+    std::vector<uint64_t> seqs(ch.pages.size());
+    for (size_t i = 0; i < ch.pages.size(); ++i) {
+        seqs[i] = ch.seq0 + i;
+        slots[i] = c->ring_slot_id(ch.seq0 + i);
+    }
+    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs);
+    if (s != KVS_OK) return s;
+    s = op_record(c, kCopy, (int)(ch.id % c->ring_n));
+    if (s != KVS_OK) return s;
+    for (size_t i = 0; i < ch.pages.size(); ++i) {
+        int64_t &last = c->slot_last_chunk[(ch.seq0 + i) % c->ring_n];
+        if (last >= 0) c->st.ring_recycles++;
+        last = (int64_t)ch.id;
+    }
+    c->st.h2d_pages += ch.pages.size();
+    c->st.h2d_bytes += ch.pages.size() * (uint64_t)c->geom.page_bytes;
+    c->st.h2d_launches += 1;
+    ch.filled = true;
+    return KVS_OK;
+}
+
+// Enqueue every copy that may go now, in queue order.
+kvs_status pump(kvs_ctx *c) {
+    for (Chunk &ch : c->queue) {
+        if (ch.filled) continue;
+        if (!fill_possible(c, ch)) break;
+        kvs_status s = fill_chunk(c, ch);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+// ---- attention launches
+
+kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
+                        const std::vector<int64_t> &slots, kvs::DecodeParams &dp) {
+    for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxItems) {
+        const int n = (int)std::min<size_t>(kvs::kMaxItems, pages.size() - i0);
+        c->st.decode_launches++;
+        c->st.kernel_launches++;
+        if (c->plan_only) {
+            log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 1, n);
+            for (int j = 0; j < n; ++j)
+                for (int g = 0; g < c->geom.Hk; ++g)
+                    log_op(c, KVS_OP_READ, kAttn, layer, 0, pages[i0 + j], slots[i0 + j], g);
+            continue;
+        }
+        dp.n_items = n;
+        for (int j = 0; j < n; ++j) {
+            dp.page[j] = (uint32_t)pages[i0 + j];
+            dp.slot[j] = (uint32_t)slots[i0 + j];
+        }
+        cudaEvent_t t0;
+        kvs_status s = timed_begin(c, &t0);
+        if (s != KVS_OK) return s;
+        cudaError_t e = kvs::launch_decode(dp, c->attn);
+        if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel launch");
+        s = timed_end(c, t0);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+bool geometry_ok(const kvs_config *cfg, std::string *why) {
+    const uint32_t P = cfg->page_tokens, D = cfg->head_dim;
+    if (!(P == 32 || P == 64 || P == 128 || P == 256)) {
+        *why = "page_tokens must be 32, 64, 128 or 256";
+        return false;
+    }
+    if (!(D == 64 || D == 128 || D == 256)) {
+        *why = "head_dim must be 64, 128 or 256";
+        return false;
+    }
+    if (cfg->n_kv_head < 1 || cfg->n_layers < 1 || cfg->max_tokens < 1) {
+        *why = "n_kv_head, n_layers and max_tokens must be positive";
+        return false;
+    }
+    if (cfg->max_q_head < cfg->n_kv_head || cfg->max_q_head % cfg->n_kv_head != 0) {
+        *why = "max_q_head must be a positive multiple of n_kv_head";
+        return false;
+    }
+    const uint32_t G = cfg->max_q_head / cfg->n_kv_head;
+    if (cfg->max_rows < 1 || G * cfg->max_rows > (uint32_t)kvs::decode_max_mma_rows()) {
+        *why = "max_rows * (max_q_head / n_kv_head) must be in 1..64";
+        return false;
+    }
+    if (cfg->k_type != KVS_TYPE_Q8_0 || cfg->v_type != KVS_TYPE_Q4_0) {
+        *why = "only K = Q8_0 and V = Q4_0 are served";
+        return false;
+    }
+    return true;
+}
+
+void sizes_of(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes, uint64_t *arena_min,
+              uint64_t *ws_min) {
+    const PageGeom g = kvs::make_geom((int)cfg->page_tokens, (int)cfg->n_kv_head, (int)cfg->head_dim);
+    const uint64_t max_pages = (cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens;
+    const uint64_t ring = cfg->ring_slots ? cfg->ring_slots : 1;
+    if (page_bytes) *page_bytes = (uint64_t)g.page_bytes;
+    if (host_bytes) *host_bytes = (uint64_t)cfg->n_layers * max_pages * (uint64_t)g.page_bytes;
+    if (arena_min) *arena_min = (2ull * cfg->n_layers + ring) * (uint64_t)g.page_bytes;
+    if (ws_min)
+        *ws_min = max_pages * cfg->max_q_head * cfg->max_rows * (uint64_t)(cfg->head_dim + 2) * 4ull;
+}
+
+}  // namespace
+
+// ======================================================================= C ABI
+
+extern "C" {
+
+int32_t kvs_version(void) { return KVS_ABI_VERSION; }
+
+const char *kvs_last_error(const kvs_ctx *ctx) {
+    return ctx ? ctx->err.c_str() : g_create_error.c_str();
+}
+
+kvs_status kvs_query_sizes(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
+                           uint64_t *arena_bytes_min, uint64_t *workspace_bytes) {
+    if (!cfg) return KVS_ERR_INVALID;
+    std::string why;
+    if (!geometry_ok(cfg, &why)) {
+        g_create_error = why;
+        return KVS_ERR_UNSUPPORTED;
+    }
+    sizes_of(cfg, page_bytes, host_bytes, arena_bytes_min, workspace_bytes);
+    return KVS_OK;
+}
+
+kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
+    if (!out) return KVS_ERR_INVALID;
+    *out = nullptr;
+    g_create_error.clear();
+    if (!cfg) {
+        g_create_error = "cfg is NULL";
+        return KVS_ERR_INVALID;
+    }
+    std::string why;
+    if (!geometry_ok(cfg, &why)) {
+        g_create_error = why;
+        return KVS_ERR_UNSUPPORTED;
+    }
+    uint64_t page_bytes, host_min, arena_min, ws_min;
+    sizes_of(cfg, &page_bytes, &host_min, &arena_min, &ws_min);
+    const bool plan_only = (cfg->flags & KVS_FLAG_PLAN_ONLY) != 0;
+    if (cfg->ring_slots < 1) {
+        g_create_error = "ring_slots must be >= 1";
+        return KVS_ERR_INVALID;
+    }
+    if (!cfg->arena || cfg->arena_bytes < arena_min) {
+        g_create_error = "arena below the minimum of 2 tail slots per layer plus the ring (" +
+                         std::to_string(arena_min) + " bytes)";
+        return KVS_ERR_ARENA;
+    }
+    if (!cfg->workspace || cfg->workspace_bytes < ws_min) {
+        g_create_error = "workspace below the minimum (" + std::to_string(ws_min) + " bytes)";
+        return KVS_ERR_ARENA;
+    }
+    if ((reinterpret_cast<uintptr_t>(cfg->arena) & 255) || (reinterpret_cast<uintptr_t>(cfg->workspace) & 255)) {
+        g_create_error = "arena and workspace must be 256-byte aligned";
+        return KVS_ERR_INVALID;
+    }
+    if ((!cfg->host && !plan_only) || cfg->host_bytes < host_min) {
+        g_create_error = "host history below the minimum (" + std::to_string(host_min) + " bytes)";
+        return KVS_ERR_HOST;
+    }
+    kvs_ctx *c = new kvs_ctx();
+    c->cfg = *cfg;
+    c->plan_only = plan_only;
+    c->geom = kvs::make_geom((int)cfg->page_tokens, (int)cfg->n_kv_head, (int)cfg->head_dim);
+    c->attn = static_cast<cudaStream_t>(cfg->attn_stream);
+    c->copy = static_cast<cudaStream_t>(cfg->copy_stream);
+    c->max_pages = (int64_t)((cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens);
+    c->layers.resize(cfg->n_layers);
+    for (auto &L : c->layers) L.pool_slot.assign(c->max_pages, -1);
+    c->n_slots = (int64_t)(cfg->arena_bytes / (uint64_t)c->geom.page_bytes);
+    c->ring_n = cfg->ring_slots;
+    c->chunk_pages = cfg->chunk_pages ? std::min(cfg->chunk_pages, cfg->ring_slots)
+                                      : std::max(1u, cfg->ring_slots / 4);
+    c->ring_first = c->n_slots - c->ring_n;
+    c->pool_n = c->ring_first - 2 * (int64_t)cfg->n_layers;
+    c->pool_layer.assign(c->pool_n, -1);
+    c->pool_page.assign(c->pool_n, -1);
+    c->slot_last_chunk.assign(c->ring_n, -1);
+    memset(&c->st, 0, sizeof(c->st));
+    c->host = static_cast<uint8_t *>(cfg->host);
+    c->host_dev = c->host;
+    if (!plan_only) {
+        if (!c->attn || !c->copy || c->attn == c->copy) {
+            delete c;
+            g_create_error = "attn_stream and copy_stream must be two distinct CUDA streams";
+            return KVS_ERR_INVALID;
+        }
+        cudaPointerAttributes pa;
+        cudaError_t e = cudaPointerGetAttributes(&pa, cfg->host);
+        if (e != cudaSuccess || pa.type != cudaMemoryTypeHost) {
+            cudaGetLastError();
+            e = cudaHostRegister(cfg->host, cfg->host_bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                delete c;
+                g_create_error = std::string("cudaHostRegister of the host history failed: ") + cudaGetErrorString(e);
+                return KVS_ERR_HOST;
+            }
+            c->host_registered = true;
+        }
+        void *dp = nullptr;
+        e = cudaHostGetDevicePointer(&dp, cfg->host, 0);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (c->host_registered) cudaHostUnregister(cfg->host);
+            delete c;
+            g_create_error = std::string("host history is not device-mapped: ") + cudaGetErrorString(e);
+            return KVS_ERR_HOST;
+        }
+        c->host_dev = static_cast<uint8_t *>(dp);
+    }
+    if (create_events(c) != KVS_OK) {
+        g_create_error = c->err;
+        destroy_events(c);
+        if (c->host_registered) cudaHostUnregister(cfg->host);
+        delete c;
+        return KVS_ERR_CUDA;
+    }
+    c->st.ring_slots = c->ring_n;
+    c->st.pool_slots = (uint64_t)c->pool_n;
+    *out = c;
+    return KVS_OK;
+}
+
+kvs_status kvs_destroy(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    if (!c->plan_only) {
+        cudaStreamSynchronize(c->attn);
+        cudaStreamSynchronize(c->copy);
+        for (auto &pr : c->timer_pending) {
+            cudaEventDestroy(pr.first);
+            cudaEventDestroy(pr.second);
+        }
+        for (cudaEvent_t e : c->timer_free) cudaEventDestroy(e);
+        if (c->host_registered) cudaHostUnregister(c->cfg.host);
+    }
+    destroy_events(c);
+    delete c;
+    return KVS_OK;
+}
+
+kvs_status kvs_length(const kvs_ctx *c, uint32_t layer, uint64_t *n) {
+    if (!c || !n || layer >= c->cfg.n_layers) return KVS_ERR_INVALID;
+    *n = c->layers[layer].T;
+    return KVS_OK;
+}
+
+kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const float *v_dev,
+                      uint32_t n_tokens) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    if (n_tokens == 0) return KVS_OK;
+    if (!c->plan_only && (!k_dev || !v_dev)) return fail(c, KVS_ERR_INVALID, "null K/V rows");
+    LayerState &L = c->layers[layer];
+    if (L.T + n_tokens > c->cfg.max_tokens) return fail(c, KVS_ERR_CAPACITY, "append beyond max_tokens");
+    const int P = c->geom.P;
+    // Pre-check every eviction this append causes, so a refusal changes nothing.
+    {
+        int64_t free_pool = c->pool_n - c->pool_used;
+        for (uint64_t t = L.T; t < L.T + n_tokens; t = (t / P + 1) * P) {
+            if (t % P != 0) continue;
+            const int64_t q = (int64_t)(t / P), old = q - 2;
+            if (old < 0 || L.tail_page[q & 1] != old) continue;
+            if (evict_target(c, layer, old, free_pool) < 0)
+                return fail(c, KVS_ERR_STATE,
+                            "append would move a page out of its tail slot while the layer has a pending "
+                            "prefetch behind which other layers are queued, and the pool has no free slot");
+            if (evict_target(c, layer, old, free_pool) == 1) free_pool--;
+        }
+    }
+    uint64_t done = 0;
+    while (done < n_tokens) {
+        const uint64_t t = L.T;
+        const int64_t q = (int64_t)(t / P);
+        const int t0 = (int)(t % P);
+        const uint32_t n = (uint32_t)std::min<uint64_t>(n_tokens - done, (uint64_t)(P - t0));
+        const int64_t tslot = c->tail_slot(layer, q);
+        kvs_status s;
+        if (t0 != 0 && L.tail_page[q & 1] != q)
+            return fail(c, KVS_ERR_STATE, "internal: the partial tail page is not in its tail slot");
+        // a D2H publish of this slot may still be reading it
+        s = op_wait(c, kAttn, c->ev_pub0 + (int)tslot);
+        if (s != KVS_OK) return s;
+        if (t0 == 0) {
+            // page q starts in tail slot q % 2: evict its previous page
+            const int64_t old = L.tail_page[q & 1];
+            if (old >= 0 && old != q) {
+                const int target = evict_target(c, layer, old, c->pool_n - c->pool_used);
+                if (target == 1) {
+                    const int64_t ps = pool_alloc(c, layer, old);
+                    L.pool_slot[old] = ps;
+                    if (c->plan_only) {
+                        log_op(c, KVS_OP_MOVE, kAttn, layer, 0, old, ps);
+                    } else {
+                        cudaError_t e = cudaMemcpyAsync(c->slot_ptr(ps), c->slot_ptr(tslot),
+                                                        (size_t)c->geom.page_bytes,
+                                                        cudaMemcpyDeviceToDevice, c->attn);
+                        if (e != cudaSuccess) return cuda_fail(c, e, "tail -> pool move");
+                    }
+                } else if (target == 2) {
+                    // stream it: it joins the pending plan of this (last announced) layer
+                    Chunk ch;
+                    ch.id = c->next_chunk++;
+                    ch.layer = layer;
+                    ch.seq0 = c->ring_seq++;
+                    ch.pages.push_back(old);
+                    c->queue.push_back(std::move(ch));
+                }
+            }
+            L.tail_page[q & 1] = q;
+            if (c->plan_only) {
+                c->st.kernel_launches++;
+            } else {
+                cudaError_t e = kvs::launch_clear_tail(c->slot_ptr(tslot), c->geom, t0, c->attn);
+                if (e != cudaSuccess) return cuda_fail(c, e, "tail page clear");
+                c->st.kernel_launches++;
+            }
+        }
+        if (c->plan_only) {
+            log_op(c, KVS_OP_WRITE, kAttn, layer, 0, q, tslot, n);
+        } else {
+            kvs::QuantizeParams qp;
+            const int64_t row = (int64_t)c->geom.Hk * c->geom.D;
+            qp.k = k_dev + (int64_t)done * row;
+            qp.v = v_dev + (int64_t)done * row;
+            qp.page = c->slot_ptr(tslot);
+            qp.geom = c->geom;
+            qp.t0 = t0;
+            qp.n = (int)n;
+            cudaError_t e = kvs::launch_quantize(qp, c->attn);
+            if (e != cudaSuccess) return cuda_fail(c, e, "quantise/append launch");
+        }
+        c->st.kernel_launches++;
+        L.T += n;
+        done += n;
+        if (L.T % P == 0) {
+            // page q is complete: publish it to the host history
+            s = join_attn_into_copy(c);
+            if (s != KVS_OK) return s;
+            if (c->plan_only) {
+                log_op(c, KVS_OP_PUBLISH, kCopy, layer, 0, q, tslot);
+            } else {
+                cudaError_t e = cudaMemcpyAsync(c->host_page(layer, q), c->slot_ptr(tslot),
+                                                (size_t)c->geom.page_bytes, cudaMemcpyDeviceToHost,
+                                                c->copy);
+                if (e != cudaSuccess) return cuda_fail(c, e, "tail publish");
+            }
+            s = op_record(c, kCopy, c->ev_pub0 + (int)tslot);
+            if (s != KVS_OK) return s;
+            c->st.d2h_pages++;
+            c->st.d2h_bytes += (uint64_t)c->geom.page_bytes;
+        }
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_truncate(kvs_ctx *c, uint32_t layer, uint64_t n_tokens) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    LayerState &L = c->layers[layer];
+    if (n_tokens > L.T) return fail(c, KVS_ERR_INVALID, "truncate beyond the current length");
+    if (n_tokens == L.T) return KVS_OK;
+    if (layer_has_plan(c, layer)) return fail(c, KVS_ERR_STATE, "layer has a pending prefetch");
+    const int P = c->geom.P;
+    const int64_t new_last = n_tokens ? (int64_t)((n_tokens - 1) / P) : -1;
+    const int64_t cur_last = (int64_t)((L.T - 1) / P);
+    // pages new_last+1 .. cur_last are dropped; the new tail page must be in a tail slot
+    if (n_tokens > 0 && n_tokens % P != 0 && L.tail_page[new_last & 1] != new_last)
+        return fail(c, KVS_ERR_UNSUPPORTED, "truncation further back than the two tail pages");
+    for (int64_t p = new_last + 1; p <= cur_last; ++p) {
+        if (L.tail_page[p & 1] == p) L.tail_page[p & 1] = -1;
+        if (p < (int64_t)L.pool_slot.size() && L.pool_slot[p] >= 0) {
+            pool_free(c, L.pool_slot[p]);
+            L.pool_slot[p] = -1;
+        }
+    }
+    if (n_tokens % P != 0 && !c->plan_only) {
+        cudaError_t e = kvs::launch_clear_tail(c->slot_ptr(c->tail_slot(layer, new_last)), c->geom,
+                                               (int)(n_tokens % P), c->attn);
+        if (e != cudaSuccess) return cuda_fail(c, e, "truncate clear");
+        c->st.kernel_launches++;
+    }
+    L.T = n_tokens;
+    return KVS_OK;
+}
+
+kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, uint64_t n_pages) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    if (n_pages > (uint64_t)c->max_pages) return fail(c, KVS_ERR_INVALID, "mask longer than max pages");
+    if (n_pages && !mask) return fail(c, KVS_ERR_INVALID, "null mask");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "residency change while prefetches are pending");
+    LayerState &L = c->layers[layer];
+    const int64_t complete = (int64_t)(L.T / c->geom.P);  // pages 0..complete-1 are full
+    std::vector<uint8_t> want(c->max_pages, 0);
+    for (uint64_t i = 0; i < n_pages; ++i) want[i] = mask[i] ? 1 : 0;
+    // count the change
+    int64_t need = 0;
+    for (int64_t p = 0; p < complete; ++p) {
+        int64_t s;
+        const int loc = locate(c, layer, p, &s);
+        if (want[p] && loc == 0) need++;
+        if (!want[p] && loc == 2) need--;
+    }
+    if (need > c->pool_n - c->pool_used)
+        return fail(c, KVS_ERR_CAPACITY, "resident pool has too few free slots for this mask");
+    L.mask.assign(want.begin(), want.begin() + std::max<int64_t>(n_pages, 0));
+    // slots leaving the pool may still be read by queued attention
+    kvs_status s = join_attn_into_copy(c);
+    if (s != KVS_OK) return s;
+    for (int64_t p = 0; p < complete; ++p) {
+        if (!want[p] && L.pool_slot[p] >= 0 && L.tail_page[p & 1] != p) {
+            pool_free(c, L.pool_slot[p]);
+            L.pool_slot[p] = -1;
+        }
+    }
+    std::vector<int64_t> pages, slots;
+    for (int64_t p = 0; p < complete; ++p) {
+        int64_t sl;
+        if (want[p] && locate(c, layer, p, &sl) == 0) {
+            const int64_t ps = pool_alloc(c, layer, p);
+            L.pool_slot[p] = ps;
+            pages.push_back(p);
+            slots.push_back(ps);
+        }
+    }
+    if (!pages.empty()) {
+        s = op_copy_pages(c, layer, pages, slots, KVS_OP_POOL_LOAD, nullptr);
+        if (s != KVS_OK) return s;
+        c->st.pool_load_bytes += pages.size() * (uint64_t)c->geom.page_bytes;
+        s = join_copy_into_attn(c);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (n_slots < 1) return fail(c, KVS_ERR_INVALID, "ring needs at least one slot");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "ring change while prefetches are pending");
+    const int64_t base = 2 * (int64_t)c->cfg.n_layers;
+    const int64_t new_pool = c->n_slots - base - (int64_t)n_slots;
+    if (new_pool < 0) return fail(c, KVS_ERR_CAPACITY, "arena too small for that ring");
+    if (c->pool_used > new_pool) return fail(c, KVS_ERR_CAPACITY, "resident pages exceed the new pool");
+    // ring and pool slots change role: order after all earlier device work
+    kvs_status s = join_attn_into_copy(c);
+    if (s != KVS_OK) return s;
+    s = join_copy_into_attn(c);
+    if (s != KVS_OK) return s;
+    // compact resident pages that sit in slots the new ring takes
+    for (int64_t i = new_pool; i < c->pool_n; ++i) {
+        if (c->pool_layer[i] < 0) continue;
+        int64_t j = 0;
+        while (j < new_pool && c->pool_layer[j] >= 0) ++j;
+        const uint32_t layer = (uint32_t)c->pool_layer[i];
+        const int64_t page = c->pool_page[i];
+        if (c->plan_only) {
+            log_op(c, KVS_OP_MOVE, kAttn, layer, 0, page, c->pool_slot_id(j));
+        } else {
+            cudaError_t e = cudaMemcpyAsync(c->slot_ptr(c->pool_slot_id(j)), c->slot_ptr(c->pool_slot_id(i)),
+                                            (size_t)c->geom.page_bytes, cudaMemcpyDeviceToDevice, c->attn);
+            if (e != cudaSuccess) return cuda_fail(c, e, "pool compaction");
+        }
+        c->pool_layer[j] = c->pool_layer[i];
+        c->pool_page[j] = page;
+        c->pool_layer[i] = -1;
+        c->pool_page[i] = -1;
+        c->layers[layer].pool_slot[page] = c->pool_slot_id(j);
+    }
+    s = join_attn_into_copy(c);
+    if (s != KVS_OK) return s;
+    // new event set for the new ring size
+    if (!c->plan_only) {
+        cudaStreamSynchronize(c->attn);
+        cudaStreamSynchronize(c->copy);
+    }
+    destroy_events(c);
+    c->ring_n = n_slots;
+    c->chunk_pages = chunk_pages ? std::min(chunk_pages, n_slots) : std::max(1u, n_slots / 4);
+    c->ring_first = c->n_slots - n_slots;
+    c->pool_layer.resize(new_pool);
+    c->pool_page.resize(new_pool);
+    if (new_pool > c->pool_n) {
+        std::fill(c->pool_layer.begin() + c->pool_n, c->pool_layer.end(), -1);
+        std::fill(c->pool_page.begin() + c->pool_n, c->pool_page.end(), -1);
+    }
+    c->pool_n = new_pool;
+    c->slot_last_chunk.assign(c->ring_n, -1);
+    c->ring_seq = 0;
+    c->st.ring_slots = c->ring_n;
+    c->st.pool_slots = (uint64_t)c->pool_n;
+    return create_events(c);
+}
+
+kvs_status kvs_prefetch(kvs_ctx *c, uint32_t layer) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    if (layer_has_plan(c, layer)) return KVS_OK;
+    plan_layer(c, layer);
+    return pump(c);
+}
+
+kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_dtype, uint32_t n_rows,
+                      uint32_t n_q_head, uint64_t pos0, float scale, float *out_dev, float *lse_dev) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    if (q_dtype != KVS_F32 && q_dtype != KVS_F16) return fail(c, KVS_ERR_INVALID, "q_dtype must be F32 or F16");
+    if (n_rows < 1) return fail(c, KVS_ERR_INVALID, "n_rows must be >= 1");
+    if (n_q_head < (uint32_t)c->geom.Hk || n_q_head % c->geom.Hk != 0 || n_q_head > c->cfg.max_q_head)
+        return fail(c, KVS_ERR_INVALID, "n_q_head must be a multiple of n_kv_head and <= max_q_head");
+    const uint32_t G = n_q_head / c->geom.Hk;
+    if (n_rows > c->cfg.max_rows || G * n_rows > (uint32_t)kvs::decode_max_mma_rows())
+        return fail(c, KVS_ERR_UNSUPPORTED, "n_rows beyond max_rows or beyond 64 query rows per kv head");
+    LayerState &L = c->layers[layer];
+    if (pos0 + n_rows > L.T) return fail(c, KVS_ERR_CAPACITY, "rows beyond the appended length");
+    if (!c->plan_only && (!q_dev || !out_dev)) return fail(c, KVS_ERR_INVALID, "null q or out");
+    if (!c->announced.empty() && c->announced.front() != layer)
+        return fail(c, KVS_ERR_STATE, "layers must be attended in the order they were prefetched");
+    if (c->announced.empty()) plan_layer(c, layer);
+
+    const int P = c->geom.P;
+    const int64_t last = (int64_t)((pos0 + n_rows - 1) / P);
+    const int64_t np = n_pages_of(c, layer);
+
+    // the plan must still cover exactly the nonresident pages
+    std::vector<int64_t> res_pages, res_slots, streamed;
+    for (int64_t p = 0; p < np; ++p) {
+        int64_t s;
+        if (locate(c, layer, p, &s) == 0) {
+            streamed.push_back(p);
+        } else if (p <= last) {
+            res_pages.push_back(p);
+            res_slots.push_back(s);
+        }
+    }
+    {
+        size_t k = 0;
+        for (const Chunk &ch : c->queue) {
+            if (ch.layer != layer) break;
+            for (int64_t p : ch.pages) {
+                if (k >= streamed.size() || streamed[k] != p)
+                    return fail(c, KVS_ERR_COVERAGE, "span plan no longer matches the layer's residency");
+                ++k;
+            }
+        }
+        if (k != streamed.size()) return fail(c, KVS_ERR_COVERAGE, "span plan leaves nonresident pages uncovered");
+    }
+
+    kvs::DecodeParams dp;
+    memset(&dp, 0, offsetof(kvs::DecodeParams, page));
+    dp.arena = static_cast<const uint8_t *>(c->cfg.arena);
+    dp.geom = c->geom;
+    dp.q = q_dev;
+    dp.q_f16 = q_dtype == KVS_F16;
+    const size_t per_split = (size_t)n_q_head * n_rows;
+    dp.part_o = static_cast<float *>(c->cfg.workspace);
+    dp.part_ml = dp.part_o + (size_t)c->max_pages * per_split * c->geom.D;
+    dp.R = (int)n_rows;
+    dp.Hq = (int)n_q_head;
+    dp.G = (int)G;
+    dp.pos0 = (long long)pos0;
+    dp.scale_log2 = scale * 1.4426950408889634f;
+
+    c->st.attend_calls++;
+    kvs_status s = pump(c);
+    if (s != KVS_OK) return s;
+    // resident and tail pages need no fence
+    if (!res_pages.empty()) {
+        s = launch_items(c, layer, res_pages, res_slots, dp);
+        if (s != KVS_OK) return s;
+        c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
+    }
+    // ring chunks in order: ready fence, read, consumed fence, refill
+    while (!c->queue.empty() && c->queue.front().layer == layer) {
+        Chunk &ch = c->queue.front();
+        if (!ch.filled) {
+            s = pump(c);
+            if (s != KVS_OK) return s;
+            if (!ch.filled) return fail(c, KVS_ERR_COVERAGE, "ring chunk could not be scheduled");
+        }
+        s = op_wait(c, kAttn, (int)(ch.id % c->ring_n));
+        if (s != KVS_OK) return s;
+        std::vector<int64_t> pg, sl;
+        for (size_t i = 0; i < ch.pages.size(); ++i) {
+            if (ch.pages[i] > last) continue;
+            pg.push_back(ch.pages[i]);
+            sl.push_back(c->ring_slot_id(ch.seq0 + i));
+        }
+        if (!pg.empty()) {
+            s = launch_items(c, layer, pg, sl, dp);
+            if (s != KVS_OK) return s;
+            c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
+        }
+        s = op_record(c, kAttn, (int)c->ring_n + (int)(ch.id % c->ring_n));
+        if (s != KVS_OK) return s;
+        c->attended = ch.id + 1;
+        c->st.ring_chunks++;
+        c->queue.pop_front();
+        s = pump(c);
+        if (s != KVS_OK) return s;
+    }
+    c->announced.pop_front();
+    // final reduction over pages in logical order
+    c->st.kernel_launches++;
+    if (c->plan_only) {
+        log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 2, (int64_t)n_rows * n_q_head);
+    } else {
+        kvs::CombineParams cp;
+        cp.part_o = dp.part_o;
+        cp.part_ml = dp.part_ml;
+        cp.out = out_dev;
+        cp.lse = lse_dev;
+        cp.R = (int)n_rows;
+        cp.Hq = (int)n_q_head;
+        cp.D = c->geom.D;
+        cp.P = P;
+        cp.pos0 = (long long)pos0;
+        cudaError_t e = kvs::launch_combine(cp, c->attn);
+        if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
+    }
+    return pump(c);
+}
+
+kvs_status kvs_sync(kvs_ctx *c, uint32_t timeout_ms) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    const auto t0 = std::chrono::steady_clock::now();
+    auto expired = [&]() {
+        return timeout_ms && std::chrono::steady_clock::now() - t0 >= std::chrono::milliseconds(timeout_ms);
+    };
+    const bool stall = c->fault == KVS_FAULT_SYNC_STALL && c->fault_nth && ++c->fault_count >= c->fault_nth;
+    if (c->plan_only) {
+        if (!stall) return KVS_OK;
+        while (!expired()) std::this_thread::sleep_for(std::chrono::microseconds(200));
+        return fail(c, KVS_ERR_TIMEOUT, "kvs_sync deadline passed");
+    }
+    kvs_status s = op_record(c, kAttn, c->ev_attn_mark);
+    if (s != KVS_OK) return s;
+    s = op_record(c, kCopy, c->ev_copy_mark);
+    if (s != KVS_OK) return s;
+    for (;;) {
+        bool done = !stall;
+        for (int ev : {c->ev_attn_mark, c->ev_copy_mark}) {
+            cudaError_t e = cudaEventQuery(c->events[ev]);
+            if (e == cudaErrorNotReady) {
+                done = false;
+            } else if (e != cudaSuccess) {
+                return cuda_fail(c, e, "kvs_sync");
+            }
+        }
+        if (done) break;
+        if (expired()) return fail(c, KVS_ERR_TIMEOUT, "kvs_sync deadline passed");
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+    harvest_timers(c);
+    return KVS_OK;
+}
+
+kvs_status kvs_flush(kvs_ctx *c, uint32_t layer) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    uint32_t l0 = layer, l1 = layer + 1;
+    if (layer == UINT32_MAX) {
+        l0 = 0;
+        l1 = c->cfg.n_layers;
+    } else if (layer >= c->cfg.n_layers) {
+        return fail(c, KVS_ERR_INVALID, "layer out of range");
+    }
+    kvs_status s = join_attn_into_copy(c);
+    if (s != KVS_OK) return s;
+    for (uint32_t l = l0; l < l1; ++l) {
+        const LayerState &L = c->layers[l];
+        if (L.T % c->geom.P == 0) continue;  // full pages were published already
+        const int64_t q = (int64_t)(L.T / c->geom.P);
+        const int64_t ts = c->tail_slot(l, q);
+        if (c->plan_only) {
+            log_op(c, KVS_OP_PUBLISH, kCopy, l, 0, q, ts);
+        } else {
+            cudaError_t e = cudaMemcpyAsync(c->host_page(l, q), c->slot_ptr(ts), (size_t)c->geom.page_bytes,
+                                            cudaMemcpyDeviceToHost, c->copy);
+            if (e != cudaSuccess) return cuda_fail(c, e, "tail flush");
+        }
+        s = op_record(c, kCopy, c->ev_pub0 + (int)ts);
+        if (s != KVS_OK) return s;
+        c->st.d2h_pages++;
+        c->st.d2h_bytes += (uint64_t)c->geom.page_bytes;
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_page_location(const kvs_ctx *c, uint32_t layer, uint64_t page, int32_t *kind, int64_t *slot) {
+    if (!c || !kind || !slot || layer >= c->cfg.n_layers || page >= (uint64_t)c->max_pages)
+        return KVS_ERR_INVALID;
+    *kind = locate(c, layer, (int64_t)page, slot);
+    return KVS_OK;
+}
+
+kvs_status kvs_read_slot(kvs_ctx *c, int64_t slot, void *host_dst) {
+    if (!c || !host_dst) return KVS_ERR_INVALID;
+    if (slot < 0 || slot >= c->n_slots) return fail(c, KVS_ERR_INVALID, "slot out of range");
+    if (c->plan_only) return fail(c, KVS_ERR_STATE, "no device memory in plan-only mode");
+    kvs_status s = kvs_sync(c, 0);
+    if (s != KVS_OK) return s;
+    cudaError_t e = cudaMemcpy(host_dst, c->slot_ptr(slot), (size_t)c->geom.page_bytes, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? KVS_OK : cuda_fail(c, e, "slot read");
+}
+
+kvs_status kvs_read_host_page(kvs_ctx *c, uint32_t layer, uint64_t page, void *host_dst) {
+    if (!c || !host_dst || layer >= c->cfg.n_layers || page >= (uint64_t)c->max_pages) return KVS_ERR_INVALID;
+    if (!c->host) return fail(c, KVS_ERR_STATE, "no host history");
+    kvs_status s = kvs_sync(c, 0);
+    if (s != KVS_OK) return s;
+    memcpy(host_dst, c->host_page(layer, (int64_t)page), (size_t)c->geom.page_bytes);
+    return KVS_OK;
+}
+
+kvs_status kvs_ring_info(const kvs_ctx *c, int64_t *first_slot, uint32_t *n_slots) {
+    if (!c) return KVS_ERR_INVALID;
+    if (first_slot) *first_slot = c->ring_first;
+    if (n_slots) *n_slots = c->ring_n;
+    return KVS_OK;
+}
+
+kvs_status kvs_stats(kvs_ctx *c, kvs_stats_t *out, int reset) {
+    if (!c || !out) return KVS_ERR_INVALID;
+    if (!c->plan_only) harvest_timers(c);
+    c->st.ring_slots = c->ring_n;
+    c->st.pool_slots = (uint64_t)c->pool_n;
+    c->st.pool_used = (uint64_t)c->pool_used;
+    *out = c->st;
+    if (reset) {
+        const uint64_t rs = c->st.ring_slots, ps = c->st.pool_slots, pu = c->st.pool_used;
+        memset(&c->st, 0, sizeof(c->st));
+        c->st.ring_slots = rs;
+        c->st.pool_slots = ps;
+        c->st.pool_used = pu;
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_set_timing(kvs_ctx *c, int enable) {
+    if (!c) return KVS_ERR_INVALID;
+    c->timing = enable != 0;
+    return KVS_OK;
+}
+
+kvs_status kvs_debug_inject(kvs_ctx *c, uint32_t fault, uint64_t nth) {
+    if (!c) return KVS_ERR_INVALID;
+    if (fault > KVS_FAULT_SYNC_STALL) return fail(c, KVS_ERR_INVALID, "unknown fault kind");
+    c->fault = nth ? fault : KVS_FAULT_NONE;
+    c->fault_nth = nth;
+    c->fault_count = 0;
+    return KVS_OK;
+}
+
+kvs_status kvs_trace_read(const kvs_ctx *c, uint64_t first, uint64_t max, kvs_trace_op *ops,
+                          uint64_t *n_out, uint64_t *n_total) {
+    if (!c) return KVS_ERR_INVALID;
+    if (!c->plan_only) return KVS_ERR_STATE;
+    const uint64_t n = c->trace.size();
+    if (n_total) *n_total = n;
+    uint64_t k = 0;
+    if (ops)
+        for (uint64_t i = first; i < n && k < max; ++i, ++k) ops[k] = c->trace[i];
+    if (n_out) *n_out = k;
+    return KVS_OK;
+}
+
+}  // extern "C"

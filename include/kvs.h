@@ -1,0 +1,321 @@
+/*
+ * kvs.h -- host-streamed, block-paged, quantised KV attention on one GB300.
+ *
+ * The complete KV history of every layer lives in host memory (pinned, or
+ * registered by kvs_create).  A bounded device arena holds resident pages of
+ * chosen layers plus ONE transfer ring shared by all layers; a copy stream
+ * refills ring slots from host memory ahead of the attention stream, fenced
+ * by a "ready" event (attention waits for the copy) and a "consumed" event
+ * (the next copy into a slot waits for its last reader), and every layer
+ * still attends over its complete history.  Design source: "Adaptive KV
+ * Streaming for llama.cpp V2" (sections "KV data movement and attention",
+ * "Keep the stock attention order", "Backend-neutral memory and streaming
+ * contracts") and "Adaptive KV Streaming for llama.cpp" (section "Adaptive KV
+ * streaming": resident pages plus one shared ring, consumed slots recycled
+ * immediately, the full history still attended).
+ *
+ * Cache types: K is Q8_0 and V is Q4_0 (32-element blocks, fp16 scale; the
+ * pages' qualified pair "--cache-type-k q8_0 --cache-type-v q4_0").  Other
+ * types are refused (KVS_ERR_UNSUPPORTED), as the pages require a backend to
+ * advertise only the K/V pairs it really supports.
+ *
+ * Conventions shared by every entry point:
+ *  - Every call returns a kvs_status; nothing aborts, throws or traps.  On
+ *    failure kvs_last_error(ctx) holds a one-line reason (valid until the
+ *    next call on that context).  Errors are returned rather than aborting
+ *    because a too-tight arena or an oversize batch must be an error return
+ *    (PR "port adaptive KV streaming", review comments).
+ *  - The library allocates no device or host memory: the caller owns the
+ *    arena, the workspace, the host history, Q, out and lse, and keeps them
+ *    alive until kvs_destroy.  It creates CUDA events only.
+ *  - All device work is ordered on the caller's two streams (attn_stream,
+ *    copy_stream).  Calls return once work is enqueued; results are valid
+ *    after the attention stream reaches that point (kvs_sync, or any later
+ *    work on attn_stream).
+ *  - A context serves one sequence and is not thread-safe.
+ *  - Sizes and layouts use these symbols: P = page_tokens, Hk = n_kv_head,
+ *    D = head_dim, Hq = query heads (a multiple of Hk; query head h reads kv
+ *    head h / (Hq / Hk)), T = tokens appended to a layer.
+ */
+#ifndef KVS_H_
+#define KVS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVS_ABI_VERSION 1
+
+typedef struct kvs_ctx kvs_ctx;
+
+typedef enum {
+    KVS_OK = 0,
+    KVS_ERR_INVALID = -1,     /* bad argument or call order */
+    KVS_ERR_UNSUPPORTED = -2, /* geometry or type this build does not serve */
+    KVS_ERR_ARENA = -3,       /* arena or workspace below the minimum */
+    KVS_ERR_HOST = -4,        /* host history too small or cannot be registered */
+    KVS_ERR_CUDA = -5,        /* a CUDA runtime call failed (message in last_error) */
+    KVS_ERR_COVERAGE = -6,    /* the span plan would leave a gap or overlap */
+    KVS_ERR_CAPACITY = -7,    /* beyond max_tokens, the resident pool, or appended length */
+    KVS_ERR_TIMEOUT = -8,     /* kvs_sync deadline passed */
+    KVS_ERR_INJECTED = -9,    /* a fault armed by kvs_debug_inject fired */
+    KVS_ERR_STATE = -10       /* call not allowed in the current state (e.g. pending prefetch) */
+} kvs_status;
+
+/* Block types, numbered as the ggml type ids of the same formats. */
+typedef enum { KVS_TYPE_Q4_0 = 2, KVS_TYPE_Q8_0 = 8 } kvs_qtype;
+/* Query element types accepted by kvs_attend. */
+typedef enum { KVS_F32 = 0, KVS_F16 = 1 } kvs_dtype;
+
+/* kvs_config.flags */
+#define KVS_FLAG_PLAN_ONLY 1u /* host scheduling only: no CUDA call is made, no
+                                 kernel runs and no output is written; every
+                                 operation the context would enqueue is logged
+                                 for kvs_trace_read.  For testing the host-side
+                                 planner on machines without a GPU. */
+
+typedef struct {
+    uint32_t page_tokens;  /* P: token positions per page; 32, 64, 128 or 256 */
+    uint32_t n_layers;     /* attention layers, each with its own history */
+    uint32_t n_kv_head;    /* Hk */
+    uint32_t head_dim;     /* D: 64, 128 or 256 */
+    uint32_t max_q_head;   /* upper bound on Hq (multiple of Hk); sizes the workspace */
+    uint32_t max_rows;     /* upper bound on query rows per kvs_attend; sizes the workspace */
+    uint64_t max_tokens;   /* history capacity per layer, tokens */
+    int32_t k_type;        /* KVS_TYPE_Q8_0 */
+    int32_t v_type;        /* KVS_TYPE_Q4_0 */
+    void *arena;           /* device bytes for page slots: 2 tail slots per layer,
+                              the resident pool and the ring; 256-byte aligned */
+    uint64_t arena_bytes;
+    void *workspace;       /* device bytes for split-K partials; 256-byte aligned */
+    uint64_t workspace_bytes;
+    void *host;            /* host history: n_layers * ceil(max_tokens/P) pages, layer-major;
+                              registered with CUDA by kvs_create if not already pinned */
+    uint64_t host_bytes;
+    uint32_t ring_slots;   /* initial ring size in page slots (>= 1) */
+    uint32_t chunk_pages;  /* ring pages per ready/consumed handshake; 0: max(1, ring_slots/4) */
+    void *attn_stream;     /* cudaStream_t for attention, quantise/append and pool moves */
+    void *copy_stream;     /* cudaStream_t for ring refills, pool loads and D2H publish */
+    uint32_t flags;        /* KVS_FLAG_* */
+} kvs_config;
+
+typedef struct {
+    uint64_t h2d_bytes;        /* ring refill bytes copied host -> device */
+    uint64_t h2d_pages;        /* ring refill pages */
+    uint64_t h2d_launches;     /* ring refill copy launches (one per chunk) */
+    uint64_t pool_load_bytes;  /* host -> resident pool bytes (kvs_set_residency) */
+    uint64_t d2h_bytes;        /* tail pages published device -> host */
+    uint64_t d2h_pages;
+    uint64_t ring_chunks;      /* ring chunks attended (ready/consumed handshakes) */
+    uint64_t ring_recycles;    /* ring slot refills that reused a previously read slot */
+    uint64_t resident_pages_read;  /* page-head items read from pool or tail slots */
+    uint64_t ring_pages_read;      /* page-head items read from ring slots */
+    uint64_t attend_calls;
+    uint64_t kernel_launches;  /* kernels this context launched (all kinds) */
+    uint64_t decode_launches;  /* split-K attention kernel launches */
+    double decode_ms;          /* summed device time of timed attention launches (kvs_set_timing) */
+    uint64_t decode_timed;     /* number of attention launches in decode_ms */
+    uint64_t ring_slots;       /* current ring size */
+    uint64_t pool_slots;       /* current resident pool size */
+    uint64_t pool_used;        /* pool slots holding a resident page */
+} kvs_stats_t;
+
+/* One logged operation of a KVS_FLAG_PLAN_ONLY context (see kvs_trace_read). */
+typedef struct {
+    uint32_t op;      /* KVS_OP_* */
+    uint32_t stream;  /* 0 = attention stream, 1 = copy stream */
+    uint32_t layer;
+    uint32_t event;   /* event id (RECORD / WAIT) */
+    int64_t a;        /* READ/FILL/POOL_LOAD/PUBLISH/WRITE: page; LAUNCH: kernel kind */
+    int64_t b;        /* READ/FILL/POOL_LOAD/PUBLISH/WRITE: device slot; LAUNCH: items */
+    int64_t c;        /* READ: kv head; FILL: ring sequence number */
+    int64_t d;        /* reserved */
+} kvs_trace_op;
+
+enum {
+    KVS_OP_RECORD = 1,    /* record event `event` on `stream` */
+    KVS_OP_WAIT = 2,      /* `stream` waits for the last record of `event` */
+    KVS_OP_FILL = 3,      /* copy stream: host page a -> ring slot b */
+    KVS_OP_READ = 4,      /* attention kernel reads page a (kv head c) from slot b */
+    KVS_OP_POOL_LOAD = 5, /* copy stream: host page a -> pool slot b */
+    KVS_OP_PUBLISH = 6,   /* copy stream: slot b -> host page a (D2H) */
+    KVS_OP_WRITE = 7,     /* attention stream: new rows quantised into page a in slot b */
+    KVS_OP_LAUNCH = 8,    /* a kernel launch of kind a over b items */
+    KVS_OP_MOVE = 9       /* attention stream: device copy of page a into pool slot b */
+};
+
+/* kvs_debug_inject fault kinds (host-side only; no GPU fault is ever made). */
+enum {
+    KVS_FAULT_NONE = 0,
+    KVS_FAULT_FILL_ENQUEUE = 1, /* the nth ring refill enqueue fails */
+    KVS_FAULT_SYNC_STALL = 2    /* kvs_sync sees the GPU as busy until its deadline */
+};
+
+/*
+ * kvs_query_sizes -- sizes a configuration needs.  Fields read: page_tokens,
+ * n_layers, n_kv_head, head_dim, max_q_head, max_rows, max_tokens, ring_slots.
+ *   page_bytes:      bytes of one page (all kv heads): Hk * P * D * 13 / 8
+ *   host_bytes:      minimum host history bytes
+ *   arena_bytes_min: minimum arena (2 tail slots per layer + ring_slots)
+ *   workspace_bytes: minimum workspace (split partials for max_rows rows)
+ * Any output pointer may be NULL.  Page layout (one head section of
+ * P*D*13/8 bytes per kv head, in kv-head order):
+ *   Kq int8 [P][D] | Ks fp16 [P][D/32] | Vq u8 [D/2][P] | Vs fp16 [D/32][P]
+ * Vq byte row b*16+c holds the Q4_0 codes of dims b*32+c (low nibble) and
+ * b*32+c+16 (high nibble) for each token; this dim-major V order lets the
+ * attention kernel load whole tensor-core fragments with one 32-bit load.
+ */
+kvs_status kvs_query_sizes(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
+                           uint64_t *arena_bytes_min, uint64_t *workspace_bytes);
+
+/*
+ * kvs_create -- validate cfg and build a context.  The arena is carved into
+ * page slots: 2 * n_layers tail slots, then ring_slots ring slots, the rest
+ * is the resident pool ("physical KV budget = resident pages across layers +
+ * shared ring slots", V2 README, "KV data movement and attention").
+ * Refusals: geometry outside the supported set or k/v types other than
+ * Q8_0/Q4_0 -> KVS_ERR_UNSUPPORTED; arena or workspace below the minimum ->
+ * KVS_ERR_ARENA (the pages refuse a too-small arena at start-up); host
+ * history too small or not registrable -> KVS_ERR_HOST.  *out is NULL on
+ * failure.
+ */
+kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out);
+
+/* kvs_destroy -- synchronise the context's streams, release events and any
+ * host registration made by kvs_create.  Never frees caller memory. */
+kvs_status kvs_destroy(kvs_ctx *ctx);
+
+/*
+ * kvs_append -- the KV writer: quantise n_tokens new rows of layer `layer`
+ * (k_dev, v_dev: device fp32 [n_tokens][Hk][D]) into the layer's device tail
+ * page(s) at positions T .. T+n_tokens-1 (K -> Q8_0, V -> Q4_0, on
+ * attn_stream).  A page that becomes full is published device -> host on the
+ * copy stream ("D2H publish changed tail when produced", V2 README); it stays
+ * readable on the device until the page after next starts, and then moves to
+ * the resident pool if the layer's residency mask asks for it and the pool
+ * has room, else it is streamed from host like any other nonresident page.
+ * KVS_ERR_CAPACITY if T + n_tokens > max_tokens.
+ */
+kvs_status kvs_append(kvs_ctx *ctx, uint32_t layer, const float *k_dev, const float *v_dev,
+                      uint32_t n_tokens);
+
+/* kvs_truncate -- shorten layer `layer` to n_tokens (<= T), e.g. to drop a
+ * rejected draft suffix.  Only the current tail page (and the page before it)
+ * may be cut into; KVS_ERR_UNSUPPORTED for a cut further back.  KVS_ERR_STATE
+ * while the layer has prefetched ring pages pending. */
+kvs_status kvs_truncate(kvs_ctx *ctx, uint32_t layer, uint64_t n_tokens);
+
+/* kvs_length -- tokens appended to layer `layer`. */
+kvs_status kvs_length(const kvs_ctx *ctx, uint32_t layer, uint64_t *n_tokens);
+
+/*
+ * kvs_set_residency -- choose which pages of `layer` live in the resident
+ * pool: mask[i] != 0 for page i (i < n_pages; pages >= n_pages are not
+ * resident).  Newly resident pages are loaded host -> pool on the copy
+ * stream; attention waits for the load before its next read.  The device
+ * tail pages are always device-readable whatever the mask says.
+ * KVS_ERR_CAPACITY if the pool has too few free slots (nothing changes);
+ * KVS_ERR_STATE while any layer has prefetched ring pages pending.
+ */
+kvs_status kvs_set_residency(kvs_ctx *ctx, uint32_t layer, const uint8_t *mask,
+                             uint64_t n_pages);
+
+/*
+ * kvs_set_ring_slots -- re-split the arena between the resident pool and the
+ * ring: ring = n_slots page slots (>= 1), chunk = chunk_pages (0: default).
+ * KVS_ERR_CAPACITY if the pool would become smaller than the pages resident
+ * now; KVS_ERR_STATE while prefetches are pending.  Waits for earlier ring
+ * work on the device (stream-ordered) before slots change role.
+ */
+kvs_status kvs_set_ring_slots(kvs_ctx *ctx, uint32_t n_slots, uint32_t chunk_pages);
+
+/*
+ * kvs_prefetch -- announce that `layer` is attended next (after any layer
+ * already announced) and enqueue host -> ring copies of its nonresident pages
+ * into ring slots whose previous reader has already been enqueued ("the copy
+ * stream can fill free slots for later layers while the attention stream
+ * computes the current layer", V2 README).  Non-blocking; copies that do not
+ * fit yet are issued by later kvs_attend calls as slots free up.  Layers must
+ * then be attended in announcement order (KVS_ERR_STATE otherwise).
+ */
+kvs_status kvs_prefetch(kvs_ctx *ctx, uint32_t layer);
+
+/*
+ * kvs_attend -- causal attention of n_rows query rows of layer `layer` over
+ * its complete history.  q_dev: device [n_rows][n_q_head][D], fp32 or fp16
+ * (q_dtype); row r sits at position pos0 + r and sees keys 0 .. pos0 + r
+ * (requires pos0 + n_rows <= T: append the rows' own K/V first).  out_dev:
+ * device fp32 [n_rows][n_q_head][D], normalised; lse_dev (nullable): device
+ * fp32 [n_rows][n_q_head], natural-log sum of exp of the scaled scores.
+ * Scores are scale * q . k.
+ * Pages are read from their tail/pool slot, or from ring slots filled from
+ * host on the copy stream; each ring chunk is attended after its ready event
+ * and its slots are released by a consumed event.  The split-K partition is
+ * one partial per (page, kv head) whatever the residency, and the final
+ * log-sum-exp combine runs over pages in logical order, so the result is
+ * bitwise identical for any residency or ring size ("Keep the stock
+ * attention order", V2 README).
+ * Rows: 1 (decode) up to floor(64 / (Hq/Hk)) (span verify, e.g. 2..6 draft
+ * rows with 6 query heads per kv head); larger n_rows -> KVS_ERR_UNSUPPORTED.
+ */
+kvs_status kvs_attend(kvs_ctx *ctx, uint32_t layer, const void *q_dev, int32_t q_dtype,
+                      uint32_t n_rows, uint32_t n_q_head, uint64_t pos0, float scale,
+                      float *out_dev, float *lse_dev);
+
+/* kvs_sync -- wait until both streams have finished the context's work, or
+ * return KVS_ERR_TIMEOUT after timeout_ms (0 = no limit).  Host-side polling
+ * of CUDA events; no device-side wait is involved. */
+kvs_status kvs_sync(kvs_ctx *ctx, uint32_t timeout_ms);
+
+/* kvs_flush -- publish the partial tail page of `layer` (or of every layer if
+ * layer == UINT32_MAX) to the host history. */
+kvs_status kvs_flush(kvs_ctx *ctx, uint32_t layer);
+
+/*
+ * kvs_page_location -- where page `page` of `layer` is device-readable now:
+ * *kind = 0 host only, 1 tail slot, 2 resident pool; *slot = device slot id
+ * (or -1).  kvs_read_slot copies device slot `slot` (page_bytes) to host_dst
+ * synchronously; kvs_read_host_page copies the host history page.  Debug and
+ * test helpers for bit-exact layout and indexing checks.
+ */
+kvs_status kvs_page_location(const kvs_ctx *ctx, uint32_t layer, uint64_t page, int32_t *kind,
+                             int64_t *slot);
+kvs_status kvs_read_slot(kvs_ctx *ctx, int64_t slot, void *host_dst);
+kvs_status kvs_read_host_page(kvs_ctx *ctx, uint32_t layer, uint64_t page, void *host_dst);
+
+/* kvs_ring_info -- first device slot id of the ring and its size. */
+kvs_status kvs_ring_info(const kvs_ctx *ctx, int64_t *first_slot, uint32_t *n_slots);
+
+/* kvs_stats -- counters since create (or the last reset when reset != 0). */
+kvs_status kvs_stats(kvs_ctx *ctx, kvs_stats_t *out, int reset);
+
+/* kvs_set_timing -- when enabled, each attention-kernel launch is bracketed by
+ * CUDA events on attn_stream and its device time is added to
+ * kvs_stats_t.decode_ms when the events complete. */
+kvs_status kvs_set_timing(kvs_ctx *ctx, int enable);
+
+/* kvs_last_error -- message of the last failed call on ctx ("" if none);
+ * with ctx == NULL, the last kvs_create failure of this thread. */
+const char *kvs_last_error(const kvs_ctx *ctx);
+
+/* kvs_debug_inject -- arm a host-side fault (KVS_FAULT_*) that fires on the
+ * nth (1-based) matching event; nth = 0 disarms. */
+kvs_status kvs_debug_inject(kvs_ctx *ctx, uint32_t fault, uint64_t nth);
+
+/* kvs_trace_read -- copy up to max logged operations of a PLAN_ONLY context
+ * starting at index `first` into ops; *n_out = number copied, *n_total = log
+ * length.  KVS_ERR_STATE for a context that is not PLAN_ONLY. */
+kvs_status kvs_trace_read(const kvs_ctx *ctx, uint64_t first, uint64_t max, kvs_trace_op *ops,
+                          uint64_t *n_out, uint64_t *n_total);
+
+/* kvs_version -- KVS_ABI_VERSION of the loaded library. */
+int32_t kvs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVS_H_ */

@@ -1,0 +1,319 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bit-exact: page bytes written by the KV writer (host history, tail slots,
+resident pool, ring slots) against the oracle's page encoder.
+Within tolerance (max over (row, head) of max_d |gpu - oracle| / max_d |oracle|
+<= 1e-3, lse absolute error <= 1e-4): attention outputs for decode (1 row) and
+span verify (2..6 causal rows) over every page size and head dim served.
+Bitwise: streamed output equals all-resident output for any residency, ring
+size and chunk size (the split-K partition never depends on them).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from host_streamed_paged_gb300 import kvs
+from kvs_testutil import (SEED, append_rows, attend, check_parity, history, make_stream,
+                          oracle_ref, queries, rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+def _fill(st, L, T, Hk, D, pieces=None, seed=SEED):
+    hist = []
+    for l in range(L):
+        k, v = history(seed, l, T, Hk, D)
+        append_rows(st, l, k, v, pieces)
+        hist.append((k, v))
+    return hist
+
+
+# ------------------------------------------------------------ bit-exact layout
+
+@pytest.mark.parametrize("P,Hk,D,T", [(64, 2, 64, 64 * 3 + 29), (256, 4, 256, 256 * 3 + 100),
+                                      (128, 1, 128, 128 * 4), (32, 3, 128, 32 * 7 + 1)])
+def test_append_pages_bit_exact(P, Hk, D, T):
+    st = make_stream(P, 1, Hk, D, Hk, 1, T + P, ring=2, chunk=1)
+    k, v = history(SEED, 0, T, Hk, D)
+    pieces = [1, 2, 37, P // 2 + 3, 3 * P // 2]  # irregular sizes crossing page boundaries
+    assert sum(pieces) < T
+    pieces.append(T - sum(pieces))
+    append_rows(st, 0, k, v, pieces)
+    st.flush()
+    st.sync()
+    ref = oracle.QuantKV(k, v)
+    npages = math.ceil(T / P)
+    for p in range(npages):
+        want = ref.encode_page(P, p)
+        assert np.array_equal(st.read_host_page(0, p), want), f"host page {p}"
+        kind, slot = st.page_location(0, p)
+        if kind:
+            assert np.array_equal(st.read_slot(slot), want), f"device page {p} (kind {kind})"
+    # resident pool copies
+    st.set_residency(0, np.ones(npages, np.uint8))
+    st.sync()
+    for p in range(npages):
+        kind, slot = st.page_location(0, p)
+        assert kind in (1, 2)
+        assert np.array_equal(st.read_slot(slot), ref.encode_page(P, p))
+
+
+def test_ring_slots_bit_exact():
+    P, Hk, D, T, ring = 64, 2, 128, 64 * 12 + 5, 5
+    st = make_stream(P, 1, Hk, D, Hk, 1, T + P, ring=ring, chunk=1)
+    k, v = history(SEED, 0, T, Hk, D)
+    append_rows(st, 0, k, v)
+    mask = np.zeros(12, np.uint8)
+    mask[[0, 3, 4, 9]] = 1
+    st.set_residency(0, mask)
+    st.prefetch(0)
+    st.sync()
+    first, n = st.ring_info()
+    streamed = [p for p in range(13) if st.page_location(0, p)[0] == 0]
+    ref = oracle.QuantKV(k, v)
+    for i, p in enumerate(streamed[:ring]):
+        assert np.array_equal(st.read_slot(first + i), ref.encode_page(P, p)), f"ring slot {i} page {p}"
+    # consume the plan
+    q = queries(SEED, 0, 1, Hk, D)
+    attend(st, 0, q, T - 1, 0.1)
+
+
+# ------------------------------------------------------------ attention parity
+
+def test_decode_small_config_all_resident():
+    """1 row at context 4096, 8 q / 2 kv heads, D 128, page 256, all 16 pages resident."""
+    P, L, Hk, Hq, D, T = 256, 1, 2, 8, 128, 4096
+    st = make_stream(P, L, Hk, D, Hq, 1, T, ring=2)
+    (k, v), = _fill(st, L, T, Hk, D)
+    st.set_residency(0, np.ones(16, np.uint8))
+    q = queries(SEED, 0, 1, Hq, D)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = attend(st, 0, q, T - 1, scale)
+    ro, rl = oracle_ref(k, v, q, T - 1, scale)
+    check_parity(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("P,D,Hk,G,R,T", [
+    (256, 256, 4, 6, 1, 256 * 5 + 77),
+    (256, 256, 4, 6, 2, 256 * 4 + 1),
+    (256, 256, 4, 6, 4, 256 * 6),
+    (256, 256, 4, 6, 6, 256 * 3 + 250),
+    (256, 128, 2, 4, 3, 256 * 4 + 9),
+    (128, 128, 2, 8, 8, 128 * 9 + 3),
+    (64, 64, 3, 2, 5, 64 * 11 + 60),
+    (32, 256, 1, 6, 6, 32 * 20 + 7),
+    (64, 256, 2, 1, 1, 64 * 3 + 2),
+    (256, 64, 1, 16, 4, 256 * 2 + 255),
+])
+def test_attention_parity_geometries(P, D, Hk, G, R, T):
+    Hq = G * Hk
+    st = make_stream(P, 1, Hk, D, Hq, R, T, ring=3, chunk=1)
+    (k, v), = _fill(st, 1, T, Hk, D)
+    npages = math.ceil(T / P)
+    mask = (synth.u64(SEED + 1, synth.tag("mask", P, D), npages) % 2).astype(np.uint8)
+    st.set_residency(0, mask)
+    q = queries(SEED, 0, R, Hq, D)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = attend(st, 0, q, T - R, scale)
+    ro, rl = oracle_ref(k, v, q, T - R, scale)
+    check_parity(out, lse, ro, rl)
+    s = st.stats()
+    assert s["h2d_pages"] > 0 or mask.sum() + 2 >= npages
+
+
+def test_rows_inside_history_and_across_page_boundary():
+    """Rows whose positions straddle a page boundary, not at the end of the history."""
+    P, D, Hk, G, R = 64, 128, 2, 6, 5
+    T = 64 * 6
+    st = make_stream(P, 1, Hk, D, G * Hk, R, T, ring=2, chunk=1)
+    (k, v), = _fill(st, 1, T, Hk, D)
+    q = queries(SEED, 3, R, G * Hk, D)
+    for pos0 in (62, 127, 0, 200):
+        out, lse = attend(st, 0, q, pos0, 0.07)
+        ro, rl = oracle_ref(k, v, q, pos0, 0.07)
+        check_parity(out, lse, ro, rl)
+
+
+def test_single_token_history():
+    P, D, Hk, G = 256, 256, 4, 6
+    st = make_stream(P, 1, Hk, D, G * Hk, 1, 512, ring=1)
+    (k, v), = _fill(st, 1, 1, Hk, D)
+    q = queries(SEED, 0, 1, G * Hk, D)
+    out, lse = attend(st, 0, q, 0, 1 / 16)
+    ro, rl = oracle_ref(k, v, q, 0, 1 / 16)
+    check_parity(out, lse, ro, rl)
+
+
+def test_constant_values_weights_sum_to_one():
+    P, D, Hk, G, R, T = 128, 256, 2, 6, 3, 128 * 5 + 17
+    st = make_stream(P, 1, Hk, D, G * Hk, R, T, ring=2, chunk=1)
+    k = synth.normal(SEED, synth.tag("K1"), (T, Hk, D))
+    v = np.ones((T, Hk, D), np.float32)
+    append_rows(st, 0, k, v)
+    q = queries(SEED, 0, R, G * Hk, D) * np.float32(4.0)
+    out, _ = attend(st, 0, q, T - R, 0.0625)
+    # o and l are summed along different fp32 paths (tensor-core MMA for o, warp
+    # shuffles for l) from f16 hi/lo parts (2^-22 relative per product); over
+    # ~700 keys that leaves a few 1e-6, far below any misweighted key (>= 1e-3)
+    assert np.abs(out - 1.0).max() <= 1e-5
+
+
+def test_f16_queries():
+    P, D, Hk, G, R, T = 256, 256, 4, 6, 2, 256 * 3 + 5
+    import torch
+    st = make_stream(P, 1, Hk, D, G * Hk, R, T, ring=2)
+    (k, v), = _fill(st, 1, T, Hk, D)
+    q = queries(SEED, 0, R, G * Hk, D).astype(np.float16).astype(np.float32)  # the f16 values exactly
+    out, lse = attend(st, 0, q, T - R, 1 / 16, dtype=torch.float16)
+    ro, rl = oracle_ref(k, v, q, T - R, 1 / 16)
+    check_parity(out, lse, ro, rl)
+
+
+# ------------------------------------------------------------ invariants
+
+def test_streamed_equals_resident_bitwise():
+    P, L, Hk, G, D, R, T = 64, 2, 2, 6, 256, 3, 64 * 10 + 33
+    Hq = G * Hk
+    st = make_stream(P, L, Hk, D, Hq, R, T, ring=8, chunk=2)
+    hist = _fill(st, L, T, Hk, D)
+    npages = math.ceil(T / P)
+    qs = [queries(SEED, l, R, Hq, D) for l in range(L)]
+    for l in range(L):
+        st.set_residency(l, np.ones(npages, np.uint8))
+    base = [attend(st, l, qs[l], T - R, 0.0625) for l in range(L)]
+    for l in range(L):
+        ro, rl = oracle_ref(*hist[l], qs[l], T - R, 0.0625)
+        check_parity(*base[l], ro, rl)
+    rng = np.random.default_rng(5)
+    for ring, chunk in [(1, 1), (2, 1), (3, 2), (8, 4), (5, 5)]:
+        for l in range(L):
+            st.set_residency(l, (rng.random(npages) < 0.4).astype(np.uint8))
+        st.set_ring_slots(ring, chunk)
+        st.stats(reset=True)
+        st.prefetch(0)
+        for l in range(L):
+            if l + 1 < L:
+                st.prefetch(l + 1)
+            out, lse = attend(st, l, qs[l], T - R, 0.0625)
+            assert np.array_equal(out, base[l][0]), f"ring {ring} chunk {chunk} layer {l}"
+            assert np.array_equal(lse, base[l][1])
+        s = st.stats()
+        assert s["h2d_pages"] > 0 and (ring == 8 or s["ring_recycles"] > 0)
+
+
+def test_page_size_changes_result_only_within_tolerance():
+    D, Hk, G, R, T = 128, 2, 4, 2, 1500
+    k, v = history(SEED, 0, T, Hk, D)
+    q = queries(SEED, 0, R, G * Hk, D)
+    outs = []
+    for P in (64, 128, 256):
+        st = make_stream(P, 1, Hk, D, G * Hk, R, T, ring=2, chunk=1)
+        append_rows(st, 0, k, v)
+        outs.append(attend(st, 0, q, T - R, 0.09))
+        st.close()
+    ro, rl = oracle_ref(k, v, q, T - R, 0.09)
+    for o, l in outs:
+        check_parity(o, l, ro, rl)
+    assert rel_err(outs[0][0], outs[2][0].astype(np.float64)) <= 1e-5
+
+
+def test_decode_loop_with_appends_and_page_starts():
+    """Decode steps that append a row per layer, cross page boundaries and prefetch ahead."""
+    P, L, Hk, G, D = 32, 3, 2, 6, 128
+    T0, steps = 32 * 4 + 30, 6
+    Hq = G * Hk
+    st = make_stream(P, L, Hk, D, Hq, 1, T0 + steps, ring=2, chunk=1, pool_pages=8)
+    full = [history(SEED, l, T0 + steps, Hk, D) for l in range(L)]
+    for l in range(L):
+        append_rows(st, l, full[l][0][:T0], full[l][1][:T0])
+        st.set_residency(l, np.array([1, 0, 1, 0, 0], np.uint8))
+    for s in range(steps):
+        T = T0 + s + 1
+        st.prefetch(0)
+        for l in range(L):
+            append_rows(st, l, full[l][0][T - 1:T], full[l][1][T - 1:T])
+            if l + 1 < L:
+                st.prefetch(l + 1)
+            q = queries(SEED, 100 * s + l, 1, Hq, D)
+            out, lse = attend(st, l, q, T - 1, 0.088)
+            ro, rl = oracle_ref(full[l][0][:T], full[l][1][:T], q, T - 1, 0.088)
+            check_parity(out, lse, ro, rl)
+
+
+def test_truncate_then_reappend():
+    P, D, Hk, G = 64, 128, 2, 6
+    T = 64 * 3 + 10
+    st = make_stream(P, 1, Hk, D, G * Hk, 1, T + 64, ring=2)
+    k, v = history(SEED, 0, T, Hk, D)
+    append_rows(st, 0, k, v)
+    st.truncate(0, T - 20)
+    k2, v2 = history(SEED + 7, 0, 20, Hk, D)
+    append_rows(st, 0, k2, v2)
+    kk = np.concatenate([k[:T - 20], k2])
+    vv = np.concatenate([v[:T - 20], v2])
+    q = queries(SEED, 0, 1, G * Hk, D)
+    out, lse = attend(st, 0, q, T - 1, 0.1)
+    ro, rl = oracle_ref(kk, vv, q, T - 1, 0.1)
+    check_parity(out, lse, ro, rl)
+    st.flush()
+    st.sync()
+    ref = oracle.QuantKV(kk, vv)
+    for p in range(4):
+        assert np.array_equal(st.read_host_page(0, p), ref.encode_page(P, p))
+
+
+def test_sync_timeout_injection_on_gpu_context():
+    st = make_stream(64, 1, 1, 64, 1, 1, 640, ring=1)
+    st.inject(kvs.KVS_FAULT_SYNC_STALL, 1)
+    with pytest.raises(kvs.KVSError) as e:
+        st.sync(30)
+    assert e.value.status == kvs.KVS_ERR_TIMEOUT
+    st.inject(kvs.KVS_FAULT_NONE, 0)
+    st.sync(1000)
+
+
+# ------------------------------------------------------------ full-size samples
+
+def test_decode_stack_sampled_layers_full_size():
+    """Context 32768, 24 q / 4 kv heads, D 256, page 256, half the pages resident
+    (seeded), 8-slot ring: the launch configuration of the decode benchmark,
+    checked on three layers against the oracle."""
+    P, Hk, Hq, D, T, L = 256, 4, 24, 256, 32768, 3
+    st = make_stream(P, L, Hk, D, Hq, 1, T, ring=8, chunk=2, pool_pages=L * 64)
+    hist = _fill(st, L, T, Hk, D)
+    for l in range(L):
+        # 62 seeded pages + the two tail pages = half of the 128 pages resident
+        res = synth.choose(SEED + 1, synth.tag("resident", l), 126, 62)
+        mask = np.zeros(128, np.uint8)
+        mask[res] = 1
+        st.set_residency(l, mask)
+    st.prefetch(0)
+    for l in range(L):
+        if l + 1 < L:
+            st.prefetch(l + 1)
+        q = queries(SEED, l, 1, Hq, D)
+        out, lse = attend(st, l, q, T - 1, 1 / 16)
+        ro, rl = oracle_ref(*hist[l], q, T - 1, 1 / 16)
+        check_parity(out, lse, ro, rl)
+    s = st.stats()
+    assert s["h2d_pages"] == L * 64 and s["ring_recycles"] > 0
+
+
+def test_span_verify_full_size_one_layer():
+    """6 causal rows at 163840..163845, 24 q / 4 kv heads, D 256, 400 resident
+    pages (prefix), the rest through an 8-slot ring."""
+    P, Hk, Hq, D, R = 256, 4, 24, 256, 6
+    T = 163840 + R
+    st = make_stream(P, 1, Hk, D, Hq, R, T, ring=8, chunk=2, pool_pages=400)
+    (k, v), = _fill(st, 1, T, Hk, D)
+    mask = np.zeros(641, np.uint8)
+    mask[:400] = 1
+    st.set_residency(0, mask)
+    q = queries(SEED, 0, R, Hq, D)
+    out, lse = attend(st, 0, q, T - R, 1 / 16)
+    ro, rl = oracle_ref(k, v, q, T - R, 1 / 16)
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] == 641 - 400 - 2  # the last two pages sit in tail slots
