@@ -59,6 +59,11 @@ struct Chunk {
     bool filled = false;
 };
 
+struct Timer {
+    cudaEvent_t start, stop;
+    uint64_t bytes;
+};
+
 struct LayerState {
     uint64_t T = 0;                  // tokens appended
     std::vector<uint8_t> mask;       // requested residency per page
@@ -100,10 +105,19 @@ struct kvs_ctx {
     std::vector<cudaEvent_t> events;
     int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0;
 
-    // timing of attention kernels
-    bool timing = false;
+    // timing of attention kernels (mask of KVS_TIME_*)
+    uint32_t timing = 0;
     std::vector<cudaEvent_t> timer_free;
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timer_pending;
+    std::vector<Timer> timer_pending;
+
+    // step graph capture / replay
+    bool capturing = false;
+    std::vector<uint8_t> ev_in_capture;  // event recorded since capture began
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t graph_exec = nullptr;
+    std::vector<cudaEvent_t> eager_events;  // the context's events while a capture is open
+    std::vector<cudaEvent_t> graph_events;  // events owned by the captured graph
+    uint64_t graph_kernel_base = 0, graph_kernels = 0;
 
     // fault injection
     uint32_t fault = KVS_FAULT_NONE;
@@ -155,6 +169,7 @@ void log_op(kvs_ctx *c, uint32_t op, int stream, uint32_t layer, uint32_t ev, in
 // ---- stream primitives (logged in plan-only mode, executed otherwise)
 
 kvs_status op_record(kvs_ctx *c, int stream, int ev) {
+    if (c->capturing) c->ev_in_capture[ev] = 1;
     if (c->plan_only) {
         log_op(c, KVS_OP_RECORD, stream, 0, (uint32_t)ev, 0, 0);
         return KVS_OK;
@@ -164,6 +179,9 @@ kvs_status op_record(kvs_ctx *c, int stream, int ev) {
 }
 
 kvs_status op_wait(kvs_ctx *c, int stream, int ev) {
+    // inside a step graph, an event last recorded before capture began was
+    // already covered by the join kvs_graph_launch makes before each replay
+    if (c->capturing && !c->ev_in_capture[ev]) return KVS_OK;
     if (c->plan_only) {
         log_op(c, KVS_OP_WAIT, stream, 0, (uint32_t)ev, 0, 0);
         return KVS_OK;
@@ -208,9 +226,7 @@ kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> 
     return KVS_OK;
 }
 
-kvs_status timed_begin(kvs_ctx *c, cudaEvent_t *ev) {
-    *ev = nullptr;
-    if (!c->timing || c->plan_only) return KVS_OK;
+kvs_status take_timer_event(kvs_ctx *c, cudaEvent_t *ev) {
     if (c->timer_free.empty()) {
         cudaEvent_t e;
         cudaError_t r = cudaEventCreate(&e);
@@ -219,39 +235,44 @@ kvs_status timed_begin(kvs_ctx *c, cudaEvent_t *ev) {
     }
     *ev = c->timer_free.back();
     c->timer_free.pop_back();
+    return KVS_OK;
+}
+
+kvs_status timed_begin(kvs_ctx *c, uint32_t kind, cudaEvent_t *ev) {
+    *ev = nullptr;
+    // graph-recorded events carry no timing: no timers inside a step capture
+    if (!(c->timing & kind) || c->plan_only || c->capturing) return KVS_OK;
+    kvs_status s = take_timer_event(c, ev);
+    if (s != KVS_OK) return s;
     cudaError_t r = cudaEventRecord(*ev, c->attn);
     return r == cudaSuccess ? KVS_OK : cuda_fail(c, r, "cudaEventRecord");
 }
 
-kvs_status timed_end(kvs_ctx *c, cudaEvent_t start) {
+kvs_status timed_end(kvs_ctx *c, cudaEvent_t start, uint64_t bytes) {
     if (!start) return KVS_OK;
-    if (c->timer_free.empty()) {
-        cudaEvent_t e;
-        cudaError_t r = cudaEventCreate(&e);
-        if (r != cudaSuccess) return cuda_fail(c, r, "cudaEventCreate");
-        c->timer_free.push_back(e);
-    }
-    cudaEvent_t stop = c->timer_free.back();
-    c->timer_free.pop_back();
+    cudaEvent_t stop = nullptr;
+    kvs_status s = take_timer_event(c, &stop);
+    if (s != KVS_OK) return s;
     cudaError_t r = cudaEventRecord(stop, c->attn);
     if (r != cudaSuccess) return cuda_fail(c, r, "cudaEventRecord");
-    c->timer_pending.push_back({start, stop});
+    c->timer_pending.push_back({start, stop, bytes});
     return KVS_OK;
 }
 
 void harvest_timers(kvs_ctx *c) {
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> keep;
-    for (auto &pr : c->timer_pending) {
-        if (cudaEventQuery(pr.second) == cudaSuccess) {
+    std::vector<Timer> keep;
+    for (auto &t : c->timer_pending) {
+        if (cudaEventQuery(t.stop) == cudaSuccess) {
             float ms = 0.f;
-            if (cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess) {
+            if (cudaEventElapsedTime(&ms, t.start, t.stop) == cudaSuccess) {
                 c->st.decode_ms += ms;
                 c->st.decode_timed += 1;
+                c->st.decode_bytes += t.bytes;
             }
-            c->timer_free.push_back(pr.first);
-            c->timer_free.push_back(pr.second);
+            c->timer_free.push_back(t.start);
+            c->timer_free.push_back(t.stop);
         } else {
-            keep.push_back(pr);
+            keep.push_back(t);
         }
     }
     c->timer_pending.swap(keep);
@@ -279,6 +300,17 @@ kvs_status create_events(kvs_ctx *c) {
         if (e != cudaSuccess) return cuda_fail(c, e, "cudaEventCreate");
     }
     return KVS_OK;
+}
+
+void release_graph(kvs_ctx *c) {
+    if (c->plan_only) return;
+    if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+    if (c->graph) cudaGraphDestroy(c->graph);
+    for (cudaEvent_t e : c->graph_events)
+        if (e) cudaEventDestroy(e);
+    c->graph_exec = nullptr;
+    c->graph = nullptr;
+    c->graph_events.clear();
 }
 
 // ---- placement
@@ -420,7 +452,7 @@ kvs_status pump(kvs_ctx *c) {
 // ---- attention launches
 
 kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
-                        const std::vector<int64_t> &slots, kvs::DecodeParams &dp) {
+                        const std::vector<int64_t> &slots, kvs::DecodeParams &dp, uint32_t kind) {
     for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxItems) {
         const int n = (int)std::min<size_t>(kvs::kMaxItems, pages.size() - i0);
         c->st.decode_launches++;
@@ -438,11 +470,11 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
             dp.slot[j] = (uint32_t)slots[i0 + j];
         }
         cudaEvent_t t0;
-        kvs_status s = timed_begin(c, &t0);
+        kvs_status s = timed_begin(c, kind, &t0);
         if (s != KVS_OK) return s;
         cudaError_t e = kvs::launch_decode(dp, c->attn);
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel launch");
-        s = timed_end(c, t0);
+        s = timed_end(c, t0, (uint64_t)n * (uint64_t)c->geom.page_bytes);
         if (s != KVS_OK) return s;
     }
     return KVS_OK;
@@ -620,11 +652,12 @@ kvs_status kvs_destroy(kvs_ctx *c) {
     if (!c->plan_only) {
         cudaStreamSynchronize(c->attn);
         cudaStreamSynchronize(c->copy);
-        for (auto &pr : c->timer_pending) {
-            cudaEventDestroy(pr.first);
-            cudaEventDestroy(pr.second);
+        for (auto &t : c->timer_pending) {
+            cudaEventDestroy(t.start);
+            cudaEventDestroy(t.stop);
         }
         for (cudaEvent_t e : c->timer_free) cudaEventDestroy(e);
+        release_graph(c);
         if (c->host_registered) cudaHostUnregister(c->cfg.host);
     }
     destroy_events(c);
@@ -782,6 +815,7 @@ kvs_status kvs_truncate(kvs_ctx *c, uint32_t layer, uint64_t n_tokens) {
 kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, uint64_t n_pages) {
     if (!c) return KVS_ERR_INVALID;
     c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
     if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
     if (n_pages > (uint64_t)c->max_pages) return fail(c, KVS_ERR_INVALID, "mask longer than max pages");
     if (n_pages && !mask) return fail(c, KVS_ERR_INVALID, "null mask");
@@ -789,6 +823,11 @@ kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, ui
         return fail(c, KVS_ERR_STATE, "residency change while prefetches are pending");
     LayerState &L = c->layers[layer];
     const int64_t complete = (int64_t)(L.T / c->geom.P);  // pages 0..complete-1 are full
+    if (c->graph_exec) {  // its baked slot schedule no longer holds
+        if (!c->plan_only) cudaStreamSynchronize(c->attn);
+        release_graph(c);
+        c->graph_kernels = 0;
+    }
     std::vector<uint8_t> want(c->max_pages, 0);
     for (uint64_t i = 0; i < n_pages; ++i) want[i] = mask[i] ? 1 : 0;
     // count the change
@@ -834,6 +873,7 @@ kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, ui
 kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages) {
     if (!c) return KVS_ERR_INVALID;
     c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
     if (n_slots < 1) return fail(c, KVS_ERR_INVALID, "ring needs at least one slot");
     if (!c->queue.empty() || !c->announced.empty())
         return fail(c, KVS_ERR_STATE, "ring change while prefetches are pending");
@@ -868,11 +908,13 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     }
     s = join_attn_into_copy(c);
     if (s != KVS_OK) return s;
-    // new event set for the new ring size
+    // new event set for the new ring size; a captured step graph is dropped
     if (!c->plan_only) {
         cudaStreamSynchronize(c->attn);
         cudaStreamSynchronize(c->copy);
     }
+    release_graph(c);
+    c->graph_kernels = 0;
     destroy_events(c);
     c->ring_n = n_slots;
     c->chunk_pages = chunk_pages ? std::min(chunk_pages, n_slots) : std::max(1u, n_slots / 4);
@@ -967,7 +1009,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
     if (s != KVS_OK) return s;
     // resident and tail pages need no fence
     if (!res_pages.empty()) {
-        s = launch_items(c, layer, res_pages, res_slots, dp);
+        s = launch_items(c, layer, res_pages, res_slots, dp, KVS_TIME_RESIDENT);
         if (s != KVS_OK) return s;
         c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
     }
@@ -988,7 +1030,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             sl.push_back(c->ring_slot_id(ch.seq0 + i));
         }
         if (!pg.empty()) {
-            s = launch_items(c, layer, pg, sl, dp);
+            s = launch_items(c, layer, pg, sl, dp, KVS_TIME_RING);
             if (s != KVS_OK) return s;
             c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
         }
@@ -1025,6 +1067,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
 kvs_status kvs_sync(kvs_ctx *c, uint32_t timeout_ms) {
     if (!c) return KVS_ERR_INVALID;
     c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "kvs_sync inside a step capture");
     const auto t0 = std::chrono::steady_clock::now();
     auto expired = [&]() {
         return timeout_ms && std::chrono::steady_clock::now() - t0 >= std::chrono::milliseconds(timeout_ms);
@@ -1098,6 +1141,7 @@ kvs_status kvs_page_location(const kvs_ctx *c, uint32_t layer, uint64_t page, in
 
 kvs_status kvs_read_slot(kvs_ctx *c, int64_t slot, void *host_dst) {
     if (!c || !host_dst) return KVS_ERR_INVALID;
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
     if (slot < 0 || slot >= c->n_slots) return fail(c, KVS_ERR_INVALID, "slot out of range");
     if (c->plan_only) return fail(c, KVS_ERR_STATE, "no device memory in plan-only mode");
     kvs_status s = kvs_sync(c, 0);
@@ -1108,6 +1152,7 @@ kvs_status kvs_read_slot(kvs_ctx *c, int64_t slot, void *host_dst) {
 
 kvs_status kvs_read_host_page(kvs_ctx *c, uint32_t layer, uint64_t page, void *host_dst) {
     if (!c || !host_dst || layer >= c->cfg.n_layers || page >= (uint64_t)c->max_pages) return KVS_ERR_INVALID;
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
     if (!c->host) return fail(c, KVS_ERR_STATE, "no host history");
     kvs_status s = kvs_sync(c, 0);
     if (s != KVS_OK) return s;
@@ -1139,11 +1184,117 @@ kvs_status kvs_stats(kvs_ctx *c, kvs_stats_t *out, int reset) {
     return KVS_OK;
 }
 
-kvs_status kvs_set_timing(kvs_ctx *c, int enable) {
+kvs_status kvs_set_timing(kvs_ctx *c, int mask) {
     if (!c) return KVS_ERR_INVALID;
-    c->timing = enable != 0;
+    c->timing = (uint32_t)mask & (KVS_TIME_RESIDENT | KVS_TIME_RING);
     return KVS_OK;
 }
+
+kvs_status kvs_graph_begin(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "a step capture is already open");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "step capture must start with no prefetch pending");
+    if (!c->plan_only) {
+        // the graph records its own events: an event recorded inside a capture
+        // cannot be waited on by work outside it
+        std::vector<cudaEvent_t> fresh(c->events.size(), nullptr);
+        for (auto &e : fresh) {
+            cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+            if (r != cudaSuccess) {
+                for (cudaEvent_t x : fresh)
+                    if (x) cudaEventDestroy(x);
+                return cuda_fail(c, r, "cudaEventCreate");
+            }
+        }
+        cudaError_t e = cudaStreamBeginCapture(c->attn, cudaStreamCaptureModeRelaxed);
+        if (e != cudaSuccess) {
+            for (cudaEvent_t x : fresh) cudaEventDestroy(x);
+            return cuda_fail(c, e, "cudaStreamBeginCapture");
+        }
+        c->eager_events.swap(c->events);
+        c->events.swap(fresh);
+    }
+    c->capturing = true;
+    c->ev_in_capture.assign(c->events.size(), 0);
+    // inside the graph the ring starts empty: its earlier readers are ordered
+    // before every replay by the join in kvs_graph_launch
+    std::fill(c->slot_last_chunk.begin(), c->slot_last_chunk.end(), -1);
+    c->graph_kernel_base = c->st.kernel_launches;
+    return join_attn_into_copy(c);  // the copy stream joins the capture
+}
+
+kvs_status kvs_graph_end(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (!c->capturing) return fail(c, KVS_ERR_STATE, "no step capture is open");
+    const bool pending = !c->queue.empty() || !c->announced.empty();
+    kvs_status s = join_copy_into_attn(c);  // the copy stream rejoins before capture ends
+    c->capturing = false;
+    cudaGraph_t g = nullptr;
+    std::vector<cudaEvent_t> cap_events;
+    if (!c->plan_only) {
+        cudaError_t e = cudaStreamEndCapture(c->attn, &g);
+        if (s == KVS_OK && e != cudaSuccess) s = cuda_fail(c, e, "cudaStreamEndCapture");
+        cap_events.swap(c->events);
+        c->events.swap(c->eager_events);
+    }
+    if (s == KVS_OK && pending) s = fail(c, KVS_ERR_STATE, "step capture ended with a prefetch pending");
+    auto drop = [&]() {
+        if (g) cudaGraphDestroy(g);
+        for (cudaEvent_t x : cap_events)
+            if (x) cudaEventDestroy(x);
+    };
+    if (s != KVS_OK) {
+        drop();
+        return s;
+    }
+    if (!c->plan_only) {
+        cudaGraphExec_t ex = nullptr;
+        cudaError_t e = cudaGraphInstantiate(&ex, g, 0);
+        if (e != cudaSuccess) {
+            drop();
+            return cuda_fail(c, e, "cudaGraphInstantiate");
+        }
+        release_graph(c);
+        c->graph = g;
+        c->graph_exec = ex;
+        c->graph_events.swap(cap_events);
+    }
+    c->graph_kernels = c->st.kernel_launches - c->graph_kernel_base;
+    c->st.graph_kernels = c->graph_kernels;
+    std::fill(c->slot_last_chunk.begin(), c->slot_last_chunk.end(), -1);
+    return KVS_OK;
+}
+
+kvs_status kvs_graph_launch(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "cannot replay while capturing");
+    if (!c->graph_exec && !c->plan_only) return fail(c, KVS_ERR_STATE, "no step graph captured");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "replay with a prefetch pending");
+    kvs_status s = join_copy_into_attn(c);
+    if (s != KVS_OK) return s;
+    if (!c->plan_only) {
+        cudaError_t e = cudaGraphLaunch(c->graph_exec, c->attn);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaGraphLaunch");
+    }
+    c->st.graph_launches++;
+    c->st.kernel_launches += c->graph_kernels;
+    return join_attn_into_copy(c);  // later copies wait for the replay's ring readers
+}
+
+kvs_status kvs_graph_destroy(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "a step capture is open");
+    if (!c->plan_only) cudaStreamSynchronize(c->attn);
+    release_graph(c);
+    c->graph_kernels = 0;
+    return KVS_OK;
+}
+
 
 kvs_status kvs_debug_inject(kvs_ctx *c, uint32_t fault, uint64_t nth) {
     if (!c) return KVS_ERR_INVALID;

@@ -69,7 +69,8 @@ class kvs_stats_t(ctypes.Structure):
         "h2d_bytes", "h2d_pages", "h2d_launches", "pool_load_bytes", "d2h_bytes", "d2h_pages",
         "ring_chunks", "ring_recycles", "resident_pages_read", "ring_pages_read", "attend_calls",
         "kernel_launches", "decode_launches")] + [("decode_ms", ctypes.c_double)] + [
-        (n, ctypes.c_uint64) for n in ("decode_timed", "ring_slots", "pool_slots", "pool_used")]
+        (n, ctypes.c_uint64) for n in ("decode_timed", "decode_bytes", "ring_slots", "pool_slots",
+                                       "pool_used", "graph_launches", "graph_kernels")]
 
 
 class kvs_trace_op(ctypes.Structure):
@@ -104,7 +105,13 @@ SIGNATURES = {
     "kvs_debug_inject": ([_P, _U32, _U64], _I32),
     "kvs_trace_read": ([_P, _U64, _U64, _P, _P, _P], _I32),
     "kvs_version": ([], _I32),
+    "kvs_graph_begin": ([_P], _I32),
+    "kvs_graph_end": ([_P], _I32),
+    "kvs_graph_launch": ([_P], _I32),
+    "kvs_graph_destroy": ([_P], _I32),
 }
+KVS_TIME_RESIDENT = 1
+KVS_TIME_RING = 2
 
 _lib = None
 
@@ -239,8 +246,26 @@ def kvs_stats(ctx, reset=False) -> dict:
     return {name: getattr(st, name) for name, _ in kvs_stats_t._fields_}
 
 
-def kvs_set_timing(ctx, enable=True) -> int:
-    return _check(ctx, load().kvs_set_timing(ctx, 1 if enable else 0))
+def kvs_set_timing(ctx, mask=KVS_TIME_RESIDENT | KVS_TIME_RING) -> int:
+    return _check(ctx, load().kvs_set_timing(ctx, int(mask)))
+
+
+def kvs_graph_begin(ctx) -> int:
+    return _check(ctx, load().kvs_graph_begin(ctx))
+
+
+def kvs_graph_end(ctx) -> int:
+    return _check(ctx, load().kvs_graph_end(ctx))
+
+
+def kvs_graph_launch(ctx) -> int:
+    return _check(ctx, load().kvs_graph_launch(ctx))
+
+
+def kvs_graph_destroy(ctx) -> int:
+    return _check(ctx, load().kvs_graph_destroy(ctx))
+
+
 
 
 def kvs_last_error(ctx) -> str:
@@ -385,8 +410,20 @@ class KVStream:
     def stats(self, reset=False):
         return kvs_stats(self.ctx, reset)
 
-    def set_timing(self, enable=True):
-        return kvs_set_timing(self.ctx, enable)
+    def set_timing(self, mask=KVS_TIME_RESIDENT | KVS_TIME_RING):
+        return kvs_set_timing(self.ctx, mask)
+
+    def graph_begin(self):
+        return kvs_graph_begin(self.ctx)
+
+    def graph_end(self):
+        return kvs_graph_end(self.ctx)
+
+    def graph_launch(self):
+        return kvs_graph_launch(self.ctx)
+
+    def graph_destroy(self):
+        return kvs_graph_destroy(self.ctx)
 
     def inject(self, fault, nth):
         return kvs_debug_inject(self.ctx, fault, nth)

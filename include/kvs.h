@@ -118,9 +118,12 @@ typedef struct {
     uint64_t decode_launches;  /* split-K attention kernel launches */
     double decode_ms;          /* summed device time of timed attention launches (kvs_set_timing) */
     uint64_t decode_timed;     /* number of attention launches in decode_ms */
+    uint64_t decode_bytes;     /* page bytes those timed launches read (items * page_bytes) */
     uint64_t ring_slots;       /* current ring size */
     uint64_t pool_slots;       /* current resident pool size */
     uint64_t pool_used;        /* pool slots holding a resident page */
+    uint64_t graph_launches;   /* kvs_graph_launch calls */
+    uint64_t graph_kernels;    /* kernels in the captured step graph */
 } kvs_stats_t;
 
 /* One logged operation of a KVS_FLAG_PLAN_ONLY context (see kvs_trace_read). */
@@ -292,10 +295,33 @@ kvs_status kvs_ring_info(const kvs_ctx *ctx, int64_t *first_slot, uint32_t *n_sl
 /* kvs_stats -- counters since create (or the last reset when reset != 0). */
 kvs_status kvs_stats(kvs_ctx *ctx, kvs_stats_t *out, int reset);
 
-/* kvs_set_timing -- when enabled, each attention-kernel launch is bracketed by
- * CUDA events on attn_stream and its device time is added to
- * kvs_stats_t.decode_ms when the events complete. */
-kvs_status kvs_set_timing(kvs_ctx *ctx, int enable);
+/* kvs_set_timing -- mask of KVS_TIME_* bits.  Each attention-kernel launch of
+ * a selected kind is bracketed by CUDA events on attn_stream; its device time
+ * and the page bytes it reads are added to kvs_stats_t.decode_ms /
+ * decode_bytes once the events complete.  0 disables. */
+#define KVS_TIME_RESIDENT 1u /* launches over tail and resident-pool pages */
+#define KVS_TIME_RING 2u     /* launches over ring chunks */
+kvs_status kvs_set_timing(kvs_ctx *ctx, int mask);
+
+/*
+ * Step graphs.  One decode (or verify) step issues many small launches and
+ * ready/consumed handshakes; capturing the step once as a CUDA graph and
+ * replaying it removes the host cost of issuing them.  kvs_graph_begin starts
+ * stream capture on attn_stream (the copy stream joins it); every kvs_* call
+ * until kvs_graph_end is recorded, not executed (host-side state still
+ * advances as if it ran once).  No prefetch may be pending at either end.
+ * kvs_graph_launch replays the step on attn_stream after the copy stream's
+ * earlier work and before its later work; a replay repeats exactly the
+ * captured positions, so a captured step should leave the lengths where it
+ * found them (e.g. append, attend, truncate).  Replays reuse the device
+ * buffers (q, k, v, out, lse) whose addresses were captured.  Attention
+ * timing (kvs_set_timing) is not recorded inside a capture.  kvs_set_residency
+ * and kvs_set_ring_slots drop a captured graph (its slot schedule is baked in).
+ */
+kvs_status kvs_graph_begin(kvs_ctx *ctx);
+kvs_status kvs_graph_end(kvs_ctx *ctx);
+kvs_status kvs_graph_launch(kvs_ctx *ctx);
+kvs_status kvs_graph_destroy(kvs_ctx *ctx);
 
 /* kvs_last_error -- message of the last failed call on ctx ("" if none);
  * with ctx == NULL, the last kvs_create failure of this thread. */
