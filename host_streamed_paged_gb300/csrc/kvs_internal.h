@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace kvs {
 
 // Byte layout of one page (see kvs_query_sizes in include/kvs.h).
@@ -92,5 +94,8 @@ struct FillParams {
     uint8_t *dst[kMaxFillPages];
 };
 cudaError_t launch_fill(const FillParams &p, cudaStream_t s);
+
+// Message returned by kvs_last_error(NULL) on this thread.
+void set_thread_error(const std::string &msg);
 
 }  // namespace kvs

@@ -524,6 +524,10 @@ void sizes_of(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
 
 }  // namespace
 
+namespace kvs {
+void set_thread_error(const std::string &msg) { g_create_error = msg; }
+}  // namespace kvs
+
 // ======================================================================= C ABI
 
 extern "C" {

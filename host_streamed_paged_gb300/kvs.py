@@ -109,6 +109,8 @@ SIGNATURES = {
     "kvs_graph_end": ([_P], _I32),
     "kvs_graph_launch": ([_P], _I32),
     "kvs_graph_destroy": ([_P], _I32),
+    "kvs_attend_pages_noalloc": ([_P, _U64, _P, _U64, _U32, _U32, _U32, _P, _I32, _U32, _U32, _U64, _F32,
+                                  _P, _P, _P], _I32),
 }
 KVS_TIME_RESIDENT = 1
 KVS_TIME_RING = 2
@@ -248,6 +250,16 @@ def kvs_stats(ctx, reset=False) -> dict:
 
 def kvs_set_timing(ctx, mask=KVS_TIME_RESIDENT | KVS_TIME_RING) -> int:
     return _check(ctx, load().kvs_set_timing(ctx, int(mask)))
+
+
+def kvs_attend_pages_noalloc(pages, pages_bytes, page_slots, page_tokens, n_kv_head, head_dim, q, q_dtype,
+                             n_rows, n_q_head, pos0, scale, out, lse=None, stream=0) -> int:
+    """Attention over caller pages with no workspace (fixed in-library scratch)."""
+    slots = np.ascontiguousarray(page_slots, dtype=np.uint32)
+    return _check(None, load().kvs_attend_pages_noalloc(_ptr(pages), pages_bytes, slots.ctypes.data, slots.size,
+                                                        page_tokens, n_kv_head, head_dim, _ptr(q), q_dtype,
+                                                        n_rows, n_q_head, pos0, float(scale), _ptr(out),
+                                                        _ptr(lse), stream))
 
 
 def kvs_graph_begin(ctx) -> int:

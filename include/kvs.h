@@ -324,7 +324,8 @@ kvs_status kvs_graph_launch(kvs_ctx *ctx);
 kvs_status kvs_graph_destroy(kvs_ctx *ctx);
 
 /* kvs_last_error -- message of the last failed call on ctx ("" if none);
- * with ctx == NULL, the last kvs_create failure of this thread. */
+ * with ctx == NULL, the last failure of this thread in a call that takes no
+ * context (kvs_query_sizes, kvs_create, kvs_attend_pages_noalloc). */
 const char *kvs_last_error(const kvs_ctx *ctx);
 
 /* kvs_debug_inject -- arm a host-side fault (KVS_FAULT_*) that fires on the
@@ -339,6 +340,39 @@ kvs_status kvs_trace_read(const kvs_ctx *ctx, uint64_t first, uint64_t max, kvs_
 
 /* kvs_version -- KVS_ABI_VERSION of the loaded library. */
 int32_t kvs_version(void);
+
+/*
+ * kvs_attend_pages_noalloc -- kvs_attend for callers that cannot allocate
+ * device memory.  (The pages describe no such call; it exists for callers
+ * running inside an allocator or memory-pool callback, plug-ins given a fixed
+ * device budget by their host, or services that must not grow their device
+ * footprint once running -- none of which can hand kvs_attend a workspace.)
+ *
+ * Computes the same causal attention as kvs_attend, with no context: the
+ * caller passes its pages in one device buffer (pages_dev, pages_bytes) laid
+ * out as kvs_query_sizes describes (page_bytes = n_kv_head * page_tokens *
+ * head_dim * 13 / 8), a host array page_slots[n_pages] giving the slot of
+ * logical page i in that buffer, the queries q_dev [n_rows][n_q_head][D]
+ * (KVS_F32 or KVS_F16; row r at position pos0 + r sees keys 0 .. pos0 + r),
+ * and outputs out_dev [n_rows][n_q_head][D] fp32 and lse_dev [n_rows][n_q_head]
+ * (nullable), all on `stream` (a cudaStream_t).
+ * It allocates nothing: split partials go to a fixed 32 MiB device array
+ * inside this library, present on every GPU that loads it until the process
+ * exits.  A call needing more, i.e. ceil((pos0 + n_rows) / page_tokens) *
+ * n_q_head * n_rows * (head_dim + 2) * 4 bytes > 32 MiB, is refused with
+ * KVS_ERR_CAPACITY before any work.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress); make that first call
+ * before any stream capture on that device.  All calls on a device share the
+ * array, which keeps the last call's contents (nothing in it needs clearing):
+ * calls whose GPU work overlaps race, so order them on one stream.
+ * Errors: kvs_last_error(NULL).
+ */
+kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t pages_bytes,
+                                    const uint32_t *page_slots, uint64_t n_pages,
+                                    uint32_t page_tokens, uint32_t n_kv_head, uint32_t head_dim,
+                                    const void *q_dev, int32_t q_dtype, uint32_t n_rows,
+                                    uint32_t n_q_head, uint64_t pos0, float scale, float *out_dev,
+                                    float *lse_dev, void *stream);
 
 #ifdef __cplusplus
 }
