@@ -39,11 +39,15 @@ WORKLOADS = {
     "decode32k": dict(
         desc=("decode stack: 64 layers x 1 row, context 32768, 24 q / 4 kv heads, D 256, page 256, "
               "Q8_0 K / Q4_0 V, 50% of pages resident (seeded), rest streamed via an 8-slot ring "
-              "with next-layer prefetch"),
-        L=64, T=32768, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, resident_frac=0.5),
+              "with next-layer prefetch (2-page chunks on 4 copy/attention lanes)"),
+        L=64, T=32768, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, lanes=4, resident_frac=0.5),
     "decode32k_small": dict(  # a reduced copy for quick checks and profiling captures
         desc="decode stack, 8 layers, otherwise as decode32k",
-        L=8, T=32768, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, resident_frac=0.5),
+        L=8, T=32768, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, lanes=4, resident_frac=0.5),
+    "resident131k": dict(  # the attention kernel over resident pages, launches far larger than L2
+        desc=("all-resident decode: 4 layers x 1 row, context 131072, 24 q / 4 kv heads, D 256, page 256, "
+              "Q8_0 K / Q4_0 V, every page resident (218 MB of pages per layer)"),
+        L=4, T=131072, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, resident_frac=1.0),
 }
 
 
@@ -198,7 +202,7 @@ def run_ours(args, wl):
     pool = int(sum(int(m.sum()) for m in masks))
     st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=max(R, 1),
                       max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"],
-                      arena_slots=2 * L + wl["ring"] + pool, device=dev)
+                      arena_slots=2 * L + wl["ring"] + pool, device=dev, lanes=wl.get("lanes", 1))
 
     ceiling = h2d_ceiling(torch, dev)
 
@@ -351,7 +355,8 @@ def run_ours(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": wl["desc"], "layers": L, "context": T, "rows": R, "q_heads": Hq, "kv_heads": Hk,
                    "head_dim": D, "page_tokens": P, "resident_fraction": wl["resident_frac"],
-                   "ring_slots": wl["ring"], "chunk_pages": wl["chunk"], "parallelism": f"replicas x{world}",
+                   "ring_slots": wl["ring"], "chunk_pages": wl["chunk"], "lanes": wl.get("lanes", 1),
+                   "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {kv_bytes_step / 1e9:.2f} GB of KV pages read per step",
                    "step": "per layer: append row, prefetch next layer, attend, truncate; one CUDA graph replay"},
         "kv_gbs": kv_bytes_step / (ms_step * 1e-3) / 1e9,
@@ -388,9 +393,18 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode32k")
     ap.add_argument("--cpu-layers", type=int, default=8, help="layers the oracle baseline samples")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--ring", type=int, default=0, help="override the workload's ring slots")
+    ap.add_argument("--chunk", type=int, default=0, help="override the workload's pages per ring chunk")
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    ap.add_argument("--lanes", type=int, default=0, help="override the workload's ring lanes")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    for key in ("ring", "chunk", "layers", "lanes"):
+        v = getattr(args, key)
+        if v:
+            wl["L" if key == "layers" else key] = v
+            wl["desc"] += f" [{key} override: {v}]"
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -87,23 +87,28 @@ __device__ __forceinline__ uint4 ld_nc_u4(const void *p) {
 }
 
 // grid = (ctas per page, pages); host pages are read through their mapped
-// device address.  Four independent 16-byte loads per thread are in flight.
-__global__ void __launch_bounds__(512) fill_kernel(const __grid_constant__ FillParams p) {
+// device address.  The grid is sized so that each thread issues all of its
+// (at most kFillUnroll) 16-byte host loads before its first store: a chunk
+// is only a few pages, so one round of host-link latency per launch is the
+// whole cost beyond the transfer itself.
+constexpr int kFillThreads = 512;
+constexpr int kFillUnroll = 4;
+
+__global__ void __launch_bounds__(kFillThreads) fill_kernel(const __grid_constant__ FillParams p) {
     const int pg = blockIdx.y;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.src[pg]);
     uint4 *dst = reinterpret_cast<uint4 *>(p.dst[pg]);
     const int64_t n = p.page_bytes / 16;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n; i += 4 * stride) {
-        const uint4 a = ld_nc_u4(src + i), b = ld_nc_u4(src + i + stride);
-        const uint4 c = ld_nc_u4(src + i + 2 * stride), d = ld_nc_u4(src + i + 3 * stride);
-        dst[i] = a;
-        dst[i + stride] = b;
-        dst[i + 2 * stride] = c;
-        dst[i + 3 * stride] = d;
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += kFillUnroll * stride) {
+        uint4 v[kFillUnroll];
+#pragma unroll
+        for (int u = 0; u < kFillUnroll; ++u)
+            if (i0 + u * stride < n) v[u] = ld_nc_u4(src + i0 + u * stride);
+#pragma unroll
+        for (int u = 0; u < kFillUnroll; ++u)
+            if (i0 + u * stride < n) dst[i0 + u * stride] = v[u];
     }
-    for (; i < n; i += stride) dst[i] = ld_nc_u4(src + i);
 }
 
 }  // namespace
@@ -126,10 +131,10 @@ cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStre
 cudaError_t launch_fill(const FillParams &p, cudaStream_t s) {
     if (p.n <= 0) return cudaSuccess;
     if (p.n > kMaxFillPages || p.page_bytes % 16 != 0) return cudaErrorInvalidValue;
-    // about 16 CTAs in total saturate the host link (measured); at least one per page
-    int per_page = (16 + p.n - 1) / p.n;
+    const int64_t units = p.page_bytes / 16;
+    const int per_page = (int)((units + (int64_t)kFillThreads * kFillUnroll - 1) / ((int64_t)kFillThreads * kFillUnroll));
     dim3 grid(per_page, p.n);
-    fill_kernel<<<grid, 512, 0, s>>>(p);
+    fill_kernel<<<grid, kFillThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -77,7 +77,9 @@ struct kvs_ctx {
     kvs_config cfg;
     PageGeom geom;
     bool plan_only = false;
-    cudaStream_t attn = nullptr, copy = nullptr;
+    cudaStream_t attn = nullptr, copy = nullptr;  // lane 0
+    int n_lanes = 1;
+    std::vector<cudaStream_t> lanes;  // stream id s: lane s/2, attention if s even, copy if odd
     std::string err;
 
     // device page slots: [0, 2L) tails, [2L, 2L + pool_n) pool, then the ring
@@ -101,9 +103,11 @@ struct kvs_ctx {
     std::deque<uint32_t> announced;        // layers announced by prefetch/attend, in order
 
     // events: [0, R) ready, [R, 2R) consumed, 2R attn mark, 2R+1 copy mark,
-    // then one publish event per tail slot
+    // one publish event per tail slot, then one mark per lane stream
     std::vector<cudaEvent_t> events;
-    int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0;
+    int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0, ev_lane0 = 0, ev_pub_last = 0;
+    uint64_t pub_generation = 0;        // publishes recorded on the copy stream
+    std::vector<uint64_t> lane_pub_seen;  // per lane: pub_generation its copy stream has waited for
 
     // timing of attention kernels (mask of KVS_TIME_*)
     uint32_t timing = 0;
@@ -138,7 +142,8 @@ struct kvs_ctx {
     uint8_t *host_page_dev(uint32_t layer, int64_t page) const {
         return host_dev + ((int64_t)layer * max_pages + page) * geom.page_bytes;
     }
-    cudaStream_t stream(int s) const { return s == kAttn ? attn : copy; }
+    cudaStream_t stream(int s) const { return lanes[s]; }
+    int n_streams() const { return 2 * n_lanes; }
 };
 
 namespace {
@@ -202,14 +207,67 @@ kvs_status join_attn_into_copy(kvs_ctx *c) {
     return s != KVS_OK ? s : op_wait(c, kCopy, c->ev_attn_mark);
 }
 
+// stream `to` waits for everything enqueued so far on stream `from`
+kvs_status join(kvs_ctx *c, int from, int to) {
+    kvs_status s = op_record(c, from, c->ev_lane0 + from);
+    return s != KVS_OK ? s : op_wait(c, to, c->ev_lane0 + from);
+}
+
+// every other lane stream waits for the primary stream of its kind
+kvs_status fork_lanes(kvs_ctx *c) {
+    for (int l = 1; l < c->n_lanes; ++l) {
+        kvs_status s = join(c, kAttn, 2 * l);
+        if (s == KVS_OK) s = join(c, kCopy, 2 * l + 1);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+// the other attention lanes wait for the primary attention stream (inputs
+// of this call in place, the previous combine done with the partials)
+kvs_status fork_attn_lanes(kvs_ctx *c) {
+    for (int l = 1; l < c->n_lanes; ++l) {
+        kvs_status s = join(c, kAttn, 2 * l);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+// a publish (D2H of a completed tail page) was just enqueued on the copy
+// stream: copy lanes that later refill from host wait for it once
+kvs_status mark_publish(kvs_ctx *c) {
+    kvs_status s = op_record(c, kCopy, c->ev_pub_last);
+    if (s == KVS_OK) c->pub_generation++;
+    c->lane_pub_seen[0] = c->pub_generation;  // lane 0 is the copy stream itself
+    return s;
+}
+
+// the primary attention stream waits for the other attention lanes
+kvs_status join_attn_lanes_into_attn(kvs_ctx *c) {
+    for (int sid = 2; sid < c->n_streams(); sid += 2) {
+        kvs_status s = join(c, sid, kAttn);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+// the primary attention stream waits for every other stream of every lane
+kvs_status join_all_into_attn(kvs_ctx *c) {
+    for (int sid = 1; sid < c->n_streams(); ++sid) {
+        kvs_status s = join(c, sid, kAttn);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
 // host pages -> device slots on the copy stream (ring fill or pool load)
 kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
                          const std::vector<int64_t> &slots, uint32_t kind,
-                         const std::vector<uint64_t> *seqs) {
+                         const std::vector<uint64_t> *seqs, int sid = kCopy) {
     c->st.kernel_launches += (pages.size() + kvs::kMaxFillPages - 1) / kvs::kMaxFillPages;
     if (c->plan_only) {
         for (size_t i = 0; i < pages.size(); ++i)
-            log_op(c, kind, kCopy, layer, 0, pages[i], slots[i], seqs ? (int64_t)(*seqs)[i] : 0);
+            log_op(c, kind, sid, layer, 0, pages[i], slots[i], seqs ? (int64_t)(*seqs)[i] : 0);
         return KVS_OK;
     }
     for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxFillPages) {
@@ -220,7 +278,7 @@ kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> 
             fp.src[j] = c->host_page_dev(layer, pages[i0 + j]);
             fp.dst[j] = c->slot_ptr(slots[i0 + j]);
         }
-        cudaError_t e = kvs::launch_fill(fp, c->copy);
+        cudaError_t e = kvs::launch_fill(fp, c->stream(sid));
         if (e != cudaSuccess) return cuda_fail(c, e, "ring/pool fill launch");
     }
     return KVS_OK;
@@ -238,22 +296,22 @@ kvs_status take_timer_event(kvs_ctx *c, cudaEvent_t *ev) {
     return KVS_OK;
 }
 
-kvs_status timed_begin(kvs_ctx *c, uint32_t kind, cudaEvent_t *ev) {
+kvs_status timed_begin(kvs_ctx *c, uint32_t kind, cudaEvent_t *ev, int sid) {
     *ev = nullptr;
     // graph-recorded events carry no timing: no timers inside a step capture
     if (!(c->timing & kind) || c->plan_only || c->capturing) return KVS_OK;
     kvs_status s = take_timer_event(c, ev);
     if (s != KVS_OK) return s;
-    cudaError_t r = cudaEventRecord(*ev, c->attn);
+    cudaError_t r = cudaEventRecord(*ev, c->stream(sid));
     return r == cudaSuccess ? KVS_OK : cuda_fail(c, r, "cudaEventRecord");
 }
 
-kvs_status timed_end(kvs_ctx *c, cudaEvent_t start, uint64_t bytes) {
+kvs_status timed_end(kvs_ctx *c, cudaEvent_t start, uint64_t bytes, int sid) {
     if (!start) return KVS_OK;
     cudaEvent_t stop = nullptr;
     kvs_status s = take_timer_event(c, &stop);
     if (s != KVS_OK) return s;
-    cudaError_t r = cudaEventRecord(stop, c->attn);
+    cudaError_t r = cudaEventRecord(stop, c->stream(sid));
     if (r != cudaSuccess) return cuda_fail(c, r, "cudaEventRecord");
     c->timer_pending.push_back({start, stop, bytes});
     return KVS_OK;
@@ -289,10 +347,14 @@ void destroy_events(kvs_ctx *c) {
 
 kvs_status create_events(kvs_ctx *c) {
     const int R = (int)c->ring_n;
-    const int n = 2 * R + 2 + 2 * (int)c->cfg.n_layers;
+    const int n = 2 * R + 2 + 2 * (int)c->cfg.n_layers + c->n_streams() + 1;
     c->ev_attn_mark = 2 * R;
     c->ev_copy_mark = 2 * R + 1;
     c->ev_pub0 = 2 * R + 2;
+    c->ev_lane0 = c->ev_pub0 + 2 * (int)c->cfg.n_layers;
+    c->ev_pub_last = c->ev_lane0 + c->n_streams();
+    c->pub_generation = 0;
+    c->lane_pub_seen.assign(c->n_lanes, 0);
     c->events.assign(n, nullptr);
     if (c->plan_only) return KVS_OK;
     for (int i = 0; i < n; ++i) {
@@ -408,13 +470,23 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
         if (++c->fault_count == c->fault_nth)
             return fail(c, KVS_ERR_INJECTED, "injected fault: ring refill enqueue");
     }
-    int64_t newest = -1;
-    for (size_t i = 0; i < ch.pages.size(); ++i)
-        newest = std::max(newest, c->slot_last_chunk[(ch.seq0 + i) % c->ring_n]);
+    const int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes) + 1;  // this chunk's copy lane
+    // wait for the last reader of every slot (readers may sit on different lanes)
+    std::vector<int64_t> prev;
+    for (size_t i = 0; i < ch.pages.size(); ++i) {
+        const int64_t p = c->slot_last_chunk[(ch.seq0 + i) % c->ring_n];
+        if (p >= 0 && std::find(prev.begin(), prev.end(), p) == prev.end()) prev.push_back(p);
+    }
     kvs_status s;
-    if (newest >= 0) {
-        s = op_wait(c, kCopy, (int)c->ring_n + (int)(newest % c->ring_n));
+    for (int64_t p : prev) {
+        s = op_wait(c, sid, (int)c->ring_n + (int)(p % c->ring_n));
         if (s != KVS_OK) return s;
+    }
+    const int lane = sid / 2;
+    if (c->lane_pub_seen[lane] < c->pub_generation) {  // host pages published since: wait for them
+        s = op_wait(c, sid, c->ev_pub_last);
+        if (s != KVS_OK) return s;
+        c->lane_pub_seen[lane] = c->pub_generation;
     }
     std::vector<int64_t> slots(ch.pages.size());
     std::vector<uint64_t> seqs(ch.pages.size());
@@ -422,9 +494,9 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
         seqs[i] = ch.seq0 + i;
         slots[i] = c->ring_slot_id(ch.seq0 + i);
     }
-    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs);
+    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs, sid);
     if (s != KVS_OK) return s;
-    s = op_record(c, kCopy, (int)(ch.id % c->ring_n));
+    s = op_record(c, sid, (int)(ch.id % c->ring_n));
     if (s != KVS_OK) return s;
     for (size_t i = 0; i < ch.pages.size(); ++i) {
         int64_t &last = c->slot_last_chunk[(ch.seq0 + i) % c->ring_n];
@@ -452,16 +524,17 @@ kvs_status pump(kvs_ctx *c) {
 // ---- attention launches
 
 kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
-                        const std::vector<int64_t> &slots, kvs::DecodeParams &dp, uint32_t kind) {
+                        const std::vector<int64_t> &slots, kvs::DecodeParams &dp, uint32_t kind,
+                        int sid = kAttn) {
     for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxItems) {
         const int n = (int)std::min<size_t>(kvs::kMaxItems, pages.size() - i0);
         c->st.decode_launches++;
         c->st.kernel_launches++;
         if (c->plan_only) {
-            log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 1, n);
+            log_op(c, KVS_OP_LAUNCH, sid, layer, 0, 1, n);
             for (int j = 0; j < n; ++j)
                 for (int g = 0; g < c->geom.Hk; ++g)
-                    log_op(c, KVS_OP_READ, kAttn, layer, 0, pages[i0 + j], slots[i0 + j], g);
+                    log_op(c, KVS_OP_READ, sid, layer, 0, pages[i0 + j], slots[i0 + j], g);
             continue;
         }
         dp.n_items = n;
@@ -470,11 +543,11 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
             dp.slot[j] = (uint32_t)slots[i0 + j];
         }
         cudaEvent_t t0;
-        kvs_status s = timed_begin(c, kind, &t0);
+        kvs_status s = timed_begin(c, kind, &t0, sid);
         if (s != KVS_OK) return s;
-        cudaError_t e = kvs::launch_decode(dp, c->attn);
+        cudaError_t e = kvs::launch_decode(dp, c->stream(sid));
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel launch");
-        s = timed_end(c, t0, (uint64_t)n * (uint64_t)c->geom.page_bytes);
+        s = timed_end(c, t0, (uint64_t)n * (uint64_t)c->geom.page_bytes, sid);
         if (s != KVS_OK) return s;
     }
     return KVS_OK;
@@ -570,6 +643,10 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         g_create_error = "ring_slots must be >= 1";
         return KVS_ERR_INVALID;
     }
+    if (cfg->n_lanes > 4) {
+        g_create_error = "n_lanes must be 1..4";
+        return KVS_ERR_INVALID;
+    }
     if (!cfg->arena || cfg->arena_bytes < arena_min) {
         g_create_error = "arena below the minimum of 2 tail slots per layer plus the ring (" +
                          std::to_string(arena_min) + " bytes)";
@@ -593,6 +670,14 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
     c->geom = kvs::make_geom((int)cfg->page_tokens, (int)cfg->n_kv_head, (int)cfg->head_dim);
     c->attn = static_cast<cudaStream_t>(cfg->attn_stream);
     c->copy = static_cast<cudaStream_t>(cfg->copy_stream);
+    c->n_lanes = cfg->n_lanes ? (int)cfg->n_lanes : 1;
+    c->lanes.assign(2 * c->n_lanes, nullptr);
+    c->lanes[0] = c->attn;
+    c->lanes[1] = c->copy;
+    for (int l = 1; l < c->n_lanes; ++l) {
+        c->lanes[2 * l] = static_cast<cudaStream_t>(cfg->lane_attn_streams[l - 1]);
+        c->lanes[2 * l + 1] = static_cast<cudaStream_t>(cfg->lane_copy_streams[l - 1]);
+    }
     c->max_pages = (int64_t)((cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens);
     c->layers.resize(cfg->n_layers);
     for (auto &L : c->layers) L.pool_slot.assign(c->max_pages, -1);
@@ -609,11 +694,13 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
     c->host = static_cast<uint8_t *>(cfg->host);
     c->host_dev = c->host;
     if (!plan_only) {
-        if (!c->attn || !c->copy || c->attn == c->copy) {
-            delete c;
-            g_create_error = "attn_stream and copy_stream must be two distinct CUDA streams";
-            return KVS_ERR_INVALID;
-        }
+        for (size_t i = 0; i < c->lanes.size(); ++i)
+            for (size_t j = 0; j < i; ++j)
+                if (!c->lanes[i] || c->lanes[i] == c->lanes[j]) {
+                    delete c;
+                    g_create_error = "attn/copy streams of all lanes must be distinct, non-null CUDA streams";
+                    return KVS_ERR_INVALID;
+                }
         cudaPointerAttributes pa;
         cudaError_t e = cudaPointerGetAttributes(&pa, cfg->host);
         if (e != cudaSuccess || pa.type != cudaMemoryTypeHost) {
@@ -654,8 +741,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
 kvs_status kvs_destroy(kvs_ctx *c) {
     if (!c) return KVS_ERR_INVALID;
     if (!c->plan_only) {
-        cudaStreamSynchronize(c->attn);
-        cudaStreamSynchronize(c->copy);
+        for (cudaStream_t st : c->lanes) cudaStreamSynchronize(st);
         for (auto &t : c->timer_pending) {
             cudaEventDestroy(t.start);
             cudaEventDestroy(t.stop);
@@ -778,6 +864,8 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
             }
             s = op_record(c, kCopy, c->ev_pub0 + (int)tslot);
             if (s != KVS_OK) return s;
+            s = mark_publish(c);
+            if (s != KVS_OK) return s;
             c->st.d2h_pages++;
             c->st.d2h_bytes += (uint64_t)c->geom.page_bytes;
         }
@@ -846,7 +934,9 @@ kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, ui
         return fail(c, KVS_ERR_CAPACITY, "resident pool has too few free slots for this mask");
     L.mask.assign(want.begin(), want.begin() + std::max<int64_t>(n_pages, 0));
     // slots leaving the pool may still be read by queued attention
-    kvs_status s = join_attn_into_copy(c);
+    kvs_status s = join_attn_lanes_into_attn(c);
+    if (s != KVS_OK) return s;
+    s = join_attn_into_copy(c);
     if (s != KVS_OK) return s;
     for (int64_t p = 0; p < complete; ++p) {
         if (!want[p] && L.pool_slot[p] >= 0 && L.tail_page[p & 1] != p) {
@@ -886,7 +976,9 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     if (new_pool < 0) return fail(c, KVS_ERR_CAPACITY, "arena too small for that ring");
     if (c->pool_used > new_pool) return fail(c, KVS_ERR_CAPACITY, "resident pages exceed the new pool");
     // ring and pool slots change role: order after all earlier device work
-    kvs_status s = join_attn_into_copy(c);
+    kvs_status s = join_all_into_attn(c);
+    if (s != KVS_OK) return s;
+    s = join_attn_into_copy(c);
     if (s != KVS_OK) return s;
     s = join_copy_into_attn(c);
     if (s != KVS_OK) return s;
@@ -913,10 +1005,8 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     s = join_attn_into_copy(c);
     if (s != KVS_OK) return s;
     // new event set for the new ring size; a captured step graph is dropped
-    if (!c->plan_only) {
-        cudaStreamSynchronize(c->attn);
-        cudaStreamSynchronize(c->copy);
-    }
+    if (!c->plan_only)
+        for (cudaStream_t st : c->lanes) cudaStreamSynchronize(st);
     release_graph(c);
     c->graph_kernels = 0;
     destroy_events(c);
@@ -1009,7 +1099,11 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
     dp.scale_log2 = scale * 1.4426950408889634f;
 
     c->st.attend_calls++;
-    kvs_status s = pump(c);
+    // other lanes start after this call's inputs (Q, the previous combine's
+    // reads of the partials, published pages) are in place
+    kvs_status s = fork_attn_lanes(c);
+    if (s != KVS_OK) return s;
+    s = pump(c);
     if (s != KVS_OK) return s;
     // resident and tail pages need no fence
     if (!res_pages.empty()) {
@@ -1025,7 +1119,8 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             if (s != KVS_OK) return s;
             if (!ch.filled) return fail(c, KVS_ERR_COVERAGE, "ring chunk could not be scheduled");
         }
-        s = op_wait(c, kAttn, (int)(ch.id % c->ring_n));
+        const int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes);  // this chunk's attention lane
+        s = op_wait(c, sid, (int)(ch.id % c->ring_n));
         if (s != KVS_OK) return s;
         std::vector<int64_t> pg, sl;
         for (size_t i = 0; i < ch.pages.size(); ++i) {
@@ -1034,11 +1129,11 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             sl.push_back(c->ring_slot_id(ch.seq0 + i));
         }
         if (!pg.empty()) {
-            s = launch_items(c, layer, pg, sl, dp, KVS_TIME_RING);
+            s = launch_items(c, layer, pg, sl, dp, KVS_TIME_RING, sid);
             if (s != KVS_OK) return s;
             c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
         }
-        s = op_record(c, kAttn, (int)c->ring_n + (int)(ch.id % c->ring_n));
+        s = op_record(c, sid, (int)c->ring_n + (int)(ch.id % c->ring_n));
         if (s != KVS_OK) return s;
         c->attended = ch.id + 1;
         c->st.ring_chunks++;
@@ -1047,6 +1142,8 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         if (s != KVS_OK) return s;
     }
     c->announced.pop_front();
+    s = join_attn_lanes_into_attn(c);
+    if (s != KVS_OK) return s;
     // final reduction over pages in logical order
     c->st.kernel_launches++;
     if (c->plan_only) {
@@ -1082,13 +1179,14 @@ kvs_status kvs_sync(kvs_ctx *c, uint32_t timeout_ms) {
         while (!expired()) std::this_thread::sleep_for(std::chrono::microseconds(200));
         return fail(c, KVS_ERR_TIMEOUT, "kvs_sync deadline passed");
     }
-    kvs_status s = op_record(c, kAttn, c->ev_attn_mark);
-    if (s != KVS_OK) return s;
-    s = op_record(c, kCopy, c->ev_copy_mark);
-    if (s != KVS_OK) return s;
+    for (int sid = 0; sid < c->n_streams(); ++sid) {
+        kvs_status s = op_record(c, sid, c->ev_lane0 + sid);
+        if (s != KVS_OK) return s;
+    }
     for (;;) {
         bool done = !stall;
-        for (int ev : {c->ev_attn_mark, c->ev_copy_mark}) {
+        for (int sid = 0; sid < c->n_streams(); ++sid) {
+            const int ev = c->ev_lane0 + sid;
             cudaError_t e = cudaEventQuery(c->events[ev]);
             if (e == cudaErrorNotReady) {
                 done = false;
@@ -1129,6 +1227,8 @@ kvs_status kvs_flush(kvs_ctx *c, uint32_t layer) {
             if (e != cudaSuccess) return cuda_fail(c, e, "tail flush");
         }
         s = op_record(c, kCopy, c->ev_pub0 + (int)ts);
+        if (s != KVS_OK) return s;
+        s = mark_publish(c);
         if (s != KVS_OK) return s;
         c->st.d2h_pages++;
         c->st.d2h_bytes += (uint64_t)c->geom.page_bytes;
@@ -1226,7 +1326,8 @@ kvs_status kvs_graph_begin(kvs_ctx *c) {
     // before every replay by the join in kvs_graph_launch
     std::fill(c->slot_last_chunk.begin(), c->slot_last_chunk.end(), -1);
     c->graph_kernel_base = c->st.kernel_launches;
-    return join_attn_into_copy(c);  // the copy stream joins the capture
+    kvs_status s = join_attn_into_copy(c);  // the copy stream joins the capture
+    return s != KVS_OK ? s : fork_lanes(c);  // and so do the other lanes
 }
 
 kvs_status kvs_graph_end(kvs_ctx *c) {
@@ -1234,7 +1335,7 @@ kvs_status kvs_graph_end(kvs_ctx *c) {
     c->err.clear();
     if (!c->capturing) return fail(c, KVS_ERR_STATE, "no step capture is open");
     const bool pending = !c->queue.empty() || !c->announced.empty();
-    kvs_status s = join_copy_into_attn(c);  // the copy stream rejoins before capture ends
+    kvs_status s = join_all_into_attn(c);  // every lane rejoins before capture ends
     c->capturing = false;
     cudaGraph_t g = nullptr;
     std::vector<cudaEvent_t> cap_events;
@@ -1279,7 +1380,7 @@ kvs_status kvs_graph_launch(kvs_ctx *c) {
     if (!c->graph_exec && !c->plan_only) return fail(c, KVS_ERR_STATE, "no step graph captured");
     if (!c->queue.empty() || !c->announced.empty())
         return fail(c, KVS_ERR_STATE, "replay with a prefetch pending");
-    kvs_status s = join_copy_into_attn(c);
+    kvs_status s = join_all_into_attn(c);
     if (s != KVS_OK) return s;
     if (!c->plan_only) {
         cudaError_t e = cudaGraphLaunch(c->graph_exec, c->attn);
@@ -1287,7 +1388,9 @@ kvs_status kvs_graph_launch(kvs_ctx *c) {
     }
     c->st.graph_launches++;
     c->st.kernel_launches += c->graph_kernels;
-    return join_attn_into_copy(c);  // later copies wait for the replay's ring readers
+    // later work on every lane waits for the replay's ring readers
+    s = join_attn_into_copy(c);
+    return s != KVS_OK ? s : fork_lanes(c);
 }
 
 kvs_status kvs_graph_destroy(kvs_ctx *c) {

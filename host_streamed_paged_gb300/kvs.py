@@ -61,6 +61,9 @@ class kvs_config(ctypes.Structure):
         ("attn_stream", ctypes.c_void_p),
         ("copy_stream", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
+        ("n_lanes", ctypes.c_uint32),
+        ("lane_attn_streams", ctypes.c_void_p * 3),
+        ("lane_copy_streams", ctypes.c_void_p * 3),
     ]
 
 
@@ -313,12 +316,13 @@ class KVStream:
 
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
                  max_tokens, ring_slots=8, chunk_pages=0, arena_slots=None, arena_bytes=None,
-                 plan_only=False, host=None, device="cuda"):
+                 plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None):
         cfg = kvs_config()
         cfg.page_tokens, cfg.n_layers, cfg.n_kv_head, cfg.head_dim = page_tokens, n_layers, n_kv_head, head_dim
         cfg.max_q_head, cfg.max_rows, cfg.max_tokens = max_q_head, max_rows, max_tokens
         cfg.k_type, cfg.v_type = KVS_TYPE_Q8_0, KVS_TYPE_Q4_0
         cfg.ring_slots, cfg.chunk_pages = ring_slots, chunk_pages
+        cfg.n_lanes = lanes
         self.page_bytes, host_bytes, arena_min, ws_bytes = kvs_query_sizes(cfg)
         self.max_pages = math.ceil(max_tokens / page_tokens)
         if arena_bytes is None:
@@ -334,8 +338,15 @@ class KVStream:
             self.arena = self.workspace = self.host = None
         else:
             import torch
+            # ring refills are the critical path of a streamed step: their copy
+            # streams get the higher scheduling priority, so fill kernels take
+            # SMs ahead of queued attention blocks
+            try:
+                hi = torch.cuda.Stream.priority_range()[1]
+            except Exception:
+                hi = -1
             self.attn_stream = torch.cuda.Stream(device=device)
-            self.copy_stream = torch.cuda.Stream(device=device)
+            self.copy_stream = torch.cuda.Stream(device=device, priority=copy_priority if copy_priority is not None else hi)
             self.arena = torch.empty(arena_bytes, dtype=torch.uint8, device=device)
             self.workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
             if host is None:
@@ -345,6 +356,13 @@ class KVStream:
             cfg.host = _ptr(host)
             cfg.attn_stream = self.attn_stream.cuda_stream
             cfg.copy_stream = self.copy_stream.cuda_stream
+            self.lane_streams = []
+            for i in range(lanes - 1):
+                a = torch.cuda.Stream(device=device)
+                c = torch.cuda.Stream(device=device, priority=copy_priority if copy_priority is not None else hi)
+                self.lane_streams += [a, c]
+                cfg.lane_attn_streams[i] = a.cuda_stream
+                cfg.lane_copy_streams[i] = c.cuda_stream
         cfg.arena_bytes, cfg.workspace_bytes, cfg.host_bytes = arena_bytes, ws_bytes, host_bytes
         self.cfg = cfg
         self.ctx = kvs_create(cfg)

@@ -100,6 +100,12 @@ typedef struct {
     void *attn_stream;     /* cudaStream_t for attention, quantise/append and pool moves */
     void *copy_stream;     /* cudaStream_t for ring refills, pool loads and D2H publish */
     uint32_t flags;        /* KVS_FLAG_* */
+    uint32_t n_lanes;      /* ring pipelines, 1..4 (0 = 1): ring chunk j is copied on copy
+                              lane j % n_lanes and attended on attention lane j % n_lanes, so
+                              neighbouring chunks' copies and reads overlap; lane 0 is
+                              (attn_stream, copy_stream) */
+    void *lane_attn_streams[3];  /* cudaStream_t of attention lanes 1 .. n_lanes-1 */
+    void *lane_copy_streams[3];  /* cudaStream_t of copy lanes 1 .. n_lanes-1 */
 } kvs_config;
 
 typedef struct {
@@ -129,7 +135,7 @@ typedef struct {
 /* One logged operation of a KVS_FLAG_PLAN_ONLY context (see kvs_trace_read). */
 typedef struct {
     uint32_t op;      /* KVS_OP_* */
-    uint32_t stream;  /* 0 = attention stream, 1 = copy stream */
+    uint32_t stream;  /* 2*lane: attention stream of that lane, 2*lane+1: its copy stream */
     uint32_t layer;
     uint32_t event;   /* event id (RECORD / WAIT) */
     int64_t a;        /* READ/FILL/POOL_LOAD/PUBLISH/WRITE: page; LAUNCH: kernel kind */

@@ -98,9 +98,9 @@ def test_create_refusals():
 class HB:
     """Happens-before over a logged two-stream trace (vector clocks)."""
 
-    def __init__(self, trace):
+    def __init__(self, trace, n_streams=8):
         self.ops = []
-        vc = [[0, 0], [0, 0]]
+        vc = [[0] * n_streams for _ in range(n_streams)]
         ev = {}
         for t in trace:
             s = t["stream"]
@@ -165,13 +165,13 @@ def _reads_of_attend(ops, layer):
     return [(o["a"], o["c"]) for o in ops if o["op"] == kvs.KVS_OP_READ and o["layer"] == layer]
 
 
-def _plan_stream(L, Hk, P, max_tokens, ring, chunk, arena_slots, G=6, R=6):
+def _plan_stream(L, Hk, P, max_tokens, ring, chunk, arena_slots, G=6, R=6, lanes=1):
     return kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=128, max_q_head=G * Hk,
                         max_rows=R, max_tokens=max_tokens, ring_slots=ring, chunk_pages=chunk,
-                        arena_slots=arena_slots, plan_only=True)
+                        arena_slots=arena_slots, plan_only=True, lanes=lanes)
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_scheduler_random_residency_fences_and_coverage(seed):
     rng = np.random.default_rng(seed)
     P = int(rng.choice([32, 64, 128, 256]))
@@ -179,10 +179,11 @@ def test_scheduler_random_residency_fences_and_coverage(seed):
     Hk = int(rng.integers(1, 3))
     ring = int(rng.integers(1, 17))
     chunk = int(rng.integers(0, ring + 1))
+    lanes = int(rng.integers(1, 5))
     T0 = int(rng.integers(1, 40 * P))
     max_tokens = T0 + 4 * P
     npages_max = math.ceil(max_tokens / P)
-    st = _plan_stream(L, Hk, P, max_tokens, ring, chunk, 2 * L + ring + L * npages_max)
+    st = _plan_stream(L, Hk, P, max_tokens, ring, chunk, 2 * L + ring + L * npages_max, lanes=lanes)
     for l in range(L):
         kvs.kvs_append(st.ctx, l, None, None, T0)
         n = math.ceil(T0 / P)

@@ -174,10 +174,11 @@ def test_f16_queries():
 
 # ------------------------------------------------------------ invariants
 
-def test_streamed_equals_resident_bitwise():
+@pytest.mark.parametrize("lanes", [1, 3])
+def test_streamed_equals_resident_bitwise(lanes):
     P, L, Hk, G, D, R, T = 64, 2, 2, 6, 256, 3, 64 * 10 + 33
     Hq = G * Hk
-    st = make_stream(P, L, Hk, D, Hq, R, T, ring=8, chunk=2)
+    st = make_stream(P, L, Hk, D, Hq, R, T, ring=8, chunk=2, lanes=lanes)
     hist = _fill(st, L, T, Hk, D)
     npages = math.ceil(T / P)
     qs = [queries(SEED, l, R, Hq, D) for l in range(L)]
@@ -277,12 +278,13 @@ def test_sync_timeout_injection_on_gpu_context():
 
 # ------------------------------------------------------------ full-size samples
 
-def test_decode_stack_sampled_layers_full_size():
+@pytest.mark.parametrize("chunk,lanes", [(2, 1), (4, 2), (2, 3)])
+def test_decode_stack_sampled_layers_full_size(chunk, lanes):
     """Context 32768, 24 q / 4 kv heads, D 256, page 256, half the pages resident
-    (seeded), 8-slot ring: the launch configuration of the decode benchmark,
+    (seeded), 8-slot ring: the launch configurations of the decode benchmark,
     checked on three layers against the oracle."""
     P, Hk, Hq, D, T, L = 256, 4, 24, 256, 32768, 3
-    st = make_stream(P, L, Hk, D, Hq, 1, T, ring=8, chunk=2, pool_pages=L * 64)
+    st = make_stream(P, L, Hk, D, Hq, 1, T, ring=8, chunk=chunk, pool_pages=L * 64, lanes=lanes)
     hist = _fill(st, L, T, Hk, D)
     for l in range(L):
         # 62 seeded pages + the two tail pages = half of the 128 pages resident
