@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     __shared__ float wo[8][D];
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nsplit = (int)((p.pos0 + r) / p.P) + 1;
+    const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
     float M = -INFINITY, Lsum = 0.f, o[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) o[i] = 0.f;

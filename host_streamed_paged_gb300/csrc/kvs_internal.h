@@ -57,6 +57,30 @@ struct DecodeParams {
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s);
 int decode_max_mma_rows();  // G*R bound served by launch_decode
 
+// ---------------------------------------------------------------- prefill
+// tcgen05 prefill: one split = up to kMaxPrefillSplitPages consecutive pages;
+// grid = (splits, Hk * G * row tiles).  Q is fp16; D must be 256.
+constexpr int kMaxPrefillSplits = 64;
+constexpr int kMaxPrefillItems = 1024;
+struct PrefillParams {
+    const uint8_t *arena;
+    PageGeom geom;
+    const void *q;     // fp16 [R][Hq][D]
+    float *part_o;     // [split][Hq][R][D]
+    float *part_ml;    // [split][Hq][R][2]
+    int *status;       // set to 1 if a bounded device wait timed out
+    int R, Hq, G;
+    long long pos0;
+    float scale_log2;
+    int n_splits;
+    int split_begin[kMaxPrefillSplits + 1];  // item range of each split
+    int split_id[kMaxPrefillSplits];         // logical split index (partials row)
+    uint32_t page[kMaxPrefillItems];
+    uint32_t slot[kMaxPrefillItems];
+};
+cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t s);
+int prefill_smem_bytes();
+
 // ---------------------------------------------------------------- combine
 struct CombineParams {
     const float *part_o;
@@ -64,6 +88,7 @@ struct CombineParams {
     float *out;   // [R][Hq][D]
     float *lse;   // [R][Hq] or null
     int R, Hq, D, P;
+    int split_pages;  // pages per split (1 for decode, the prefill split otherwise)
     long long pos0;
 };
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);

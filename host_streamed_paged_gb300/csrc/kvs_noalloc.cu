@@ -153,6 +153,7 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
     cp.Hq = (int)n_q_head;
     cp.D = (int)D;
     cp.P = (int)P;
+    cp.split_pages = 1;
     cp.pos0 = (long long)pos0;
     cudaError_t e = kvs::launch_combine(cp, st);
     if (e != cudaSuccess) {

@@ -90,6 +90,8 @@ struct kvs_ctx {
     int64_t pool_used = 0;
 
     int64_t max_pages = 0;
+    int64_t prefill_split = 8;  // pages per tensor-core prefill split
+    bool check_status = false;  // a kernel with bounded device waits ran since the last kvs_sync
     std::vector<LayerState> layers;
 
     uint8_t *host = nullptr;      // host history (host address)
@@ -444,14 +446,18 @@ void plan_layer(kvs_ctx *c, uint32_t layer) {
         int64_t s;
         if (locate(c, layer, p, &s) == 0) streamed.push_back(p);
     }
-    for (size_t i = 0; i < streamed.size(); i += c->chunk_pages) {
+    // chunks of up to chunk_pages pages that never cross a prefill split
+    for (size_t i = 0; i < streamed.size();) {
         Chunk ch;
         ch.id = c->next_chunk++;
         ch.layer = layer;
         ch.seq0 = c->ring_seq;
-        const size_t n = std::min<size_t>(c->chunk_pages, streamed.size() - i);
+        const int64_t split = streamed[i] / c->prefill_split;
+        size_t n = 0;
+        while (i + n < streamed.size() && n < c->chunk_pages && streamed[i + n] / c->prefill_split == split) ++n;
         ch.pages.assign(streamed.begin() + i, streamed.begin() + i + n);
         c->ring_seq += n;
+        i += n;
         c->queue.push_back(std::move(ch));
     }
     c->announced.push_back(layer);
@@ -553,6 +559,14 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
     return KVS_OK;
 }
 
+constexpr uint64_t kStatusBytes = 256;  // device status word at the start of the workspace
+
+uint64_t prefill_split_of(const kvs_config *cfg) {
+    uint64_t sp = cfg->prefill_split_pages ? cfg->prefill_split_pages : 8;
+    const uint64_t ring = cfg->ring_slots ? cfg->ring_slots : 1;
+    return std::max<uint64_t>(1, std::min(sp, ring));
+}
+
 bool geometry_ok(const kvs_config *cfg, std::string *why) {
     const uint32_t P = cfg->page_tokens, D = cfg->head_dim;
     if (!(P == 32 || P == 64 || P == 128 || P == 256)) {
@@ -572,8 +586,13 @@ bool geometry_ok(const kvs_config *cfg, std::string *why) {
         return false;
     }
     const uint32_t G = cfg->max_q_head / cfg->n_kv_head;
-    if (cfg->max_rows < 1 || G * cfg->max_rows > (uint32_t)kvs::decode_max_mma_rows()) {
-        *why = "max_rows * (max_q_head / n_kv_head) must be in 1..64";
+    if (cfg->max_rows < 1 || cfg->max_rows > 256) {
+        *why = "max_rows must be in 1..256";
+        return false;
+    }
+    if (G * cfg->max_rows > (uint32_t)kvs::decode_max_mma_rows() && (D != 256 || P % 64 != 0)) {
+        *why = "more than 64 query rows per kv head (the tensor-core prefill path) needs head_dim 256 "
+               "and page_tokens a multiple of 64";
         return false;
     }
     if (cfg->k_type != KVS_TYPE_Q8_0 || cfg->v_type != KVS_TYPE_Q4_0) {
@@ -591,8 +610,20 @@ void sizes_of(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
     if (page_bytes) *page_bytes = (uint64_t)g.page_bytes;
     if (host_bytes) *host_bytes = (uint64_t)cfg->n_layers * max_pages * (uint64_t)g.page_bytes;
     if (arena_min) *arena_min = (2ull * cfg->n_layers + ring) * (uint64_t)g.page_bytes;
-    if (ws_min)
-        *ws_min = max_pages * cfg->max_q_head * cfg->max_rows * (uint64_t)(cfg->head_dim + 2) * 4ull;
+    if (ws_min) {
+        // decode / verify: one partial per page for Hq * R <= 64 * Hk query rows
+        const uint64_t dec_rows = std::min<uint64_t>((uint64_t)cfg->max_q_head * cfg->max_rows,
+                                                     64ull * cfg->n_kv_head);
+        uint64_t need = max_pages * dec_rows * (uint64_t)(cfg->head_dim + 2) * 4ull;
+        // prefill: one partial per split
+        if ((uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head) {
+            const uint64_t sp = prefill_split_of(cfg);
+            const uint64_t splits = (max_pages + sp - 1) / sp;
+            need = std::max<uint64_t>(need, splits * cfg->max_q_head * cfg->max_rows *
+                                                (uint64_t)(cfg->head_dim + 2) * 4ull);
+        }
+        *ws_min = kStatusBytes + need;
+    }
 }
 
 }  // namespace
@@ -679,6 +710,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         c->lanes[2 * l + 1] = static_cast<cudaStream_t>(cfg->lane_copy_streams[l - 1]);
     }
     c->max_pages = (int64_t)((cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens);
+    c->prefill_split = (int64_t)prefill_split_of(cfg);
     c->layers.resize(cfg->n_layers);
     for (auto &L : c->layers) L.pool_slot.assign(c->max_pages, -1);
     c->n_slots = (int64_t)(cfg->arena_bytes / (uint64_t)c->geom.page_bytes);
@@ -731,6 +763,16 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         if (c->host_registered) cudaHostUnregister(cfg->host);
         delete c;
         return KVS_ERR_CUDA;
+    }
+    if (!plan_only) {
+        cudaError_t e = cudaMemset(cfg->workspace, 0, kStatusBytes);
+        if (e != cudaSuccess) {
+            g_create_error = std::string("workspace status clear: ") + cudaGetErrorString(e);
+            destroy_events(c);
+            if (c->host_registered) cudaHostUnregister(cfg->host);
+            delete c;
+            return KVS_ERR_CUDA;
+        }
     }
     c->st.ring_slots = c->ring_n;
     c->st.pool_slots = (uint64_t)c->pool_n;
@@ -1036,6 +1078,141 @@ kvs_status kvs_prefetch(kvs_ctx *c, uint32_t layer) {
     return pump(c);
 }
 
+// Prefill branch of kvs_attend: one tensor-core launch per batch of fully
+// device-resident splits, then one per streamed split once all of its ring
+// chunks are ready; each split's partial lands in its own row of the workspace.
+kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_t n_rows, uint32_t n_q_head,
+                          uint64_t pos0, float scale, int64_t last, float *part_o, float *part_ml) {
+    const int64_t SP = c->prefill_split;
+    const int64_t n_split = last / SP + 1;
+    kvs::PrefillParams pp;
+    memset(&pp, 0, offsetof(kvs::PrefillParams, split_begin));
+    pp.arena = static_cast<const uint8_t *>(c->cfg.arena);
+    pp.geom = c->geom;
+    pp.q = q_dev;
+    pp.part_o = part_o;
+    pp.part_ml = part_ml;
+    pp.status = static_cast<int *>(c->cfg.workspace);
+    pp.R = (int)n_rows;
+    pp.Hq = (int)n_q_head;
+    pp.G = (int)(n_q_head / c->geom.Hk);
+    pp.pos0 = (long long)pos0;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+
+    // (pages, slots) of one split; slot -1 where the page is in the ring
+    auto split_pages = [&](int64_t sidx, std::vector<int64_t> &pg, std::vector<int64_t> &sl) {
+        pg.clear();
+        sl.clear();
+        for (int64_t q = sidx * SP; q < std::min((sidx + 1) * SP, last + 1); ++q) {
+            int64_t slot;
+            const int kind = locate(c, layer, q, &slot);
+            pg.push_back(q);
+            sl.push_back(kind ? slot : -1);
+        }
+    };
+    auto launch = [&](const std::vector<int64_t> &ids, const std::vector<std::vector<int64_t>> &pgs,
+                      const std::vector<std::vector<int64_t>> &sls) -> kvs_status {
+        c->st.kernel_launches++;
+        c->st.decode_launches++;
+        if (c->plan_only) {
+            int64_t items = 0;
+            for (auto &v : pgs) items += (int64_t)v.size();
+            log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 3, items);
+            for (size_t i = 0; i < ids.size(); ++i)
+                for (size_t j = 0; j < pgs[i].size(); ++j)
+                    for (int g = 0; g < c->geom.Hk; ++g)
+                        log_op(c, KVS_OP_READ, kAttn, layer, 0, pgs[i][j], sls[i][j], g);
+            return KVS_OK;
+        }
+        pp.n_splits = (int)ids.size();
+        int it = 0;
+        for (size_t i = 0; i < ids.size(); ++i) {
+            pp.split_begin[i] = it;
+            pp.split_id[i] = (int)ids[i];
+            for (size_t j = 0; j < pgs[i].size(); ++j, ++it) {
+                pp.page[it] = (uint32_t)pgs[i][j];
+                pp.slot[it] = (uint32_t)sls[i][j];
+            }
+        }
+        pp.split_begin[ids.size()] = it;
+        cudaError_t e = kvs::launch_prefill(pp, c->attn);
+        if (e != cudaSuccess) return cuda_fail(c, e, "prefill kernel launch");
+        c->check_status = true;
+        return KVS_OK;
+    };
+
+    kvs_status s = pump(c);
+    if (s != KVS_OK) return s;
+    // fully device-resident splits, batched
+    {
+        std::vector<int64_t> ids;
+        std::vector<std::vector<int64_t>> pgs, sls;
+        std::vector<int64_t> pg, sl;
+        int items = 0;
+        for (int64_t sidx = 0; sidx < n_split; ++sidx) {
+            split_pages(sidx, pg, sl);
+            if (std::find(sl.begin(), sl.end(), (int64_t)-1) != sl.end()) continue;
+            if ((int)ids.size() == kvs::kMaxPrefillSplits || items + (int)pg.size() > kvs::kMaxPrefillItems) {
+                s = launch(ids, pgs, sls);
+                if (s != KVS_OK) return s;
+                ids.clear();
+                pgs.clear();
+                sls.clear();
+                items = 0;
+            }
+            ids.push_back(sidx);
+            pgs.push_back(pg);
+            sls.push_back(sl);
+            items += (int)pg.size();
+            c->st.resident_pages_read += pg.size() * (uint64_t)c->geom.Hk;
+        }
+        if (!ids.empty()) {
+            s = launch(ids, pgs, sls);
+            if (s != KVS_OK) return s;
+        }
+    }
+    // streamed splits: all of a split's chunks ready, one launch, all released
+    while (!c->queue.empty() && c->queue.front().layer == layer) {
+        const int64_t sidx = c->queue.front().pages[0] / SP;
+        std::vector<Chunk *> group;
+        for (Chunk &ch : c->queue) {
+            if (ch.layer != layer || ch.pages[0] / SP != sidx) break;
+            group.push_back(&ch);
+        }
+        for (Chunk *ch : group) {
+            if (!ch->filled) {
+                s = pump(c);
+                if (s != KVS_OK) return s;
+                if (!ch->filled)
+                    return fail(c, KVS_ERR_COVERAGE, "a prefill split's ring chunks do not fit in the ring together");
+            }
+            s = op_wait(c, kAttn, (int)(ch->id % c->ring_n));
+            if (s != KVS_OK) return s;
+        }
+        if (sidx < n_split) {
+            std::vector<int64_t> pg, sl;
+            split_pages(sidx, pg, sl);
+            for (Chunk *ch : group)
+                for (size_t i = 0; i < ch->pages.size(); ++i)
+                    for (size_t j = 0; j < pg.size(); ++j)
+                        if (pg[j] == ch->pages[i]) sl[j] = c->ring_slot_id(ch->seq0 + i);
+            s = launch({sidx}, {pg}, {sl});
+            if (s != KVS_OK) return s;
+            c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
+        }
+        for (Chunk *ch : group) {
+            s = op_record(c, kAttn, (int)c->ring_n + (int)(ch->id % c->ring_n));
+            if (s != KVS_OK) return s;
+            c->attended = ch->id + 1;
+            c->st.ring_chunks++;
+        }
+        for (size_t i = 0; i < group.size(); ++i) c->queue.pop_front();
+        s = pump(c);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
 kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_dtype, uint32_t n_rows,
                       uint32_t n_q_head, uint64_t pos0, float scale, float *out_dev, float *lse_dev) {
     if (!c) return KVS_ERR_INVALID;
@@ -1046,8 +1223,12 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
     if (n_q_head < (uint32_t)c->geom.Hk || n_q_head % c->geom.Hk != 0 || n_q_head > c->cfg.max_q_head)
         return fail(c, KVS_ERR_INVALID, "n_q_head must be a multiple of n_kv_head and <= max_q_head");
     const uint32_t G = n_q_head / c->geom.Hk;
-    if (n_rows > c->cfg.max_rows || G * n_rows > (uint32_t)kvs::decode_max_mma_rows())
-        return fail(c, KVS_ERR_UNSUPPORTED, "n_rows beyond max_rows or beyond 64 query rows per kv head");
+    if (n_rows > c->cfg.max_rows) return fail(c, KVS_ERR_UNSUPPORTED, "n_rows beyond max_rows");
+    const bool prefill = G * n_rows > (uint32_t)kvs::decode_max_mma_rows();
+    if (prefill && (q_dtype != KVS_F16 || c->geom.D != 256 || c->geom.P % 64 != 0))
+        return fail(c, KVS_ERR_UNSUPPORTED,
+                    "more than 64 query rows per kv head run on the tensor-core prefill path, which needs fp16 "
+                    "queries, head_dim 256 and page_tokens a multiple of 64");
     LayerState &L = c->layers[layer];
     if (pos0 + n_rows > L.T) return fail(c, KVS_ERR_CAPACITY, "rows beyond the appended length");
     if (!c->plan_only && (!q_dev || !out_dev)) return fail(c, KVS_ERR_INVALID, "null q or out");
@@ -1083,81 +1264,91 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         if (k != streamed.size()) return fail(c, KVS_ERR_COVERAGE, "span plan leaves nonresident pages uncovered");
     }
 
-    kvs::DecodeParams dp;
-    memset(&dp, 0, offsetof(kvs::DecodeParams, page));
-    dp.arena = static_cast<const uint8_t *>(c->cfg.arena);
-    dp.geom = c->geom;
-    dp.q = q_dev;
-    dp.q_f16 = q_dtype == KVS_F16;
     const size_t per_split = (size_t)n_q_head * n_rows;
-    dp.part_o = static_cast<float *>(c->cfg.workspace);
-    dp.part_ml = dp.part_o + (size_t)c->max_pages * per_split * c->geom.D;
-    dp.R = (int)n_rows;
-    dp.Hq = (int)n_q_head;
-    dp.G = (int)G;
-    dp.pos0 = (long long)pos0;
-    dp.scale_log2 = scale * 1.4426950408889634f;
-
+    float *part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes);
+    const int64_t n_partials = prefill ? (c->max_pages + c->prefill_split - 1) / c->prefill_split : c->max_pages;
+    float *part_ml = part_o + (size_t)n_partials * per_split * c->geom.D;
     c->st.attend_calls++;
-    // other lanes start after this call's inputs (Q, the previous combine's
-    // reads of the partials, published pages) are in place
-    kvs_status s = fork_attn_lanes(c);
-    if (s != KVS_OK) return s;
-    s = pump(c);
-    if (s != KVS_OK) return s;
-    // resident and tail pages need no fence
-    if (!res_pages.empty()) {
-        s = launch_items(c, layer, res_pages, res_slots, dp, KVS_TIME_RESIDENT);
+    kvs_status s;
+    if (prefill) {
+        s = attend_prefill(c, layer, q_dev, n_rows, n_q_head, pos0, scale, last, part_o, part_ml);
         if (s != KVS_OK) return s;
-        c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
-    }
-    // ring chunks in order: ready fence, read, consumed fence, refill
-    while (!c->queue.empty() && c->queue.front().layer == layer) {
-        Chunk &ch = c->queue.front();
-        if (!ch.filled) {
+    } else {
+        kvs::DecodeParams dp;
+        memset(&dp, 0, offsetof(kvs::DecodeParams, page));
+        dp.arena = static_cast<const uint8_t *>(c->cfg.arena);
+        dp.geom = c->geom;
+        dp.q = q_dev;
+        dp.q_f16 = q_dtype == KVS_F16;
+        dp.part_o = part_o;
+        dp.part_ml = part_ml;
+        dp.R = (int)n_rows;
+        dp.Hq = (int)n_q_head;
+        dp.G = (int)G;
+        dp.pos0 = (long long)pos0;
+        dp.scale_log2 = scale * 1.4426950408889634f;
+
+        // other lanes start after this call's inputs (Q, the previous combine's
+        // reads of the partials, published pages) are in place
+        s = fork_attn_lanes(c);
+        if (s != KVS_OK) return s;
+        s = pump(c);
+        if (s != KVS_OK) return s;
+        // resident and tail pages need no fence
+        if (!res_pages.empty()) {
+            s = launch_items(c, layer, res_pages, res_slots, dp, KVS_TIME_RESIDENT);
+            if (s != KVS_OK) return s;
+            c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
+        }
+        // ring chunks in order: ready fence, read, consumed fence, refill
+        while (!c->queue.empty() && c->queue.front().layer == layer) {
+            Chunk &ch = c->queue.front();
+            if (!ch.filled) {
+                s = pump(c);
+                if (s != KVS_OK) return s;
+                if (!ch.filled) return fail(c, KVS_ERR_COVERAGE, "ring chunk could not be scheduled");
+            }
+            const int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes);  // this chunk's attention lane
+            s = op_wait(c, sid, (int)(ch.id % c->ring_n));
+            if (s != KVS_OK) return s;
+            std::vector<int64_t> pg, sl;
+            for (size_t i = 0; i < ch.pages.size(); ++i) {
+                if (ch.pages[i] > last) continue;
+                pg.push_back(ch.pages[i]);
+                sl.push_back(c->ring_slot_id(ch.seq0 + i));
+            }
+            if (!pg.empty()) {
+                s = launch_items(c, layer, pg, sl, dp, KVS_TIME_RING, sid);
+                if (s != KVS_OK) return s;
+                c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
+            }
+            s = op_record(c, sid, (int)c->ring_n + (int)(ch.id % c->ring_n));
+            if (s != KVS_OK) return s;
+            c->attended = ch.id + 1;
+            c->st.ring_chunks++;
+            c->queue.pop_front();
             s = pump(c);
             if (s != KVS_OK) return s;
-            if (!ch.filled) return fail(c, KVS_ERR_COVERAGE, "ring chunk could not be scheduled");
         }
-        const int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes);  // this chunk's attention lane
-        s = op_wait(c, sid, (int)(ch.id % c->ring_n));
-        if (s != KVS_OK) return s;
-        std::vector<int64_t> pg, sl;
-        for (size_t i = 0; i < ch.pages.size(); ++i) {
-            if (ch.pages[i] > last) continue;
-            pg.push_back(ch.pages[i]);
-            sl.push_back(c->ring_slot_id(ch.seq0 + i));
-        }
-        if (!pg.empty()) {
-            s = launch_items(c, layer, pg, sl, dp, KVS_TIME_RING, sid);
-            if (s != KVS_OK) return s;
-            c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
-        }
-        s = op_record(c, sid, (int)c->ring_n + (int)(ch.id % c->ring_n));
-        if (s != KVS_OK) return s;
-        c->attended = ch.id + 1;
-        c->st.ring_chunks++;
-        c->queue.pop_front();
-        s = pump(c);
+        s = join_attn_lanes_into_attn(c);
         if (s != KVS_OK) return s;
     }
     c->announced.pop_front();
-    s = join_attn_lanes_into_attn(c);
-    if (s != KVS_OK) return s;
-    // final reduction over pages in logical order
+    // final reduction over splits in logical order
     c->st.kernel_launches++;
     if (c->plan_only) {
         log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 2, (int64_t)n_rows * n_q_head);
     } else {
         kvs::CombineParams cp;
-        cp.part_o = dp.part_o;
-        cp.part_ml = dp.part_ml;
+        cp.part_o = part_o;
+        cp.part_ml = part_ml;
         cp.out = out_dev;
         cp.lse = lse_dev;
         cp.R = (int)n_rows;
         cp.Hq = (int)n_q_head;
         cp.D = c->geom.D;
         cp.P = P;
+        cp.split_pages = prefill ? (int)c->prefill_split : 1;
         cp.pos0 = (long long)pos0;
         cudaError_t e = kvs::launch_combine(cp, c->attn);
         if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
@@ -1199,6 +1390,16 @@ kvs_status kvs_sync(kvs_ctx *c, uint32_t timeout_ms) {
         std::this_thread::sleep_for(std::chrono::microseconds(20));
     }
     harvest_timers(c);
+    if (c->check_status) {
+        c->check_status = false;
+        int status = 0;
+        cudaError_t e = cudaMemcpy(&status, c->cfg.workspace, sizeof(int), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(c, e, "status read");
+        if (status != 0) {
+            cudaMemset(c->cfg.workspace, 0, sizeof(int));
+            return fail(c, KVS_ERR_CUDA, "a bounded device-side wait in the prefill kernel timed out");
+        }
+    }
     return KVS_OK;
 }
 

@@ -64,6 +64,7 @@ class kvs_config(ctypes.Structure):
         ("n_lanes", ctypes.c_uint32),
         ("lane_attn_streams", ctypes.c_void_p * 3),
         ("lane_copy_streams", ctypes.c_void_p * 3),
+        ("prefill_split_pages", ctypes.c_uint32),
     ]
 
 
@@ -316,13 +317,15 @@ class KVStream:
 
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
                  max_tokens, ring_slots=8, chunk_pages=0, arena_slots=None, arena_bytes=None,
-                 plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None):
+                 plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None,
+                 prefill_split_pages=0):
         cfg = kvs_config()
         cfg.page_tokens, cfg.n_layers, cfg.n_kv_head, cfg.head_dim = page_tokens, n_layers, n_kv_head, head_dim
         cfg.max_q_head, cfg.max_rows, cfg.max_tokens = max_q_head, max_rows, max_tokens
         cfg.k_type, cfg.v_type = KVS_TYPE_Q8_0, KVS_TYPE_Q4_0
         cfg.ring_slots, cfg.chunk_pages = ring_slots, chunk_pages
         cfg.n_lanes = lanes
+        cfg.prefill_split_pages = prefill_split_pages
         self.page_bytes, host_bytes, arena_min, ws_bytes = kvs_query_sizes(cfg)
         self.max_pages = math.ceil(max_tokens / page_tokens)
         if arena_bytes is None:

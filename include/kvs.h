@@ -106,6 +106,8 @@ typedef struct {
                               (attn_stream, copy_stream) */
     void *lane_attn_streams[3];  /* cudaStream_t of attention lanes 1 .. n_lanes-1 */
     void *lane_copy_streams[3];  /* cudaStream_t of copy lanes 1 .. n_lanes-1 */
+    uint32_t prefill_split_pages; /* pages per split of the tensor-core prefill path (0 = 8,
+                                     at most ring_slots); ring chunks never cross a split */
 } kvs_config;
 
 typedef struct {
@@ -169,7 +171,8 @@ enum {
  *   page_bytes:      bytes of one page (all kv heads): Hk * P * D * 13 / 8
  *   host_bytes:      minimum host history bytes
  *   arena_bytes_min: minimum arena (2 tail slots per layer + ring_slots)
- *   workspace_bytes: minimum workspace (split partials for max_rows rows)
+ *   workspace_bytes: minimum workspace (a 256-byte status word, then split
+ *                    partials for max_rows rows)
  * Any output pointer may be NULL.  Page layout (one head section of
  * P*D*13/8 bytes per kv head, in kv-head order):
  *   Kq int8 [P][D] | Ks fp16 [P][D/32] | Vq u8 [D/2][P] | Vs fp16 [D/32][P]
@@ -268,7 +271,14 @@ kvs_status kvs_prefetch(kvs_ctx *ctx, uint32_t layer);
  * bitwise identical for any residency or ring size ("Keep the stock
  * attention order", V2 README).
  * Rows: 1 (decode) up to floor(64 / (Hq/Hk)) (span verify, e.g. 2..6 draft
- * rows with 6 query heads per kv head); larger n_rows -> KVS_ERR_UNSUPPORTED.
+ * rows with 6 query heads per kv head) run on the split-K kernel with one
+ * partial per page.  More rows (a prefill chunk, up to 256 rows) run on the
+ * tcgen05 tensor-core kernel with one partial per prefill split (a fixed
+ * group of prefill_split_pages pages, so the result is again independent of
+ * residency and ring size); that path needs q_dtype KVS_F16, head_dim 256 and
+ * page_tokens a multiple of 64 (KVS_ERR_UNSUPPORTED otherwise).  A timed-out
+ * device-side wait in that kernel is reported by the next kvs_sync as
+ * KVS_ERR_CUDA.
  */
 kvs_status kvs_attend(kvs_ctx *ctx, uint32_t layer, const void *q_dev, int32_t q_dtype,
                       uint32_t n_rows, uint32_t n_q_head, uint64_t pos0, float scale,

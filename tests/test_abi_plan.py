@@ -49,14 +49,14 @@ def test_query_sizes_formulas():
     assert pb == 4 * 256 * 256 * 13 // 8 == 425984  # 416 KiB per page
     assert hb == 4 * 128 * pb
     assert amin == (2 * 4 + 8) * pb
-    assert wmin == 128 * 24 * 6 * (256 + 2) * 4
+    assert wmin == 256 + 128 * 24 * 6 * (256 + 2) * 4  # status word + one partial per page
     pb2, *_ = kvs.kvs_query_sizes(_cfg(page_tokens=256, n_kv_head=2, head_dim=128, max_q_head=8))
     assert pb2 == 2 * 256 * 128 * 13 // 8 == 106496  # 104 KiB
 
 
 @pytest.mark.parametrize("kw", [dict(page_tokens=48), dict(head_dim=96), dict(k_type=kvs.KVS_TYPE_Q4_0),
-                                dict(v_type=kvs.KVS_TYPE_Q8_0), dict(max_q_head=6), dict(max_rows=11),
-                                dict(max_q_head=0)])
+                                dict(v_type=kvs.KVS_TYPE_Q8_0), dict(max_q_head=6), dict(max_rows=257),
+                                dict(max_q_head=0), dict(max_rows=11, head_dim=128), dict(max_rows=11, page_tokens=32)])
 def test_unsupported_configs_refused(kw):
     with pytest.raises(kvs.KVSError) as e:
         kvs.kvs_query_sizes(_cfg(**kw))
@@ -346,3 +346,29 @@ def test_page_boundary_append_with_pending_prefetch_keeps_plan():
     for l in range(2):
         reads = sorted(p for p, g in _reads_of_attend(ops, l))
         assert reads == list(range(7))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_prefill_scheduling_fences_and_split_coverage(seed):
+    """Prefill attends (more than 64 query rows per kv head) read every page of
+    every split once, with each split's ring chunks ready before its launch."""
+    rng = np.random.default_rng(100 + seed)
+    P, L, Hk, R = 64, 2, 1, 40
+    ring = int(rng.integers(4, 12))
+    split = int(rng.integers(1, ring + 1))
+    T0 = int(rng.integers(R + 1, 30 * P))
+    st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=256, max_q_head=6 * Hk, max_rows=R,
+                      max_tokens=T0 + R, ring_slots=ring, chunk_pages=int(rng.integers(1, ring + 1)),
+                      arena_slots=2 * L + ring + 64, plan_only=True, lanes=int(rng.integers(1, 4)),
+                      prefill_split_pages=split)
+    for l in range(L):
+        kvs.kvs_append(st.ctx, l, None, None, T0 + R)
+        st.set_residency(l, (rng.random(math.ceil((T0 + R) / P)) < 0.4).astype(np.uint8))
+    st.prefetch(0)
+    st.prefetch(1)
+    for l in range(L):
+        n0 = len(st.trace())
+        kvs.kvs_attend(st.ctx, l, None, kvs.KVS_F16, R, 6 * Hk, T0, 1.0, None, None)
+        reads = sorted(p for p, g in _reads_of_attend(st.trace()[n0:], l))
+        assert reads == list(range(math.ceil((T0 + R) / P)))
+    check_trace(st, 6 * Hk)

@@ -370,3 +370,43 @@ def test_step_graph_replay_matches_eager_bitwise():
     st.sync()
     assert np.array_equal(out.cpu().numpy(), eager[0])
     assert st.stats()["d2h_pages"] >= 2 * L
+
+
+# ------------------------------------------------------------ tensor-core prefill
+
+def _prefill_case(R, T, mask_fn=None, ring=8, chunk=2, lanes=1, split=8, seed=SEED):
+    import torch
+    P, Hk, G, D = 256, 4, 6, 256
+    Hq = G * Hk
+    st = kvs.KVStream(page_tokens=P, n_layers=1, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
+                      max_tokens=T, ring_slots=ring, chunk_pages=chunk, lanes=lanes,
+                      arena_slots=2 + ring + math.ceil(T / P), prefill_split_pages=split)
+    (k, v), = _fill(st, 1, T, Hk, D, seed=seed)
+    npages = math.ceil(T / P)
+    if mask_fn is not None:
+        st.set_residency(0, mask_fn(npages))
+    q = queries(seed, 0, R, Hq, D).astype(np.float16).astype(np.float32)  # the f16 values exactly
+    out, lse = attend(st, 0, q, T - R, 1 / 16, dtype=torch.float16)
+    return st, k, v, q, out, lse
+
+
+@pytest.mark.parametrize("R,T", [(256, 256 * 6 + 37), (256, 256 * 4), (100, 256 * 3 + 200), (11, 256 * 2 + 5)])
+def test_prefill_tensor_core_parity(R, T):
+    st, k, v, q, out, lse = _prefill_case(R, T, mask_fn=lambda n: np.ones(n, np.uint8))
+    ro, rl = oracle_ref(k, v, q, T - R, 1 / 16)
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] == 0
+
+
+def test_prefill_streamed_equals_resident_bitwise():
+    R, T = 256, 256 * 20 + 100
+    base = _prefill_case(R, T, mask_fn=lambda n: np.ones(n, np.uint8))
+    ro, rl = oracle_ref(base[1], base[2], base[3], T - R, 1 / 16)
+    check_parity(base[4], base[5], ro, rl)
+    rng = np.random.default_rng(3)
+    for ring, chunk, lanes in [(8, 2, 1), (8, 3, 2), (12, 4, 1)]:
+        st, _, _, _, out, lse = _prefill_case(
+            R, T, mask_fn=lambda n: (rng.random(n) < 0.5).astype(np.uint8), ring=ring, chunk=chunk, lanes=lanes)
+        assert st.stats()["h2d_pages"] > 0
+        assert np.array_equal(out, base[4]) and np.array_equal(lse, base[5]), (ring, chunk, lanes)
+        st.close()
