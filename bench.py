@@ -1,18 +1,27 @@
-"""Benchmark: streamed paged Q8_0-K / Q4_0-V decode attention on GB300.
+"""Benchmark: streamed paged Q8_0-K / Q4_0-V attention on one GB300.
 
-Workload (default, "decode32k"): a 64-layer decode step with one query row
-at context 32768, 24 query / 4 kv heads, head dim 256, 256-token pages, K as
+Default workload ("decode32k"): a 64-layer decode step with one query row at
+context 32768, 24 query / 4 kv heads, head dim 256, 256-token pages, K as
 Q8_0 and V as Q4_0 from seeded N(0,1) data; half of every layer's pages
 resident (62 seeded pages + the two tail pages), the other 64 streamed from
 host memory through an 8-slot ring with next-layer prefetch.  One step = for
-every layer: append the new row (quantise into the tail page, publish the
-completed page to host), announce the next layer, attend over all 32768 keys,
-truncate back so every step attends the same context.  The step is captured
-once as a CUDA graph (kvs_graph_*) and replayed.
+every layer: append the step's rows (quantise into the tail page, publish a
+completed page to host), announce the next layer, attend over the whole
+history, truncate back so every step sees the same context.  The step is
+captured once as a CUDA graph (kvs_graph_*) and replayed.
 
-Prints one JSON line.  ``--impl reference`` times the oracle (fp64 CPU) on the
-same workload instead.  Under torchrun each rank runs an independent replica
-(the path has no exchange between GPUs); rank 0 prints the aggregate.
+Other workloads (``--workload``): ``verify163k`` (6 causal rows at 163840,
+400 resident pages per layer), ``prefill131k`` (a 256-row fp16 prefill chunk
+at 131072 on the tensor-core path; ``--layers 1`` for the one-layer case and
+``--resident`` for its residency), ``long262k`` (1 or 4 rows at 262144 in a
+fixed 2048 MiB arena, ``--sweep`` over the resident fraction 0..100 % prints
+one line per point), ``resident131k`` (the attention kernel over resident
+pages only).
+
+Prints one JSON line per measured configuration.  ``--impl reference`` times
+the oracle (fp64, host cores) on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica (the path has no
+exchange between GPUs); rank 0 prints the aggregate.
 """
 from __future__ import annotations
 
@@ -34,21 +43,36 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 SEED, RES_SEED = 1234, 1235
+ARENA_PAGE_SLOTS_2GIB = (2048 << 20) // 425984  # 5041 page slots of 416 KiB
 
 WORKLOADS = {
     "decode32k": dict(
         desc=("decode stack: 64 layers x 1 row, context 32768, 24 q / 4 kv heads, D 256, page 256, "
               "Q8_0 K / Q4_0 V, 50% of pages resident (seeded), rest streamed via an 8-slot ring "
               "with next-layer prefetch (2-page chunks on 4 copy/attention lanes)"),
-        L=64, T=32768, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, lanes=4, resident_frac=0.5),
+        L=64, T=32768, R=1, ring=8, chunk=2, lanes=4, residency=("random", 0.5)),
     "decode32k_small": dict(  # a reduced copy for quick checks and profiling captures
         desc="decode stack, 8 layers, otherwise as decode32k",
-        L=8, T=32768, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, lanes=4, resident_frac=0.5),
+        L=8, T=32768, R=1, ring=8, chunk=2, lanes=4, residency=("random", 0.5)),
+    "verify163k": dict(
+        desc=("span verify: 6 causal rows at positions 163840..163845, 64 layers, 24 q / 4 kv heads, D 256, "
+              "page 256, Q8_0 K / Q4_0 V; 400 resident pages per layer (prefix), the rest via an 8-slot ring"),
+        L=64, T=163840 + 6, R=6, ring=8, chunk=2, lanes=4, residency=("prefix_pages", 400)),
+    "prefill131k": dict(
+        desc=("prefill chunk: 256 fp16 query rows appended at context 131072, causal, 24 q / 4 kv heads, D 256, "
+              "page 256, Q8_0 K / Q4_0 V, tcgen05 tensor-core path"),
+        L=64, T=131072 + 256, R=256, ring=8, chunk=2, lanes=2, residency=("prefix_frac", 1.0), q_f16=True),
+    "long262k": dict(
+        desc=("long-context decode: 64 layers, context 262144, 24 q / 4 kv heads, D 256, page 256, Q8_0 K / "
+              "Q4_0 V, fixed 2048 MiB arena split between resident pages (per-layer prefixes) and the ring"),
+        L=64, T=262144, R=1, ring=8, chunk=2, lanes=4, residency=("arena_frac", 0.5),
+        arena_slots=ARENA_PAGE_SLOTS_2GIB),
     "resident131k": dict(  # the attention kernel over resident pages, launches far larger than L2
         desc=("all-resident decode: 4 layers x 1 row, context 131072, 24 q / 4 kv heads, D 256, page 256, "
               "Q8_0 K / Q4_0 V, every page resident (218 MB of pages per layer)"),
-        L=4, T=131072, R=1, Hq=24, Hk=4, D=256, P=256, ring=8, chunk=2, resident_frac=1.0),
+        L=4, T=131072, R=1, ring=8, chunk=2, lanes=1, residency=("prefix_frac", 1.0)),
 }
+GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 
 
 def _rank_env():
@@ -59,18 +83,30 @@ def _measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
-    return 6800.0, "fallback 6.8 TB/s"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "measured (MEASURED_PEAKS.json)")
+    return 6800.0, 1900.0, 1700.0, "fallback (6.8 TB/s, 1.9 PFLOP/s)"
 
 
-def _resident_mask(wl, layer):
-    """Seeded residency: resident_frac of the pages, counting the two tail pages."""
+def _masks(wl, pool_pages=None):
+    """Per-layer residency masks (the two tail pages are device-readable besides)."""
     n = math.ceil(wl["T"] / wl["P"])
-    want = int(round(wl["resident_frac"] * n)) - 2
-    mask = np.zeros(n, np.uint8)
-    if want > 0:
-        mask[synth.choose(RES_SEED, synth.tag("resident", layer), n - 2, want)] = 1
-    return mask
+    kind, x = wl["residency"]
+    out = []
+    for layer in range(wl["L"]):
+        mask = np.zeros(n, np.uint8)
+        if kind == "random":  # x of all pages, counting the two tail pages
+            want = int(round(x * n)) - 2
+            if want > 0:
+                mask[synth.choose(RES_SEED, synth.tag("resident", layer), n - 2, want)] = 1
+        elif kind == "prefix_pages":
+            mask[:min(int(x), n)] = 1
+        elif kind == "prefix_frac":
+            mask[:int(round(x * n))] = 1
+        elif kind == "arena_frac":  # x of the arena's pool slots, spread evenly as prefixes
+            mask[:min(n, pool_pages // wl["L"])] = 1
+        out.append(mask)
+    return out
 
 
 class ClockSampler:
@@ -103,8 +139,9 @@ class ClockSampler:
         self.out.seek(0)
         rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
         os.unlink(self.out.name)
-        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        num = lambda t: t.strip().replace(".", "", 1).isdigit()  # noqa: E731
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and num(r[1])]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for r in rows:
@@ -137,15 +174,49 @@ def h2d_ceiling(torch, dev):
     return n / (best * 1e-3) / 1e9
 
 
-def oracle_layer_sample(wl, layer, k_hist, v_hist, k_new, v_new, q, threads=0):
-    """The oracle's decode of one layer: returns (seconds, o, lse)."""
+def alg_flops_per_layer(wl):
+    """QK^T and PV multiply-adds, 2 flops each, over the keys each row sees."""
+    T, R, Hq, D = wl["T"], wl["R"], wl["Hq"], wl["D"]
+    keys = sum(T - R + r + 1 for r in range(R))
+    return 4.0 * D * Hq * keys
+
+
+def oracle_sample(wl, k_hist, v_hist, k_new, v_new, q, rows=None, threads=0):
+    """The oracle on one layer (optionally a subset of its rows): (seconds, o, lse)."""
     import oracle
     k = np.concatenate([k_hist, k_new])
     v = np.concatenate([v_hist, v_new])
     qkv = oracle.QuantKV(k, v)
+    T, R = wl["T"], wl["R"]
+    rows = rows if rows is not None else list(range(R))
     t0 = time.perf_counter()
-    o, lse = qkv.attend(q, wl["T"] - 1, 1.0 / math.sqrt(wl["D"]), threads=threads)
-    return time.perf_counter() - t0, o, lse
+    outs = [qkv.attend(q[r:r + 1], T - R + r, 1.0 / math.sqrt(wl["D"]), threads=threads) for r in rows]
+    dt = time.perf_counter() - t0
+    return dt, np.concatenate([o for o, _ in outs]), np.concatenate([l for _, l in outs])
+
+
+def layer_inputs(wl, layer):
+    T, R, Hk, D = wl["T"], wl["R"], wl["Hk"], wl["D"]
+    k = synth.normal(SEED, synth.tag("K", layer), (T - R, Hk, D))
+    v = synth.normal(SEED, synth.tag("V", layer), (T - R, Hk, D))
+    return k, v
+
+
+def step_inputs(wl, layer):
+    R, Hq, Hk, D = wl["R"], wl["Hq"], wl["Hk"], wl["D"]
+    q = synth.normal(SEED, synth.tag("Q", layer), (R, Hq, D))
+    if wl.get("q_f16"):
+        q = q.astype(np.float16).astype(np.float32)
+    kn = synth.normal(SEED, synth.tag("Knew", layer), (R, Hk, D))
+    vn = synth.normal(SEED, synth.tag("Vnew", layer), (R, Hk, D))
+    return q, kn, vn
+
+
+def cpu_rows_sample(wl):
+    # rows of one layer the oracle baseline times: all rows for decode/verify,
+    # 8 rows spread over the chunk for prefill
+    R = wl["R"]
+    return list(range(R)) if R <= 8 else list(range(0, R, R // 8))[:8]
 
 
 def run_reference(args, wl):
@@ -154,27 +225,25 @@ def run_reference(args, wl):
     rank, world, _ = _rank_env()
     if rank != 0:
         return
-    T, Hk, D, Hq = wl["T"], wl["Hk"], wl["D"], wl["Hq"]
+    rows = cpu_rows_sample(wl)
     times = []
     for step in range(args.warmup + args.steps):
         layer = step % wl["L"]
-        k = synth.normal(SEED, synth.tag("K", layer), (T - 1, Hk, D))
-        v = synth.normal(SEED, synth.tag("V", layer), (T - 1, Hk, D))
-        kn = synth.normal(SEED, synth.tag("Knew", layer), (1, Hk, D))
-        vn = synth.normal(SEED, synth.tag("Vnew", layer), (1, Hk, D))
-        q = synth.normal(SEED, synth.tag("Q", layer), (1, Hq, D))
-        t, _, _ = oracle_layer_sample(wl, layer, k, v, kn, vn, q)
+        k, v = layer_inputs(wl, layer)
+        q, kn, vn = step_inputs(wl, layer)
+        t, _, _ = oracle_sample(wl, k, v, kn, vn, q, rows)
         if step >= args.warmup:
             times.append(t)
-    step_s = statistics.mean(times) * wl["L"]
+    step_s = statistics.mean(times) * wl["L"] * wl["R"] / len(rows)
     value = wl["R"] / step_s
     cores = oracle.threads()
-    sample = f"oracle fp64 decode of 1 of {wl['L']} layers per step (24 heads x {T} keys), time x {wl['L']}"
+    sample = (f"oracle fp64 attention of {len(rows)} of {wl['R']} rows of 1 of {wl['L']} layers per step "
+              f"({wl['Hq']} heads x {wl['T']} keys), time scaled to the whole step")
     line = {
         "impl": "reference", "metric": "streamed-attention tokens/s", "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl["desc"], "layers": wl["L"], "context": T},
+        "config": {"workload": wl["desc"], "layers": wl["L"], "context": wl["T"]},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -196,44 +265,50 @@ def run_ours(args, wl):
     kvs.load()
 
     L, T, R, Hq, Hk, D, P = (wl[k] for k in ("L", "T", "R", "Hq", "Hk", "D", "P"))
-    T0 = T - 1  # history before the step's appended row
+    T0 = T - R  # history before the step's appended rows
     npages = math.ceil(T / P)
-    masks = [_resident_mask(wl, l) for l in range(L)]
-    pool = int(sum(int(m.sum()) for m in masks))
-    st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=max(R, 1),
-                      max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"],
-                      arena_slots=2 * L + wl["ring"] + pool, device=dev, lanes=wl.get("lanes", 1))
-
+    fixed_arena = wl.get("arena_slots")
+    free = (fixed_arena - 2 * L) if fixed_arena else 0  # pool + ring slots of a fixed arena
+    masks0 = _masks(wl, pool_pages=(free - wl["ring"]) if fixed_arena else None)
+    pool = int(sum(int(m.sum()) for m in masks0))
+    arena_slots = fixed_arena if fixed_arena else 2 * L + wl["ring"] + pool
+    st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
+                      max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"], arena_slots=arena_slots,
+                      device=dev, lanes=wl.get("lanes", 1))
     ceiling = h2d_ceiling(torch, dev)
 
-    # history: seeded rows appended through the KV writer, then residency
-    keep = {}  # oracle sample layers
+    # history: seeded rows appended through the KV writer
+    rows_cpu = cpu_rows_sample(wl)
     n_cpu_layers = max(1, min(L, args.cpu_layers))
-    cpu_layers = list(range(0, L, max(1, L // n_cpu_layers)))[:n_cpu_layers] if rank == 0 else []
+    cpu_layers = list(range(0, L, max(1, L // n_cpu_layers)))[:n_cpu_layers] if (rank == 0 and not args.no_cpu) else []
+    keep = {}
+    t_prep = time.perf_counter()
     for l in range(L):
-        k = synth.normal(SEED, synth.tag("K", l), (T0, Hk, D))
-        v = synth.normal(SEED, synth.tag("V", l), (T0, Hk, D))
+        k, v = layer_inputs(wl, l)
         kt = torch.from_numpy(k).to(dev)
         vt = torch.from_numpy(v).to(dev)
         torch.cuda.synchronize(dev)
         st.append(l, kt, vt)
         st.sync()
         del kt, vt
-        st.set_residency(l, masks[l])
         if l in cpu_layers:
             keep[l] = (k, v)
-    st.sync()
+    prep_s = time.perf_counter() - t_prep
 
     # per-step inputs (device) and their pinned host copies for the e2e leg
-    q_h = torch.from_numpy(np.stack([synth.normal(SEED, synth.tag("Q", l), (R, Hq, D)) for l in range(L)])).pin_memory()
-    kn_h = torch.from_numpy(np.stack([synth.normal(SEED, synth.tag("Knew", l), (R, Hk, D)) for l in range(L)])).pin_memory()
-    vn_h = torch.from_numpy(np.stack([synth.normal(SEED, synth.tag("Vnew", l), (R, Hk, D)) for l in range(L)])).pin_memory()
+    qs, kns, vns = zip(*[step_inputs(wl, l) for l in range(L)])
+    qdt = torch.float16 if wl.get("q_f16") else torch.float32
+    q_h = torch.from_numpy(np.stack(qs)).to(qdt).pin_memory()
+    kn_h = torch.from_numpy(np.stack(kns)).pin_memory()
+    vn_h = torch.from_numpy(np.stack(vns)).pin_memory()
     q_d, kn_d, vn_d = q_h.to(dev), kn_h.to(dev), vn_h.to(dev)
     out_d = torch.empty((L, R, Hq, D), dtype=torch.float32, device=dev)
     lse_d = torch.empty((L, R, Hq), dtype=torch.float32, device=dev)
     out_h = torch.empty_like(out_d, device="cpu").pin_memory()
     torch.cuda.synchronize(dev)
     scale = 1.0 / math.sqrt(D)
+    q_type = kvs.KVS_F16 if wl.get("q_f16") else kvs.KVS_F32
+    prefill = R * Hq // Hk > 64
 
     def step():
         st.prefetch(0)
@@ -241,25 +316,8 @@ def run_ours(args, wl):
             kvs.kvs_append(st.ctx, l, kn_d[l], vn_d[l], R)
             if l + 1 < L:
                 st.prefetch(l + 1)
-            kvs.kvs_attend(st.ctx, l, q_d[l], kvs.KVS_F32, R, Hq, T - R, scale, out_d[l], lse_d[l])
+            kvs.kvs_attend(st.ctx, l, q_d[l], q_type, R, Hq, T0, scale, out_d[l], lse_d[l])
             st.truncate(l, T0)
-
-    # one eager step (host-issued), timed for context
-    st.sync()
-    t0 = time.perf_counter()
-    step()
-    st.sync()
-    eager_ms = (time.perf_counter() - t0) * 1e3
-    s_eager = st.stats(reset=True)
-
-    # capture the step once; replays re-execute every kernel and copy in it
-    st.set_timing(0)
-    st.graph_begin()
-    step()
-    st.graph_end()
-    gstats = st.stats(reset=True)
-    kernels_per_step = gstats["graph_kernels"]
-    h2d_bytes_step = gstats["h2d_bytes"]
 
     attn = st.attn_stream
 
@@ -289,96 +347,150 @@ def run_ours(args, wl):
             ms = float(t.item())
         return ms
 
-    for _ in range(args.warmup):
-        st.graph_launch()
-    st.sync()
-    clocks = ClockSampler(local)
-    clocks.start()
-    ms_step = timed(args.steps)
-    clk = clocks.stop()
-    st.sync()
-    out_ref = out_d.detach().cpu().numpy()
+    hbm_peak, tc_peak, _, peak_src = _measured_peaks()
+    fracs = [None]
+    if args.sweep and wl["residency"][0] == "arena_frac":
+        fracs = [i / 10 for i in range(11)]
+    for frac in fracs:
+        # residency (and, in a fixed arena, the ring gets every slot the pool does not)
+        if fixed_arena:
+            f = wl["residency"][1] if frac is None else frac
+            pool_slots = int(round(f * (free - 8)))
+            per_layer = min(npages, pool_slots // L)
+            ring = free - per_layer * L
+            masks = []
+            for _ in range(L):
+                m = np.zeros(npages, np.uint8)
+                m[:per_layer] = 1
+                masks.append(m)
+            for l in range(L):
+                st.set_residency(l, np.zeros(npages, np.uint8))
+            st.set_ring_slots(ring, wl["chunk"])
+        else:
+            masks = masks0
+            ring = wl["ring"]
+        for l in range(L):
+            st.set_residency(l, masks[l])
+        st.sync()
 
-    # e2e: the same step with host inputs copied in and outputs copied out
-    for _ in range(args.warmup):
-        st.graph_launch()
-    e2e_ms = timed(args.steps, e2e=True)
-    h2d_in = q_h.numel() * 4 + kn_h.numel() * 4 + vn_h.numel() * 4
-    d2h_out = out_h.numel() * 4
-
-    # roofline leg: host-issued steps with CUDA events around each resident-page
-    # attention launch (the HBM-bound part; the ring-chunk launches wait on
-    # copies), timed in their own region; graph-recorded events carry no timing
-    st.graph_destroy()
-    for _ in range(2):
+        # one eager (host-issued) step, timed for context
+        t0 = time.perf_counter()
         step()
-    st.sync()
-    st.stats(reset=True)
-    st.set_timing(kvs.KVS_TIME_RESIDENT)
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    n_eager = max(3, min(args.steps, 10))
-    for _ in range(n_eager):
+        st.sync()
+        eager_ms = (time.perf_counter() - t0) * 1e3
+        st.stats(reset=True)
+
+        # capture the step once; replays re-execute every kernel and copy in it
+        st.set_timing(0)
+        st.graph_begin()
         step()
-    st.sync()
-    ms_timed_eager = (time.perf_counter() - t0) * 1e3 / n_eager
-    st.set_timing(0)
-    rs = st.stats(reset=True)
-    r_ms, r_n, r_bytes = rs["decode_ms"], rs["decode_timed"], rs["decode_bytes"]
+        st.graph_end()
+        gstats = st.stats(reset=True)
+        kernels_per_step = gstats["graph_kernels"]
+        h2d_bytes_step = gstats["h2d_bytes"]
 
-    hbm_peak, peak_src = _measured_peaks()
-    achieved = (r_bytes / (r_ms * 1e-3) / 1e9) if r_ms > 0 else 0.0
+        for _ in range(args.warmup):
+            st.graph_launch()
+        st.sync()
+        clocks = ClockSampler(local)
+        clocks.start()
+        ms_step = timed(args.steps)
+        clk = clocks.stop()
+        st.sync()
+        out_ref = out_d.detach().cpu().numpy()
 
-    # CPU baseline (rank 0): the oracle on sampled layers, scaled to the step
-    cpu = None
-    parity = None
-    if rank == 0 and cpu_layers and not args.no_cpu:
-        import oracle
-        tsum, errs = 0.0, []
-        for l in cpu_layers:
-            k, v = keep[l]
-            t, o, lse = oracle_layer_sample(wl, l, k, v, kn_h[l].numpy(), vn_h[l].numpy(), q_h[l].numpy())
-            tsum += t
-            g = out_ref[l].astype(np.float64)
-            errs.append(float((np.abs(g - o).max(axis=-1) / np.abs(o).max(axis=-1)).max()))
-        step_s = tsum / len(cpu_layers) * L
-        cpu = {"value": R / step_s, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-               "sample": (f"oracle fp64 decode of {len(cpu_layers)} of the {L} layers of one step "
-                          f"({Hq} heads x {T} keys each), time scaled x {L}/{len(cpu_layers)}")}
-        parity = {"layers_checked": cpu_layers, "max_rel_err": max(errs), "tol": 1e-3}
+        for _ in range(args.warmup):
+            st.graph_launch()
+        e2e_ms = timed(args.steps, e2e=True)
+        h2d_in = q_h.numel() * q_h.element_size() + kn_h.numel() * 4 + vn_h.numel() * 4
+        d2h_out = out_h.numel() * 4
 
-    value = world * R / (ms_step * 1e-3)
-    kv_bytes_step = L * npages * st.page_bytes
-    line = {
-        "metric": "streamed-attention tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": wl["desc"], "layers": L, "context": T, "rows": R, "q_heads": Hq, "kv_heads": Hk,
-                   "head_dim": D, "page_tokens": P, "resident_fraction": wl["resident_frac"],
-                   "ring_slots": wl["ring"], "chunk_pages": wl["chunk"], "lanes": wl.get("lanes", 1),
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {kv_bytes_step / 1e9:.2f} GB of KV pages read per step",
-                   "step": "per layer: append row, prefetch next layer, attend, truncate; one CUDA graph replay"},
-        "kv_gbs": kv_bytes_step / (ms_step * 1e-3) / 1e9,
-        "h2d": {"achieved_gbs": h2d_bytes_step / (ms_step * 1e-3) / 1e9, "ceiling_gbs": ceiling,
-                "frac": h2d_bytes_step / (ms_step * 1e-3) / 1e9 / ceiling, "bytes_per_step": h2d_bytes_step,
-                "ceiling_how": "pinned cudaMemcpyAsync 1 GiB, best of 5"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
-                     "kernel": f"decode_kernel<{D},1> launches over resident + tail pages",
-                     "launches_timed": r_n, "bytes_per_launch": r_bytes / max(r_n, 1),
-                     "ms_per_launch": r_ms / max(r_n, 1), "peak_source": peak_src,
-                     "timed_region": f"{n_eager} host-issued steps ({ms_timed_eager:.2f} ms/step)"},
-        "cpu_baseline": cpu,
-        "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d_in,
-                "d2h_bytes_per_step": d2h_out},
-        "gpu_launches": kernels_per_step * args.steps,
-        "clocks": clk,
-        "eager_ms_per_step": eager_ms,
-        "parity": parity,
-    }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+        # roofline leg: host-issued steps with CUDA events around each attention
+        # launch over device-resident pages (for prefill, every launch), timed in
+        # their own region; graph-recorded events carry no timing
+        st.graph_destroy()
+        step()
+        st.sync()
+        st.stats(reset=True)
+        st.set_timing(kvs.KVS_TIME_RESIDENT | (kvs.KVS_TIME_RING if prefill else 0))
+        n_eager = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(n_eager):
+            step()
+        st.sync()
+        ms_timed_eager = (time.perf_counter() - t0) * 1e3 / n_eager
+        st.set_timing(0)
+        rs = st.stats(reset=True)
+        r_ms, r_n, r_bytes = rs["decode_ms"], rs["decode_timed"], rs["decode_bytes"]
+        if prefill:  # tensor-core prefill: algorithmic flops over the timed launches
+            flops_step = alg_flops_per_layer(wl) * L
+            achieved = flops_step * n_eager / (r_ms * 1e-3) / 1e12 if r_ms > 0 else 0.0
+            roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tc_peak, "traffic": None,
+                    "kernel": "prefill_kernel (tcgen05 kind::f16, M128 x N64/N256, TMEM accumulators)",
+                    "flops_per_step_algorithmic": flops_step, "launches_timed": r_n,
+                    "ms_per_launch": r_ms / max(r_n, 1),
+                    "peak_source": peak_src + " bf16 burst (f16 runs at the same rate)",
+                    "timed_region": f"{n_eager} host-issued steps ({ms_timed_eager:.2f} ms/step)"}
+        else:
+            achieved = (r_bytes / (r_ms * 1e-3) / 1e9) if r_ms > 0 else 0.0
+            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": None,
+                    "kernel": f"decode_kernel<{D},{math.ceil(R * Hq / Hk / 8)}> launches over resident + tail pages",
+                    "launches_timed": r_n, "bytes_per_launch": r_bytes / max(r_n, 1),
+                    "ms_per_launch": r_ms / max(r_n, 1), "peak_source": peak_src + " hbm_gbs",
+                    "timed_region": f"{n_eager} host-issued steps ({ms_timed_eager:.2f} ms/step)"}
+
+        # CPU baseline (rank 0): the oracle on sampled layers/rows, scaled to the step
+        cpu = parity = None
+        if rank == 0 and cpu_layers and frac in (None, fracs[0]):
+            import oracle
+            tsum, errs = 0.0, []
+            for l in cpu_layers:
+                k, v = keep[l]
+                t, o, lse = oracle_sample(wl, k, v, kn_h[l].numpy(), vn_h[l].numpy(),
+                                          q_h[l].float().numpy(), rows_cpu)
+                tsum += t
+                g = out_ref[l][rows_cpu].astype(np.float64)
+                errs.append(float((np.abs(g - o).max(axis=-1) / np.abs(o).max(axis=-1)).max()))
+            step_s = tsum / len(cpu_layers) * L * R / len(rows_cpu)
+            cpu = {"value": R / step_s, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                   "sample": (f"oracle fp64 attention of {len(rows_cpu)} of {R} rows on {len(cpu_layers)} of the "
+                              f"{L} layers of one step ({Hq} heads x {T} keys), time scaled to the whole step")}
+            parity = {"layers_checked": cpu_layers, "rows_checked": rows_cpu, "max_rel_err": max(errs), "tol": 1e-3}
+
+        value = world * R / (ms_step * 1e-3)
+        kv_bytes_step = L * npages * st.page_bytes
+        res_pages = int(sum(int(m.sum()) for m in masks))
+        line = {
+            "metric": "streamed-attention tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": wl["desc"], "layers": L, "context": T, "rows": R, "q_heads": Hq, "kv_heads": Hk,
+                       "head_dim": D, "page_tokens": P, "resident_pages_per_step": res_pages,
+                       "resident_fraction": res_pages / (L * npages), "ring_slots": ring,
+                       "chunk_pages": wl["chunk"], "lanes": wl.get("lanes", 1),
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {kv_bytes_step / 1e9:.2f} GB of KV pages read per step",
+                       "step": "per layer: append rows, prefetch next layer, attend, truncate; one CUDA graph replay"},
+            "kv_gbs": kv_bytes_step / (ms_step * 1e-3) / 1e9,
+            "h2d": {"achieved_gbs": h2d_bytes_step / (ms_step * 1e-3) / 1e9, "ceiling_gbs": ceiling,
+                    "frac": h2d_bytes_step / (ms_step * 1e-3) / 1e9 / ceiling, "bytes_per_step": h2d_bytes_step,
+                    "ceiling_how": "pinned cudaMemcpyAsync 1 GiB, best of 5"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d_in,
+                    "d2h_bytes_per_step": d2h_out},
+            "gpu_launches": kernels_per_step * args.steps,
+            "clocks": clk,
+            "eager_ms_per_step": eager_ms,
+            "parity": parity,
+            "prep_s": prep_s,
+        }
+        if prefill:
+            line["tflops"] = alg_flops_per_layer(wl) * L / (ms_step * 1e-3) / 1e12
+        if rank == 0:
+            print(json.dumps(line), flush=True)
     st.close()
     if dist:
         dist.destroy_process_group()
@@ -397,14 +509,27 @@ def main():
     ap.add_argument("--chunk", type=int, default=0, help="override the workload's pages per ring chunk")
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
     ap.add_argument("--lanes", type=int, default=0, help="override the workload's ring lanes")
+    ap.add_argument("--rows", type=int, default=0, help="override the workload's query rows")
+    ap.add_argument("--resident", type=float, default=-1.0,
+                    help="override the resident fraction (prefix of each layer; for long262k of the arena)")
+    ap.add_argument("--sweep", action="store_true", help="long262k: sweep the resident fraction 0..100%%")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(WORKLOADS[args.workload])
-    for key in ("ring", "chunk", "layers", "lanes"):
+    wl.update(GEOM)
+    for key, name in (("ring", "ring"), ("chunk", "chunk"), ("layers", "L"), ("lanes", "lanes")):
         v = getattr(args, key)
         if v:
-            wl["L" if key == "layers" else key] = v
+            wl[name] = v
             wl["desc"] += f" [{key} override: {v}]"
+    if args.rows:
+        wl["T"] = wl["T"] - wl["R"] + args.rows
+        wl["R"] = args.rows
+        wl["desc"] += f" [rows override: {args.rows}]"
+    if args.resident >= 0:
+        kind = "arena_frac" if wl["residency"][0] == "arena_frac" else "prefix_frac"
+        wl["residency"] = (kind, args.resident)
+        wl["desc"] += f" [resident override: {args.resident}]"
     if args.impl == "reference":
         run_reference(args, wl)
     else:

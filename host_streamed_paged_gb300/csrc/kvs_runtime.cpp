@@ -32,6 +32,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <climits>
 #include <chrono>
 #include <cmath>
 #include <deque>
@@ -91,6 +92,7 @@ struct kvs_ctx {
 
     int64_t max_pages = 0;
     int64_t prefill_split = 8;  // pages per tensor-core prefill split
+    bool split_chunks = false;  // ring chunks stop at prefill split boundaries (prefill-capable context)
     bool check_status = false;  // a kernel with bounded device waits ran since the last kvs_sync
     std::vector<LayerState> layers;
 
@@ -446,15 +448,17 @@ void plan_layer(kvs_ctx *c, uint32_t layer) {
         int64_t s;
         if (locate(c, layer, p, &s) == 0) streamed.push_back(p);
     }
-    // chunks of up to chunk_pages pages that never cross a prefill split
+    // chunks of up to chunk_pages pages; in a context that can run the prefill
+    // path they never cross a prefill split (that path attends split by split)
+    const int64_t align = c->split_chunks ? c->prefill_split : INT64_MAX;
     for (size_t i = 0; i < streamed.size();) {
         Chunk ch;
         ch.id = c->next_chunk++;
         ch.layer = layer;
         ch.seq0 = c->ring_seq;
-        const int64_t split = streamed[i] / c->prefill_split;
+        const int64_t split = streamed[i] / align;
         size_t n = 0;
-        while (i + n < streamed.size() && n < c->chunk_pages && streamed[i + n] / c->prefill_split == split) ++n;
+        while (i + n < streamed.size() && n < c->chunk_pages && streamed[i + n] / align == split) ++n;
         ch.pages.assign(streamed.begin() + i, streamed.begin() + i + n);
         c->ring_seq += n;
         i += n;
@@ -711,6 +715,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
     }
     c->max_pages = (int64_t)((cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens);
     c->prefill_split = (int64_t)prefill_split_of(cfg);
+    c->split_chunks = (uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head;
     c->layers.resize(cfg->n_layers);
     for (auto &L : c->layers) L.pool_slot.assign(c->max_pages, -1);
     c->n_slots = (int64_t)(cfg->arena_bytes / (uint64_t)c->geom.page_bytes);
@@ -1111,7 +1116,7 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
         }
     };
     auto launch = [&](const std::vector<int64_t> &ids, const std::vector<std::vector<int64_t>> &pgs,
-                      const std::vector<std::vector<int64_t>> &sls) -> kvs_status {
+                      const std::vector<std::vector<int64_t>> &sls, uint32_t kind) -> kvs_status {
         c->st.kernel_launches++;
         c->st.decode_launches++;
         if (c->plan_only) {
@@ -1135,10 +1140,13 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
             }
         }
         pp.split_begin[ids.size()] = it;
+        cudaEvent_t t0;
+        kvs_status ts = timed_begin(c, kind, &t0, kAttn);
+        if (ts != KVS_OK) return ts;
         cudaError_t e = kvs::launch_prefill(pp, c->attn);
         if (e != cudaSuccess) return cuda_fail(c, e, "prefill kernel launch");
         c->check_status = true;
-        return KVS_OK;
+        return timed_end(c, t0, (uint64_t)it * (uint64_t)c->geom.page_bytes, kAttn);
     };
 
     kvs_status s = pump(c);
@@ -1153,7 +1161,7 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
             split_pages(sidx, pg, sl);
             if (std::find(sl.begin(), sl.end(), (int64_t)-1) != sl.end()) continue;
             if ((int)ids.size() == kvs::kMaxPrefillSplits || items + (int)pg.size() > kvs::kMaxPrefillItems) {
-                s = launch(ids, pgs, sls);
+                s = launch(ids, pgs, sls, KVS_TIME_RESIDENT);
                 if (s != KVS_OK) return s;
                 ids.clear();
                 pgs.clear();
@@ -1167,7 +1175,7 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
             c->st.resident_pages_read += pg.size() * (uint64_t)c->geom.Hk;
         }
         if (!ids.empty()) {
-            s = launch(ids, pgs, sls);
+            s = launch(ids, pgs, sls, KVS_TIME_RESIDENT);
             if (s != KVS_OK) return s;
         }
     }
@@ -1196,7 +1204,7 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
                 for (size_t i = 0; i < ch->pages.size(); ++i)
                     for (size_t j = 0; j < pg.size(); ++j)
                         if (pg[j] == ch->pages[i]) sl[j] = c->ring_slot_id(ch->seq0 + i);
-            s = launch({sidx}, {pg}, {sl});
+            s = launch({sidx}, {pg}, {sl}, KVS_TIME_RING);
             if (s != KVS_OK) return s;
             c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
         }
