@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const QuantizeParams p) {
     const float d = __fdiv_rn(amax, 127.0f);
     const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
     const int qk = (int)roundf(__fmul_rn(x, id));
-    hb[(int64_t)t * D + b * 32 + lane] = (uint8_t)(int8_t)qk;
+    hb[kq_byte(t, b * 32 + lane, NB)] = (uint8_t)(int8_t)qk;
     if (lane == 0) reinterpret_cast<__half *>(hb + p.geom.ks_off)[(int64_t)t * NB + b] = __float2half_rn(d);
 
     // V -> Q4_0
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const QuantizeParams p) {
     int c = __float2int_rz(u);
     c = c > 15 ? 15 : (c < 0 ? 0 : c);
     const int chi = __shfl_down_sync(0xffffffffu, c, 16);
-    if (lane < 16) hb[p.geom.vq_off + (int64_t)(b * 16 + lane) * P + t] = (uint8_t)(c | (chi << 4));
+    if (lane < 16) hb[p.geom.vq_off + vq_byte(t, b * 16 + lane, NB)] = (uint8_t)(c | (chi << 4));
     if (lane == 0) reinterpret_cast<__half *>(hb + p.geom.vs_off)[(int64_t)b * P + t] = __float2half_rn(dv);
 }
 
@@ -69,11 +69,12 @@ __global__ void clear_tail_kernel(uint8_t *page, PageGeom g, int t0) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t off = i % g.head_bytes;
+        const int NB = g.D / 32;
         int64_t tok;
-        if (off < g.ks_off) tok = off / g.D;
-        else if (off < g.vq_off) tok = (off - g.ks_off) / (g.D / 16);
-        else if (off < g.vs_off) tok = (off - g.vq_off) % g.P;
-        else tok = ((off - g.vs_off) / 2) % g.P;
+        if (off < g.ks_off) tok = off / (NB * 512) * 16 + (off / 32) % 16;               // K lines
+        else if (off < g.vq_off) tok = (off - g.ks_off) / (g.D / 16);                     // K scales
+        else if (off < g.vs_off) tok = (off - g.vq_off) / (NB * 512) * 32 + (off - g.vq_off) % 32;  // V lines
+        else tok = ((off - g.vs_off) / 2) % g.P;                                          // V scales
         if (tok >= t0) page[i] = 0;
     }
 }

@@ -1,9 +1,9 @@
 // Split-K paged attention for 1..N query rows over a Q8_0-K / Q4_0-V page,
 // and the log-sum-exp combine of the per-page partials.
 //
-// One CTA = one (page, kv head) work item.  Every query head of the kv
-// head's group and every query row is served by that CTA, so each K/V byte
-// is read from memory once per step ("Q8_0 K and Q4_0 V are converted in
+// One work unit = one (page, kv head).  Every query head of the kv head's
+// group and every query row is served by the same unit, so each K/V byte is
+// read from memory once per step ("Q8_0 K and Q4_0 V are converted in
 // small tiles, not copied into another full FP16 cache", Adaptive KV
 // Streaming for llama.cpp V2, "Keep the stock attention order").
 //
@@ -25,14 +25,18 @@
 //   QK: thread (gid, tig) of a k-step in 32-dim block b holds dims
 //       32b + 8*tig + 4*s + {0..3} (s = k-step within the block), i.e. one
 //       32-bit word of an 8-byte load of the key row.
-//   PV: the page stores V dim-major (byte row = dim pair, column = token), a
+//   PV: the page stores V by byte row (= dim pair) with 32 tokens per line, a
 //       thread's word holds 4 consecutive keys of one dim pair; the four MMA
 //       k positions (2t, 2t+1, 2t+8, 2t+9) map to keys (+0, +2, +1, +3) and
 //       the MMA rows (gid, gid+8) to the low/high nibble dims of that byte.
 // The int8 -> f16 and nibble -> f16 conversions use the exponent-bias trick
 // described by Kim et al., "Who Says Elephants Can't Run: Bringing Large
 // Scale MoE Models into Cloud Scale Production" (2022): a small integer u
-// placed in the mantissa under exponent 0x64 is the half 1024 + u.
+// placed in the mantissa under exponent 0x64 is the half 1024 + u.  K codes
+// enter the MMA as 1152 + x (no subtraction); 1152 * sum(q) over each 32-dim
+// block is removed from the fp32 block dot afterwards (q has both signs, so the
+// offset costs well under 1e-5 relative).  High V nibbles are taken in
+// mantissa bits 4-7 as 16 * (code - 8) and their output rows scaled by 1/16.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -52,28 +56,33 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 4 int8 (bytes x0..x3 of w) -> f16x2 (x0, x1) and (x2, x3), exact.
-__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t u = w ^ 0x80808080u;  // x + 128 as unsigned bytes
-    uint32_t t0, t1;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(t0) : "r"(u), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(t1) : "r"(u), "r"(0x64646464u));
-    const uint32_t bias = 0x64806480u;  // half2(1152, 1152)
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(t0), "r"(bias));
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(t1), "r"(bias));
+// 4 int8 (bytes x0..x3 of w) -> f16x2 (1152 + x0, 1152 + x1) and (1152 + x2,
+// 1152 + x3), exact; the 1152 offset is taken out after the MMA (see below).
+__device__ __forceinline__ void i8x4_to_f16_biased(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
 }
 
-// 4 packed bytes (keys k0..k3, byte = lo | hi << 4) -> A fragment of (code - 8):
-// a0 = (lo k0, lo k2), a1 = (hi k0, hi k2), a2 = (lo k1, lo k3), a3 = (hi k1, hi k3).
-__device__ __forceinline__ void u4x8_to_frag(uint32_t w, uint32_t (&a)[4]) {
-    const uint32_t magic = 0x64006400u, mask = 0x000f000fu, bias = 0x64086408u;  // 1032
-    uint32_t t[4];
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t[0]) : "r"(w), "r"(mask), "r"(magic));
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t[1]) : "r"(w >> 4), "r"(mask), "r"(magic));
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t[2]) : "r"(w >> 8), "r"(mask), "r"(magic));
-    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t[3]) : "r"(w >> 12), "r"(mask), "r"(magic));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) asm("sub.f16x2 %0, %1, %2;" : "=r"(a[i]) : "r"(t[i]), "r"(bias));
+// 4 packed bytes (keys k0..k3, byte = lo | hi << 4) -> A fragment:
+// a0 = (lo k0, lo k2) - 8, a2 = (lo k1, lo k3) - 8 and, for the high nibbles,
+// a1 = 16 * ((hi k0, hi k2) - 8), a3 = 16 * ((hi k1, hi k3) - 8): the nibble
+// stays in mantissa bits 4-7, so the MMA rows it feeds come out 16 times too
+// large and are scaled by 1/16 (exactly) at the end.
+__device__ __forceinline__ void u4x8_to_frag16(uint32_t w, uint32_t (&a)[4]) {
+    const uint32_t magic = 0x64006400u, lo = 0x000f000fu, hi = 0x00f000f0u;
+    const uint32_t bias_lo = 0x64086408u;  // 1032 = 1024 + 8
+    const uint32_t bias_hi = 0x64806480u;  // 1152 = 1024 + 16 * 8
+    const uint32_t w8 = w >> 8;
+    uint32_t t0, t1, t2, t3;
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t0) : "r"(w), "r"(lo), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t1) : "r"(w), "r"(hi), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t2) : "r"(w8), "r"(lo), "r"(magic));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(t3) : "r"(w8), "r"(hi), "r"(magic));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(a[0]) : "r"(t0), "r"(bias_lo));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(a[1]) : "r"(t1), "r"(bias_hi));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(a[2]) : "r"(t2), "r"(bias_lo));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(a[3]) : "r"(t3), "r"(bias_hi));
 }
 
 // (x, y) fp32 -> f16x2 hi = rn(x, y), lo = rn(x - hi, y - hi).
@@ -85,248 +94,282 @@ __device__ __forceinline__ void split_f16(float x, float y, uint32_t &hi, uint32
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-__device__ __forceinline__ uint2 ldg_nc_u2(const void *p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(v.x), "=r"(v.y)
-                 : "l"(p));
-    return v;
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+// bounded wait for phase `parity` of an mbarrier; false on timeout
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
 }
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem));
+// one page-head section (global, contiguous) -> shared stage, completion on `bar`
+__device__ __forceinline__ void stage_load(uint32_t dst, const uint8_t *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    // in pieces of at most 64 KiB
+    for (uint32_t off = 0; off < bytes; off += 65536u) {
+        const uint32_t n = (bytes - off) < 65536u ? (bytes - off) : 65536u;
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         dst + off),
+                     "l"(src + off), "r"(n), "r"(bar)
+                     : "memory");
+    }
 }
 
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
-
-// Shared-memory carve of decode_kernel<D, NT> for page size P (bytes).
+// Shared-memory carve of decode_kernel<D, NT> (bytes; page size P, S stages).
 struct DecodeSmem {
-    int qf, sc, rmax, rsum, sv, svs, red, total;
+    int stage, sc, rmax, rsum, red, obuf, bar, total, stages;
 };
-__host__ __device__ inline int align16(int x) { return (x + 15) & ~15; }
-__host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int P) {
+__host__ __device__ inline int align_to(int x, int a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int P, int stages) {
     DecodeSmem s;
     const int MR = NT * 8, SP = P + 4, NB = D / 32;
     int parts = 8 / NB;
     if (parts > P / 32) parts = P / 32;
-    s.qf = 0;
-    s.sc = align16(s.qf + NT * (D / 16) * 32 * 16);
-    s.rmax = align16(s.sc + MR * SP * 4);
-    s.rsum = align16(s.rmax + MR * 4);
-    s.sv = align16(s.rsum + MR * 4);
-    s.svs = align16(s.sv + (D / 2) * (P + 32));
-    s.red = align16(s.svs + (D / 32) * P * 2);
-    s.total = align16(s.red + (parts - 1) * MR * D * 4);
+    const int head = P * D * 13 / 8;
+    s.stages = stages;
+    s.stage = 0;
+    s.sc = align_to(stages * head, 128);
+    s.rmax = align_to(s.sc + MR * SP * 4, 16);
+    s.rsum = align_to(s.rmax + MR * 4, 16);
+    s.red = align_to(s.rsum + MR * 4, 16);
+    const int red_end = s.red + (parts - 1) * MR * D * 4;
+    // the output tile reuses the score buffer when it fits there
+    s.obuf = (SP >= D) ? s.sc : align_to(red_end, 16);
+    const int obuf_end = (SP >= D) ? red_end : s.obuf + MR * D * 4;
+    s.bar = align_to(red_end > obuf_end ? red_end : obuf_end, 16);
+    s.total = s.bar + 16 * stages;
     return s;
 }
 
+// Persistent split-K attention over (page, kv head) units.  Units are ordered
+// head-major; CTA c takes units [c*U/C, (c+1)*U/C), so it rebuilds its Q
+// fragments only when the kv head changes.  Page-head sections stream into
+// `stages` shared-memory stages by bulk asynchronous copies: while the warps
+// work on one unit the next one is already on its way.
 template <int D, int NT>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NB = D / 32;  // 32-dim scale blocks
     constexpr int KS = D / 16;  // QK k-steps
     constexpr int MR = NT * 8;  // MMA rows (query rows x heads, padded to 8)
     const int P = p.geom.P;
-    const int SP = P + 4;   // score row stride, floats
-    const int SVS = P + 32;  // V nibble row stride in shared memory, bytes
-    const DecodeSmem L = decode_smem(D, NT, P);
-    uint4 *qf = reinterpret_cast<uint4 *>(smem + L.qf);
+    const int SP = P + 4;  // score row stride, floats
+    const DecodeSmem L = decode_smem(D, NT, P, p.stages);
     float *sc = reinterpret_cast<float *>(smem + L.sc);
     float *rmax = reinterpret_cast<float *>(smem + L.rmax);
     float *rsum = reinterpret_cast<float *>(smem + L.rsum);
-    uint8_t *sv = smem + L.sv;
-    __half *svs = reinterpret_cast<__half *>(smem + L.svs);
     float *red = reinterpret_cast<float *>(smem + L.red);
+    float *obuf = reinterpret_cast<float *>(smem + L.obuf);
+    const uint32_t bar0 = smem_u32(smem + L.bar);
+    const int head_bytes = (int)p.geom.head_bytes;
 
-    const int item = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    const uint32_t page = p.page[item];
-    const uint8_t *hb =
-        p.arena + (int64_t)p.slot[item] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
     const int G = p.G, R = p.R, rows = G * R;
+    const int U = p.n_items * p.geom.Hk;
+    const int u0 = (int)((int64_t)blockIdx.x * U / gridDim.x), u1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
+    if (u0 >= u1) return;
+    const int S = L.stages;
 
-    // Stage the V section (nibbles + scales) into shared memory asynchronously.
-    {
-        const uint8_t *gvq = hb + p.geom.vq_off;
-        const int cpr = P / 16;  // 16-byte chunks per nibble row
-        for (int c = threadIdx.x; c < (D / 2) * cpr; c += kThreads) {
-            const int row = c / cpr, col = c - row * cpr;
-            cp_async16(sv + row * SVS + col * 16, gvq + (int64_t)row * P + col * 16);
-        }
-        const uint8_t *gvs = hb + p.geom.vs_off;
-        for (int c = threadIdx.x; c < (D / 32) * P * 2 / 16; c += kThreads)
-            cp_async16(reinterpret_cast<uint8_t *>(svs) + c * 16, gvs + c * 16);
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    }
-
-    // Q fragments: qf[nt][ks][lane] = {b0_hi, b1_hi, b0_lo, b1_lo}.
-    for (int e = threadIdx.x; e < NT * KS * 32; e += kThreads) {
-        const int ln = e & 31, ks = (e >> 5) % KS, nt = e / (KS * 32);
-        const int m = nt * 8 + (ln >> 2);
-        const int d0 = 32 * (ks >> 1) + 8 * (ln & 3) + 4 * (ks & 1);
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m < rows) {
-            const int r = m / G, h = g * G + (m - r * G);
-            const int64_t off = ((int64_t)r * p.Hq + h) * D + d0;
-            if (p.q_f16) {
-                const __half *q = reinterpret_cast<const __half *>(p.q) + off;
-                const uint2 raw = *reinterpret_cast<const uint2 *>(q);
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-                x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-            } else {
-                const float4 v = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.q) + off);
-                x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-            }
-        }
-        uint32_t h0, l0, h1, l1;
-        split_f16(x[0], x[1], h0, l0);
-        split_f16(x[2], x[3], h1, l1);
-        qf[e] = make_uint4(h0, h1, l0, l1);
+    auto src_of = [&](int u) {
+        const int g = u / p.n_items, item = u - g * p.n_items;
+        return p.arena + (int64_t)p.slot[item] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
+    };
+    bool pending[2] = {false, false};      // a load into this stage is not consumed yet
+    uint32_t pend_parity[2] = {0u, 0u};    // the phase that load completes
+    for (int s = 0; s < S && u0 + s < u1; ++s) pending[s] = true;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 16 * s));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int s = 0; s < S && u0 + s < u1; ++s)
+            stage_load(smem_u32(smem + L.stage + s * head_bytes), src_of(u0 + s), (uint32_t)head_bytes, bar0 + 16 * s);
     }
     __syncthreads();
 
-    // Scores: warp w owns keys [32w, 32w + 32) as two 16-key MMA row tiles.
-    const long long kpos0 = (long long)page * P;
-    if (warp < P / 32) {
+    bool ok = true;
+    for (int u = u0, i = 0; u < u1; ++u, ++i) {
+        const int stage = i % S;
+        const uint32_t parity = (uint32_t)((i / S) & 1);
+        const int g = u / p.n_items, item = u - g * p.n_items;
+        const uint32_t page = p.page[item];
+        const uint8_t *hs = smem + L.stage + stage * head_bytes;  // this unit's page-head section
+
+        // Q fragments of kv head g (built by qprep_kernel): qf[nt][ks][lane] and
+        // qs[m][b] = sum over 32-dim block b of q as the MMA sees it (hi + lo)
+        const uint4 *qf = p.qf + (int64_t)g * NT * KS * 32;
+        const float *qs = p.qs + (int64_t)g * MR * NB;
+        if (!mbar_wait(bar0 + 16 * stage, parity)) ok = false;
+        if (!__syncthreads_and(ok)) break;
+        pending[stage] = false;
+
+        // Scores: warp w owns keys [32w, 32w + 32) as two 16-key MMA row tiles.
+        const long long kpos0 = (long long)page * P;
+        if (warp < P / 32) {
 #pragma unroll 1
-        for (int mt = 0; mt < 2; ++mt) {
-            const int k0 = warp * 32 + mt * 16 + gid, k1 = k0 + 8;
-            const uint8_t *kr0 = hb + (int64_t)k0 * D + 8 * tig;
-            const uint8_t *kr1 = hb + (int64_t)k1 * D + 8 * tig;
-            const __half *ks0 = reinterpret_cast<const __half *>(hb + p.geom.ks_off) + k0 * NB;
-            const __half *ks1 = reinterpret_cast<const __half *>(hb + p.geom.ks_off) + k1 * NB;
-            uint2 kv0[NB], kv1[NB];
+            for (int mt = 0; mt < 2; ++mt) {
+                const int kg = 2 * warp + mt;  // 16-key group
+                const int k0 = 16 * kg + gid, k1 = k0 + 8;
+                const __half *ksc = reinterpret_cast<const __half *>(hs + p.geom.ks_off);
+                float S_[NT][4];
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                kv0[b] = ldg_nc_u2(kr0 + 32 * b);
-                kv1[b] = ldg_nc_u2(kr1 + 32 * b);
-            }
-            float sk0[NB], sk1[NB];
+                for (int nt = 0; nt < NT; ++nt) S_[nt][0] = S_[nt][1] = S_[nt][2] = S_[nt][3] = 0.f;
+#pragma unroll(NT <= 2 ? NB : 1)
+                for (int b = 0; b < NB; ++b) {
+                    const uint8_t *line = hs + ((kg * NB + b) * 16) * 32 + 8 * tig;
+                    const uint2 kv0 = *reinterpret_cast<const uint2 *>(line + gid * 32);
+                    const uint2 kv1 = *reinterpret_cast<const uint2 *>(line + (gid + 8) * 32);
+                    const float sk0 = __half2float(ksc[k0 * NB + b]), sk1 = __half2float(ksc[k1 * NB + b]);
+                    float cb[NT][4];
 #pragma unroll
-            for (int b = 0; b < NB; b += 2) {
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(ks0 + b));
-                const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(ks1 + b));
-                sk0[b] = a.x; sk0[b + 1] = a.y;
-                sk1[b] = c.x; sk1[b + 1] = c.y;
-            }
-            float S[NT][4];
+                    for (int nt = 0; nt < NT; ++nt) cb[nt][0] = cb[nt][1] = cb[nt][2] = cb[nt][3] = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
+                    for (int s = 0; s < 2; ++s) {
+                        uint32_t a[4];
+                        i8x4_to_f16_biased(s ? kv0.y : kv0.x, a[0], a[2]);
+                        i8x4_to_f16_biased(s ? kv1.y : kv1.x, a[1], a[3]);
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                float cb[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) cb[nt][0] = cb[nt][1] = cb[nt][2] = cb[nt][3] = 0.f;
-#pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    uint32_t a[4];
-                    i8x4_to_f16(s ? kv0[b].y : kv0[b].x, a[0], a[2]);
-                    i8x4_to_f16(s ? kv1[b].y : kv1[b].x, a[1], a[3]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint4 qv = qf[(nt * KS + 2 * b + s) * 32 + lane];
+                            mma16816(cb[nt], a, qv.x, qv.y);
+                            mma16816(cb[nt], a, qv.z, qv.w);
+                        }
+                    }
+                    // the A operand carried 1152 + x: take 1152 * sum(q) of the block back out
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const uint4 qv = qf[(nt * KS + 2 * b + s) * 32 + lane];
-                        mma16816(cb[nt], a, qv.x, qv.y);
-                        mma16816(cb[nt], a, qv.z, qv.w);
+                        const float q0 = qs[(nt * 8 + 2 * tig) * NB + b];
+                        const float q1 = qs[(nt * 8 + 2 * tig + 1) * NB + b];
+                        const float c0 = fmaf(-1152.f, q0, cb[nt][0]), c1 = fmaf(-1152.f, q1, cb[nt][1]);
+                        const float c2 = fmaf(-1152.f, q0, cb[nt][2]), c3 = fmaf(-1152.f, q1, cb[nt][3]);
+                        S_[nt][0] = fmaf(c0, sk0, S_[nt][0]);
+                        S_[nt][1] = fmaf(c1, sk0, S_[nt][1]);
+                        S_[nt][2] = fmaf(c2, sk1, S_[nt][2]);
+                        S_[nt][3] = fmaf(c3, sk1, S_[nt][3]);
                     }
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    S[nt][0] += cb[nt][0] * sk0[b];
-                    S[nt][1] += cb[nt][1] * sk0[b];
-                    S[nt][2] += cb[nt][2] * sk1[b];
-                    S[nt][3] += cb[nt][3] * sk1[b];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = (e < 2) ? k0 : k1;
+                        const int m = nt * 8 + 2 * tig + (e & 1);
+                        const bool valid = m < rows && kpos0 + key <= p.pos0 + m / G;
+                        sc[m * SP + key] = valid ? S_[nt][e] * p.scale_log2 : -INFINITY;
+                    }
                 }
             }
+        }
+        __syncthreads();
+
+        // Softmax over the page's keys, one row per warp at a time.
+        const int split = (int)page;
+        for (int m = warp; m < MR; m += 8) {
+            float mx = -INFINITY;
+            for (int k = lane; k < P; k += 32) mx = fmaxf(mx, sc[m * SP + k]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float sum = 0.f;
+            if (mx == -INFINITY) {
+                for (int k = lane; k < P; k += 32) sc[m * SP + k] = 0.f;
+            } else {
+                for (int k = lane; k < P; k += 32) {
+                    const float e = exp2f(sc[m * SP + k] - mx);
+                    sc[m * SP + k] = e;
+                    sum += e;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            }
+            if (lane == 0) {
+                rmax[m] = mx;
+                rsum[m] = sum;
+                if (m < rows) {
+                    const int r = m / G, h = g * G + (m - r * G);
+                    float *ml = p.part_ml + (((int64_t)split * p.Hq + h) * R + r) * 2;
+                    ml[0] = mx;
+                    ml[1] = sum;
+                }
+            }
+        }
+        __syncthreads();
+
+        // O^T = V^T P'^T: warp -> (32-dim block b, key part).
+        int parts = 8 / NB;
+        if (parts > P / 32) parts = P / 32;
+        const int b = warp % NB, part = warp / NB;
+        // P' hi and P' lo parts on two independent MMA chains when registers allow
+        constexpr int NL = NT <= 2 ? NT : 1;
+        float acc[2][NT][4], accl[2][NL][4];
+#pragma unroll
+        for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i2][nt][e] = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+            for (int nt = 0; nt < NL; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) accl[i2][nt][e] = 0.f;
+        if (part < parts) {
+            const int kspan = P / parts;
+            const __half *vsc = reinterpret_cast<const __half *>(hs + p.geom.vs_off);
+#pragma unroll 1
+            for (int kb = part * kspan; kb < (part + 1) * kspan; kb += 32) {
+                const uint8_t *vl = hs + p.geom.vq_off + ((kb / 32 * NB + b) * 16) * 32 + 8 * tig;
+                const uint2 v0 = *reinterpret_cast<const uint2 *>(vl + gid * 32);
+                const uint2 v1 = *reinterpret_cast<const uint2 *>(vl + (gid + 8) * 32);
+                const uint4 dvr = *reinterpret_cast<const uint4 *>(vsc + b * P + kb + 8 * tig);
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    uint32_t a0[4], a1[4];
+                    u4x8_to_frag16(s ? v0.y : v0.x, a0);
+                    u4x8_to_frag16(s ? v1.y : v1.x, a1);
+                    const float2 dA = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.z : &dvr.x));
+                    const float2 dB = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.w : &dvr.y));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
+                        uint32_t bh0, bl0, bh1, bl1;
+                        split_f16(pv.x * dA.x, pv.z * dB.x, bh0, bl0);  // keys +0, +2
+                        split_f16(pv.y * dA.y, pv.w * dB.y, bh1, bl1);  // keys +1, +3
+                        mma16816(acc[0][nt], a0, bh0, bh1);
+                        mma16816(acc[1][nt], a1, bh0, bh1);
+                        if constexpr (NT <= 2) {
+                            mma16816(accl[0][nt], a0, bl0, bl1);
+                            mma16816(accl[1][nt], a1, bl0, bl1);
+                        } else {
+                            mma16816(acc[0][nt], a0, bl0, bl1);
+                            mma16816(acc[1][nt], a1, bl0, bl1);
+                        }
+                    }
+                }
+            }
+        }
+        // merge the chains; rows gid + 8 (high-nibble dims) carried 16 * (code - 8)
+#pragma unroll
+        for (int i2 = 0; i2 < 2; ++i2)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
+                if constexpr (NT <= 2) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = (e < 2) ? k0 : k1;
-                    const int m = nt * 8 + 2 * tig + (e & 1);
-                    const bool ok = m < rows && kpos0 + key <= p.pos0 + m / G;
-                    sc[m * SP + key] = ok ? S[nt][e] * p.scale_log2 : -INFINITY;
+                    for (int e = 0; e < 4; ++e) acc[i2][nt][e] += accl[i2][nt < NL ? nt : 0][e];
                 }
+                acc[i2][nt][2] *= 0.0625f;
+                acc[i2][nt][3] *= 0.0625f;
             }
-        }
-    }
-    __syncthreads();
-
-    // Softmax over the page's keys, one row per warp at a time.
-    const int split = (int)page;
-    for (int m = warp; m < MR; m += 8) {
-        float mx = -INFINITY;
-        for (int k = lane; k < P; k += 32) mx = fmaxf(mx, sc[m * SP + k]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float sum = 0.f;
-        if (mx == -INFINITY) {
-            for (int k = lane; k < P; k += 32) sc[m * SP + k] = 0.f;
-        } else {
-            for (int k = lane; k < P; k += 32) {
-                const float e = exp2f(sc[m * SP + k] - mx);
-                sc[m * SP + k] = e;
-                sum += e;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        }
-        if (lane == 0) {
-            rmax[m] = mx;
-            rsum[m] = sum;
-            if (m < rows) {
-                const int r = m / G, h = g * G + (m - r * G);
-                float *ml = p.part_ml + (((int64_t)split * p.Hq + h) * R + r) * 2;
-                ml[0] = mx;
-                ml[1] = sum;
-            }
-        }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-
-    // O^T = V^T P'^T: warp -> (32-dim block b, key part).
-    int parts = 8 / NB;
-    if (parts > P / 32) parts = P / 32;
-    const int b = warp % NB, part = warp / NB;
-    float acc[2][NT][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc[i][nt][0] = acc[i][nt][1] = acc[i][nt][2] = acc[i][nt][3] = 0.f;
-    if (part < parts) {
-        const int kspan = P / parts;
-#pragma unroll 1
-        for (int kb = part * kspan; kb < (part + 1) * kspan; kb += 32) {
-            const uint2 v0 = *reinterpret_cast<const uint2 *>(sv + (b * 16 + gid) * SVS + kb + 8 * tig);
-            const uint2 v1 = *reinterpret_cast<const uint2 *>(sv + (b * 16 + 8 + gid) * SVS + kb + 8 * tig);
-            const uint4 dvr = *reinterpret_cast<const uint4 *>(svs + b * P + kb + 8 * tig);
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                uint32_t a0[4], a1[4];
-                u4x8_to_frag(s ? v0.y : v0.x, a0);
-                u4x8_to_frag(s ? v1.y : v1.x, a1);
-                const float2 dA = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.z : &dvr.x));
-                const float2 dB = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.w : &dvr.y));
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float4 pv = *reinterpret_cast<const float4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
-                    uint32_t bh0, bl0, bh1, bl1;
-                    split_f16(pv.x * dA.x, pv.z * dB.x, bh0, bl0);  // keys +0, +2
-                    split_f16(pv.y * dA.y, pv.w * dB.y, bh1, bl1);  // keys +1, +3
-                    mma16816(acc[0][nt], a0, bh0, bh1);
-                    mma16816(acc[0][nt], a0, bl0, bl1);
-                    mma16816(acc[1][nt], a1, bh0, bh1);
-                    mma16816(acc[1][nt], a1, bl0, bl1);
-                }
-            }
-        }
-    }
-    if (parts > 1) {
-        if (part >= 1 && part < parts) {
+        if (parts > 1 && part >= 1 && part < parts) {
             float *dst = red + (part - 1) * MR * D;
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
@@ -339,7 +382,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                         dst[m * D + dim] = acc[mt][nt][e];
                     }
         }
-        __syncthreads();
+        __syncthreads();  // every read of this stage (and of sc) is done
+        if (u + S < u1) {
+            pending[stage] = true;
+            pend_parity[stage] = parity ^ 1u;
+            if (threadIdx.x == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                stage_load(smem_u32(smem + L.stage + stage * head_bytes), src_of(u + S), (uint32_t)head_bytes,
+                           bar0 + 16 * stage);
+            }
+        }
         if (part == 0) {
             for (int q = 1; q < parts; ++q) {
                 const float *src = red + (q - 1) * MR * D;
@@ -354,36 +406,124 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
                             acc[mt][nt][e] += src[m * D + dim];
                         }
             }
-        }
-    }
-    if (part == 0) {
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int m = nt * 8 + 2 * tig + (e & 1);
-                    if (m < rows) {
+                    for (int e = 0; e < 4; ++e) {
                         const int dim = 32 * b + mt * 8 + gid + ((e >= 2) ? 16 : 0);
-                        const int r = m / G, h = g * G + (m - r * G);
-                        p.part_o[(((int64_t)split * p.Hq + h) * R + r) * D + dim] = acc[mt][nt][e];
+                        const int m = nt * 8 + 2 * tig + (e & 1);
+                        obuf[m * D + dim] = acc[mt][nt][e];
                     }
-                }
+        }
+        __syncthreads();
+        // coalesced partial store of the valid rows
+        for (int c = threadIdx.x; c < rows * (D / 4); c += kThreads) {
+            const int m = c / (D / 4), d4 = (c % (D / 4)) * 4;
+            const int r = m / G, h = g * G + (m - r * G);
+            *reinterpret_cast<float4 *>(p.part_o + (((int64_t)split * p.Hq + h) * R + r) * D + d4) =
+                *reinterpret_cast<const float4 *>(obuf + m * D + d4);
+        }
+        __syncthreads();  // obuf / sc free for the next unit
+    }
+    if (!ok) {
+        // a wait gave up: before the CTA exits, wait (bounded again) for every
+        // stage load still in flight, so no copy lands in reassigned memory
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < S; ++s)
+                if (pending[s]) mbar_wait(bar0 + 16 * s, pend_parity[s]);
+            atomicExch(p.status, 1);
+        }
+        __syncthreads();
     }
 }
 
+// Q fragments for every kv head, once per attend: qf [Hk][NT][KS][32] uint4
+// = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand and qs [Hk][MR][NB].
 template <int D, int NT>
-cudaError_t launch_decode_t(const DecodeParams &p, cudaStream_t s) {
-    const DecodeSmem L = decode_smem(D, NT, p.geom.P);
+__global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__ DecodeParams p) {
+    constexpr int NB = D / 32, KS = D / 16, MR = NT * 8;
+    const int g = blockIdx.x, G = p.G, rows = G * p.R;
+    uint4 *qf = const_cast<uint4 *>(p.qf) + (int64_t)g * NT * KS * 32;
+    float *qs = const_cast<float *>(p.qs) + (int64_t)g * MR * NB;
+    __shared__ uint4 sq[NT * KS * 32];
+    for (int e = threadIdx.x; e < NT * KS * 32; e += kThreads) {
+        const int ln = e & 31, ks = (e >> 5) % KS, nt = e / (KS * 32);
+        const int m = nt * 8 + (ln >> 2);
+        const int d0 = 32 * (ks >> 1) + 8 * (ln & 3) + 4 * (ks & 1);
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m < rows) {
+            const int r = m / G, h = g * G + (m - r * G);
+            const int64_t off = ((int64_t)r * p.Hq + h) * D + d0;
+            if (p.q_f16) {
+                const uint2 raw = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __half *>(p.q) + off);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+                x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+            } else {
+                const float4 v = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.q) + off);
+                x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+            }
+        }
+        uint32_t h0, l0, h1, l1;
+        split_f16(x[0], x[1], h0, l0);
+        split_f16(x[2], x[3], h1, l1);
+        sq[e] = make_uint4(h0, h1, l0, l1);
+        qf[e] = sq[e];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < MR * NB; e += kThreads) {
+        const int m = e / NB, bb = e % NB, nt = m >> 3, gm = m & 7;
+        float acc_q = 0.f;
+        for (int s2 = 0; s2 < 2; ++s2)
+            for (int t = 0; t < 4; ++t) {
+                const uint4 v = sq[(nt * KS + 2 * bb + s2) * 32 + gm * 4 + t];
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w4[j]));
+                    acc_q += f.x + f.y;
+                }
+            }
+        qs[e] = acc_q;
+    }
+}
+
+int g_num_sms = 0;
+
+template <int D, int NT>
+cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
+    DecodeParams p = p_in;
+    if (p.prep_q) {
+        qprep_kernel<D, NT><<<p.geom.Hk, kThreads, 0, s>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (p.n_items == 0) return cudaSuccess;
+    }
+    const int maxsm = 232448;
+    // one stage per CTA and two CTAs per SM when they fit (the other CTA's copy
+    // overlaps this one's compute); otherwise two stages in one CTA
+    int occ = NT == 1 ? 2 : 1;
+    DecodeSmem L = decode_smem(D, NT, p.geom.P, occ == 2 ? 1 : 2);
+    if (occ == 2 && 2 * (L.total + 1024) > 233472) occ = 1, L = decode_smem(D, NT, p.geom.P, 2);
+    if (L.total > maxsm) L = decode_smem(D, NT, p.geom.P, 1);
+    if (L.total > maxsm) return cudaErrorInvalidValue;
+    p.stages = L.stages;
     static int configured = 0;
     if (configured < L.total) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
         if (e != cudaSuccess) return e;
         configured = L.total;
     }
-    dim3 grid(p.n_items, p.geom.Hk);
+    if (!g_num_sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 1;
+    }
+    const int U = p.n_items * p.geom.Hk;
+    const int per_cta = (U + occ * g_num_sms - 1) / (occ * g_num_sms);
+    const int grid = (U + per_cta - 1) / per_cta;
     decode_kernel<D, NT><<<grid, kThreads, L.total, s>>>(p);
     return cudaGetLastError();
 }
@@ -473,7 +613,7 @@ int decode_max_mma_rows() { return 64; }
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s) {
     const int rows = p.G * p.R;
-    if (rows < 1 || rows > 64 || p.n_items < 1 || p.n_items > kMaxItems) return cudaErrorInvalidValue;
+    if (rows < 1 || rows > 64 || (p.n_items < 1 && !p.prep_q) || p.n_items > kMaxItems) return cudaErrorInvalidValue;
     const int nt = (rows + 7) / 8;
     switch (p.geom.D) {
         case 64: return launch_decode_d<64>(p, nt, s);

@@ -9,7 +9,18 @@
 
 namespace kvs {
 
-// Byte layout of one page (see kvs_query_sizes in include/kvs.h).
+// Byte layout of one page (see kvs_query_sizes in include/kvs.h).  Inside a
+// head section, K codes sit in 16-token groups of one 32-byte line per
+// (32-dim block, token) and V nibbles in 32-token chunks of one 32-byte line
+// per (block, byte row); every tensor-core fragment is then one conflict-free
+// 8-byte shared-memory load, and a whole head section is one bulk copy.
+__host__ __device__ inline int64_t kq_byte(int64_t t, int d, int NB) {
+    return ((t / 16 * NB + d / 32) * 16 + t % 16) * 32 + d % 32;
+}
+__host__ __device__ inline int64_t vq_byte(int64_t t, int row, int NB) {
+    return ((t / 32 * NB + row / 16) * 16 + row % 16) * 32 + t % 32;
+}
+
 struct PageGeom {
     int P;               // tokens per page
     int Hk;              // kv heads
@@ -35,8 +46,9 @@ inline PageGeom make_geom(int P, int Hk, int D) {
 }
 
 // ---------------------------------------------------------------- decode
-// One work item = one (page, device slot) pair; the grid is (items, Hk).
-constexpr int kMaxItems = 256;
+// One item = one (page, device slot) pair; work units are (item, kv head),
+// spread over persistent CTAs (at most one per SM).
+constexpr int kMaxItems = 1024;
 
 struct DecodeParams {
     const uint8_t *arena;  // slot 0 of the page-slot array
@@ -45,17 +57,30 @@ struct DecodeParams {
     int q_f16;
     float *part_o;         // [split][Hq][R][D]   split = logical page
     float *part_ml;        // [split][Hq][R][2]   (max in log2 units, sum)
+    int *status;           // set to 1 if a bounded device wait timed out
     int R, Hq, G;
     long long pos0;
     float scale_log2;      // scale * log2(e)
+    int stages;            // shared-memory stages (set by launch_decode)
+    const uint4 *qf;       // Q fragments [Hk][NT][D/16][32] (written by the Q prep kernel)
+    const float *qs;       // per-block sums of Q [Hk][NT*8][D/32]
+    int prep_q;            // launch_decode first (re)builds qf/qs from q
     int n_items;
     uint32_t page[kMaxItems];
     uint32_t slot[kMaxItems];
 };
 
 // Returns cudaErrorInvalidValue for an unsupported (D, rows) combination.
+// With p.prep_q set it first rebuilds the Q fragments (p.qf/p.qs) from p.q;
+// n_items may then be 0 (Q prep only).
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s);
 int decode_max_mma_rows();  // G*R bound served by launch_decode
+// bytes of the Q-fragment area (qf then qs) for Hk kv heads of head dim D
+inline int64_t qfrag_bytes(int Hk, int D) {
+    const int64_t qf = (int64_t)Hk * 8 * (D / 16) * 32 * 16;
+    const int64_t qs = (int64_t)Hk * 64 * (D / 32) * 4;
+    return (qf + qs + 255) / 256 * 256;
+}
 
 // ---------------------------------------------------------------- prefill
 // tcgen05 prefill: one split = up to kMaxPrefillSplitPages consecutive pages;

@@ -11,10 +11,13 @@
 //
 // The array is a fixed kNoallocScratchBytes (32 MiB) on every GPU that loads
 // this library, held until the process exits.  Every call on a device shares
-// it and it keeps the previous call's contents; nothing in it needs to start
-// at zero, because each partial the final combine reads is written earlier in
-// the same call.  Calls whose work overlaps on the GPU (two streams, or two
-// host threads) race on the array: order them on one stream.
+// it and it keeps the previous call's contents.  Its first 256 bytes hold the
+// kernels' timeout flag, which starts at zero (a static device array is
+// zero-initialised) and is only ever set by a device wait that gave up; then
+// come the query fragments and the split partials, which need no clearing
+// because each call writes them before it reads them.  Calls whose work
+// overlaps on the GPU (two streams, or two host threads) race on the array:
+// order them on one stream.
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -29,6 +32,7 @@
 namespace {
 
 constexpr uint64_t kNoallocScratchBytes = 32ull << 20;
+constexpr uint64_t kStatusBytes = 256;  // timeout flag at the start of the array
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -106,7 +110,8 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
         }
     }
     const uint64_t per_split = (uint64_t)n_q_head * n_rows;
-    const uint64_t need = n_split * per_split * (D + 2) * sizeof(float);
+    const uint64_t qfrag = (uint64_t)kvs::qfrag_bytes((int)Hk, (int)D);
+    const uint64_t need = kStatusBytes + qfrag + n_split * per_split * (D + 2) * sizeof(float);
     if (need > kNoallocScratchBytes) {
         kvs::set_thread_error("needs " + std::to_string(need) + " bytes of split partials; the fixed scratch "
                               "holds " + std::to_string(kNoallocScratchBytes) +
@@ -124,13 +129,18 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
     dp.geom = geom;
     dp.q = q_dev;
     dp.q_f16 = q_dtype == KVS_F16;
-    dp.part_o = static_cast<float *>(scratch);
+    dp.status = static_cast<int *>(scratch);
+    uint8_t *qf_area = static_cast<uint8_t *>(scratch) + kStatusBytes;
+    dp.qf = reinterpret_cast<const uint4 *>(qf_area);
+    dp.qs = reinterpret_cast<const float *>(qf_area + (int64_t)Hk * 8 * (D / 16) * 32 * 16);
+    dp.part_o = reinterpret_cast<float *>(qf_area + qfrag);
     dp.part_ml = dp.part_o + n_split * per_split * D;
     dp.R = (int)n_rows;
     dp.Hq = (int)n_q_head;
     dp.G = (int)(n_q_head / Hk);
     dp.pos0 = (long long)pos0;
     dp.scale_log2 = scale * 1.4426950408889634f;
+    dp.prep_q = 1;  // the first launch also builds the query fragments
     for (uint64_t i0 = 0; i0 < n_split; i0 += kvs::kMaxItems) {
         const int n = (int)((n_split - i0) < (uint64_t)kvs::kMaxItems ? (n_split - i0) : kvs::kMaxItems);
         dp.n_items = n;
@@ -143,6 +153,7 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
             kvs::set_thread_error(std::string("attention kernel launch: ") + cudaGetErrorString(e));
             return KVS_ERR_CUDA;
         }
+        dp.prep_q = 0;
     }
     kvs::CombineParams cp;
     cp.part_o = dp.part_o;

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             const __half *ks = reinterpret_cast<const __half *>(hb + p.geom.ks_off);
             for (int c = tid; c < kBN * (kD / 8); c += kPThreads) {
                 const int key = c / (kD / 8), k = (c % (kD / 8)) * 8;
-                const uint2 raw = *reinterpret_cast<const uint2 *>(hb + (int64_t)(kb + key) * kD + k);
+                const uint2 raw = *reinterpret_cast<const uint2 *>(hb + kq_byte(kb + key, k, kD / 32));
                 const float d = __half2float(ks[(kb + key) * (kD / 32) + k / 32]);
                 const int8_t *b8 = reinterpret_cast<const int8_t *>(&raw);
                 uint32_t hi[4], lo[4];
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 const int blk = dim >> 5, within = dim & 31;
                 const int brow = blk * 16 + (within & 15);
                 const int shift = within < 16 ? 0 : 4;
-                const uint2 raw = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + (int64_t)brow * P + kb + k);
+                const uint2 raw = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + vq_byte(kb + k, brow, kD / 32));
                 const uint8_t *b8 = reinterpret_cast<const uint8_t *>(&raw);
                 uint32_t hi[4], lo[4];
 #pragma unroll

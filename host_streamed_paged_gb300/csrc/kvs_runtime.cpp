@@ -557,6 +557,7 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
         if (s != KVS_OK) return s;
         cudaError_t e = kvs::launch_decode(dp, c->stream(sid));
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel launch");
+        c->check_status = true;
         s = timed_end(c, t0, (uint64_t)n * (uint64_t)c->geom.page_bytes, sid);
         if (s != KVS_OK) return s;
     }
@@ -626,7 +627,7 @@ void sizes_of(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
             need = std::max<uint64_t>(need, splits * cfg->max_q_head * cfg->max_rows *
                                                 (uint64_t)(cfg->head_dim + 2) * 4ull);
         }
-        *ws_min = kStatusBytes + need;
+        *ws_min = kStatusBytes + (uint64_t)kvs::qfrag_bytes((int)cfg->n_kv_head, (int)cfg->head_dim) + need;
     }
 }
 
@@ -1273,7 +1274,8 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
     }
 
     const size_t per_split = (size_t)n_q_head * n_rows;
-    float *part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes);
+    uint8_t *qfrag = static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes;
+    float *part_o = reinterpret_cast<float *>(qfrag + kvs::qfrag_bytes(c->geom.Hk, c->geom.D));
     const int64_t n_partials = prefill ? (c->max_pages + c->prefill_split - 1) / c->prefill_split : c->max_pages;
     float *part_ml = part_o + (size_t)n_partials * per_split * c->geom.D;
     c->st.attend_calls++;
@@ -1290,14 +1292,28 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         dp.q_f16 = q_dtype == KVS_F16;
         dp.part_o = part_o;
         dp.part_ml = part_ml;
+        dp.status = static_cast<int *>(c->cfg.workspace);
+        dp.qf = reinterpret_cast<const uint4 *>(qfrag);
+        dp.qs = reinterpret_cast<const float *>(qfrag + (int64_t)c->geom.Hk * 8 * (c->geom.D / 16) * 32 * 16);
         dp.R = (int)n_rows;
         dp.Hq = (int)n_q_head;
         dp.G = (int)G;
         dp.pos0 = (long long)pos0;
         dp.scale_log2 = scale * 1.4426950408889634f;
 
-        // other lanes start after this call's inputs (Q, the previous combine's
-        // reads of the partials, published pages) are in place
+        // Q fragments for every kv head, once per call (primary attention stream)
+        c->st.kernel_launches++;
+        if (c->plan_only) {
+            log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 4, c->geom.Hk);
+        } else {
+            dp.prep_q = 1;
+            dp.n_items = 0;
+            cudaError_t e = kvs::launch_decode(dp, c->attn);
+            if (e != cudaSuccess) return cuda_fail(c, e, "query fragment launch");
+            dp.prep_q = 0;
+        }
+        // other lanes start after this call's inputs (Q and its fragments, the
+        // previous combine's reads of the partials, published pages) are in place
         s = fork_attn_lanes(c);
         if (s != KVS_OK) return s;
         s = pump(c);
@@ -1405,7 +1421,7 @@ kvs_status kvs_sync(kvs_ctx *c, uint32_t timeout_ms) {
         if (e != cudaSuccess) return cuda_fail(c, e, "status read");
         if (status != 0) {
             cudaMemset(c->cfg.workspace, 0, sizeof(int));
-            return fail(c, KVS_ERR_CUDA, "a bounded device-side wait in the prefill kernel timed out");
+            return fail(c, KVS_ERR_CUDA, "a bounded device-side wait in an attention kernel timed out");
         }
     }
     return KVS_OK;

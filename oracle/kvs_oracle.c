@@ -34,7 +34,8 @@
  *  - The page layout (V2 README, "KV data movement and attention": a page
  *    holds 256 token positions and its K/V byte sizes follow the quant
  *    types).  The byte order inside a page is this library's own choice and
- *    is spelled out at kvs_oracle_encode_page.
+ *    is spelled out at kvs_oracle_encode_page; the oracle writes it from that
+ *    definition only, to pin the bytes the device path stores.
  *
  *  - The split/combine identity (V2 README, "Keep the stock attention order":
  *    one ordered history, then the stock-style final reduction; PR "port
@@ -168,20 +169,31 @@ void kvs_oracle_quantize_kv(int64_t T, int Hk, int D, const float *k, const floa
 /*
  * Page bytes of page `page` (tokens page*P .. page*P+P-1) of a history of T
  * tokens.  The page is Hk consecutive head sections; head section g holds,
- * at these byte offsets (HS = P*D*13/8 bytes per section):
- *   Kq  int8  [P][D]      at 0                 (token-major K codes)
- *   Ks  fp16  [P][D/32]   at P*D               (token-major K scales)
- *   Vq  uint8 [D/2][P]    at P*D + P*D/16      (dim-major V nibbles: byte row
- *                                               b*16 + c, column t, holds the
- *                                               codes of dims b*32+c (low) and
- *                                               b*32+c+16 (high) of token t)
- *   Vs  fp16  [D/32][P]   at P*D + P*D/16 + P*D/2 (dim-major V scales)
+ * at these byte offsets (HS = P*D*13/8 bytes per section, NB = D/32):
+ *   Kq  int8  at 0               byte of (token t, dim d):
+ *                                ((t/16 * NB + d/32) * 16 + t%16) * 32 + d%32
+ *                                (16-token groups; inside a group, one
+ *                                32-byte line per (block, token))
+ *   Ks  fp16  [P][NB]   at P*D   (token-major K scales)
+ *   Vq  uint8 at P*D + P*D/16    byte of (byte row i = b*16 + c, token t):
+ *                                ((t/32 * NB + b) * 16 + c) * 32 + t%32;
+ *                                byte row b*16 + c holds the codes of dims
+ *                                b*32+c (low nibble) and b*32+c+16 (high)
+ *   Vs  fp16  [NB][P]   at P*D + P*D/16 + P*D/2 (dim-major V scales)
  * fp16 values are little-endian.  Token slots at or beyond T are zero bytes.
  */
+static int64_t kq_at(int64_t t, int d, int NB) {
+    return ((t / 16 * NB + d / 32) * 16 + t % 16) * 32 + d % 32;
+}
+
+static int64_t vq_at(int64_t t, int row, int NB) {
+    return ((t / 32 * NB + row / 16) * 16 + row % 16) * 32 + t % 32;
+}
+
 void kvs_oracle_encode_page(int P, int Hk, int D, int64_t T, int64_t page,
                             const int8_t *kq, const uint16_t *kd, const uint8_t *vq,
                             const uint16_t *vd, uint8_t *out) {
-    const int64_t nbk = D / 32;
+    const int nbk = D / 32;
     const int64_t HS = (int64_t)P * D * 13 / 8;
     const int64_t ks_off = (int64_t)P * D;
     const int64_t vq_off = ks_off + (int64_t)P * D / 16;
@@ -193,7 +205,7 @@ void kvs_oracle_encode_page(int P, int Hk, int D, int64_t T, int64_t page,
             int64_t tok = page * P + t;
             if (tok >= T) break;
             const int64_t row = tok * Hk + g;
-            for (int d = 0; d < D; ++d) sec[(int64_t)t * D + d] = (uint8_t)kq[row * D + d];
+            for (int d = 0; d < D; ++d) sec[kq_at(t, d, nbk)] = (uint8_t)kq[row * D + d];
             for (int b = 0; b < nbk; ++b) {
                 uint16_t s = kd[row * nbk + b];
                 sec[ks_off + ((int64_t)t * nbk + b) * 2 + 0] = (uint8_t)(s & 0xff);
@@ -204,7 +216,7 @@ void kvs_oracle_encode_page(int P, int Hk, int D, int64_t T, int64_t page,
                 for (int c = 0; c < 16; ++c) {
                     uint8_t lo = vq[row * D + b * 32 + c];
                     uint8_t hi = vq[row * D + b * 32 + c + 16];
-                    sec[vq_off + ((int64_t)(b * 16 + c)) * P + t] = (uint8_t)(lo | (hi << 4));
+                    sec[vq_off + vq_at(t, b * 16 + c, nbk)] = (uint8_t)(lo | (hi << 4));
                 }
             }
         }

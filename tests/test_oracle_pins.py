@@ -117,9 +117,20 @@ def test_q4_0_bounds_random():
 
 # ---------------------------------------------------------- page layout
 
+def _kq_at(t, d, NB):
+    # K byte of (token t, dim d): 16-token groups, one 32-byte line per (block, token)
+    return ((t // 16 * NB + d // 32) * 16 + t % 16) * 32 + d % 32
+
+
+def _vq_at(t, row, NB):
+    # V nibble byte of (byte row b*16+c, token t): 32-token chunks, one 32-byte line per (block, byte row)
+    return ((t // 32 * NB + row // 16) * 16 + row % 16) * 32 + t % 32
+
+
 def test_page_layout_bytes():
     """Byte positions of the page layout, worked out from its stated definition."""
     P, Hk, D = 32, 2, 64
+    NB = D // 32
     T = 45  # page 1 holds tokens 32..44, slots 13..31 are empty
     k = np.zeros((T, Hk, D), np.float32)
     v = np.zeros((T, Hk, D), np.float32)
@@ -135,19 +146,23 @@ def test_page_layout_bytes():
     pg = qkv.encode_page(P, 1)
     HS = P * D * 13 // 8
     assert pg.size == Hk * HS
+    # hand-placed examples: token 0 dim 5 -> line (group 0, block 0, token 0) byte 5 = 5;
+    # token 12 dim 63 -> ((0*2+1)*16+12)*32+31 = 927; token 3 dim 33 -> (16+3)*32+1 = 609
+    assert [_kq_at(0, 5, NB), _kq_at(12, 63, NB), _kq_at(3, 33, NB), _kq_at(7, 32, NB)] == [5, 927, 609, 736]
     for (t, g, d) in [(0, 0, 5), (12, 1, 63), (3, 1, 33), (7, 0, 32)]:
         tok = 32 + t
-        assert pg[g * HS + t * D + d].view(np.int8) == k[tok, g, d]
+        assert pg[g * HS + _kq_at(t, d, NB)].view(np.int8) == k[tok, g, d]
     # K scales: fp16(1.0) = 0x3c00, little-endian, token-major [P][D/32]
     off = 1 * HS + P * D + (5 * 2 + 1) * 2
     assert pg[off] == 0x00 and pg[off + 1] == 0x3C
-    # V nibbles: byte row b*16 + c, column t holds dims b*32+c (low) and b*32+c+16 (high)
+    # V nibbles: byte row b*16 + c holds dims b*32+c (low) and b*32+c+16 (high)
     vq0 = P * D + P * D // 16
+    assert [_vq_at(0, 3, NB), _vq_at(12, 31, NB), _vq_at(5, 0, NB), _vq_at(9, 23, NB)] == [96, 1004, 5, 745]
     for (t, g, b, c) in [(0, 0, 0, 3), (12, 1, 1, 15), (5, 1, 0, 0), (9, 0, 1, 7)]:
         tok = 32 + t
         lo = int(v[tok, g, 32 * b + c]) + 8
         hi = int(v[tok, g, 32 * b + c + 16]) + 8
-        assert pg[g * HS + vq0 + (b * 16 + c) * P + t] == lo | (hi << 4)
+        assert pg[g * HS + vq0 + _vq_at(t, b * 16 + c, NB)] == lo | (hi << 4)
     # V scales: dim-major [D/32][P]
     vs0 = vq0 + P * D // 2
     off = 1 * HS + vs0 + (1 * P + 12) * 2
@@ -155,14 +170,16 @@ def test_page_layout_bytes():
     # empty token slots are zero bytes in every section
     for g in range(Hk):
         sec = pg[g * HS:(g + 1) * HS]
-        assert not sec[13 * D:P * D].any()
-        for row in range(D // 2):
-            assert not sec[vq0 + row * P + 13: vq0 + row * P + P].any()
+        for t in range(13, P):
+            assert not any(sec[_kq_at(t, d, NB)] for d in range(D))
+            assert not any(sec[vq0 + _vq_at(t, r, NB)] for r in range(D // 2))
+            assert not sec[P * D + t * NB * 2: P * D + (t + 1) * NB * 2].any()
 
 
 def test_page_roundtrip_parse():
     """Parsing the page bytes per the layout recovers every code and scale."""
     P, Hk, D, T = 64, 3, 128, 150
+    NB = D // 32
     k = synth.normal(5, synth.tag("pk"), (T, Hk, D))
     v = synth.normal(5, synth.tag("pv"), (T, Hk, D))
     qkv = oracle.QuantKV(k, v)
@@ -172,16 +189,19 @@ def test_page_roundtrip_parse():
         n = min(P, T - page * P)
         for g in range(Hk):
             sec = pg[g * HS:(g + 1) * HS]
-            kq = sec[:P * D].view(np.int8).reshape(P, D)
-            ks = sec[P * D:P * D + P * D // 16].view(np.uint16).reshape(P, D // 32)
-            vq = sec[P * D + P * D // 16: P * D + P * D // 16 + P * D // 2].reshape(D // 2, P)
-            vs = sec[P * D + P * D // 16 + P * D // 2:].view(np.uint16).reshape(D // 32, P)
+            # Kq: [P/16][NB][16][32] -> [P][D]
+            kq = sec[:P * D].view(np.int8).reshape(P // 16, NB, 16, 32).transpose(0, 2, 1, 3).reshape(P, D)
+            ks = sec[P * D:P * D + P * D // 16].view(np.uint16).reshape(P, NB)
+            # Vq: [P/32][NB][16][32] -> [NB*16][P]
+            vq = sec[P * D + P * D // 16: P * D + P * D // 16 + P * D // 2].reshape(P // 32, NB, 16, 32)
+            vq = vq.transpose(1, 2, 0, 3).reshape(NB * 16, P)
+            vs = sec[P * D + P * D // 16 + P * D // 2:].view(np.uint16).reshape(NB, P)
             toks = slice(page * P, page * P + n)
             assert np.array_equal(kq[:n], qkv.kq[toks, g])
             assert np.array_equal(ks[:n], qkv.kd[toks, g])
             assert np.array_equal(vs[:, :n].T, qkv.vd[toks, g])
             codes = np.empty((n, D), np.uint8)
-            for b in range(D // 32):
+            for b in range(NB):
                 rows = vq[b * 16:(b + 1) * 16, :n]  # [16][n]
                 codes[:, b * 32:b * 32 + 16] = (rows & 0xF).T
                 codes[:, b * 32 + 16:b * 32 + 32] = (rows >> 4).T
