@@ -64,8 +64,9 @@ WORKLOADS = {
         L=64, T=131072 + 256, R=256, ring=8, chunk=2, lanes=2, residency=("prefix_frac", 1.0), q_f16=True),
     "long262k": dict(
         desc=("long-context decode: 64 layers, context 262144, 24 q / 4 kv heads, D 256, page 256, Q8_0 K / "
-              "Q4_0 V, fixed 2048 MiB arena split between resident pages (per-layer prefixes) and the ring"),
-        L=64, T=262144, R=1, ring=8, chunk=2, lanes=4, residency=("arena_frac", 0.5),
+              "Q4_0 V, fixed 2048 MiB arena split between resident pages (per-layer prefixes) and the ring "
+              "(chunks of a quarter of the ring, at most 32 pages)"),
+        L=64, T=262144, R=1, ring=8, chunk=0, lanes=4, residency=("arena_frac", 0.5),
         arena_slots=ARENA_PAGE_SLOTS_2GIB),
     "resident131k": dict(  # the attention kernel over resident pages, launches far larger than L2
         desc=("all-resident decode: 4 layers x 1 row, context 131072, 24 q / 4 kv heads, D 256, page 256, "
@@ -274,7 +275,7 @@ def run_ours(args, wl):
     arena_slots = fixed_arena if fixed_arena else 2 * L + wl["ring"] + pool
     st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
                       max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"], arena_slots=arena_slots,
-                      device=dev, lanes=wl.get("lanes", 1))
+                      device=dev, lanes=wl.get("lanes", 1), dma_fill=wl.get("dma", False))
     ceiling = h2d_ceiling(torch, dev)
 
     # history: seeded rows appended through the KV writer
@@ -387,6 +388,7 @@ def run_ours(args, wl):
         st.graph_end()
         gstats = st.stats(reset=True)
         kernels_per_step = gstats["graph_kernels"]
+        chunk_eff = int(gstats["chunk_pages"])
         h2d_bytes_step = gstats["h2d_bytes"]
 
         for _ in range(args.warmup):
@@ -469,7 +471,8 @@ def run_ours(args, wl):
             "config": {"workload": wl["desc"], "layers": L, "context": T, "rows": R, "q_heads": Hq, "kv_heads": Hk,
                        "head_dim": D, "page_tokens": P, "resident_pages_per_step": res_pages,
                        "resident_fraction": res_pages / (L * npages), "ring_slots": ring,
-                       "chunk_pages": wl["chunk"], "lanes": wl.get("lanes", 1),
+                       "chunk_pages": chunk_eff, "lanes": wl.get("lanes", 1),
+                       "fill": "copy engines" if wl.get("dma") else "SM fill kernel",
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {kv_bytes_step / 1e9:.2f} GB of KV pages read per step",
                        "step": "per layer: append rows, prefetch next layer, attend, truncate; one CUDA graph replay"},
@@ -513,6 +516,8 @@ def main():
     ap.add_argument("--resident", type=float, default=-1.0,
                     help="override the resident fraction (prefix of each layer; for long262k of the arena)")
     ap.add_argument("--sweep", action="store_true", help="long262k: sweep the resident fraction 0..100%%")
+    ap.add_argument("--fill", choices=["default", "sm", "dma"], default="default",
+                    help="ring refills by the SM fill kernel or the copy engines (default: the workload's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(WORKLOADS[args.workload])
@@ -522,6 +527,9 @@ def main():
         if v:
             wl[name] = v
             wl["desc"] += f" [{key} override: {v}]"
+    if args.fill != "default":
+        wl["dma"] = args.fill == "dma"
+        wl["desc"] += f" [fill override: {args.fill}]"
     if args.rows:
         wl["T"] = wl["T"] - wl["R"] + args.rows
         wl["R"] = args.rows

@@ -87,28 +87,38 @@ __device__ __forceinline__ uint4 ld_nc_u4(const void *p) {
     return v;
 }
 
-// grid = (ctas per page, pages); host pages are read through their mapped
-// device address.  The grid is sized so that each thread issues all of its
-// (at most kFillUnroll) 16-byte host loads before its first store: a chunk
-// is only a few pages, so one round of host-link latency per launch is the
-// whole cost beyond the transfer itself.
+// Host pages are read through their mapped device address, 16 bytes per
+// load, kFillUnroll loads in flight per thread before the first store.  The
+// grid covers the chunk's pages as one flat range and is capped at
+// kFillMaxCtas: that keeps about 2 MiB of host reads in flight (far more
+// than the host link's bandwidth x latency) while leaving the SMs to the
+// attention launches that run beside the copy.
 constexpr int kFillThreads = 512;
 constexpr int kFillUnroll = 4;
+constexpr int kFillMaxCtas = 64;
 
 __global__ void __launch_bounds__(kFillThreads) fill_kernel(const __grid_constant__ FillParams p) {
-    const int pg = blockIdx.y;
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.src[pg]);
-    uint4 *dst = reinterpret_cast<uint4 *>(p.dst[pg]);
-    const int64_t n = p.page_bytes / 16;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += kFillUnroll * stride) {
+    const uint32_t upp = (uint32_t)(p.page_bytes / 16);  // 16-byte units per page
+    const uint32_t n = upp * (uint32_t)p.n;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += kFillUnroll * stride) {
         uint4 v[kFillUnroll];
 #pragma unroll
-        for (int u = 0; u < kFillUnroll; ++u)
-            if (i0 + u * stride < n) v[u] = ld_nc_u4(src + i0 + u * stride);
+        for (int u = 0; u < kFillUnroll; ++u) {
+            const uint32_t i = i0 + u * stride;
+            if (i < n) {
+                const uint32_t pg = i / upp;
+                v[u] = ld_nc_u4(reinterpret_cast<const uint4 *>(p.src[pg]) + (i - pg * upp));
+            }
+        }
 #pragma unroll
-        for (int u = 0; u < kFillUnroll; ++u)
-            if (i0 + u * stride < n) dst[i0 + u * stride] = v[u];
+        for (int u = 0; u < kFillUnroll; ++u) {
+            const uint32_t i = i0 + u * stride;
+            if (i < n) {
+                const uint32_t pg = i / upp;
+                reinterpret_cast<uint4 *>(p.dst[pg])[i - pg * upp] = v[u];
+            }
+        }
     }
 }
 
@@ -129,13 +139,29 @@ cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStre
     return cudaGetLastError();
 }
 
-cudaError_t launch_fill(const FillParams &p, cudaStream_t s) {
+cudaError_t launch_fill(const FillParams &p, cudaStream_t s, bool pdl) {
     if (p.n <= 0) return cudaSuccess;
     if (p.n > kMaxFillPages || p.page_bytes % 16 != 0) return cudaErrorInvalidValue;
-    const int64_t units = p.page_bytes / 16;
-    const int per_page = (int)((units + (int64_t)kFillThreads * kFillUnroll - 1) / ((int64_t)kFillThreads * kFillUnroll));
-    dim3 grid(per_page, p.n);
-    fill_kernel<<<grid, kFillThreads, 0, s>>>(p);
+    const int64_t units = p.page_bytes / 16 * p.n;
+    if (units >= (int64_t)1 << 31) return cudaErrorInvalidValue;
+    int64_t ctas = (units + (int64_t)kFillThreads * kFillUnroll - 1) / ((int64_t)kFillThreads * kFillUnroll);
+    if (ctas > kFillMaxCtas) ctas = kFillMaxCtas;
+    if (!pdl) {
+        fill_kernel<<<(unsigned)ctas, kFillThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kFillThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fill_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -125,24 +125,31 @@ __device__ __forceinline__ void stage_load(uint32_t dst, const uint8_t *src, uin
     }
 }
 
-// Shared-memory carve of decode_kernel<D, NT> (bytes; page size P, S stages).
+// Key parts of the P.V product.  A page's O^T is the ordered sum
+// part 0 + part 1 + ... of per-key-range MMA chains, whatever the launch
+// shape, so a page's partial is bitwise the same from every launch shape.
+__host__ __device__ inline int pv_parts(int D, int P) {
+    int parts = 8 / (D / 32);
+    if (parts < 2) parts = 2;
+    if (parts > P / 32) parts = P / 32;
+    return parts < 1 ? 1 : parts;
+}
+
+// Shared-memory carve of decode_kernel<D, NT, W> (bytes; page size P, S stages).
 struct DecodeSmem {
-    int stage, sc, rmax, rsum, red, obuf, bar, total, stages;
+    int stage, sc, red, obuf, bar, total, stages;
 };
 __host__ __device__ inline int align_to(int x, int a) { return (x + a - 1) / a * a; }
-__host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int P, int stages) {
+__host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, int stages) {
     DecodeSmem s;
-    const int MR = NT * 8, SP = P + 4, NB = D / 32;
-    int parts = 8 / NB;
-    if (parts > P / 32) parts = P / 32;
+    const int MR = NT * 8, SP = P + 4;
+    const bool in_reg = (W == D / 32);  // a warp keeps every key part of its dim block in registers
     const int head = P * D * 13 / 8;
     s.stages = stages;
     s.stage = 0;
     s.sc = align_to(stages * head, 128);
-    s.rmax = align_to(s.sc + MR * SP * 4, 16);
-    s.rsum = align_to(s.rmax + MR * 4, 16);
-    s.red = align_to(s.rsum + MR * 4, 16);
-    const int red_end = s.red + (parts - 1) * MR * D * 4;
+    s.red = align_to(s.sc + MR * SP * 4, 16);
+    const int red_end = s.red + (in_reg ? 0 : (pv_parts(D, P) - 1) * MR * D * 4);
     // the output tile reuses the score buffer when it fits there
     s.obuf = (SP >= D) ? s.sc : align_to(red_end, 16);
     const int obuf_end = (SP >= D) ? red_end : s.obuf + MR * D * 4;
@@ -151,23 +158,31 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int P, int stag
     return s;
 }
 
-// Persistent split-K attention over (page, kv head) units.  Units are ordered
-// head-major; CTA c takes units [c*U/C, (c+1)*U/C), so it rebuilds its Q
-// fragments only when the kv head changes.  Page-head sections stream into
-// `stages` shared-memory stages by bulk asynchronous copies: while the warps
-// work on one unit the next one is already on its way.
-template <int D, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+// Persistent split-K attention over work units.  A unit is one (page, kv
+// head) with all NT row tiles (resident pages), or, in tile mode, one (page,
+// kv head, row tile) (NT = 1: ring chunks, where a chunk is a few pages and
+// the time until its slots can be refilled matters more than throughput).
+// Both shapes run the same arithmetic per row tile, for any warp count W.
+// Units are ordered head-major; CTA c takes units [c*U/C, (c+1)*U/C).
+// Page-head sections stream into `stages` shared-memory stages by bulk
+// asynchronous copies: while the warps work on one unit the next one is
+// already on its way.
+template <int D, int NT, int W>
+__global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int NB = D / 32;  // 32-dim scale blocks
     constexpr int KS = D / 16;  // QK k-steps
     constexpr int MR = NT * 8;  // MMA rows (query rows x heads, padded to 8)
+    constexpr int NTH = W * 32;
+    constexpr bool kInReg = (W == NB);                 // see decode_smem
+    constexpr int PM = kInReg ? 2 : 1;                 // key parts a warp accumulates
+    constexpr int KPW = (NT == 1 && W == 8) ? 2 : 1;   // 16-key groups a warp scores at once
     const int P = p.geom.P;
     const int SP = P + 4;  // score row stride, floats
-    const DecodeSmem L = decode_smem(D, NT, P, p.stages);
+    const int parts = pv_parts(D, P);
+    const DecodeSmem L = decode_smem(D, NT, W, P, p.stages);
     float *sc = reinterpret_cast<float *>(smem + L.sc);
-    float *rmax = reinterpret_cast<float *>(smem + L.rmax);
-    float *rsum = reinterpret_cast<float *>(smem + L.rsum);
     float *red = reinterpret_cast<float *>(smem + L.red);
     float *obuf = reinterpret_cast<float *>(smem + L.obuf);
     const uint32_t bar0 = smem_u32(smem + L.bar);
@@ -175,13 +190,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
     const int G = p.G, R = p.R, rows = G * R;
-    const int U = p.n_items * p.geom.Hk;
+    const int T = p.tile_mode ? p.run_tiles : 1;
+    const int U = p.n_items * p.geom.Hk * T;
     const int u0 = (int)((int64_t)blockIdx.x * U / gridDim.x), u1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
     if (u0 >= u1) return;
     const int S = L.stages;
 
     auto src_of = [&](int u) {
-        const int g = u / p.n_items, item = u - g * p.n_items;
+        const int gi = u / T, g = gi / p.n_items, item = gi - g * p.n_items;
         return p.arena + (int64_t)p.slot[item] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
     };
     bool pending[2] = {false, false};      // a load into this stage is not consumed yet
@@ -200,71 +216,107 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
     for (int u = u0, i = 0; u < u1; ++u, ++i) {
         const int stage = i % S;
         const uint32_t parity = (uint32_t)((i / S) & 1);
-        const int g = u / p.n_items, item = u - g * p.n_items;
+        const int tile = u % T, gi = u / T;
+        const int g = gi / p.n_items, item = gi - g * p.n_items;
+        const int mo = tile * 8;  // first query row x head of this unit's tiles
         const uint32_t page = p.page[item];
         const uint8_t *hs = smem + L.stage + stage * head_bytes;  // this unit's page-head section
 
-        // Q fragments of kv head g (built by qprep_kernel): qf[nt][ks][lane] and
+        // Q fragments of kv head g (built by qprep_kernel): qf[tile][ks][lane] and
         // qs[m][b] = sum over 32-dim block b of q as the MMA sees it (hi + lo)
-        const uint4 *qf = p.qf + (int64_t)g * NT * KS * 32;
-        const float *qs = p.qs + (int64_t)g * MR * NB;
+        const uint4 *qf = p.qf + ((int64_t)g * p.qtiles + tile) * KS * 32;
+        const float *qs = p.qs + ((int64_t)g * p.qtiles * 8 + mo) * NB;
         if (!mbar_wait(bar0 + 16 * stage, parity)) ok = false;
         if (!__syncthreads_and(ok)) break;
         pending[stage] = false;
+        // every page section this CTA reads is now in shared memory: a refill
+        // of those slots launched as this grid's programmatic dependent may
+        // start (it begins once every CTA has signalled or exited)
+        if (u == u1 - 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-        // Scores: warp w owns keys [32w, 32w + 32) as two 16-key MMA row tiles.
+        // Scores: each warp takes KPW 16-key groups at a time as MMA row tiles.
         const long long kpos0 = (long long)page * P;
-        if (warp < P / 32) {
+        const int NKG = P / 16;
+        const __half *ksc = reinterpret_cast<const __half *>(hs + p.geom.ks_off);
 #pragma unroll 1
-            for (int mt = 0; mt < 2; ++mt) {
-                const int kg = 2 * warp + mt;  // 16-key group
-                const int k0 = 16 * kg + gid, k1 = k0 + 8;
-                const __half *ksc = reinterpret_cast<const __half *>(hs + p.geom.ks_off);
-                float S_[NT][4];
+        for (int kgb = 0; kgb < NKG; kgb += W * KPW) {
+            if (kgb + warp >= NKG) break;
+            int kg[KPW];
+            bool kvalid[KPW];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) S_[nt][0] = S_[nt][1] = S_[nt][2] = S_[nt][3] = 0.f;
+            for (int q = 0; q < KPW; ++q) {
+                kg[q] = kgb + warp + W * q;
+                kvalid[q] = kg[q] < NKG;
+                if (!kvalid[q]) kg[q] = kgb + warp;  // computed, never stored
+            }
+            float S_[KPW][NT][4];
+#pragma unroll
+            for (int q = 0; q < KPW; ++q)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) S_[q][nt][0] = S_[q][nt][1] = S_[q][nt][2] = S_[q][nt][3] = 0.f;
 #pragma unroll(NT <= 2 ? NB : 1)
-                for (int b = 0; b < NB; ++b) {
-                    const uint8_t *line = hs + ((kg * NB + b) * 16) * 32 + 8 * tig;
-                    const uint2 kv0 = *reinterpret_cast<const uint2 *>(line + gid * 32);
-                    const uint2 kv1 = *reinterpret_cast<const uint2 *>(line + (gid + 8) * 32);
-                    const float sk0 = __half2float(ksc[k0 * NB + b]), sk1 = __half2float(ksc[k1 * NB + b]);
-                    float cb[NT][4];
+            for (int b = 0; b < NB; ++b) {
+                uint2 kv0[KPW], kv1[KPW];
+                float sk0[KPW], sk1[KPW];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) cb[nt][0] = cb[nt][1] = cb[nt][2] = cb[nt][3] = 0.f;
+                for (int q = 0; q < KPW; ++q) {
+                    const uint8_t *line = hs + ((kg[q] * NB + b) * 16) * 32 + 8 * tig;
+                    kv0[q] = *reinterpret_cast<const uint2 *>(line + gid * 32);
+                    kv1[q] = *reinterpret_cast<const uint2 *>(line + (gid + 8) * 32);
+                    sk0[q] = __half2float(ksc[(16 * kg[q] + gid) * NB + b]);
+                    sk1[q] = __half2float(ksc[(16 * kg[q] + gid + 8) * NB + b]);
+                }
+                float cb[KPW][NT][4];
 #pragma unroll
-                    for (int s = 0; s < 2; ++s) {
-                        uint32_t a[4];
-                        i8x4_to_f16_biased(s ? kv0.y : kv0.x, a[0], a[2]);
-                        i8x4_to_f16_biased(s ? kv1.y : kv1.x, a[1], a[3]);
+                for (int q = 0; q < KPW; ++q)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint4 qv = qf[(nt * KS + 2 * b + s) * 32 + lane];
-                            mma16816(cb[nt], a, qv.x, qv.y);
-                            mma16816(cb[nt], a, qv.z, qv.w);
-                        }
+                    for (int nt = 0; nt < NT; ++nt) cb[q][nt][0] = cb[q][nt][1] = cb[q][nt][2] = cb[q][nt][3] = 0.f;
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    uint32_t a[KPW][4];
+#pragma unroll
+                    for (int q = 0; q < KPW; ++q) {
+                        i8x4_to_f16_biased(s ? kv0[q].y : kv0[q].x, a[q][0], a[q][2]);
+                        i8x4_to_f16_biased(s ? kv1[q].y : kv1[q].x, a[q][1], a[q][3]);
                     }
-                    // the A operand carried 1152 + x: take 1152 * sum(q) of the block back out
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const float q0 = qs[(nt * 8 + 2 * tig) * NB + b];
-                        const float q1 = qs[(nt * 8 + 2 * tig + 1) * NB + b];
-                        const float c0 = fmaf(-1152.f, q0, cb[nt][0]), c1 = fmaf(-1152.f, q1, cb[nt][1]);
-                        const float c2 = fmaf(-1152.f, q0, cb[nt][2]), c3 = fmaf(-1152.f, q1, cb[nt][3]);
-                        S_[nt][0] = fmaf(c0, sk0, S_[nt][0]);
-                        S_[nt][1] = fmaf(c1, sk0, S_[nt][1]);
-                        S_[nt][2] = fmaf(c2, sk1, S_[nt][2]);
-                        S_[nt][3] = fmaf(c3, sk1, S_[nt][3]);
+                        const uint4 qv = qf[(nt * KS + 2 * b + s) * 32 + lane];
+#pragma unroll
+                        for (int q = 0; q < KPW; ++q) {
+                            mma16816(cb[q][nt], a[q], qv.x, qv.y);
+                            mma16816(cb[q][nt], a[q], qv.z, qv.w);
+                        }
                     }
                 }
+                // the A operand carried 1152 + x: take 1152 * sum(q) of the block back out
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float q0 = qs[(nt * 8 + 2 * tig) * NB + b];
+                    const float q1 = qs[(nt * 8 + 2 * tig + 1) * NB + b];
+#pragma unroll
+                    for (int q = 0; q < KPW; ++q) {
+                        const float c0 = fmaf(-1152.f, q0, cb[q][nt][0]), c1 = fmaf(-1152.f, q1, cb[q][nt][1]);
+                        const float c2 = fmaf(-1152.f, q0, cb[q][nt][2]), c3 = fmaf(-1152.f, q1, cb[q][nt][3]);
+                        S_[q][nt][0] = fmaf(c0, sk0[q], S_[q][nt][0]);
+                        S_[q][nt][1] = fmaf(c1, sk0[q], S_[q][nt][1]);
+                        S_[q][nt][2] = fmaf(c2, sk1[q], S_[q][nt][2]);
+                        S_[q][nt][3] = fmaf(c3, sk1[q], S_[q][nt][3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < KPW; ++q) {
+                if (!kvalid[q]) continue;
+                const int k0 = 16 * kg[q] + gid, k1 = k0 + 8;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = (e < 2) ? k0 : k1;
-                        const int m = nt * 8 + 2 * tig + (e & 1);
-                        const bool valid = m < rows && kpos0 + key <= p.pos0 + m / G;
-                        sc[m * SP + key] = valid ? S_[nt][e] * p.scale_log2 : -INFINITY;
+                        const int m = nt * 8 + 2 * tig + (e & 1), mg = mo + m;
+                        const bool valid = mg < rows && kpos0 + key <= p.pos0 + mg / G;
+                        sc[m * SP + key] = valid ? S_[q][nt][e] * p.scale_log2 : -INFINITY;
                     }
                 }
             }
@@ -273,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
 
         // Softmax over the page's keys, one row per warp at a time.
         const int split = (int)page;
-        for (int m = warp; m < MR; m += 8) {
+        for (int m = warp; m < MR; m += W) {
             float mx = -INFINITY;
             for (int k = lane; k < P; k += 32) mx = fmaxf(mx, sc[m * SP + k]);
 #pragma unroll
@@ -290,87 +342,84 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             }
-            if (lane == 0) {
-                rmax[m] = mx;
-                rsum[m] = sum;
-                if (m < rows) {
-                    const int r = m / G, h = g * G + (m - r * G);
-                    float *ml = p.part_ml + (((int64_t)split * p.Hq + h) * R + r) * 2;
-                    ml[0] = mx;
-                    ml[1] = sum;
-                }
+            const int mg = mo + m;
+            if (lane == 0 && mg < rows) {
+                const int r = mg / G, h = g * G + (mg - r * G);
+                float *ml = p.part_ml + (((int64_t)split * p.Hq + h) * R + r) * 2;
+                ml[0] = mx;
+                ml[1] = sum;
             }
         }
         __syncthreads();
 
-        // O^T = V^T P'^T: warp -> (32-dim block b, key part).
-        int parts = 8 / NB;
-        if (parts > P / 32) parts = P / 32;
-        const int b = warp % NB, part = warp / NB;
-        // P' hi and P' lo parts on two independent MMA chains when registers allow
-        constexpr int NL = NT <= 2 ? NT : 1;
-        float acc[2][NT][4], accl[2][NL][4];
+        // O^T = V^T P'^T over key parts: job j = (dim block j % NB, key part j / NB).
+        // A warp owns every part of its block (kInReg) or one job.
+        int b, part0;
+        bool has_job;
+        if (kInReg) {
+            b = warp;
+            part0 = 0;
+            has_job = true;
+        } else {
+            b = warp % NB;
+            part0 = warp / NB;
+            has_job = part0 < parts;
+        }
+        const int kspan = P / parts;
+        float acc[PM][2][NT][4];
 #pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2)
+        for (int pp = 0; pp < PM; ++pp)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int i2 = 0; i2 < 2; ++i2)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i2][nt][e] = 0.f;
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2)
-#pragma unroll
-            for (int nt = 0; nt < NL; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) accl[i2][nt][e] = 0.f;
-        if (part < parts) {
-            const int kspan = P / parts;
+                    for (int e = 0; e < 4; ++e) acc[pp][i2][nt][e] = 0.f;
+        if (has_job) {
             const __half *vsc = reinterpret_cast<const __half *>(hs + p.geom.vs_off);
 #pragma unroll 1
-            for (int kb = part * kspan; kb < (part + 1) * kspan; kb += 32) {
-                const uint8_t *vl = hs + p.geom.vq_off + ((kb / 32 * NB + b) * 16) * 32 + 8 * tig;
-                const uint2 v0 = *reinterpret_cast<const uint2 *>(vl + gid * 32);
-                const uint2 v1 = *reinterpret_cast<const uint2 *>(vl + (gid + 8) * 32);
-                const uint4 dvr = *reinterpret_cast<const uint4 *>(vsc + b * P + kb + 8 * tig);
+            for (int i0 = 0; i0 < kspan; i0 += 32) {
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    uint32_t a0[4], a1[4];
-                    u4x8_to_frag16(s ? v0.y : v0.x, a0);
-                    u4x8_to_frag16(s ? v1.y : v1.x, a1);
-                    const float2 dA = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.z : &dvr.x));
-                    const float2 dB = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.w : &dvr.y));
+                for (int pp = 0; pp < PM; ++pp) {
+                    if (kInReg && pp >= parts) continue;
+                    const int kb = (kInReg ? pp : part0) * kspan + i0;
+                    const uint8_t *vl = hs + p.geom.vq_off + ((kb / 32 * NB + b) * 16) * 32 + 8 * tig;
+                    const uint2 v0 = *reinterpret_cast<const uint2 *>(vl + gid * 32);
+                    const uint2 v1 = *reinterpret_cast<const uint2 *>(vl + (gid + 8) * 32);
+                    const uint4 dvr = *reinterpret_cast<const uint4 *>(vsc + b * P + kb + 8 * tig);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float4 pv = *reinterpret_cast<const float4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
-                        uint32_t bh0, bl0, bh1, bl1;
-                        split_f16(pv.x * dA.x, pv.z * dB.x, bh0, bl0);  // keys +0, +2
-                        split_f16(pv.y * dA.y, pv.w * dB.y, bh1, bl1);  // keys +1, +3
-                        mma16816(acc[0][nt], a0, bh0, bh1);
-                        mma16816(acc[1][nt], a1, bh0, bh1);
-                        if constexpr (NT <= 2) {
-                            mma16816(accl[0][nt], a0, bl0, bl1);
-                            mma16816(accl[1][nt], a1, bl0, bl1);
-                        } else {
-                            mma16816(acc[0][nt], a0, bl0, bl1);
-                            mma16816(acc[1][nt], a1, bl0, bl1);
+                    for (int s = 0; s < 2; ++s) {
+                        uint32_t a0[4], a1[4];
+                        u4x8_to_frag16(s ? v0.y : v0.x, a0);
+                        u4x8_to_frag16(s ? v1.y : v1.x, a1);
+                        const float2 dA = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.z : &dvr.x));
+                        const float2 dB = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.w : &dvr.y));
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const float4 pv =
+                                *reinterpret_cast<const float4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
+                            uint32_t bh0, bl0, bh1, bl1;
+                            split_f16(pv.x * dA.x, pv.z * dB.x, bh0, bl0);  // keys +0, +2
+                            split_f16(pv.y * dA.y, pv.w * dB.y, bh1, bl1);  // keys +1, +3
+                            mma16816(acc[pp][0][nt], a0, bh0, bh1);
+                            mma16816(acc[pp][1][nt], a1, bh0, bh1);
+                            mma16816(acc[pp][0][nt], a0, bl0, bl1);
+                            mma16816(acc[pp][1][nt], a1, bl0, bl1);
                         }
                     }
                 }
             }
         }
-        // merge the chains; rows gid + 8 (high-nibble dims) carried 16 * (code - 8)
+        if (kInReg && parts > 1) {
 #pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2)
+            for (int i2 = 0; i2 < 2; ++i2)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                if constexpr (NT <= 2) {
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[i2][nt][e] += accl[i2][nt < NL ? nt : 0][e];
-                }
-                acc[i2][nt][2] *= 0.0625f;
-                acc[i2][nt][3] *= 0.0625f;
-            }
-        if (parts > 1 && part >= 1 && part < parts) {
-            float *dst = red + (part - 1) * MR * D;
+                    for (int e = 0; e < 4; ++e) acc[0][i2][nt][e] += acc[PM - 1][i2][nt][e];
+        }
+        if (!kInReg && has_job && part0 >= 1) {
+            float *dst = red + (part0 - 1) * MR * D;
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -379,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
                     for (int e = 0; e < 4; ++e) {
                         const int dim = 32 * b + mt * 8 + gid + ((e >= 2) ? 16 : 0);
                         const int m = nt * 8 + 2 * tig + (e & 1);
-                        dst[m * D + dim] = acc[mt][nt][e];
+                        dst[m * D + dim] = acc[0][mt][nt][e];
                     }
         }
         __syncthreads();  // every read of this stage (and of sc) is done
@@ -392,20 +441,23 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
                            bar0 + 16 * stage);
             }
         }
-        if (part == 0) {
-            for (int q = 1; q < parts; ++q) {
-                const float *src = red + (q - 1) * MR * D;
+        if (part0 == 0) {
+            if (!kInReg) {
+                for (int q = 1; q < parts; ++q) {
+                    const float *src = red + (q - 1) * MR * D;
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
+                        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int dim = 32 * b + mt * 8 + gid + ((e >= 2) ? 16 : 0);
-                            const int m = nt * 8 + 2 * tig + (e & 1);
-                            acc[mt][nt][e] += src[m * D + dim];
-                        }
+                            for (int e = 0; e < 4; ++e) {
+                                const int dim = 32 * b + mt * 8 + gid + ((e >= 2) ? 16 : 0);
+                                const int m = nt * 8 + 2 * tig + (e & 1);
+                                acc[0][mt][nt][e] += src[m * D + dim];
+                            }
+                }
             }
+            // rows gid + 8 (high-nibble dims) carried 16 * (code - 8)
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -414,14 +466,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) decode_kernel(const
                     for (int e = 0; e < 4; ++e) {
                         const int dim = 32 * b + mt * 8 + gid + ((e >= 2) ? 16 : 0);
                         const int m = nt * 8 + 2 * tig + (e & 1);
-                        obuf[m * D + dim] = acc[mt][nt][e];
+                        obuf[m * D + dim] = (e >= 2) ? acc[0][mt][nt][e] * 0.0625f : acc[0][mt][nt][e];
                     }
         }
         __syncthreads();
         // coalesced partial store of the valid rows
-        for (int c = threadIdx.x; c < rows * (D / 4); c += kThreads) {
-            const int m = c / (D / 4), d4 = (c % (D / 4)) * 4;
-            const int r = m / G, h = g * G + (m - r * G);
+        const int urows = rows - mo < MR ? rows - mo : MR;
+        for (int c = threadIdx.x; c < urows * (D / 4); c += NTH) {
+            const int m = c / (D / 4), d4 = (c % (D / 4)) * 4, mg = mo + m;
+            const int r = mg / G, h = g * G + (mg - r * G);
             *reinterpret_cast<float4 *>(p.part_o + (((int64_t)split * p.Hq + h) * R + r) * D + d4) =
                 *reinterpret_cast<const float4 *>(obuf + m * D + d4);
         }
@@ -491,7 +544,7 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
 
 int g_num_sms = 0;
 
-template <int D, int NT>
+template <int D, int NT, int W>
 cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     DecodeParams p = p_in;
     if (p.prep_q) {
@@ -501,109 +554,151 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
         if (p.n_items == 0) return cudaSuccess;
     }
     const int maxsm = 232448;
-    // one stage per CTA and two CTAs per SM when they fit (the other CTA's copy
-    // overlaps this one's compute); otherwise two stages in one CTA
-    int occ = NT == 1 ? 2 : 1;
-    DecodeSmem L = decode_smem(D, NT, p.geom.P, occ == 2 ? 1 : 2);
-    if (occ == 2 && 2 * (L.total + 1024) > 233472) occ = 1, L = decode_smem(D, NT, p.geom.P, 2);
-    if (L.total > maxsm) L = decode_smem(D, NT, p.geom.P, 1);
-    if (L.total > maxsm) return cudaErrorInvalidValue;
-    p.stages = L.stages;
-    static int configured = 0;
-    if (configured < L.total) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-        if (e != cudaSuccess) return e;
-        configured = L.total;
-    }
+    // W = 8, one row tile: one stage per CTA and two CTAs per SM when they fit
+    // (the other CTA's copy overlaps this one's compute); otherwise one CTA
+    // per SM with two stages
+    int occ = (NT == 1 && W == 8) ? 2 : 1;
     if (!g_num_sms) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
         if (g_num_sms <= 0) g_num_sms = 1;
     }
-    const int U = p.n_items * p.geom.Hk;
-    const int per_cta = (U + occ * g_num_sms - 1) / (occ * g_num_sms);
+    DecodeSmem L = decode_smem(D, NT, W, p.geom.P, occ == 2 ? 1 : 2);
+    if (occ == 2 && 2 * (L.total + 1024) > 233472) occ = 1, L = decode_smem(D, NT, W, p.geom.P, 2);
+    if (L.total > maxsm) L = decode_smem(D, NT, W, p.geom.P, 1);
+    if (L.total > maxsm) return cudaErrorInvalidValue;
+    p.stages = L.stages;
+    static int configured = 0;
+    if (configured < L.total) {
+        cudaError_t e =
+            cudaFuncSetAttribute(decode_kernel<D, NT, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+        if (e != cudaSuccess) return e;
+        configured = L.total;
+    }
+    const int U = p.n_items * p.geom.Hk * (p.tile_mode ? p.run_tiles : 1);
+    int max_ctas = occ * g_num_sms;
+    if (p.reserve_sms > 0) {  // leave reserve_sms SMs' worth of CTA slots free
+        const int keep = g_num_sms - (p.reserve_sms < g_num_sms / 2 ? p.reserve_sms : g_num_sms / 2);
+        max_ctas = occ * keep;
+    }
+    const int per_cta = (U + max_ctas - 1) / max_ctas;
     const int grid = (U + per_cta - 1) / per_cta;
-    decode_kernel<D, NT><<<grid, kThreads, L.total, s>>>(p);
+    decode_kernel<D, NT, W><<<grid, W * 32, L.total, s>>>(p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_decode_d(const DecodeParams &p, int nt, cudaStream_t s) {
+    if (p.tile_mode) return launch_decode_t<D, 1, 8>(p, s);
     switch (nt) {
-        case 1: return launch_decode_t<D, 1>(p, s);
-        case 2: return launch_decode_t<D, 2>(p, s);
-        case 3: return launch_decode_t<D, 3>(p, s);
-        case 4: return launch_decode_t<D, 4>(p, s);
-        case 5: return launch_decode_t<D, 5>(p, s);
-        case 6: return launch_decode_t<D, 6>(p, s);
-        case 7:
-        case 8: return launch_decode_t<D, 8>(p, s);
+        case 1: return launch_decode_t<D, 1, 8>(p, s);
+        case 2: return launch_decode_t<D, 2, 8>(p, s);
+        case 3: return launch_decode_t<D, 3, 8>(p, s);
+        case 4: return launch_decode_t<D, 4, 8>(p, s);
+        case 5: return launch_decode_t<D, 5, 8>(p, s);
+        case 6: return launch_decode_t<D, 6, 8>(p, s);
+        case 8: return launch_decode_t<D, 8, 8>(p, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
 // ------------------------------------------------------------------ combine
 
+// One CTA per (row, q head, 64-dim slice).  The largest split max M comes
+// first (every split's (m, l) is read once, in parallel); then each warp sums
+// w_s * o_s with w_s = 2^(m_s - M) over its splits s = warp, warp + 8, ...
+// (independent loads, no running rescale) and the eight warp sums are added
+// in warp order: a fixed order, so the result does not depend on timing.
+constexpr int kCombineDims = 64;
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
-    constexpr int VPL = D / 32;  // values per lane
-    __shared__ float wm[8], wl[8];
-    __shared__ float wo[8][D];
+    constexpr int DS = D < kCombineDims ? D : kCombineDims;
+    constexpr int VPL = DS / 32;  // dims per lane
+    constexpr int NW = kThreads / 32;
+    __shared__ float wmax[NW], wl[NW];
+    __shared__ float wo[NW][DS];
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
+    const int d0 = blockIdx.y * DS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
-    float M = -INFINITY, Lsum = 0.f, o[VPL];
+    auto base_of = [&](int s) { return ((int64_t)s * p.Hq + h) * p.R + r; };
+
+    float mx = -INFINITY;
+    for (int s = threadIdx.x; s < nsplit; s += kThreads) {
+        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2);
+        if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) wmax[warp] = mx;
+    __syncthreads();
+    float M = wmax[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) M = fmaxf(M, wmax[w]);
+
+    float o[VPL], Ls = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) o[i] = 0.f;
-    for (int s = warp; s < nsplit; s += 8) {
-        const int64_t base = ((int64_t)s * p.Hq + h) * p.R + r;
-        const float ms = p.part_ml[base * 2], ls = p.part_ml[base * 2 + 1];
-        if (!(ls > 0.f)) continue;
-        const float Mn = fmaxf(M, ms);
-        const float a = exp2f(M - Mn), c = exp2f(ms - Mn);
-        const float *src = p.part_o + base * D + lane * VPL;
-        float v[VPL];
+    if (M != -INFINITY) {
+        constexpr int U4 = 4;  // splits in flight per warp
+        for (int s0 = warp; s0 < nsplit; s0 += NW * U4) {
+            float w[U4], l[U4], v[U4][VPL];
 #pragma unroll
-        for (int i = 0; i < VPL; i += 2) {
-            const float2 t = *reinterpret_cast<const float2 *>(src + i);
-            v[i] = t.x;
-            v[i + 1] = t.y;
+            for (int j = 0; j < U4; ++j) {
+                const int s = s0 + j * NW;
+                w[j] = 0.f;
+                l[j] = 0.f;
+                if (s < nsplit) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2);
+                    if (ml.y > 0.f) {
+                        w[j] = exp2f(ml.x - M);
+                        l[j] = ml.y;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) v[j][i] = 0.f;
+                if (w[j] > 0.f) {
+                    const float *src = p.part_o + base_of(s) * D + d0 + lane * VPL;
+                    if (VPL == 2) {
+                        const float2 t = *reinterpret_cast<const float2 *>(src);
+                        v[j][0] = t.x;
+                        v[j][VPL - 1] = t.y;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < VPL; ++i) v[j][i] = src[i];
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < U4; ++j) {
+                if (!(w[j] > 0.f)) continue;
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) o[i] = fmaf(w[j], v[j][i], o[i]);
+                Ls = fmaf(w[j], l[j], Ls);
+            }
         }
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) o[i] = o[i] * a + v[i] * c;
-        Lsum = Lsum * a + ls * c;
-        M = Mn;
     }
-    if (lane == 0) {
-        wm[warp] = M;
-        wl[warp] = Lsum;
-    }
+    if (lane == 0) wl[warp] = Ls;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) wo[warp][lane * VPL + i] = o[i];
     __syncthreads();
     if (warp == 0) {
-        float Mt = -INFINITY;
-        for (int w = 0; w < 8; ++w)
-            if (wl[w] > 0.f) Mt = fmaxf(Mt, wm[w]);
         float Lt = 0.f, ot[VPL];
 #pragma unroll
         for (int i = 0; i < VPL; ++i) ot[i] = 0.f;
-        if (Mt != -INFINITY) {
-            for (int w = 0; w < 8; ++w) {
-                if (!(wl[w] > 0.f)) continue;
-                const float c = exp2f(wm[w] - Mt);
-                Lt += wl[w] * c;
+        for (int w = 0; w < NW; ++w) {
+            Lt += wl[w];
 #pragma unroll
-                for (int i = 0; i < VPL; ++i) ot[i] += wo[w][lane * VPL + i] * c;
-            }
+            for (int i = 0; i < VPL; ++i) ot[i] += wo[w][lane * VPL + i];
         }
-        float *dst = p.out + ((int64_t)r * p.Hq + h) * D + lane * VPL;
+        float *dst = p.out + ((int64_t)r * p.Hq + h) * D + d0 + lane * VPL;
         const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) dst[i] = ot[i] * inv;
-        if (p.lse && lane == 0)
-            p.lse[(int64_t)r * p.Hq + h] = (Lt > 0.f) ? (Mt + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+        if (p.lse && lane == 0 && blockIdx.y == 0)
+            p.lse[(int64_t)r * p.Hq + h] = (Lt > 0.f) ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
     }
 }
 
@@ -614,11 +709,15 @@ int decode_max_mma_rows() { return 64; }
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s) {
     const int rows = p.G * p.R;
     if (rows < 1 || rows > 64 || (p.n_items < 1 && !p.prep_q) || p.n_items > kMaxItems) return cudaErrorInvalidValue;
+    if (p.tile_mode && p.prep_q) return cudaErrorInvalidValue;
     const int nt = (rows + 7) / 8;
+    DecodeParams q = p;
+    q.qtiles = nt == 7 ? 8 : nt;  // row tiles of the fragment layout (the variant's)
+    q.run_tiles = nt;
     switch (p.geom.D) {
-        case 64: return launch_decode_d<64>(p, nt, s);
-        case 128: return launch_decode_d<128>(p, nt, s);
-        case 256: return launch_decode_d<256>(p, nt, s);
+        case 64: return launch_decode_d<64>(q, q.qtiles, s);
+        case 128: return launch_decode_d<128>(q, q.qtiles, s);
+        case 256: return launch_decode_d<256>(q, q.qtiles, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -626,10 +725,11 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s) {
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s) {
     const int blocks = p.R * p.Hq;
     if (blocks < 1) return cudaSuccess;
+    const dim3 grid(blocks, p.D > kCombineDims ? p.D / kCombineDims : 1);
     switch (p.D) {
-        case 64: combine_kernel<64><<<blocks, kThreads, 0, s>>>(p); break;
-        case 128: combine_kernel<128><<<blocks, kThreads, 0, s>>>(p); break;
-        case 256: combine_kernel<256><<<blocks, kThreads, 0, s>>>(p); break;
+        case 64: combine_kernel<64><<<grid, kThreads, 0, s>>>(p); break;
+        case 128: combine_kernel<128><<<grid, kThreads, 0, s>>>(p); break;
+        case 256: combine_kernel<256><<<grid, kThreads, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -65,6 +65,10 @@ struct DecodeParams {
     const uint4 *qf;       // Q fragments [Hk][NT][D/16][32] (written by the Q prep kernel)
     const float *qs;       // per-block sums of Q [Hk][NT*8][D/32]
     int prep_q;            // launch_decode first (re)builds qf/qs from q
+    int tile_mode;         // one CTA per (page, kv head, row tile) (ring chunks)
+    int reserve_sms;       // leave this many SMs free of this launch (capped at half the GPU):
+                           // one CTA per SM, so concurrent ring-chunk launches find whole SMs
+    int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run
     int n_items;
     uint32_t page[kMaxItems];
     uint32_t slot[kMaxItems];
@@ -143,7 +147,9 @@ struct FillParams {
     const uint8_t *src[kMaxFillPages];
     uint8_t *dst[kMaxFillPages];
 };
-cudaError_t launch_fill(const FillParams &p, cudaStream_t s);
+// pdl: programmatic dependent launch (may start once the previous kernel on
+// `s` has signalled its dependents; see decode_kernel)
+cudaError_t launch_fill(const FillParams &p, cudaStream_t s, bool pdl = false);
 
 // Message returned by kvs_last_error(NULL) on this thread.
 void set_thread_error(const std::string &msg);

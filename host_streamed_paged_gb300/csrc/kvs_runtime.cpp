@@ -111,7 +111,8 @@ struct kvs_ctx {
     std::vector<cudaEvent_t> events;
     int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0, ev_lane0 = 0, ev_pub_last = 0;
     uint64_t pub_generation = 0;        // publishes recorded on the copy stream
-    std::vector<uint64_t> lane_pub_seen;  // per lane: pub_generation its copy stream has waited for
+    std::vector<uint64_t> lane_pub_seen;  // per stream: pub_generation it has waited for
+    std::vector<int> chunk_reader_sid;    // per chunk id % ring_n: stream its attention read ran on
 
     // timing of attention kernels (mask of KVS_TIME_*)
     uint32_t timing = 0;
@@ -147,7 +148,13 @@ struct kvs_ctx {
         return host_dev + ((int64_t)layer * max_pages + page) * geom.page_bytes;
     }
     cudaStream_t stream(int s) const { return lanes[s]; }
-    int n_streams() const { return 2 * n_lanes; }
+    // lane streams, then the library's own resident-page stream (id res_sid())
+    int n_streams() const { return 2 * n_lanes + 1; }
+    int res_sid() const { return 2 * n_lanes; }
+    cudaStream_t res_stream = nullptr;  // created by kvs_create, lowest priority
+    ~kvs_ctx() {
+        if (res_stream) cudaStreamDestroy(res_stream);
+    }
 };
 
 namespace {
@@ -217,24 +224,25 @@ kvs_status join(kvs_ctx *c, int from, int to) {
     return s != KVS_OK ? s : op_wait(c, to, c->ev_lane0 + from);
 }
 
-// every other lane stream waits for the primary stream of its kind
+// every other lane stream waits for the primary stream of its kind (the
+// resident-page stream counts as an attention stream)
 kvs_status fork_lanes(kvs_ctx *c) {
     for (int l = 1; l < c->n_lanes; ++l) {
         kvs_status s = join(c, kAttn, 2 * l);
         if (s == KVS_OK) s = join(c, kCopy, 2 * l + 1);
         if (s != KVS_OK) return s;
     }
-    return KVS_OK;
+    return join(c, kAttn, c->res_sid());
 }
 
-// the other attention lanes wait for the primary attention stream (inputs
+// the other attention streams wait for the primary attention stream (inputs
 // of this call in place, the previous combine done with the partials)
 kvs_status fork_attn_lanes(kvs_ctx *c) {
     for (int l = 1; l < c->n_lanes; ++l) {
         kvs_status s = join(c, kAttn, 2 * l);
         if (s != KVS_OK) return s;
     }
-    return KVS_OK;
+    return join(c, kAttn, c->res_sid());
 }
 
 // a publish (D2H of a completed tail page) was just enqueued on the copy
@@ -242,11 +250,11 @@ kvs_status fork_attn_lanes(kvs_ctx *c) {
 kvs_status mark_publish(kvs_ctx *c) {
     kvs_status s = op_record(c, kCopy, c->ev_pub_last);
     if (s == KVS_OK) c->pub_generation++;
-    c->lane_pub_seen[0] = c->pub_generation;  // lane 0 is the copy stream itself
+    c->lane_pub_seen[kCopy] = c->pub_generation;  // the copy stream itself
     return s;
 }
 
-// the primary attention stream waits for the other attention lanes
+// the primary attention stream waits for the other attention streams
 kvs_status join_attn_lanes_into_attn(kvs_ctx *c) {
     for (int sid = 2; sid < c->n_streams(); sid += 2) {
         kvs_status s = join(c, sid, kAttn);
@@ -267,11 +275,24 @@ kvs_status join_all_into_attn(kvs_ctx *c) {
 // host pages -> device slots on the copy stream (ring fill or pool load)
 kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
                          const std::vector<int64_t> &slots, uint32_t kind,
-                         const std::vector<uint64_t> *seqs, int sid = kCopy) {
-    c->st.kernel_launches += (pages.size() + kvs::kMaxFillPages - 1) / kvs::kMaxFillPages;
+                         const std::vector<uint64_t> *seqs, int sid = kCopy, bool pdl = false) {
+    if (!(c->cfg.flags & KVS_FLAG_DMA_FILL))
+        c->st.kernel_launches += (pages.size() + kvs::kMaxFillPages - 1) / kvs::kMaxFillPages;
     if (c->plan_only) {
         for (size_t i = 0; i < pages.size(); ++i)
             log_op(c, kind, sid, layer, 0, pages[i], slots[i], seqs ? (int64_t)(*seqs)[i] : 0);
+        return KVS_OK;
+    }
+    if (c->cfg.flags & KVS_FLAG_DMA_FILL) {
+        for (size_t i = 0; i < pages.size();) {
+            size_t j = i + 1;
+            while (j < pages.size() && pages[j] == pages[j - 1] + 1 && slots[j] == slots[j - 1] + 1) ++j;
+            cudaError_t e = cudaMemcpyAsync(c->slot_ptr(slots[i]), c->host_page(layer, pages[i]),
+                                            (size_t)(j - i) * (size_t)c->geom.page_bytes, cudaMemcpyHostToDevice,
+                                            c->stream(sid));
+            if (e != cudaSuccess) return cuda_fail(c, e, "ring/pool copy");
+            i = j;
+        }
         return KVS_OK;
     }
     for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxFillPages) {
@@ -282,7 +303,7 @@ kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> 
             fp.src[j] = c->host_page_dev(layer, pages[i0 + j]);
             fp.dst[j] = c->slot_ptr(slots[i0 + j]);
         }
-        cudaError_t e = kvs::launch_fill(fp, c->stream(sid));
+        cudaError_t e = kvs::launch_fill(fp, c->stream(sid), pdl && i0 == 0);
         if (e != cudaSuccess) return cuda_fail(c, e, "ring/pool fill launch");
     }
     return KVS_OK;
@@ -358,7 +379,7 @@ kvs_status create_events(kvs_ctx *c) {
     c->ev_lane0 = c->ev_pub0 + 2 * (int)c->cfg.n_layers;
     c->ev_pub_last = c->ev_lane0 + c->n_streams();
     c->pub_generation = 0;
-    c->lane_pub_seen.assign(c->n_lanes, 0);
+    c->lane_pub_seen.assign(c->n_streams(), 0);
     c->events.assign(n, nullptr);
     if (c->plan_only) return KVS_OK;
     for (int i = 0; i < n; ++i) {
@@ -440,6 +461,12 @@ int evict_target(const kvs_ctx *c, uint32_t layer, int64_t page, int64_t free_po
 
 // ---- ring scheduling
 
+// chunk size when the caller leaves it open: a quarter of the ring, so four
+// chunks are in flight, and at most 32 pages so one chunk's copy stays short
+uint32_t default_chunk_pages(uint32_t ring_slots) {
+    return std::min(32u, std::max(1u, ring_slots / 4));
+}
+
 // Plan the nonresident pages of `layer` into chunks at the end of the queue.
 void plan_layer(kvs_ctx *c, uint32_t layer) {
     const int64_t np = n_pages_of(c, layer);
@@ -480,23 +507,35 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
         if (++c->fault_count == c->fault_nth)
             return fail(c, KVS_ERR_INJECTED, "injected fault: ring refill enqueue");
     }
-    const int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes) + 1;  // this chunk's copy lane
-    // wait for the last reader of every slot (readers may sit on different lanes)
+    // the last reader of every slot (readers may sit on different streams)
     std::vector<int64_t> prev;
     for (size_t i = 0; i < ch.pages.size(); ++i) {
         const int64_t p = c->slot_last_chunk[(ch.seq0 + i) % c->ring_n];
         if (p >= 0 && std::find(prev.begin(), prev.end(), p) == prev.end()) prev.push_back(p);
     }
+    // Immediate recycle: when every previous reader ran on one attention
+    // stream, the refill follows them on that stream as a programmatic
+    // dependent launch.  An attention CTA signals its dependents once its
+    // page sections sit in shared memory, so the copy overlaps the rest of
+    // the read; stream order covers the slots.  Otherwise the refill goes to
+    // the chunk's copy lane and waits for each reader's consumed event.
+    int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes) + 1;  // this chunk's copy lane
+    bool follow = !prev.empty();
+    const int rsid = follow ? c->chunk_reader_sid[prev[0] % c->ring_n] : -1;
+    for (int64_t p : prev) follow = follow && rsid >= 0 && c->chunk_reader_sid[p % c->ring_n] == rsid;
     kvs_status s;
-    for (int64_t p : prev) {
-        s = op_wait(c, sid, (int)c->ring_n + (int)(p % c->ring_n));
-        if (s != KVS_OK) return s;
+    if (follow) {
+        sid = rsid;
+    } else {
+        for (int64_t p : prev) {
+            s = op_wait(c, sid, (int)c->ring_n + (int)(p % c->ring_n));
+            if (s != KVS_OK) return s;
+        }
     }
-    const int lane = sid / 2;
-    if (c->lane_pub_seen[lane] < c->pub_generation) {  // host pages published since: wait for them
+    if (c->lane_pub_seen[sid] < c->pub_generation) {  // host pages published since: wait for them
         s = op_wait(c, sid, c->ev_pub_last);
         if (s != KVS_OK) return s;
-        c->lane_pub_seen[lane] = c->pub_generation;
+        c->lane_pub_seen[sid] = c->pub_generation;
     }
     std::vector<int64_t> slots(ch.pages.size());
     std::vector<uint64_t> seqs(ch.pages.size());
@@ -504,7 +543,7 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
         seqs[i] = ch.seq0 + i;
         slots[i] = c->ring_slot_id(ch.seq0 + i);
     }
-    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs, sid);
+    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs, sid, follow);
     if (s != KVS_OK) return s;
     s = op_record(c, sid, (int)(ch.id % c->ring_n));
     if (s != KVS_OK) return s;
@@ -513,6 +552,7 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
         if (last >= 0) c->st.ring_recycles++;
         last = (int64_t)ch.id;
     }
+    c->chunk_reader_sid[ch.id % c->ring_n] = -1;
     c->st.h2d_pages += ch.pages.size();
     c->st.h2d_bytes += ch.pages.size() * (uint64_t)c->geom.page_bytes;
     c->st.h2d_launches += 1;
@@ -548,6 +588,9 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
             continue;
         }
         dp.n_items = n;
+        // ring chunks: one CTA per (page, kv head, row tile), so the chunk's
+        // slots are read (and can be refilled) as soon as possible
+        dp.tile_mode = kind == KVS_TIME_RING ? 1 : 0;
         for (int j = 0; j < n; ++j) {
             dp.page[j] = (uint32_t)pages[i0 + j];
             dp.slot[j] = (uint32_t)slots[i0 + j];
@@ -679,8 +722,8 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         g_create_error = "ring_slots must be >= 1";
         return KVS_ERR_INVALID;
     }
-    if (cfg->n_lanes > 4) {
-        g_create_error = "n_lanes must be 1..4";
+    if (cfg->n_lanes > 8) {
+        g_create_error = "n_lanes must be 1..8";
         return KVS_ERR_INVALID;
     }
     if (!cfg->arena || cfg->arena_bytes < arena_min) {
@@ -722,12 +765,13 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
     c->n_slots = (int64_t)(cfg->arena_bytes / (uint64_t)c->geom.page_bytes);
     c->ring_n = cfg->ring_slots;
     c->chunk_pages = cfg->chunk_pages ? std::min(cfg->chunk_pages, cfg->ring_slots)
-                                      : std::max(1u, cfg->ring_slots / 4);
+                                      : default_chunk_pages(cfg->ring_slots);
     c->ring_first = c->n_slots - c->ring_n;
     c->pool_n = c->ring_first - 2 * (int64_t)cfg->n_layers;
     c->pool_layer.assign(c->pool_n, -1);
     c->pool_page.assign(c->pool_n, -1);
     c->slot_last_chunk.assign(c->ring_n, -1);
+    c->chunk_reader_sid.assign(c->ring_n, -1);
     memset(&c->st, 0, sizeof(c->st));
     c->host = static_cast<uint8_t *>(cfg->host);
     c->host_dev = c->host;
@@ -763,6 +807,23 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         }
         c->host_dev = static_cast<uint8_t *>(dp);
     }
+    c->lanes.push_back(nullptr);  // the resident-page stream
+    if (!plan_only) {
+        // resident pages of a layer that also reads ring chunks run beside
+        // them at the lowest priority: ring reads gate the refills, resident
+        // reads only fill the remaining SMs
+        int least = 0, greatest = 0;
+        cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        cudaError_t e = cudaStreamCreateWithPriority(&c->res_stream, cudaStreamNonBlocking, least);
+        if (e != cudaSuccess) {
+            c->res_stream = nullptr;
+            if (c->host_registered) cudaHostUnregister(cfg->host);
+            delete c;
+            g_create_error = std::string("cudaStreamCreateWithPriority: ") + cudaGetErrorString(e);
+            return KVS_ERR_CUDA;
+        }
+        c->lanes.back() = c->res_stream;
+    }
     if (create_events(c) != KVS_OK) {
         g_create_error = c->err;
         destroy_events(c);
@@ -781,6 +842,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         }
     }
     c->st.ring_slots = c->ring_n;
+    c->st.chunk_pages = c->chunk_pages;
     c->st.pool_slots = (uint64_t)c->pool_n;
     *out = c;
     return KVS_OK;
@@ -1059,7 +1121,7 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     c->graph_kernels = 0;
     destroy_events(c);
     c->ring_n = n_slots;
-    c->chunk_pages = chunk_pages ? std::min(chunk_pages, n_slots) : std::max(1u, n_slots / 4);
+    c->chunk_pages = chunk_pages ? std::min(chunk_pages, n_slots) : default_chunk_pages(n_slots);
     c->ring_first = c->n_slots - n_slots;
     c->pool_layer.resize(new_pool);
     c->pool_page.resize(new_pool);
@@ -1069,8 +1131,10 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     }
     c->pool_n = new_pool;
     c->slot_last_chunk.assign(c->ring_n, -1);
+    c->chunk_reader_sid.assign(c->ring_n, -1);
     c->ring_seq = 0;
     c->st.ring_slots = c->ring_n;
+    c->st.chunk_pages = c->chunk_pages;
     c->st.pool_slots = (uint64_t)c->pool_n;
     return create_events(c);
 }
@@ -1210,6 +1274,7 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
             c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
         }
         for (Chunk *ch : group) {
+            c->chunk_reader_sid[ch->id % c->ring_n] = kAttn;
             s = op_record(c, kAttn, (int)c->ring_n + (int)(ch->id % c->ring_n));
             if (s != KVS_OK) return s;
             c->attended = ch->id + 1;
@@ -1318,9 +1383,21 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         if (s != KVS_OK) return s;
         s = pump(c);
         if (s != KVS_OK) return s;
-        // resident and tail pages need no fence
+        // resident and tail pages need no fence.  When the layer also reads
+        // ring chunks they go to the low-priority resident stream and leave
+        // room (two chunk-read CTAs per SM) for the chunk reads in flight:
+        // lanes x chunk pages x kv heads x row tiles.
         if (!res_pages.empty()) {
-            s = launch_items(c, layer, res_pages, res_slots, dp, KVS_TIME_RESIDENT);
+            const bool ring_too = !c->queue.empty() && c->queue.front().layer == layer;
+            int sid = kAttn;
+            if (ring_too) {
+                sid = c->res_sid();
+                const int64_t ring_ctas =
+                    (int64_t)c->n_lanes * c->chunk_pages * c->geom.Hk * ((G * n_rows + 7) / 8);
+                dp.reserve_sms = (int)std::min<int64_t>(1 << 20, (ring_ctas + 1) / 2);
+            }
+            s = launch_items(c, layer, res_pages, res_slots, dp, KVS_TIME_RESIDENT, sid);
+            dp.reserve_sms = 0;
             if (s != KVS_OK) return s;
             c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
         }
@@ -1346,6 +1423,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
                 if (s != KVS_OK) return s;
                 c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
             }
+            c->chunk_reader_sid[ch.id % c->ring_n] = sid;
             s = op_record(c, sid, (int)c->ring_n + (int)(ch.id % c->ring_n));
             if (s != KVS_OK) return s;
             c->attended = ch.id + 1;
@@ -1500,6 +1578,7 @@ kvs_status kvs_stats(kvs_ctx *c, kvs_stats_t *out, int reset) {
     if (!c || !out) return KVS_ERR_INVALID;
     if (!c->plan_only) harvest_timers(c);
     c->st.ring_slots = c->ring_n;
+    c->st.chunk_pages = c->chunk_pages;
     c->st.pool_slots = (uint64_t)c->pool_n;
     c->st.pool_used = (uint64_t)c->pool_used;
     *out = c->st;

@@ -33,6 +33,7 @@ KVS_TYPE_Q8_0 = 8
 KVS_F32 = 0
 KVS_F16 = 1
 KVS_FLAG_PLAN_ONLY = 1
+KVS_FLAG_DMA_FILL = 2
 
 KVS_OP_RECORD, KVS_OP_WAIT, KVS_OP_FILL, KVS_OP_READ, KVS_OP_POOL_LOAD = 1, 2, 3, 4, 5
 KVS_OP_PUBLISH, KVS_OP_WRITE, KVS_OP_LAUNCH, KVS_OP_MOVE = 6, 7, 8, 9
@@ -62,8 +63,8 @@ class kvs_config(ctypes.Structure):
         ("copy_stream", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
         ("n_lanes", ctypes.c_uint32),
-        ("lane_attn_streams", ctypes.c_void_p * 3),
-        ("lane_copy_streams", ctypes.c_void_p * 3),
+        ("lane_attn_streams", ctypes.c_void_p * 7),
+        ("lane_copy_streams", ctypes.c_void_p * 7),
         ("prefill_split_pages", ctypes.c_uint32),
     ]
 
@@ -74,7 +75,8 @@ class kvs_stats_t(ctypes.Structure):
         "ring_chunks", "ring_recycles", "resident_pages_read", "ring_pages_read", "attend_calls",
         "kernel_launches", "decode_launches")] + [("decode_ms", ctypes.c_double)] + [
         (n, ctypes.c_uint64) for n in ("decode_timed", "decode_bytes", "ring_slots", "pool_slots",
-                                       "pool_used", "graph_launches", "graph_kernels")]
+                                       "pool_used", "graph_launches", "graph_kernels",
+                                       "chunk_pages")]
 
 
 class kvs_trace_op(ctypes.Structure):
@@ -318,7 +320,7 @@ class KVStream:
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
                  max_tokens, ring_slots=8, chunk_pages=0, arena_slots=None, arena_bytes=None,
                  plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None,
-                 prefill_split_pages=0):
+                 prefill_split_pages=0, dma_fill=False):
         cfg = kvs_config()
         cfg.page_tokens, cfg.n_layers, cfg.n_kv_head, cfg.head_dim = page_tokens, n_layers, n_kv_head, head_dim
         cfg.max_q_head, cfg.max_rows, cfg.max_tokens = max_q_head, max_rows, max_tokens
@@ -326,6 +328,7 @@ class KVStream:
         cfg.ring_slots, cfg.chunk_pages = ring_slots, chunk_pages
         cfg.n_lanes = lanes
         cfg.prefill_split_pages = prefill_split_pages
+        cfg.flags = KVS_FLAG_DMA_FILL if dma_fill else 0
         self.page_bytes, host_bytes, arena_min, ws_bytes = kvs_query_sizes(cfg)
         self.max_pages = math.ceil(max_tokens / page_tokens)
         if arena_bytes is None:
@@ -335,7 +338,7 @@ class KVStream:
         self.plan_only = plan_only
         self.geom = dict(P=page_tokens, L=n_layers, Hk=n_kv_head, D=head_dim)
         if plan_only:
-            cfg.flags = KVS_FLAG_PLAN_ONLY
+            cfg.flags |= KVS_FLAG_PLAN_ONLY
             cfg.arena, cfg.workspace = 1 << 20, 1 << 21  # never dereferenced
             cfg.host = 0
             self.arena = self.workspace = self.host = None

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define KVS_ABI_VERSION 1
+#define KVS_ABI_VERSION 2
 
 typedef struct kvs_ctx kvs_ctx;
 
@@ -76,6 +76,11 @@ typedef enum { KVS_F32 = 0, KVS_F16 = 1 } kvs_dtype;
                                  operation the context would enqueue is logged
                                  for kvs_trace_read.  For testing the host-side
                                  planner on machines without a GPU. */
+#define KVS_FLAG_DMA_FILL 2u  /* ring refills and pool loads by the copy engines
+                                 (one cudaMemcpyAsync per run of pages that are
+                                 consecutive in both host and device memory)
+                                 instead of the SM-driven fill kernel: no SM
+                                 time, a fixed cost per copy */
 
 typedef struct {
     uint32_t page_tokens;  /* P: token positions per page; 32, 64, 128 or 256 */
@@ -96,16 +101,17 @@ typedef struct {
                               registered with CUDA by kvs_create if not already pinned */
     uint64_t host_bytes;
     uint32_t ring_slots;   /* initial ring size in page slots (>= 1) */
-    uint32_t chunk_pages;  /* ring pages per ready/consumed handshake; 0: max(1, ring_slots/4) */
+    uint32_t chunk_pages;  /* ring pages per ready/consumed handshake; 0: ring_slots/4
+                              clamped to 1..32 */
     void *attn_stream;     /* cudaStream_t for attention, quantise/append and pool moves */
     void *copy_stream;     /* cudaStream_t for ring refills, pool loads and D2H publish */
     uint32_t flags;        /* KVS_FLAG_* */
-    uint32_t n_lanes;      /* ring pipelines, 1..4 (0 = 1): ring chunk j is copied on copy
+    uint32_t n_lanes;      /* ring pipelines, 1..8 (0 = 1): ring chunk j is copied on copy
                               lane j % n_lanes and attended on attention lane j % n_lanes, so
                               neighbouring chunks' copies and reads overlap; lane 0 is
                               (attn_stream, copy_stream) */
-    void *lane_attn_streams[3];  /* cudaStream_t of attention lanes 1 .. n_lanes-1 */
-    void *lane_copy_streams[3];  /* cudaStream_t of copy lanes 1 .. n_lanes-1 */
+    void *lane_attn_streams[7];  /* cudaStream_t of attention lanes 1 .. n_lanes-1 */
+    void *lane_copy_streams[7];  /* cudaStream_t of copy lanes 1 .. n_lanes-1 */
     uint32_t prefill_split_pages; /* pages per split of the tensor-core prefill path (0 = 8,
                                      at most ring_slots); when max_q_head * max_rows allows
                                      that path, ring chunks never cross a split */
@@ -133,6 +139,7 @@ typedef struct {
     uint64_t pool_used;        /* pool slots holding a resident page */
     uint64_t graph_launches;   /* kvs_graph_launch calls */
     uint64_t graph_kernels;    /* kernels in the captured step graph */
+    uint64_t chunk_pages;      /* current ring chunk size, pages */
 } kvs_stats_t;
 
 /* One logged operation of a KVS_FLAG_PLAN_ONLY context (see kvs_trace_read). */

@@ -26,11 +26,11 @@ def queries(seed, layer, R, Hq, D, tag="Q"):
     return synth.normal(seed, synth.tag(tag, layer), (R, Hq, D))
 
 
-def make_stream(P, L, Hk, D, Hq, R, max_tokens, ring=8, chunk=0, pool_pages=None, lanes=1):
+def make_stream(P, L, Hk, D, Hq, R, max_tokens, ring=8, chunk=0, pool_pages=None, lanes=1, dma=False):
     pool = pool_pages if pool_pages is not None else L * math.ceil(max_tokens / P)
     return kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq,
                         max_rows=R, max_tokens=max_tokens, ring_slots=ring, chunk_pages=chunk,
-                        arena_slots=2 * L + ring + pool, lanes=lanes)
+                        arena_slots=2 * L + ring + pool, lanes=lanes, dma_fill=dma)
 
 
 def append_rows(st, layer, k, v, pieces=None):

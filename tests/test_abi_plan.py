@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     for name in sorted(declared):
         assert hasattr(lib, name), name
     assert declared <= set(kvs.SIGNATURES), declared - set(kvs.SIGNATURES)
-    assert kvs.kvs_version() == 1
+    assert kvs.kvs_version() == 2
 
 
 def _cfg(**kw):
@@ -99,8 +99,10 @@ def test_create_refusals():
 class HB:
     """Happens-before over a logged two-stream trace (vector clocks)."""
 
-    def __init__(self, trace, n_streams=8):
+    def __init__(self, trace, n_streams=None):
         self.ops = []
+        if n_streams is None:
+            n_streams = 1 + max([t["stream"] for t in trace] + [0])
         vc = [[0] * n_streams for _ in range(n_streams)]
         ev = {}
         for t in trace:
@@ -180,7 +182,7 @@ def test_scheduler_random_residency_fences_and_coverage(seed):
     Hk = int(rng.integers(1, 3))
     ring = int(rng.integers(1, 17))
     chunk = int(rng.integers(0, ring + 1))
-    lanes = int(rng.integers(1, 5))
+    lanes = int(rng.integers(1, 9))
     T0 = int(rng.integers(1, 40 * P))
     max_tokens = T0 + 4 * P
     npages_max = math.ceil(max_tokens / P)

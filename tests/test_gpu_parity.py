@@ -174,11 +174,16 @@ def test_f16_queries():
 
 # ------------------------------------------------------------ invariants
 
-@pytest.mark.parametrize("lanes", [1, 3])
-def test_streamed_equals_resident_bitwise(lanes):
-    P, L, Hk, G, D, R, T = 64, 2, 2, 6, 256, 3, 64 * 10 + 33
+# Resident pages go through the multi-tile attention launch, ring chunks
+# through the one-tile-per-CTA launch: the output must not depend on which.
+@pytest.mark.parametrize("lanes,R,D,P,dma", [(1, 3, 256, 64, False), (3, 3, 256, 64, False), (8, 1, 256, 64, False),
+                                             (4, 6, 256, 128, False), (2, 5, 128, 64, False),
+                                             (5, 2, 64, 256, False), (4, 6, 256, 64, True), (1, 1, 128, 64, True)])
+def test_streamed_equals_resident_bitwise(lanes, R, D, P, dma):
+    L, Hk, G = 2, 2, 6
+    T = P * (640 // P) + 33
     Hq = G * Hk
-    st = make_stream(P, L, Hk, D, Hq, R, T, ring=8, chunk=2, lanes=lanes)
+    st = make_stream(P, L, Hk, D, Hq, R, T, ring=8, chunk=2, lanes=lanes, dma=dma)
     hist = _fill(st, L, T, Hk, D)
     npages = math.ceil(T / P)
     qs = [queries(SEED, l, R, Hq, D) for l in range(L)]
@@ -202,7 +207,7 @@ def test_streamed_equals_resident_bitwise(lanes):
             assert np.array_equal(out, base[l][0]), f"ring {ring} chunk {chunk} layer {l}"
             assert np.array_equal(lse, base[l][1])
         s = st.stats()
-        assert s["h2d_pages"] > 0 and (ring == 8 or s["ring_recycles"] > 0)
+        assert s["h2d_pages"] > 0 and (s["h2d_pages"] <= ring or s["ring_recycles"] > 0)
 
 
 def test_page_size_changes_result_only_within_tolerance():
