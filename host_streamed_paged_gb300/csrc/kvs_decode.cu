@@ -32,11 +32,10 @@
 // The int8 -> f16 and nibble -> f16 conversions use the exponent-bias trick
 // described by Kim et al., "Who Says Elephants Can't Run: Bringing Large
 // Scale MoE Models into Cloud Scale Production" (2022): a small integer u
-// placed in the mantissa under exponent 0x64 is the half 1024 + u.  K codes
-// enter the MMA as 1152 + x (no subtraction); 1152 * sum(q) over each 32-dim
-// block is removed from the fp32 block dot afterwards (q has both signs, so the
-// offset costs well under 1e-5 relative).  High V nibbles are taken in
-// mantissa bits 4-7 as 16 * (code - 8) and their output rows scaled by 1/16.
+// placed in the mantissa under exponent 0x64 is the half 1024 + u.  A K code
+// x becomes 1152 + x that way and one f16x2 subtraction gives x exactly.
+// High V nibbles are taken in mantissa bits 4-7 as 16 * (code - 8) and their
+// output rows scaled by 1/16.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -56,12 +55,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 4 int8 (bytes x0..x3 of w) -> f16x2 (1152 + x0, 1152 + x1) and (1152 + x2,
-// 1152 + x3), exact; the 1152 offset is taken out after the MMA (see below).
-__device__ __forceinline__ void i8x4_to_f16_biased(uint32_t w, uint32_t &lo, uint32_t &hi) {
+// 4 int8 (bytes x0..x3 of w) -> f16x2 (x0, x1) and (x2, x3), exact: the
+// byte x + 128 under exponent 0x64 is 1024 + 128 + x, minus 1152 (0x6480).
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const uint32_t u = w ^ 0x80808080u;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+    uint32_t bl, bh;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(bl) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(bh) : "r"(u), "r"(0x64646464u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(bl), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(bh), "r"(0x64806480u));
 }
 
 // 4 packed bytes (keys k0..k3, byte = lo | hi << 4) -> A fragment:
@@ -222,10 +224,8 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         const uint32_t page = p.page[item];
         const uint8_t *hs = smem + L.stage + stage * head_bytes;  // this unit's page-head section
 
-        // Q fragments of kv head g (built by qprep_kernel): qf[tile][ks][lane] and
-        // qs[m][b] = sum over 32-dim block b of q as the MMA sees it (hi + lo)
+        // Q fragments of kv head g (built by qprep_kernel): qf[tile][ks][lane]
         const uint4 *qf = p.qf + ((int64_t)g * p.qtiles + tile) * KS * 32;
-        const float *qs = p.qs + ((int64_t)g * p.qtiles * 8 + mo) * NB;
         if (!mbar_wait(bar0 + 16 * stage, parity)) ok = false;
         if (!__syncthreads_and(ok)) break;
         pending[stage] = false;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
             for (int q = 0; q < KPW; ++q)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) S_[q][nt][0] = S_[q][nt][1] = S_[q][nt][2] = S_[q][nt][3] = 0.f;
-#pragma unroll(NT <= 2 ? NB : 1)
+#pragma unroll(NT == 1 ? NB : (NT == 2 ? 2 : 1))
             for (int b = 0; b < NB; ++b) {
                 uint2 kv0[KPW], kv1[KPW];
                 float sk0[KPW], sk1[KPW];
@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                     uint32_t a[KPW][4];
 #pragma unroll
                     for (int q = 0; q < KPW; ++q) {
-                        i8x4_to_f16_biased(s ? kv0[q].y : kv0[q].x, a[q][0], a[q][2]);
-                        i8x4_to_f16_biased(s ? kv1[q].y : kv1[q].x, a[q][1], a[q][3]);
+                        i8x4_to_f16(s ? kv0[q].y : kv0[q].x, a[q][0], a[q][2]);
+                        i8x4_to_f16(s ? kv1[q].y : kv1[q].x, a[q][1], a[q][3]);
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
@@ -289,21 +289,16 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                         }
                     }
                 }
-                // the A operand carried 1152 + x: take 1152 * sum(q) of the block back out
+                // the block's Q8_0 scale multiplies its fp32 partial dot
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float q0 = qs[(nt * 8 + 2 * tig) * NB + b];
-                    const float q1 = qs[(nt * 8 + 2 * tig + 1) * NB + b];
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int q = 0; q < KPW; ++q) {
-                        const float c0 = fmaf(-1152.f, q0, cb[q][nt][0]), c1 = fmaf(-1152.f, q1, cb[q][nt][1]);
-                        const float c2 = fmaf(-1152.f, q0, cb[q][nt][2]), c3 = fmaf(-1152.f, q1, cb[q][nt][3]);
-                        S_[q][nt][0] = fmaf(c0, sk0[q], S_[q][nt][0]);
-                        S_[q][nt][1] = fmaf(c1, sk0[q], S_[q][nt][1]);
-                        S_[q][nt][2] = fmaf(c2, sk1[q], S_[q][nt][2]);
-                        S_[q][nt][3] = fmaf(c3, sk1[q], S_[q][nt][3]);
+                        S_[q][nt][0] = fmaf(cb[q][nt][0], sk0[q], S_[q][nt][0]);
+                        S_[q][nt][1] = fmaf(cb[q][nt][1], sk0[q], S_[q][nt][1]);
+                        S_[q][nt][2] = fmaf(cb[q][nt][2], sk1[q], S_[q][nt][2]);
+                        S_[q][nt][3] = fmaf(cb[q][nt][3], sk1[q], S_[q][nt][3]);
                     }
-                }
             }
 #pragma unroll
             for (int q = 0; q < KPW; ++q) {
@@ -493,14 +488,12 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 }
 
 // Q fragments for every kv head, once per attend: qf [Hk][NT][KS][32] uint4
-// = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand and qs [Hk][MR][NB].
+// = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand.
 template <int D, int NT>
 __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__ DecodeParams p) {
-    constexpr int NB = D / 32, KS = D / 16, MR = NT * 8;
+    constexpr int KS = D / 16;
     const int g = blockIdx.x, G = p.G, rows = G * p.R;
     uint4 *qf = const_cast<uint4 *>(p.qf) + (int64_t)g * NT * KS * 32;
-    float *qs = const_cast<float *>(p.qs) + (int64_t)g * MR * NB;
-    __shared__ uint4 sq[NT * KS * 32];
     for (int e = threadIdx.x; e < NT * KS * 32; e += kThreads) {
         const int ln = e & 31, ks = (e >> 5) % KS, nt = e / (KS * 32);
         const int m = nt * 8 + (ln >> 2);
@@ -522,23 +515,7 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
         uint32_t h0, l0, h1, l1;
         split_f16(x[0], x[1], h0, l0);
         split_f16(x[2], x[3], h1, l1);
-        sq[e] = make_uint4(h0, h1, l0, l1);
-        qf[e] = sq[e];
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < MR * NB; e += kThreads) {
-        const int m = e / NB, bb = e % NB, nt = m >> 3, gm = m & 7;
-        float acc_q = 0.f;
-        for (int s2 = 0; s2 < 2; ++s2)
-            for (int t = 0; t < 4; ++t) {
-                const uint4 v = sq[(nt * KS + 2 * bb + s2) * 32 + gm * 4 + t];
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w4[j]));
-                    acc_q += f.x + f.y;
-                }
-            }
-        qs[e] = acc_q;
+        qf[e] = make_uint4(h0, h1, l0, l1);
     }
 }
 
@@ -606,18 +583,23 @@ cudaError_t launch_decode_d(const DecodeParams &p, int nt, cudaStream_t s) {
 // ------------------------------------------------------------------ combine
 
 // One CTA per (row, q head, 64-dim slice).  The largest split max M comes
-// first (every split's (m, l) is read once, in parallel); then each warp sums
-// w_s * o_s with w_s = 2^(m_s - M) over its splits s = warp, warp + 8, ...
-// (independent loads, no running rescale) and the eight warp sums are added
-// in warp order: a fixed order, so the result does not depend on timing.
+// first; then, block by block of splits, the weights w_s = 2^(m_s - M) go to
+// shared memory and each warp sums w_s * o_s over its splits s = warp,
+// warp + NW, ... with kCombineUnroll partial loads in flight; the warp sums
+// are added in warp order.  A fixed order: the result does not depend on
+// timing.
 constexpr int kCombineDims = 64;
+constexpr int kCombineThreads = 512;
+constexpr int kCombineBlock = 1024;  // splits per weight block
+constexpr int kCombineUnroll = 8;
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
     constexpr int DS = D < kCombineDims ? D : kCombineDims;
-    constexpr int VPL = DS / 32;  // dims per lane
-    constexpr int NW = kThreads / 32;
+    constexpr int VPL = DS / 32;  // dims per lane (2)
+    constexpr int NW = kCombineThreads / 32;
     __shared__ float wmax[NW], wl[NW];
+    __shared__ float wsm[kCombineBlock], lsm[kCombineBlock];
     __shared__ float wo[NW][DS];
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
     const int d0 = blockIdx.y * DS;
@@ -626,7 +608,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
     auto base_of = [&](int s) { return ((int64_t)s * p.Hq + h) * p.R + r; };
 
     float mx = -INFINITY;
-    for (int s = threadIdx.x; s < nsplit; s += kThreads) {
+    for (int s = threadIdx.x; s < nsplit; s += kCombineThreads) {
         const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2);
         if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
     }
@@ -642,41 +624,38 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const CombineParams p
 #pragma unroll
     for (int i = 0; i < VPL; ++i) o[i] = 0.f;
     if (M != -INFINITY) {
-        constexpr int U4 = 4;  // splits in flight per warp
-        for (int s0 = warp; s0 < nsplit; s0 += NW * U4) {
-            float w[U4], l[U4], v[U4][VPL];
-#pragma unroll
-            for (int j = 0; j < U4; ++j) {
-                const int s = s0 + j * NW;
-                w[j] = 0.f;
-                l[j] = 0.f;
-                if (s < nsplit) {
-                    const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2);
-                    if (ml.y > 0.f) {
-                        w[j] = exp2f(ml.x - M);
-                        l[j] = ml.y;
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < VPL; ++i) v[j][i] = 0.f;
-                if (w[j] > 0.f) {
-                    const float *src = p.part_o + base_of(s) * D + d0 + lane * VPL;
-                    if (VPL == 2) {
-                        const float2 t = *reinterpret_cast<const float2 *>(src);
-                        v[j][0] = t.x;
-                        v[j][VPL - 1] = t.y;
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < VPL; ++i) v[j][i] = src[i];
-                    }
-                }
+        for (int b0 = 0; b0 < nsplit; b0 += kCombineBlock) {
+            const int nb = nsplit - b0 < kCombineBlock ? nsplit - b0 : kCombineBlock;
+            __syncthreads();  // the previous block's weights are consumed
+            for (int j = threadIdx.x; j < nb; j += kCombineThreads) {
+                const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(b0 + j) * 2);
+                const bool live = ml.y > 0.f;
+                wsm[j] = live ? exp2f(ml.x - M) : 0.f;
+                lsm[j] = live ? ml.y : 0.f;
             }
+            __syncthreads();
+            for (int j0 = warp; j0 < nb; j0 += NW * kCombineUnroll) {
+                float v[kCombineUnroll][VPL];
 #pragma unroll
-            for (int j = 0; j < U4; ++j) {
-                if (!(w[j] > 0.f)) continue;
+                for (int u = 0; u < kCombineUnroll; ++u) {
+                    const int j = j0 + u * NW;
+                    v[u][0] = v[u][1] = 0.f;
+                    if (j < nb && wsm[j] > 0.f) {
+                        const float2 t =
+                            *reinterpret_cast<const float2 *>(p.part_o + base_of(b0 + j) * D + d0 + lane * VPL);
+                        v[u][0] = t.x;
+                        v[u][1] = t.y;
+                    }
+                }
 #pragma unroll
-                for (int i = 0; i < VPL; ++i) o[i] = fmaf(w[j], v[j][i], o[i]);
-                Ls = fmaf(w[j], l[j], Ls);
+                for (int u = 0; u < kCombineUnroll; ++u) {
+                    const int j = j0 + u * NW;
+                    if (j < nb && wsm[j] > 0.f) {
+                        o[0] = fmaf(wsm[j], v[u][0], o[0]);
+                        o[1] = fmaf(wsm[j], v[u][1], o[1]);
+                        Ls = fmaf(wsm[j], lsm[j], Ls);
+                    }
+                }
             }
         }
     }
@@ -727,9 +706,9 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t s) {
     if (blocks < 1) return cudaSuccess;
     const dim3 grid(blocks, p.D > kCombineDims ? p.D / kCombineDims : 1);
     switch (p.D) {
-        case 64: combine_kernel<64><<<grid, kThreads, 0, s>>>(p); break;
-        case 128: combine_kernel<128><<<grid, kThreads, 0, s>>>(p); break;
-        case 256: combine_kernel<256><<<grid, kThreads, 0, s>>>(p); break;
+        case 64: combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p); break;
+        case 128: combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p); break;
+        case 256: combine_kernel<256><<<grid, kCombineThreads, 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -63,7 +63,6 @@ struct DecodeParams {
     float scale_log2;      // scale * log2(e)
     int stages;            // shared-memory stages (set by launch_decode)
     const uint4 *qf;       // Q fragments [Hk][NT][D/16][32] (written by the Q prep kernel)
-    const float *qs;       // per-block sums of Q [Hk][NT*8][D/32]
     int prep_q;            // launch_decode first (re)builds qf/qs from q
     int tile_mode;         // one CTA per (page, kv head, row tile) (ring chunks)
     int reserve_sms;       // leave this many SMs free of this launch (capped at half the GPU):
@@ -79,11 +78,10 @@ struct DecodeParams {
 // n_items may then be 0 (Q prep only).
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s);
 int decode_max_mma_rows();  // G*R bound served by launch_decode
-// bytes of the Q-fragment area (qf then qs) for Hk kv heads of head dim D
+// bytes of the Q-fragment area for Hk kv heads of head dim D
 inline int64_t qfrag_bytes(int Hk, int D) {
     const int64_t qf = (int64_t)Hk * 8 * (D / 16) * 32 * 16;
-    const int64_t qs = (int64_t)Hk * 64 * (D / 32) * 4;
-    return (qf + qs + 255) / 256 * 256;
+    return (qf + 255) / 256 * 256;
 }
 
 // ---------------------------------------------------------------- prefill

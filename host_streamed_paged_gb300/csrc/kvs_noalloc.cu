@@ -132,7 +132,6 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
     dp.status = static_cast<int *>(scratch);
     uint8_t *qf_area = static_cast<uint8_t *>(scratch) + kStatusBytes;
     dp.qf = reinterpret_cast<const uint4 *>(qf_area);
-    dp.qs = reinterpret_cast<const float *>(qf_area + (int64_t)Hk * 8 * (D / 16) * 32 * 16);
     dp.part_o = reinterpret_cast<float *>(qf_area + qfrag);
     dp.part_ml = dp.part_o + n_split * per_split * D;
     dp.R = (int)n_rows;

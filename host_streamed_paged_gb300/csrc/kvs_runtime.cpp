@@ -1359,7 +1359,6 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         dp.part_ml = part_ml;
         dp.status = static_cast<int *>(c->cfg.workspace);
         dp.qf = reinterpret_cast<const uint4 *>(qfrag);
-        dp.qs = reinterpret_cast<const float *>(qfrag + (int64_t)c->geom.Hk * 8 * (c->geom.D / 16) * 32 * 16);
         dp.R = (int)n_rows;
         dp.Hq = (int)n_q_head;
         dp.G = (int)G;

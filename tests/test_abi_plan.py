@@ -49,7 +49,7 @@ def test_query_sizes_formulas():
     assert pb == 4 * 256 * 256 * 13 // 8 == 425984  # 416 KiB per page
     assert hb == 4 * 128 * pb
     assert amin == (2 * 4 + 8) * pb
-    qfrag = 4 * 8 * 16 * 32 * 16 + 4 * 64 * 8 * 4  # query fragments of 4 kv heads (already 256-aligned)
+    qfrag = 4 * 8 * 16 * 32 * 16  # query fragments of 4 kv heads (already 256-aligned)
     assert wmin == 256 + qfrag + 128 * 24 * 6 * (256 + 2) * 4  # status word + fragments + one partial per page
     pb2, *_ = kvs.kvs_query_sizes(_cfg(page_tokens=256, n_kv_head=2, head_dim=128, max_q_head=8))
     assert pb2 == 2 * 256 * 128 * 13 // 8 == 106496  # 104 KiB
