@@ -555,8 +555,8 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     }
     const int U = p.n_items * p.geom.Hk * (p.tile_mode ? p.run_tiles : 1);
     int max_ctas = occ * g_num_sms;
-    if (p.reserve_sms > 0) {  // leave reserve_sms SMs' worth of CTA slots free
-        const int keep = g_num_sms - (p.reserve_sms < g_num_sms / 2 ? p.reserve_sms : g_num_sms / 2);
+    if (p.reserve_sms > 0) {  // leave reserve_sms SMs' worth of CTA slots free, at most a third
+        const int keep = g_num_sms - (p.reserve_sms < g_num_sms / 3 ? p.reserve_sms : g_num_sms / 3);
         max_ctas = occ * keep;
     }
     const int per_cta = (U + max_ctas - 1) / max_ctas;

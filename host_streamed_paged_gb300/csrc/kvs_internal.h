@@ -65,8 +65,8 @@ struct DecodeParams {
     const uint4 *qf;       // Q fragments [Hk][NT][D/16][32] (written by the Q prep kernel)
     int prep_q;            // launch_decode first (re)builds qf/qs from q
     int tile_mode;         // one CTA per (page, kv head, row tile) (ring chunks)
-    int reserve_sms;       // leave this many SMs free of this launch (capped at half the GPU):
-                           // one CTA per SM, so concurrent ring-chunk launches find whole SMs
+    int reserve_sms;       // leave this many SMs' worth of CTA slots free of this launch (at
+                           // most a third of the GPU) for concurrent ring-chunk launches
     int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run
     int n_items;
     uint32_t page[kMaxItems];
