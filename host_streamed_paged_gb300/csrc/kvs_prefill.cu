@@ -8,20 +8,27 @@
 // Streaming for llama.cpp, "Batch and micro-batch sizes") holds because one
 // launch covers every query tile of a key split.
 //
-// CTA = (key split, kv head, 128-row tile of one query head).  Per 64-key
-// block of the split:
-//   1. all 8 warps dequantise the block's K (Q8_0) and V (Q4_0) into shared
-//      memory as f16 pairs hi + lo (code * scale is exact in fp32; hi/lo keep
-//      ~22 of its bits), in the 128-byte-swizzled K-major layout tcgen05 reads;
-//   2. one thread issues S = Q K_hi^T + Q K_lo^T (M 128, N 64, K 256) into TMEM;
-//   3. warps 0-3 (one thread per row, TMEM lane = row) read S, scale, mask,
-//      run the online softmax and write P (f16) to shared memory; O in TMEM is
-//      rescaled only when a row's running max grows by more than 2^8 (the
-//      weights are then formed against the stale max, which is exact);
-//   4. one thread issues O += P V_hi + P V_lo (M 128, N 256, K 64).
-// At the end warps 0-3 write the split's unnormalised partial (m, l, O) for
-// the log-sum-exp combine shared with the decode path.  Every mbarrier wait
-// is bounded: on timeout the kernel records a status code and skips the rest.
+// CTA = (key split, kv head, 128-row tile of one query head); 64-key blocks
+// flow through a warp-specialised pipeline:
+//   warps 4-7 (producers) dequantise block j's K (Q8_0) and V (Q4_0) into
+//     shared memory as f16 pairs hi + lo, in the 128-byte-swizzled K-major
+//     layout tcgen05 reads: hi = rn(d * x), lo = rn(d * x - hi) by one f16x2
+//     multiply and one fused multiply-add (d * x has at most 18 significant
+//     bits, so hi + lo is exact);
+//   warp 8 (one thread) issues S_j = Q K_j^T (hi + lo, M 128, N 64, K 256)
+//     into one of two TMEM score buffers, S_{j+1} before O += P_j V_j (hi + lo,
+//     M 128, N 256, K 64), so the tensor pipe has work while the softmax runs;
+//   warps 0-3 (one thread per row, TMEM lane = row) read S_j, scale, mask, run
+//     the online softmax and write P_j (f16) to shared memory; O in TMEM is
+//     rescaled only when a row's running max grows by more than 2^8 (the
+//     weights are then formed against the stale max, which is exact).
+// K, V and P are single-buffered: a block's K is rewritten once S_j is done,
+// its V and P once PV_j is done; the fences are mbarriers (producer and
+// softmax arrivals, tcgen05.commit for the MMAs).  At the end warps 0-3 write
+// the split's unnormalised partial (m, l, O) for the log-sum-exp combine
+// shared with the decode path.  Every wait is bounded; on a timeout the CTA
+// raises an abort flag that ends every role's loop, waits (bounded) for its
+// MMAs in flight and records a status code.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -30,7 +37,7 @@
 namespace kvs {
 namespace {
 
-constexpr int kPThreads = 256;
+constexpr int kPThreads = 288;    // 4 softmax warps, 4 producer warps, 1 MMA warp
 constexpr int kBN = 64;           // keys per block
 constexpr int kD = 256;           // head dim served by this kernel
 constexpr int kTileRows = 128;    // MMA M
@@ -47,12 +54,19 @@ constexpr int kOffKl = kOffKh + kKBytes;
 constexpr int kOffVh = kOffKl + kKBytes;
 constexpr int kOffVl = kOffVh + kVBytes;
 constexpr int kOffP = kOffVl + kVBytes;
-constexpr int kOffBar = kOffP + kPBytes;      // 2 mbarriers
-constexpr int kOffTmem = kOffBar + 16;        // TMEM base address written by tcgen05.alloc
-constexpr int kSmemBytes = kOffTmem + 16 + 1024;  // + slack to align the base to 1024
+constexpr int kOffBar = kOffP + kPBytes;      // mbarriers (kNumBars x 8 B)
+constexpr int kNumBars = 10;
+constexpr int kOffTmem = kOffBar + kNumBars * 8;  // TMEM base address written by tcgen05.alloc
+constexpr int kOffAbort = kOffTmem + 8;
+constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack to align the base to 1024
 
-constexpr uint32_t kTmemCols = 512;  // S at [0, 64), O at [64, 320)
-constexpr uint32_t kColS = 0, kColO = 64;
+constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 64) and [64, 128), O at [128, 384)
+constexpr uint32_t kColS = 0, kColO = 128;
+// barrier indices
+constexpr int kBarKFull = 0, kBarVFull = 1, kBarPFull = 2, kBarKEmpty = 3, kBarODone = 4;
+constexpr int kBarSFull = 5;   // + buffer (2)
+constexpr int kBarSEmpty = 7;  // + buffer (2)
+constexpr int kBarFinal = 9;
 
 // byte offset of element (row, k) in a 128B-swizzled K-major tile whose rows
 // are 128-byte lines of 64 f16 (one swizzle atom per 64 elements of k)
@@ -83,8 +97,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
 
-// bounded wait for phase `parity` of an mbarrier; false on timeout
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// bounded wait for phase `parity` of an mbarrier; false on timeout or once
+// another role of the CTA has raised *abort (which this wait also raises)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
         asm volatile(
@@ -93,8 +108,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
+        if ((i & 255) == 255 && *abort) return false;
     }
+    *abort = 1;
     return false;
+}
+
+// the same wait taken by every lane of a warp, with one warp-wide outcome
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -143,35 +169,66 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
-// (x, y) fp32 -> f16x2 hi = rn(x, y), lo = rn(x - hi, y - hi)
-__device__ __forceinline__ void split_f16(float x, float y, uint32_t &hi, uint32_t &lo) {
-    const __half2 h = __floats2half2_rn(x, y);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
+// 4 int8 (bytes of w) -> f16x2 (x0, x1), (x2, x3), exact (see kvs_decode.cu)
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &a, uint32_t &b) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t bl, bh;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(bl) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(bh) : "r"(u), "r"(0x64646464u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(a) : "r"(bl), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(b) : "r"(bh), "r"(0x64806480u));
+}
+
+// x * d -> (hi, lo) with hi = rn(x d), lo = rn(x d - hi) (exact remainder)
+__device__ __forceinline__ void mul_split(uint32_t x, uint32_t d, uint32_t &hi, uint32_t &lo) {
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(x), "r"(d));
+    const uint32_t nh = hi ^ 0x80008000u;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(x), "r"(d), "r"(nh));
 }
 
 __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split_idx = blockIdx.x;
     const int G = p.G, R = p.R, rt = (R + kTileRows - 1) / kTileRows;
     const int g = blockIdx.y / (G * rt);
     const int tile = blockIdx.y % (G * rt);
     const int hl = tile / rt, r0 = (tile % rt) * kTileRows;
     const int h = g * G + hl;
-    const int P = p.geom.P;
+    const int P = p.geom.P, bpp = P / kBN;  // blocks per page
     const int it0 = p.split_begin[split_idx], it1 = p.split_begin[split_idx + 1];
     const int split = p.split_id[split_idx];
+    const long long last_pos = p.pos0 + ((r0 + kTileRows < R) ? (r0 + kTileRows) : R) - 1;  // tile's last row
 
-    const uint32_t bar_s = smem_u32(smem + kOffBar), bar_o = bar_s + 8;
+    const uint32_t bar0 = smem_u32(smem + kOffBar);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffAbort);
+
+    // blocks of this split the tile can see (pages ascend, so the first masked one ends the list)
+    int nblk = 0;
+    for (int j = 0; j < (it1 - it0) * bpp; ++j) {
+        const long long kpos0 = (long long)p.page[it0 + j / bpp] * P + (j % bpp) * kBN;
+        if (kpos0 > last_pos) break;
+        nblk = j + 1;
+    }
+    auto page_base = [&](int j) {
+        return p.arena + (int64_t)p.slot[it0 + j / bpp] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
+    };
 
     if (tid == 0) {
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
+        mbar_init(bar(kBarKFull), 4);
+        mbar_init(bar(kBarVFull), 4);
+        mbar_init(bar(kBarPFull), 4);
+        mbar_init(bar(kBarKEmpty), 1);
+        mbar_init(bar(kBarODone), 1);
+        mbar_init(bar(kBarSFull), 1);
+        mbar_init(bar(kBarSFull + 1), 1);
+        mbar_init(bar(kBarSEmpty), 4);
+        mbar_init(bar(kBarSEmpty + 1), 4);
+        mbar_init(bar(kBarFinal), 1);
+        *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -195,185 +252,243 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
     tc_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    // per-row running state (warps 0-3: row = tid)
-    const int row = tid;
-    const bool row_owner = tid < kTileRows;
-    const long long qpos = p.pos0 + r0 + row;  // this row's position
-    const bool row_valid = row_owner && (r0 + row < R);
-    float m_used = -INFINITY, l_sum = 0.f;
-    const long long last_pos = p.pos0 + ((r0 + kTileRows < R) ? (r0 + kTileRows) : R) - 1;  // tile's last row
-    uint32_t phase_s = 0, phase_o = 0;
-    bool ok = true;
-    bool any_o = false;  // O written at least once
-
-    for (int it = it0; it < it1 && ok; ++it) {
-        const int page = (int)p.page[it];
-        const uint8_t *hb = p.arena + (int64_t)p.slot[it] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
-        for (int kb = 0; kb < P && ok; kb += kBN) {
-            const long long kpos0 = (long long)page * P + kb;
-            if (kpos0 > last_pos) break;  // every later key is masked for every row of the tile
-            // ---- dequantise K block (64 keys x 256 dims) -> K_hi, K_lo
-            const __half *ks = reinterpret_cast<const __half *>(hb + p.geom.ks_off);
-            for (int c = tid; c < kBN * (kD / 8); c += kPThreads) {
-                const int key = c / (kD / 8), k = (c % (kD / 8)) * 8;
-                const uint2 raw = *reinterpret_cast<const uint2 *>(hb + kq_byte(kb + key, k, kD / 32));
-                const float d = __half2float(ks[(kb + key) * (kD / 32) + k / 32]);
-                const int8_t *b8 = reinterpret_cast<const int8_t *>(&raw);
-                uint32_t hi[4], lo[4];
+    if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ producers
+        const int pt = tid - 128;  // 0..127
+        for (int j = 0; j < nblk; ++j) {  // every exit is a warp-uniform wait outcome
+            const uint8_t *hb = page_base(j);
+            const int kb = (j % bpp) * kBN;
+            // K: 64 keys x 32 chunks of 8 dims; loads first, then the wait
+            {
+                const __half *ks = reinterpret_cast<const __half *>(hb + p.geom.ks_off);
+                uint2 raw[16];
+                __half sc[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) split_f16((float)b8[2 * e] * d, (float)b8[2 * e + 1] * d, hi[e], lo[e]);
-                const uint32_t off = sw128(kBN, key, k);
-                *reinterpret_cast<uint4 *>(smem + kOffKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + kOffKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            // ---- dequantise V block -> V_hi, V_lo as [dim][key] (K-major for the PV MMA)
-            const __half *vs = reinterpret_cast<const __half *>(hb + p.geom.vs_off);
-            for (int c = tid; c < kD * (kBN / 8); c += kPThreads) {
-                const int dim = c / (kBN / 8), k = (c % (kBN / 8)) * 8;
-                const int blk = dim >> 5, within = dim & 31;
-                const int brow = blk * 16 + (within & 15);
-                const int shift = within < 16 ? 0 : 4;
-                const uint2 raw = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + vq_byte(kb + k, brow, kD / 32));
-                const uint8_t *b8 = reinterpret_cast<const uint8_t *>(&raw);
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float d0 = __half2float(vs[blk * P + kb + k + 2 * e]);
-                    const float d1 = __half2float(vs[blk * P + kb + k + 2 * e + 1]);
-                    const float x0 = (float)(((b8[2 * e] >> shift) & 15) - 8) * d0;
-                    const float x1 = (float)(((b8[2 * e + 1] >> shift) & 15) - 8) * d1;
-                    split_f16(x0, x1, hi[e], lo[e]);
+                for (int i = 0; i < 16; ++i) {
+                    const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
+                    raw[i] = *reinterpret_cast<const uint2 *>(hb + kq_byte(kb + key, k, kD / 32));
+                    sc[i] = ks[(kb + key) * (kD / 32) + (k >> 5)];
                 }
-                const uint32_t off = sw128(kD, dim, k);
-                *reinterpret_cast<uint4 *>(smem + kOffVh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + kOffVl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                if (j >= 1 && !mbar_wait_warp(bar(kBarKEmpty), (uint32_t)((j - 1) & 1), abort)) break;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
+                    const __half2 d2 = __halves2half2(sc[i], sc[i]);
+                    const uint32_t d = *reinterpret_cast<const uint32_t *>(&d2);
+                    uint32_t x[4], hi[4], lo[4];
+                    i8x4_to_f16(raw[i].x, x[0], x[1]);
+                    i8x4_to_f16(raw[i].y, x[2], x[3]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mul_split(x[e], d, hi[e], lo[e]);
+                    const uint32_t off = sw128(kBN, key, k);
+                    *reinterpret_cast<uint4 *>(smem + kOffKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(smem + kOffKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                proxy_fence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarKFull));
             }
-            proxy_fence();
-            tc_before_sync();
-            __syncthreads();
-            tc_after_sync();
-            // ---- S = Q K^T (hi + lo)
-            if (tid == 0) {
-                const uint32_t qa = smem_u32(smem + kOffQ), kh = smem_u32(smem + kOffKh), kl = smem_u32(smem + kOffKl);
-                const uint32_t id = idesc_f16(kTileRows, kBN);
+            // V: 128 byte rows (dim pairs) x 8 chunks of 8 keys -> [dim][key] tiles
+            {
+                const __half *vs = reinterpret_cast<const __half *>(hb + p.geom.vs_off);
+                uint2 raw[8];
+                uint4 sv[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
+                    raw[i] = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + vq_byte(kb + k8, br, kD / 32));
+                    sv[i] = *reinterpret_cast<const uint4 *>(vs + (br >> 4) * P + kb + k8);
+                }
+                if (j >= 1 && !mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort)) break;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
+                    const int dA = (br >> 4) * 32 + (br & 15), dB = dA + 16;
+                    const uint32_t w[2] = {raw[i].x, raw[i].y};
+                    const uint32_t dv[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};  // (k, k+1) scale pairs
+                    uint32_t ah[4], al[4], bh[4], bl[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // keys 2e, 2e+1: bytes of w[e/2] at positions 2(e%2), 2(e%2)+1
+                        uint32_t sp;
+                        const uint32_t sel = (e & 1) ? 0x7372u : 0x7170u;  // bytes 2,3 or 0,1 -> low byte of each half
+                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sp) : "r"(w[e >> 1]), "r"(0u), "r"(sel));
+                        uint32_t lo_n, hi_n, xa, xb;
+                        asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(lo_n) : "r"(sp), "r"(0x000f000fu), "r"(0x64006400u));
+                        asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(hi_n) : "r"(sp >> 4), "r"(0x000f000fu), "r"(0x64006400u));
+                        asm("sub.f16x2 %0, %1, %2;" : "=r"(xa) : "r"(lo_n), "r"(0x64086408u));  // code - 8
+                        asm("sub.f16x2 %0, %1, %2;" : "=r"(xb) : "r"(hi_n), "r"(0x64086408u));
+                        mul_split(xa, dv[e], ah[e], al[e]);
+                        mul_split(xb, dv[e], bh[e], bl[e]);
+                    }
+                    const uint32_t oa = sw128(kD, dA, k8), ob = sw128(kD, dB, k8);
+                    *reinterpret_cast<uint4 *>(smem + kOffVh + oa) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+                    *reinterpret_cast<uint4 *>(smem + kOffVl + oa) = make_uint4(al[0], al[1], al[2], al[3]);
+                    *reinterpret_cast<uint4 *>(smem + kOffVh + ob) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+                    *reinterpret_cast<uint4 *>(smem + kOffVl + ob) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+                }
+                proxy_fence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarVFull));
+            }
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ MMA issue (one thread)
+        if (lane == 0) {
+            const uint32_t qa = smem_u32(smem + kOffQ), kh = smem_u32(smem + kOffKh), kl = smem_u32(smem + kOffKl);
+            const uint32_t pa = smem_u32(smem + kOffP), vh = smem_u32(smem + kOffVh), vl = smem_u32(smem + kOffVl);
+            const uint32_t id_s = idesc_f16(kTileRows, kBN), id_o = idesc_f16(kTileRows, kD);
+            auto issue_s = [&](int j) {
+                const uint32_t ts = tmem + kColS + (uint32_t)((j & 1) * kBN);
 #pragma unroll 1
                 for (int s = 0; s < kD / 16; ++s) {
                     const uint32_t ao = (s >> 2) * (kTileRows * 128) + (s & 3) * 32;
                     const uint32_t bo = (s >> 2) * (kBN * 128) + (s & 3) * 32;
-                    mma_f16(tmem + kColS, smem_desc(qa + ao), smem_desc(kh + bo), id, s > 0);
-                    mma_f16(tmem + kColS, smem_desc(qa + ao), smem_desc(kl + bo), id, 1);
+                    mma_f16(ts, smem_desc(qa + ao), smem_desc(kh + bo), id_s, s > 0);
+                    mma_f16(ts, smem_desc(qa + ao), smem_desc(kl + bo), id_s, 1);
                 }
-                mma_commit(bar_s);
+                mma_commit(bar(kBarSFull + (j & 1)));
+                mma_commit(bar(kBarKEmpty));
+            };
+            bool ok = true;
+            if (nblk > 0) {
+                ok = mbar_wait(bar(kBarKFull), 0u, abort);
+                if (ok) {
+                    tc_after_sync();
+                    issue_s(0);
+                }
             }
-            if (!mbar_wait(bar_s, phase_s)) ok = false;
-            phase_s ^= 1;
-            ok = __syncthreads_and(ok);
+            for (int j = 0; j < nblk && ok; ++j) {
+                if (j + 1 < nblk) {
+                    ok = mbar_wait(bar(kBarKFull), (uint32_t)((j + 1) & 1), abort);
+                    if (ok && j + 1 >= 2) ok = mbar_wait(bar(kBarSEmpty + ((j + 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
+                    if (!ok) break;
+                    tc_after_sync();
+                    issue_s(j + 1);
+                }
+                ok = mbar_wait(bar(kBarPFull), (uint32_t)(j & 1), abort) &&
+                     mbar_wait(bar(kBarVFull), (uint32_t)(j & 1), abort);
+                if (!ok) break;
+                tc_after_sync();
+#pragma unroll 1
+                for (int s = 0; s < kBN / 16; ++s) {
+                    mma_f16(tmem + kColO, smem_desc(pa + s * 32), smem_desc(vh + s * 32), id_o, (j > 0 || s > 0) ? 1u : 0u);
+                    mma_f16(tmem + kColO, smem_desc(pa + s * 32), smem_desc(vl + s * 32), id_o, 1);
+                }
+                mma_commit(bar(kBarODone));
+            }
+            // every MMA this thread issued has finished before TMEM is read or freed
+            mma_commit(bar(kBarFinal));
+            volatile int no_abort = 0;
+            mbar_wait(bar(kBarFinal), 0u, &no_abort);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax rows (warps 0-3)
+        const int row = tid;
+        const long long qpos = p.pos0 + r0 + row;
+        const bool row_valid = r0 + row < R;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_used = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nblk && ok; ++j) {
+            const long long kpos0 = (long long)p.page[it0 + j / bpp] * P + (j % bpp) * kBN;
+            ok = mbar_wait_warp(bar(kBarSFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort);
+            if (!ok) break;
             tc_after_sync();
-            // ---- softmax rows (warps 0-3), P -> shared memory
-            int need_rescale = 0;
-            float alpha = 1.f;
-            if (row_owner && ok) {
-                float s[kBN];
-                const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + kColS;
+            float s[kBN];
+            {
                 float t32[32];
+                const uint32_t ta = lane_base + kColS + (uint32_t)((j & 1) * kBN);
                 tmem_ld32(ta, t32);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[i] = t32[i];
                 tmem_ld32(ta + 32, t32);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[32 + i] = t32[i];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    const bool valid = row_valid && (kpos0 + i <= qpos);
-                    s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[i]);
-                }
-                if (mx > m_used + 8.f || (m_used == -INFINITY && mx != -INFINITY)) {
-                    alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - mx);
-                    need_rescale = 1;
-                    l_sum *= alpha;
-                    m_used = mx;
-                }
-                float bsum = 0.f;
-                uint32_t pk[kBN / 2];
-#pragma unroll
-                for (int i = 0; i < kBN; i += 2) {
-                    const float e0 = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_used);
-                    const float e1 = (s[i + 1] == -INFINITY) ? 0.f : exp2f(s[i + 1] - m_used);
-                    const __half2 hp = __floats2half2_rn(e0, e1);
-                    const float2 hf = __half22float2(hp);
-                    bsum += hf.x + hf.y;  // l sums exactly the weights the MMA uses
-                    pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
-                }
-                l_sum += bsum;
-#pragma unroll
-                for (int c8 = 0; c8 < kBN / 8; ++c8)
-                    *reinterpret_cast<uint4 *>(smem + kOffP + sw128(kTileRows, row, c8 * 8)) =
-                        make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
             }
-            // rescale O rows whose max moved (warp-collective TMEM access)
-            if (warp < 4 && ok && any_o && __any_sync(0xffffffffu, need_rescale)) {
-                const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + kColO;
-                for (int c = 0; c < kD; c += 32) {
-                    float v[32];
-                    tmem_ld32(ta + c, v);
+            tc_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSEmpty + (j & 1)));
+            float mx = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                    tmem_st32(ta + c, v);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            for (int i = 0; i < kBN; ++i) {
+                const bool valid = row_valid && (kpos0 + i <= qpos);
+                s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[i]);
             }
+            int need_rescale = 0;
+            float alpha = 1.f;
+            if (mx > m_used + 8.f || (m_used == -INFINITY && mx != -INFINITY)) {
+                alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - mx);
+                need_rescale = 1;
+                l_sum *= alpha;
+                m_used = mx;
+            }
+            float bsum = 0.f;
+            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int i = 0; i < kBN; i += 2) {
+                const float e0 = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_used);
+                const float e1 = (s[i + 1] == -INFINITY) ? 0.f : exp2f(s[i + 1] - m_used);
+                const __half2 hp = __floats2half2_rn(e0, e1);
+                const float2 hf = __half22float2(hp);
+                bsum += hf.x + hf.y;  // l sums exactly the weights the MMA uses
+                pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+            }
+            l_sum += bsum;
+            // PV_{j-1} done: P may be rewritten and O is stable
+            if (j >= 1) {
+                ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort);
+                if (!ok) break;
+                tc_after_sync();
+                if (__any_sync(0xffffffffu, need_rescale)) {
+                    const uint32_t ta = lane_base + kColO;
+                    for (int c = 0; c < kD; c += 32) {
+                        float v[32];
+                        tmem_ld32(ta + c, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                        tmem_st32(ta + c, v);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < kBN / 8; ++c8)
+                *reinterpret_cast<uint4 *>(smem + kOffP + sw128(kTileRows, row, c8 * 8)) =
+                    make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
             proxy_fence();
             tc_before_sync();
-            __syncthreads();
-            tc_after_sync();
-            // ---- O += P V (hi + lo)
-            if (tid == 0 && ok) {
-                const uint32_t pa = smem_u32(smem + kOffP), vh = smem_u32(smem + kOffVh), vl = smem_u32(smem + kOffVl);
-                const uint32_t id = idesc_f16(kTileRows, kD);
-#pragma unroll 1
-                for (int s = 0; s < kBN / 16; ++s) {
-                    mma_f16(tmem + kColO, smem_desc(pa + s * 32), smem_desc(vh + s * 32), id, (any_o || s > 0) ? 1u : 0u);
-                    mma_f16(tmem + kColO, smem_desc(pa + s * 32), smem_desc(vl + s * 32), id, 1);
-                }
-                mma_commit(bar_o);
-            }
-            if (ok && !mbar_wait(bar_o, phase_o)) ok = false;
-            phase_o ^= 1;
-            any_o = true;
-            ok = __syncthreads_and(ok);
-            tc_after_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarPFull));
         }
-    }
-    if (!ok && tid == 0) atomicExch(p.status, 1);
-    // ---- partial out: unnormalised O, m (log2 units), l
-    if (row_owner && ok) {
-        const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + kColO;
-        float v[32];
-        const bool write = row_valid && (r0 + row < R);
-        const int64_t base = (((int64_t)split * p.Hq + h) * R + (r0 + row));
-        for (int c = 0; c < kD; c += 32) {
-            tmem_ld32(ta + c, v);
-            if (write) {
-                float *dst = p.part_o + base * kD + c;
-                if (any_o) {
+        // the last PV, then the partial: unnormalised O, m (log2 units), l
+        if (ok && nblk > 0) ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((nblk - 1) & 1), abort);
+        if (ok) {
+            tc_after_sync();
+            const uint32_t ta = lane_base + kColO;
+            const int64_t base = (((int64_t)split * p.Hq + h) * R + (r0 + row));
+            float v[32];
+            for (int c = 0; c < kD; c += 32) {
+                if (nblk > 0) tmem_ld32(ta + c, v);
+                if (row_valid) {
+                    float *dst = p.part_o + base * kD + c;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) = nblk > 0 ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3])
+                                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-        }
-        if (write) {
-            p.part_ml[base * 2] = m_used;
-            p.part_ml[base * 2 + 1] = l_sum;
+            if (row_valid) {
+                p.part_ml[base * 2] = m_used;
+                p.part_ml[base * 2 + 1] = l_sum;
+            }
         }
     }
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
+    if (tid == 0 && *abort) atomicExch(p.status, 1);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
