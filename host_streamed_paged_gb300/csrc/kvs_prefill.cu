@@ -53,20 +53,23 @@ constexpr int kOffKh = kOffQ + kQBytes;
 constexpr int kOffKl = kOffKh + kKBytes;
 constexpr int kOffVh = kOffKl + kKBytes;
 constexpr int kOffVl = kOffVh + kVBytes;
-constexpr int kOffP = kOffVl + kVBytes;
-constexpr int kOffBar = kOffP + kPBytes;      // mbarriers (kNumBars x 8 B)
-constexpr int kNumBars = 10;
+constexpr int kOffP = kOffVl + kVBytes;       // two P buffers
+constexpr int kOffBar = kOffP + 2 * kPBytes;  // mbarriers (kNumBars x 8 B)
+constexpr int kNumBars = 12;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;  // TMEM base address written by tcgen05.alloc
 constexpr int kOffAbort = kOffTmem + 8;
 constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack to align the base to 1024
 
 constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 64) and [64, 128), O at [128, 384)
 constexpr uint32_t kColS = 0, kColO = 128;
-// barrier indices
-constexpr int kBarKFull = 0, kBarVFull = 1, kBarPFull = 2, kBarKEmpty = 3, kBarODone = 4;
-constexpr int kBarSFull = 5;   // + buffer (2)
-constexpr int kBarSEmpty = 7;  // + buffer (2)
-constexpr int kBarFinal = 9;
+// barrier indices; a "+ buffer" barrier has one phase per use of that buffer,
+// so no waiter can fall two phases behind the barrier it waits on
+constexpr int kBarKFull = 0, kBarVFull = 1, kBarKEmpty = 2;
+constexpr int kBarPFull = 3;   // + P buffer (2)
+constexpr int kBarODone = 5;   // + P buffer (2): PV_j done, committed on buffer j & 1
+constexpr int kBarSFull = 7;   // + S buffer (2)
+constexpr int kBarSEmpty = 9;  // + S buffer (2)
+constexpr int kBarFinal = 11;
 
 // byte offset of element (row, k) in a 128B-swizzled K-major tile whose rows
 // are 128-byte lines of 64 f16 (one swizzle atom per 64 elements of k)
@@ -221,8 +224,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
         mbar_init(bar(kBarKFull), 4);
         mbar_init(bar(kBarVFull), 4);
         mbar_init(bar(kBarPFull), 4);
+        mbar_init(bar(kBarPFull + 1), 4);
         mbar_init(bar(kBarKEmpty), 1);
         mbar_init(bar(kBarODone), 1);
+        mbar_init(bar(kBarODone + 1), 1);
         mbar_init(bar(kBarSFull), 1);
         mbar_init(bar(kBarSFull + 1), 1);
         mbar_init(bar(kBarSEmpty), 4);
@@ -254,98 +259,123 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
 
     if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ producers
+        // Raw bytes of block j+1 are loaded into registers before the wait
+        // for block j's slot, so their latency hides behind the pipeline.
         const int pt = tid - 128;  // 0..127
-        for (int j = 0; j < nblk; ++j) {  // every exit is a warp-uniform wait outcome
+        uint2 rk[16], rv[8];
+        __half sk[16];
+        uint4 sv[8];
+        auto load_k = [&](int j) {
             const uint8_t *hb = page_base(j);
             const int kb = (j % bpp) * kBN;
-            // K: 64 keys x 32 chunks of 8 dims; loads first, then the wait
-            {
-                const __half *ks = reinterpret_cast<const __half *>(hb + p.geom.ks_off);
-                uint2 raw[16];
-                __half sc[16];
+            const __half *ks = reinterpret_cast<const __half *>(hb + p.geom.ks_off);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
-                    raw[i] = *reinterpret_cast<const uint2 *>(hb + kq_byte(kb + key, k, kD / 32));
-                    sc[i] = ks[(kb + key) * (kD / 32) + (k >> 5)];
-                }
-                if (j >= 1 && !mbar_wait_warp(bar(kBarKEmpty), (uint32_t)((j - 1) & 1), abort)) break;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
-                    const __half2 d2 = __halves2half2(sc[i], sc[i]);
-                    const uint32_t d = *reinterpret_cast<const uint32_t *>(&d2);
-                    uint32_t x[4], hi[4], lo[4];
-                    i8x4_to_f16(raw[i].x, x[0], x[1]);
-                    i8x4_to_f16(raw[i].y, x[2], x[3]);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) mul_split(x[e], d, hi[e], lo[e]);
-                    const uint32_t off = sw128(kBN, key, k);
-                    *reinterpret_cast<uint4 *>(smem + kOffKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(smem + kOffKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
-                proxy_fence();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarKFull));
+            for (int i = 0; i < 16; ++i) {
+                const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
+                rk[i] = *reinterpret_cast<const uint2 *>(hb + kq_byte(kb + key, k, kD / 32));
+                sk[i] = ks[(kb + key) * (kD / 32) + (k >> 5)];
             }
-            // V: 128 byte rows (dim pairs) x 8 chunks of 8 keys -> [dim][key] tiles
-            {
-                const __half *vs = reinterpret_cast<const __half *>(hb + p.geom.vs_off);
-                uint2 raw[8];
-                uint4 sv[8];
+        };
+        auto load_v = [&](int j) {
+            const uint8_t *hb = page_base(j);
+            const int kb = (j % bpp) * kBN;
+            const __half *vs = reinterpret_cast<const __half *>(hb + p.geom.vs_off);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
-                    raw[i] = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + vq_byte(kb + k8, br, kD / 32));
-                    sv[i] = *reinterpret_cast<const uint4 *>(vs + (br >> 4) * P + kb + k8);
-                }
-                if (j >= 1 && !mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort)) break;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
-                    const int dA = (br >> 4) * 32 + (br & 15), dB = dA + 16;
-                    const uint32_t w[2] = {raw[i].x, raw[i].y};
-                    const uint32_t dv[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};  // (k, k+1) scale pairs
-                    uint32_t ah[4], al[4], bh[4], bl[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // keys 2e, 2e+1: bytes of w[e/2] at positions 2(e%2), 2(e%2)+1
-                        uint32_t sp;
-                        const uint32_t sel = (e & 1) ? 0x7372u : 0x7170u;  // bytes 2,3 or 0,1 -> low byte of each half
-                        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sp) : "r"(w[e >> 1]), "r"(0u), "r"(sel));
-                        uint32_t lo_n, hi_n, xa, xb;
-                        asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(lo_n) : "r"(sp), "r"(0x000f000fu), "r"(0x64006400u));
-                        asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(hi_n) : "r"(sp >> 4), "r"(0x000f000fu), "r"(0x64006400u));
-                        asm("sub.f16x2 %0, %1, %2;" : "=r"(xa) : "r"(lo_n), "r"(0x64086408u));  // code - 8
-                        asm("sub.f16x2 %0, %1, %2;" : "=r"(xb) : "r"(hi_n), "r"(0x64086408u));
-                        mul_split(xa, dv[e], ah[e], al[e]);
-                        mul_split(xb, dv[e], bh[e], bl[e]);
-                    }
-                    const uint32_t oa = sw128(kD, dA, k8), ob = sw128(kD, dB, k8);
-                    *reinterpret_cast<uint4 *>(smem + kOffVh + oa) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-                    *reinterpret_cast<uint4 *>(smem + kOffVl + oa) = make_uint4(al[0], al[1], al[2], al[3]);
-                    *reinterpret_cast<uint4 *>(smem + kOffVh + ob) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-                    *reinterpret_cast<uint4 *>(smem + kOffVl + ob) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-                }
-                proxy_fence();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarVFull));
+            for (int i = 0; i < 8; ++i) {
+                const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
+                rv[i] = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + vq_byte(kb + k8, br, kD / 32));
+                sv[i] = *reinterpret_cast<const uint4 *>(vs + (br >> 4) * P + kb + k8);
             }
+        };
+        // K of block j+1 needs only S_j finished, V of block j needs PV_{j-1}
+        // finished; S_j runs before PV_{j-1}, so K goes first.
+        auto write_k = [&](int j) {
+            const int kb = (j % bpp) * kBN;
+            (void)kb;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
+                const __half2 d2 = __halves2half2(sk[i], sk[i]);
+                const uint32_t d = *reinterpret_cast<const uint32_t *>(&d2);
+                uint32_t x[4], hi[4], lo[4];
+                i8x4_to_f16(rk[i].x, x[0], x[1]);
+                i8x4_to_f16(rk[i].y, x[2], x[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mul_split(x[e], d, hi[e], lo[e]);
+                const uint32_t off = sw128(kBN, key, k);
+                *reinterpret_cast<uint4 *>(smem + kOffKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(smem + kOffKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            proxy_fence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarKFull));
+        };
+        // V: 128 byte rows (dim pairs) x 8 chunks of 8 keys -> [dim][key] tiles
+        auto write_v = [&]() {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
+                const int dA = (br >> 4) * 32 + (br & 15), dB = dA + 16;
+                const uint32_t w[2] = {rv[i].x, rv[i].y};
+                const uint32_t dv[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};  // (k, k+1) scale pairs
+                uint32_t ah[4], al[4], bh[4], bl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    // keys 2e, 2e+1: bytes 2(e%2), 2(e%2)+1 of w[e/2], one per f16 half
+                    uint32_t sp;
+                    const uint32_t sel = (e & 1) ? 0x7372u : 0x7170u;
+                    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sp) : "r"(w[e >> 1]), "r"(0u), "r"(sel));
+                    uint32_t lo_n, hi_n, xa, xb;
+                    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(lo_n) : "r"(sp), "r"(0x000f000fu), "r"(0x64006400u));
+                    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(hi_n) : "r"(sp >> 4), "r"(0x000f000fu), "r"(0x64006400u));
+                    asm("sub.f16x2 %0, %1, %2;" : "=r"(xa) : "r"(lo_n), "r"(0x64086408u));  // code - 8
+                    asm("sub.f16x2 %0, %1, %2;" : "=r"(xb) : "r"(hi_n), "r"(0x64086408u));
+                    mul_split(xa, dv[e], ah[e], al[e]);
+                    mul_split(xb, dv[e], bh[e], bl[e]);
+                }
+                const uint32_t oa = sw128(kD, dA, k8), ob = sw128(kD, dB, k8);
+                *reinterpret_cast<uint4 *>(smem + kOffVh + oa) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+                *reinterpret_cast<uint4 *>(smem + kOffVl + oa) = make_uint4(al[0], al[1], al[2], al[3]);
+                *reinterpret_cast<uint4 *>(smem + kOffVh + ob) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+                *reinterpret_cast<uint4 *>(smem + kOffVl + ob) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+            }
+            proxy_fence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarVFull));
+        };
+        if (nblk > 0) {
+            load_k(0);
+            load_v(0);
+            write_k(0);
+            if (nblk > 1) load_k(1);
+        }
+        for (int j = 0; j < nblk; ++j) {  // every exit is a warp-uniform wait outcome
+            if (j + 1 < nblk) {
+                if (!mbar_wait_warp(bar(kBarKEmpty), (uint32_t)(j & 1), abort)) break;  // S_j done
+                write_k(j + 1);
+                if (j + 2 < nblk) load_k(j + 2);
+            }
+            if (j >= 1 && !mbar_wait_warp(bar(kBarODone + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort))
+                break;  // PV_{j-1} done
+            write_v();
+            if (j + 1 < nblk) load_v(j + 1);
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------ MMA issue (one thread)
         if (lane == 0) {
-            const uint32_t qa = smem_u32(smem + kOffQ), kh = smem_u32(smem + kOffKh), kl = smem_u32(smem + kOffKl);
-            const uint32_t pa = smem_u32(smem + kOffP), vh = smem_u32(smem + kOffVh), vl = smem_u32(smem + kOffVl);
+            // descriptors of the tile bases; a k-step adds its byte offset / 16
+            const uint64_t dq = smem_desc(smem_u32(smem + kOffQ)), dkh = smem_desc(smem_u32(smem + kOffKh));
+            const uint64_t dkl = smem_desc(smem_u32(smem + kOffKl)), dvh = smem_desc(smem_u32(smem + kOffVh));
+            const uint64_t dvl = smem_desc(smem_u32(smem + kOffVl)), dp = smem_desc(smem_u32(smem + kOffP));
             const uint32_t id_s = idesc_f16(kTileRows, kBN), id_o = idesc_f16(kTileRows, kD);
             auto issue_s = [&](int j) {
                 const uint32_t ts = tmem + kColS + (uint32_t)((j & 1) * kBN);
-#pragma unroll 1
+#pragma unroll
                 for (int s = 0; s < kD / 16; ++s) {
-                    const uint32_t ao = (s >> 2) * (kTileRows * 128) + (s & 3) * 32;
-                    const uint32_t bo = (s >> 2) * (kBN * 128) + (s & 3) * 32;
-                    mma_f16(ts, smem_desc(qa + ao), smem_desc(kh + bo), id_s, s > 0);
-                    mma_f16(ts, smem_desc(qa + ao), smem_desc(kl + bo), id_s, 1);
+                    const uint32_t ao = ((s >> 2) * (kTileRows * 128) + (s & 3) * 32) >> 4;
+                    const uint32_t bo = ((s >> 2) * (kBN * 128) + (s & 3) * 32) >> 4;
+                    mma_f16(ts, dq + ao, dkh + bo, id_s, s > 0);
+                    mma_f16(ts, dq + ao, dkl + bo, id_s, 1);
                 }
                 mma_commit(bar(kBarSFull + (j & 1)));
                 mma_commit(bar(kBarKEmpty));
@@ -366,16 +396,17 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     tc_after_sync();
                     issue_s(j + 1);
                 }
-                ok = mbar_wait(bar(kBarPFull), (uint32_t)(j & 1), abort) &&
+                ok = mbar_wait(bar(kBarPFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort) &&
                      mbar_wait(bar(kBarVFull), (uint32_t)(j & 1), abort);
                 if (!ok) break;
                 tc_after_sync();
-#pragma unroll 1
+                const uint64_t dpj = dp + (uint64_t)(((j & 1) * kPBytes) >> 4);
+#pragma unroll
                 for (int s = 0; s < kBN / 16; ++s) {
-                    mma_f16(tmem + kColO, smem_desc(pa + s * 32), smem_desc(vh + s * 32), id_o, (j > 0 || s > 0) ? 1u : 0u);
-                    mma_f16(tmem + kColO, smem_desc(pa + s * 32), smem_desc(vl + s * 32), id_o, 1);
+                    mma_f16(tmem + kColO, dpj + (s * 32 >> 4), dvh + (s * 32 >> 4), id_o, (j > 0 || s > 0) ? 1u : 0u);
+                    mma_f16(tmem + kColO, dpj + (s * 32 >> 4), dvl + (s * 32 >> 4), id_o, 1);
                 }
-                mma_commit(bar(kBarODone));
+                mma_commit(bar(kBarODone + (j & 1)));
             }
             // every MMA this thread issued has finished before TMEM is read or freed
             mma_commit(bar(kBarFinal));
@@ -409,13 +440,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             tc_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarSEmpty + (j & 1)));
-            float mx = -INFINITY;
+            // causal mask only where the block reaches past this row (keys i > lim)
+            const long long lim64 = row_valid ? qpos - kpos0 : -1;
+            if (lim64 < kBN - 1) {
+                const int lim = (int)(lim64 < -1 ? -1 : lim64);
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) {
-                const bool valid = row_valid && (kpos0 + i <= qpos);
-                s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[i]);
+                for (int i = 0; i < kBN; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
             }
+            // raw-score max in four independent chains; scale > 0 keeps the order
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < kBN; ++i) m4[i & 3] = fmaxf(m4[i & 3], s[i]);
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
             int need_rescale = 0;
             float alpha = 1.f;
             if (mx > m_used + 8.f || (m_used == -INFINITY && mx != -INFINITY)) {
@@ -424,24 +460,27 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 l_sum *= alpha;
                 m_used = mx;
             }
-            float bsum = 0.f;
+            // weights 2^(s * scale - m) <= 2^8 (a masked s = -inf gives +0)
+            const float mneg = (m_used == -INFINITY) ? 0.f : -m_used;
+            float b4[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[kBN / 2];
 #pragma unroll
             for (int i = 0; i < kBN; i += 2) {
-                const float e0 = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_used);
-                const float e1 = (s[i + 1] == -INFINITY) ? 0.f : exp2f(s[i + 1] - m_used);
+                float e0, e1;
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fmaf(s[i], p.scale_log2, mneg)));
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fmaf(s[i + 1], p.scale_log2, mneg)));
                 const __half2 hp = __floats2half2_rn(e0, e1);
                 const float2 hf = __half22float2(hp);
-                bsum += hf.x + hf.y;  // l sums exactly the weights the MMA uses
+                b4[(i >> 1) & 3] += hf.x + hf.y;  // l sums exactly the weights the MMA uses
                 pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
             }
-            l_sum += bsum;
-            // PV_{j-1} done: P may be rewritten and O is stable
-            if (j >= 1) {
-                ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort);
+            l_sum += (b4[0] + b4[1]) + (b4[2] + b4[3]);
+            // a rescale of O needs PV_{j-1} done; P buffer j & 1 needs PV_{j-2} done
+            if (j >= 1 && __any_sync(0xffffffffu, need_rescale)) {
+                ok = mbar_wait_warp(bar(kBarODone + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
                 if (!ok) break;
                 tc_after_sync();
-                if (__any_sync(0xffffffffu, need_rescale)) {
+                {
                     const uint32_t ta = lane_base + kColO;
                     for (int c = 0; c < kD; c += 32) {
                         float v[32];
@@ -453,17 +492,23 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
             }
+            if (j >= 2) {
+                ok = mbar_wait_warp(bar(kBarODone + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort);
+                if (!ok) break;
+            }
+            uint8_t *pbuf = smem + kOffP + (j & 1) * kPBytes;
 #pragma unroll
             for (int c8 = 0; c8 < kBN / 8; ++c8)
-                *reinterpret_cast<uint4 *>(smem + kOffP + sw128(kTileRows, row, c8 * 8)) =
+                *reinterpret_cast<uint4 *>(pbuf + sw128(kTileRows, row, c8 * 8)) =
                     make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
             proxy_fence();
             tc_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarPFull));
+            if (lane == 0) mbar_arrive(bar(kBarPFull + (j & 1)));
         }
         // the last PV, then the partial: unnormalised O, m (log2 units), l
-        if (ok && nblk > 0) ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((nblk - 1) & 1), abort);
+        if (ok && nblk > 0)
+            ok = mbar_wait_warp(bar(kBarODone + ((nblk - 1) & 1)), (uint32_t)(((nblk - 1) >> 1) & 1), abort);
         if (ok) {
             tc_after_sync();
             const uint32_t ta = lane_base + kColO;
