@@ -253,7 +253,7 @@ def run_reference(args, wl):
 
 def run_ours(args, wl):
     import torch
-    from host_streamed_paged_gb300 import kvs
+    from host_streamed_paged_gb300 import kvs, replicas
 
     rank, world, local = _rank_env()
     dist = None
@@ -341,12 +341,7 @@ def run_ours(args, wl):
         e1.record(attn)
         torch.cuda.synchronize(dev)
         st.sync()
-        ms = e0.elapsed_time(e1) / n
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return replicas.max_over_ranks(e0.elapsed_time(e1) / n, dist, dev)
 
     hbm_peak, tc_peak, _, peak_src = _measured_peaks()
     fracs = [None]
@@ -461,7 +456,7 @@ def run_ours(args, wl):
                               f"{L} layers of one step ({Hq} heads x {T} keys), time scaled to the whole step")}
             parity = {"layers_checked": cpu_layers, "rows_checked": rows_cpu, "max_rel_err": max(errs), "tol": 1e-3}
 
-        value = world * R / (ms_step * 1e-3)
+        value = replicas.aggregate_rows_per_s(R, ms_step, world)
         kv_bytes_step = L * npages * st.page_bytes
         res_pages = int(sum(int(m.sum()) for m in masks))
         line = {
@@ -482,7 +477,8 @@ def run_ours(args, wl):
                     "ceiling_how": "pinned cudaMemcpyAsync 1 GiB, best of 5"},
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d_in,
+            "e2e": {"value": replicas.aggregate_rows_per_s(R, e2e_ms, world), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d_in,
                     "d2h_bytes_per_step": d2h_out},
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clk,
