@@ -75,6 +75,12 @@ WORKLOADS = {
 }
 GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 
+# DRAM bytes (read + write) per timed launch of the roofline kernel, from the ncu capture in
+# profiles/ named here; a workload missing from this table reports traffic as null
+TRAFFIC = {
+    "resident131k": (228.08e6, "profiles/decode_kernel_resident131k.md"),
+}
+
 
 def _rank_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
@@ -431,9 +437,11 @@ def run_ours(args, wl):
                     "timed_region": f"{n_eager} host-issued steps ({ms_timed_eager:.2f} ms/step)"}
         else:
             achieved = (r_bytes / (r_ms * 1e-3) / 1e9) if r_ms > 0 else 0.0
+            tr = TRAFFIC.get(args.workload)
             roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": None,
-                    "kernel": f"decode_kernel<{D},{math.ceil(R * Hq / Hk / 8)}> launches over resident + tail pages",
+                    "frac": achieved / hbm_peak, "traffic": tr[0] if tr and L == WORKLOADS[args.workload]["L"] else None,
+                    "traffic_source": tr[1] if tr else None,
+                    "kernel": f"decode_kernel<{D},{math.ceil(R * Hq / Hk / 8)},8> launches over resident + tail pages",
                     "launches_timed": r_n, "bytes_per_launch": r_bytes / max(r_n, 1),
                     "ms_per_launch": r_ms / max(r_n, 1), "peak_source": peak_src + " hbm_gbs",
                     "timed_region": f"{n_eager} host-issued steps ({ms_timed_eager:.2f} ms/step)"}

@@ -18,7 +18,10 @@
 // Q4_0 scale is folded into P' per (key, 32-dim block).  Splitting the fp32
 // operand into two f16 parts keeps ~22 significand bits, so the result
 // tracks fp32 arithmetic (tested against the fp64 oracle at 1e-3 relative).
-// Softmax over the page's keys runs in fp32 with exp2 on log2-scaled scores.
+// Softmax over the page's keys runs in fp32 with exp2 on log2-scaled scores;
+// each weight p is split once into f16 hi + lo, and every 32-dim block forms
+// its P' = (hi + lo) * dV with f16x2 arithmetic: rn(hi dV), the exact
+// remainder of that product by a fused multiply-add, plus lo dV.
 //
 // Fragment orders.  The reduction index of each MMA is permuted so that one
 // 64-bit load gives a thread its whole fragment:
@@ -85,6 +88,15 @@ __device__ __forceinline__ void u4x8_to_frag16(uint32_t w, uint32_t (&a)[4]) {
     asm("sub.f16x2 %0, %1, %2;" : "=r"(a[1]) : "r"(t1), "r"(bias_hi));
     asm("sub.f16x2 %0, %1, %2;" : "=r"(a[2]) : "r"(t2), "r"(bias_lo));
     asm("sub.f16x2 %0, %1, %2;" : "=r"(a[3]) : "r"(t3), "r"(bias_hi));
+}
+
+// (hi + lo) * d for f16x2 pairs: ph = rn(hi d), pl = rn(lo d + (hi d - ph)),
+// where hi d - ph is formed exactly by a fused multiply-add
+__device__ __forceinline__ void scale_split(uint32_t hi, uint32_t lo, uint32_t d, uint32_t &ph, uint32_t &pl) {
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(ph) : "r"(hi), "r"(d));
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(hi), "r"(d), "r"(ph ^ 0x80008000u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(pl) : "r"(lo), "r"(d), "r"(r));
 }
 
 // (x, y) fp32 -> f16x2 hi = rn(x, y), lo = rn(x - hi, y - hi).
@@ -318,25 +330,44 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         }
         __syncthreads();
 
-        // Softmax over the page's keys, one row per warp at a time.
+        // Softmax over the page's keys, one row per warp at a time.  Each lane
+        // owns 4-key groups (at most two: P <= 256) and rewrites a group's four
+        // fp32 scores in place as the PV B-fragment record of its weights e as
+        // f16 pairs hi = rn(e), lo = rn(e - hi): {hi k0,k2 | hi k1,k3 | lo k0,k2 |
+        // lo k1,k3}, the key order of the MMA's k positions (2t, 2t+1, 2t+8, 2t+9).
         const int split = (int)page;
         for (int m = warp; m < MR; m += W) {
+            float4 sg[2];
             float mx = -INFINITY;
-            for (int k = lane; k < P; k += 32) mx = fmaxf(mx, sc[m * SP + k]);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int k4 = 4 * (lane + 32 * q);
+                sg[q] = k4 < P ? *reinterpret_cast<const float4 *>(sc + m * SP + k4)
+                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                mx = fmaxf(fmaxf(mx, fmaxf(sg[q].x, sg[q].y)), fmaxf(sg[q].z, sg[q].w));
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
             float sum = 0.f;
-            if (mx == -INFINITY) {
-                for (int k = lane; k < P; k += 32) sc[m * SP + k] = 0.f;
-            } else {
-                for (int k = lane; k < P; k += 32) {
-                    const float e = exp2f(sc[m * SP + k] - mx);
-                    sc[m * SP + k] = e;
-                    sum += e;
-                }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            for (int q = 0; q < 2; ++q) {
+                const int k4 = 4 * (lane + 32 * q);
+                if (k4 >= P) continue;
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                if (mx != -INFINITY) {
+                    e[0] = exp2f(sg[q].x - mx);
+                    e[1] = exp2f(sg[q].y - mx);
+                    e[2] = exp2f(sg[q].z - mx);
+                    e[3] = exp2f(sg[q].w - mx);
+                }
+                sum += (e[0] + e[1]) + (e[2] + e[3]);
+                uint32_t h02, l02, h13, l13;
+                split_f16(e[0], e[2], h02, l02);
+                split_f16(e[1], e[3], h13, l13);
+                *reinterpret_cast<uint4 *>(sc + m * SP + k4) = make_uint4(h02, h13, l02, l13);
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             const int mg = mo + m;
             if (lane == 0 && mg < rows) {
                 const int r = mg / G, h = g * G + (mg - r * G);
@@ -387,15 +418,19 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                         uint32_t a0[4], a1[4];
                         u4x8_to_frag16(s ? v0.y : v0.x, a0);
                         u4x8_to_frag16(s ? v1.y : v1.x, a1);
-                        const float2 dA = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.z : &dvr.x));
-                        const float2 dB = __half22float2(*reinterpret_cast<const __half2 *>(s ? &dvr.w : &dvr.y));
+                        // Q4_0 scales of keys (+0, +2) and (+1, +3) as f16 pairs
+                        const uint32_t dlo = s ? dvr.z : dvr.x, dhi = s ? dvr.w : dvr.y;
+                        uint32_t d02, d13;
+                        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(d02) : "r"(dlo), "r"(dhi));
+                        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d13) : "r"(dlo), "r"(dhi));
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const float4 pv =
-                                *reinterpret_cast<const float4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
+                            const uint4 pr =
+                                *reinterpret_cast<const uint4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
+                            // P' = (hi + lo) * d: hi * d rounded, its exact remainder, plus lo * d
                             uint32_t bh0, bl0, bh1, bl1;
-                            split_f16(pv.x * dA.x, pv.z * dB.x, bh0, bl0);  // keys +0, +2
-                            split_f16(pv.y * dA.y, pv.w * dB.y, bh1, bl1);  // keys +1, +3
+                            scale_split(pr.x, pr.z, d02, bh0, bl0);  // keys +0, +2
+                            scale_split(pr.y, pr.w, d13, bh1, bl1);  // keys +1, +3
                             mma16816(acc[pp][0][nt], a0, bh0, bh1);
                             mma16816(acc[pp][1][nt], a1, bh0, bh1);
                             mma16816(acc[pp][0][nt], a0, bl0, bl1);
