@@ -281,7 +281,8 @@ def run_ours(args, wl):
     arena_slots = fixed_arena if fixed_arena else 2 * L + wl["ring"] + pool
     st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
                       max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"], arena_slots=arena_slots,
-                      device=dev, lanes=wl.get("lanes", 1), dma_fill=wl.get("dma", False))
+                      device=dev, lanes=wl.get("lanes", 1), dma_fill=wl.get("dma", False),
+                      host_alloc=args.host_alloc)
     ceiling = h2d_ceiling(torch, dev)
 
     # history: seeded rows appended through the KV writer
@@ -476,6 +477,7 @@ def run_ours(args, wl):
                        "resident_fraction": res_pages / (L * npages), "ring_slots": ring,
                        "chunk_pages": chunk_eff, "lanes": wl.get("lanes", 1),
                        "fill": "copy engines" if wl.get("dma") else "SM fill kernel",
+                       "host_alloc": args.host_alloc,
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {kv_bytes_step / 1e9:.2f} GB of KV pages read per step",
                        "step": "per layer: append rows, prefetch next layer, attend, truncate; one CUDA graph replay"},
@@ -520,6 +522,8 @@ def main():
     ap.add_argument("--resident", type=float, default=-1.0,
                     help="override the resident fraction (prefix of each layer; for long262k of the arena)")
     ap.add_argument("--sweep", action="store_true", help="long262k: sweep the resident fraction 0..100%%")
+    ap.add_argument("--host-alloc", choices=["pageable", "pinned", "hugepage"], default="pinned",
+                    help="host history buffer: registered numpy memory, CUDA pinned, or huge-page advised")
     ap.add_argument("--fill", choices=["default", "sm", "dma"], default="default",
                     help="ring refills by the SM fill kernel or the copy engines (default: the workload's)")
     args = ap.parse_args()

@@ -151,7 +151,7 @@ __host__ __device__ inline int pv_parts(int D, int P) {
 
 // Shared-memory carve of decode_kernel<D, NT, W> (bytes; page size P, S stages).
 struct DecodeSmem {
-    int stage, sc, red, obuf, bar, total, stages;
+    int stage, sc, red, obuf, rowoff, bar, total, stages;
 };
 __host__ __device__ inline int align_to(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, int stages) {
@@ -167,7 +167,8 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, i
     // the output tile reuses the score buffer when it fits there
     s.obuf = (SP >= D) ? s.sc : align_to(red_end, 16);
     const int obuf_end = (SP >= D) ? red_end : s.obuf + MR * D * 4;
-    s.bar = align_to(red_end > obuf_end ? red_end : obuf_end, 16);
+    s.rowoff = align_to(red_end > obuf_end ? red_end : obuf_end, 16);  // MR ints: partial row offsets
+    s.bar = align_to(s.rowoff + MR * 4, 16);
     s.total = s.bar + 16 * stages;
     return s;
 }
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     float *sc = reinterpret_cast<float *>(smem + L.sc);
     float *red = reinterpret_cast<float *>(smem + L.red);
     float *obuf = reinterpret_cast<float *>(smem + L.obuf);
+    int *rowoff = reinterpret_cast<int *>(smem + L.rowoff);
     const uint32_t bar0 = smem_u32(smem + L.bar);
     const int head_bytes = (int)p.geom.head_bytes;
 
@@ -248,6 +250,16 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 
         // Scores: each warp takes KPW 16-key groups at a time as MMA row tiles.
         const long long kpos0 = (long long)page * P;
+        // per stored row (nt, parity): the last visible key of this page, -1 if none
+        int klim[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int par = 0; par < 2; ++par) {
+                const int mg = mo + nt * 8 + 2 * tig + par;
+                const long long l = mg < rows ? p.pos0 + mg / G - kpos0 : -1;
+                klim[nt][par] = l < -1 ? -1 : (l > P ? P : (int)l);
+            }
         const int NKG = P / 16;
         const __half *ksc = reinterpret_cast<const __half *>(hs + p.geom.ks_off);
 #pragma unroll 1
@@ -321,8 +333,8 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = (e < 2) ? k0 : k1;
-                        const int m = nt * 8 + 2 * tig + (e & 1), mg = mo + m;
-                        const bool valid = mg < rows && kpos0 + key <= p.pos0 + mg / G;
+                        const int m = nt * 8 + 2 * tig + (e & 1);
+                        const bool valid = key <= klim[nt][e & 1];
                         sc[m * SP + key] = valid ? S_[q][nt][e] * p.scale_log2 : -INFINITY;
                     }
                 }
@@ -371,6 +383,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
             const int mg = mo + m;
             if (lane == 0 && mg < rows) {
                 const int r = mg / G, h = g * G + (mg - r * G);
+                rowoff[m] = h * R + r;
                 float *ml = p.part_ml + (((int64_t)split * p.Hq + h) * R + r) * 2;
                 ml[0] = mx;
                 ml[1] = sum;
@@ -500,12 +513,12 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                     }
         }
         __syncthreads();
-        // coalesced partial store of the valid rows
+        // coalesced partial store of the valid rows (row offsets from the table)
         const int urows = rows - mo < MR ? rows - mo : MR;
+        const int64_t split_base = (int64_t)split * p.Hq * R;
         for (int c = threadIdx.x; c < urows * (D / 4); c += NTH) {
-            const int m = c / (D / 4), d4 = (c % (D / 4)) * 4, mg = mo + m;
-            const int r = mg / G, h = g * G + (mg - r * G);
-            *reinterpret_cast<float4 *>(p.part_o + (((int64_t)split * p.Hq + h) * R + r) * D + d4) =
+            const int m = c / (D / 4), d4 = (c % (D / 4)) * 4;
+            *reinterpret_cast<float4 *>(p.part_o + (split_base + rowoff[m]) * D + d4) =
                 *reinterpret_cast<const float4 *>(obuf + m * D + d4);
         }
         __syncthreads();  // obuf / sc free for the next unit

@@ -308,6 +308,29 @@ def kvs_trace_read(ctx):
 
 # ------------------------------------------------------------ owner class
 
+def _alloc_host(nbytes, how):
+    """Host history buffer.  "pinned" (default): CUDA-allocated pinned memory
+    (torch); "pageable": numpy memory that kvs_create registers with CUDA;
+    "hugepage": an anonymous mapping advised for transparent huge pages, then
+    registered.  Measured on GB300 with 64 layers x 262144 tokens (27 GB): ring
+    refills from CUDA-allocated memory ran at 89 % of the host-link ceiling,
+    from registered pageable memory at 7.5 % (the GPU maps it with small pages),
+    from huge-page advised memory at 57 %."""
+    if how == "pageable":
+        return np.empty(nbytes, dtype=np.uint8)
+    if how == "pinned":
+        import torch
+        return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    if how == "hugepage":
+        import mmap
+        m = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        if hasattr(m, "madvise") and hasattr(mmap, "MADV_HUGEPAGE"):
+            m.madvise(mmap.MADV_HUGEPAGE)
+        return np.frombuffer(m, dtype=np.uint8)
+    raise ValueError(f"unknown host allocation {how!r}")
+
+
+
 class KVStream:
     """A kvs context with its torch-owned arena, workspace, streams and host history.
 
@@ -320,7 +343,7 @@ class KVStream:
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
                  max_tokens, ring_slots=8, chunk_pages=0, arena_slots=None, arena_bytes=None,
                  plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None,
-                 prefill_split_pages=0, dma_fill=False):
+                 prefill_split_pages=0, dma_fill=False, host_alloc="pinned"):
         cfg = kvs_config()
         cfg.page_tokens, cfg.n_layers, cfg.n_kv_head, cfg.head_dim = page_tokens, n_layers, n_kv_head, head_dim
         cfg.max_q_head, cfg.max_rows, cfg.max_tokens = max_q_head, max_rows, max_tokens
@@ -356,7 +379,7 @@ class KVStream:
             self.arena = torch.empty(arena_bytes, dtype=torch.uint8, device=device)
             self.workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
             if host is None:
-                host = np.empty(host_bytes, dtype=np.uint8)
+                host = _alloc_host(host_bytes, host_alloc)
             self.host = host
             cfg.arena, cfg.workspace = self.arena.data_ptr(), self.workspace.data_ptr()
             cfg.host = _ptr(host)

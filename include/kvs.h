@@ -98,7 +98,12 @@ typedef struct {
     void *workspace;       /* device bytes for split-K partials; 256-byte aligned */
     uint64_t workspace_bytes;
     void *host;            /* host history: n_layers * ceil(max_tokens/P) pages, layer-major;
-                              registered with CUDA by kvs_create if not already pinned */
+                              registered with CUDA by kvs_create if not already pinned.
+                              Prefer memory from cudaHostAlloc: ring refills read it
+                              through the GPU's mappings, and registered pageable memory
+                              is mapped with small pages (on GB300 a 27 GB registered
+                              history streamed at 7.5 % of the link, a cudaHostAlloc one
+                              at 89 %) */
     uint64_t host_bytes;
     uint32_t ring_slots;   /* initial ring size in page slots (>= 1) */
     uint32_t chunk_pages;  /* ring pages per ready/consumed handshake; 0: ring_slots/4
