@@ -186,6 +186,9 @@ template <int D, int NT, int W>
 __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    // launched as a programmatic dependent: nothing is read before the grids
+    // this launch depends on have completed and their writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int NB = D / 32;  // 32-dim scale blocks
     constexpr int KS = D / 16;  // QK k-steps
     constexpr int MR = NT * 8;  // MMA rows (query rows x heads, padded to 8)
@@ -539,6 +542,8 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 // = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand.
 template <int D, int NT>
 __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__ DecodeParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");            // q and the previous readers of qf
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // attention may be scheduled
     constexpr int KS = D / 16;
     const int g = blockIdx.x, G = p.G, rows = G * p.R;
     uint4 *qf = const_cast<uint4 *>(p.qf) + (int64_t)g * NT * KS * 32;
@@ -569,12 +574,30 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
 
 int g_num_sms = 0;
 
+// Launch as a programmatic dependent of the previous kernel on `s`: the grid
+// may be scheduled once that kernel signals (griddepcontrol.launch_dependents)
+// and waits in griddepcontrol.wait for its completion before touching memory.
+template <typename K, typename A>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, int smem, cudaStream_t s, const A &arg) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, arg);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int D, int NT, int W>
 cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     DecodeParams p = p_in;
     if (p.prep_q) {
-        qprep_kernel<D, NT><<<p.geom.Hk, kThreads, 0, s>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(qprep_kernel<D, NT>, dim3(p.geom.Hk), dim3(kThreads), 0, s, p);
         if (e != cudaSuccess) return e;
         if (p.n_items == 0) return cudaSuccess;
     }
@@ -609,8 +632,7 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     }
     const int per_cta = (U + max_ctas - 1) / max_ctas;
     const int grid = (U + per_cta - 1) / per_cta;
-    decode_kernel<D, NT, W><<<grid, W * 32, L.total, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel<D, NT, W>, dim3(grid), dim3(W * 32), L.total, s, p);
 }
 
 template <int D>
@@ -649,14 +671,24 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     __shared__ float wmax[NW], wl[NW];
     __shared__ float wsm[kCombineBlock], lsm[kCombineBlock];
     __shared__ float wo[NW][DS];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next call's Q prep may be scheduled
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
     const int d0 = blockIdx.y * DS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
     auto base_of = [&](int s) { return ((int64_t)s * p.Hq + h) * p.R + r; };
 
+    // (m, l) of the first weight block stay in registers for its weights
+    constexpr int kKeep = kCombineBlock / kCombineThreads;
+    float2 keep[kKeep];
     float mx = -INFINITY;
-    for (int s = threadIdx.x; s < nsplit; s += kCombineThreads) {
+#pragma unroll
+    for (int q = 0; q < kKeep; ++q) {
+        const int s = threadIdx.x + q * kCombineThreads;
+        keep[q] = s < nsplit ? *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2) : make_float2(0.f, 0.f);
+        if (keep[q].y > 0.f) mx = fmaxf(mx, keep[q].x);
+    }
+    for (int s = threadIdx.x + kCombineBlock; s < nsplit; s += kCombineThreads) {
         const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2);
         if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
     }
@@ -675,11 +707,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
         for (int b0 = 0; b0 < nsplit; b0 += kCombineBlock) {
             const int nb = nsplit - b0 < kCombineBlock ? nsplit - b0 : kCombineBlock;
             __syncthreads();  // the previous block's weights are consumed
-            for (int j = threadIdx.x; j < nb; j += kCombineThreads) {
-                const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(b0 + j) * 2);
-                const bool live = ml.y > 0.f;
-                wsm[j] = live ? exp2f(ml.x - M) : 0.f;
-                lsm[j] = live ? ml.y : 0.f;
+            if (b0 == 0) {
+#pragma unroll
+                for (int q = 0; q < kKeep; ++q) {
+                    const int j = threadIdx.x + q * kCombineThreads;
+                    if (j >= nb) continue;
+                    const bool live = keep[q].y > 0.f;
+                    wsm[j] = live ? exp2f(keep[q].x - M) : 0.f;
+                    lsm[j] = live ? keep[q].y : 0.f;
+                }
+            } else {
+                for (int j = threadIdx.x; j < nb; j += kCombineThreads) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(b0 + j) * 2);
+                    const bool live = ml.y > 0.f;
+                    wsm[j] = live ? exp2f(ml.x - M) : 0.f;
+                    lsm[j] = live ? ml.y : 0.f;
+                }
             }
             __syncthreads();
             for (int j0 = warp; j0 < nb; j0 += NW * kCombineUnroll) {
