@@ -49,11 +49,11 @@ WORKLOADS = {
     "decode32k": dict(
         desc=("decode stack: 64 layers x 1 row, context 32768, 24 q / 4 kv heads, D 256, page 256, "
               "Q8_0 K / Q4_0 V, 50% of pages resident (seeded), rest streamed via an 8-slot ring "
-              "with next-layer prefetch (2-page chunks on 4 copy/attention lanes)"),
-        L=64, T=32768, R=1, ring=8, chunk=2, lanes=4, residency=("random", 0.5)),
+              "with next-layer prefetch (4-page chunks on 2 lanes)"),
+        L=64, T=32768, R=1, ring=8, chunk=4, lanes=2, residency=("random", 0.5)),
     "decode32k_small": dict(  # a reduced copy for quick checks and profiling captures
         desc="decode stack, 8 layers, otherwise as decode32k",
-        L=8, T=32768, R=1, ring=8, chunk=2, lanes=4, residency=("random", 0.5)),
+        L=8, T=32768, R=1, ring=8, chunk=4, lanes=2, residency=("random", 0.5)),
     "verify163k": dict(
         desc=("span verify: 6 causal rows at positions 163840..163845, 64 layers, 24 q / 4 kv heads, D 256, "
               "page 256, Q8_0 K / Q4_0 V; 400 resident pages per layer (prefix), the rest via an 8-slot ring"),
