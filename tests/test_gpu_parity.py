@@ -326,6 +326,51 @@ def test_span_verify_full_size_one_layer():
     assert st.stats()["h2d_pages"] == 641 - 400 - 2  # the last two pages sit in tail slots
 
 
+@pytest.mark.parametrize("R,resident", [(1, 0.5), (4, 0.0)])
+def test_long_context_full_size_one_layer(R, resident):
+    """Context 262144 (1024 pages of 256), 24 q / 4 kv heads, D 256: a resident
+    prefix, the rest through a large ring in 32-page chunks on 4 lanes, as the
+    long-context benchmark runs it; every row against the oracle."""
+    P, Hk, Hq, D = 256, 4, 24, 256
+    T = 262144 + R - 1
+    npages = -(-T // P)
+    n_res = int(resident * npages)
+    st = make_stream(P, 1, Hk, D, Hq, R, T, ring=1009, chunk=32, pool_pages=max(n_res, 1), lanes=4)
+    (k, v), = _fill(st, 1, T, Hk, D)
+    mask = np.zeros(npages, np.uint8)
+    mask[:n_res] = 1
+    st.set_residency(0, mask)
+    q = queries(SEED, 0, R, Hq, D)
+    out, lse = attend(st, 0, q, T - R, 1 / 16)
+    ro, rl = oracle_ref(k, v, q, T - R, 1 / 16)
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] == npages - n_res - 2
+
+
+def test_prefill_full_size_sampled_rows():
+    """A 256-row fp16 prefill chunk at context 131072 (tensor-core path), half
+    the pages resident as a prefix and the rest through the 8-slot ring;
+    eight sampled rows against the oracle (each row at its own position)."""
+    import torch
+    P, Hk, G, D, R = 256, 4, 6, 256, 256
+    Hq = G * Hk
+    T = 131072 + R
+    npages = -(-T // P)
+    st = kvs.KVStream(page_tokens=P, n_layers=1, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
+                      max_tokens=T, ring_slots=8, chunk_pages=2, lanes=2, arena_slots=2 + 8 + npages)
+    (k, v), = _fill(st, 1, T, Hk, D)
+    mask = np.zeros(npages, np.uint8)
+    mask[:npages // 2] = 1
+    st.set_residency(0, mask)
+    q = queries(SEED, 0, R, Hq, D).astype(np.float16).astype(np.float32)  # the f16 values exactly
+    out, lse = attend(st, 0, q, T - R, 1 / 16, dtype=torch.float16)
+    qkv = oracle.QuantKV(k, v)
+    for r in (0, 1, 63, 64, 127, 128, 200, 255):
+        ro, rl = qkv.attend(q[r:r + 1], T - R + r, 1 / 16)
+        check_parity(out[r:r + 1], lse[r:r + 1], ro, rl)
+    assert st.stats()["h2d_pages"] > 0
+
+
 def test_step_graph_replay_matches_eager_bitwise():
     """A decode step captured with kvs_graph_* replays to the eager step's exact outputs."""
     import torch
