@@ -151,7 +151,7 @@ __host__ __device__ inline int pv_parts(int D, int P) {
 
 // Shared-memory carve of decode_kernel<D, NT, W> (bytes; page size P, S stages).
 struct DecodeSmem {
-    int stage, sc, red, obuf, rowoff, bar, total, stages;
+    int stage, sc, red, obuf, rowoff, rowtab, bar, total, stages;
 };
 __host__ __device__ inline int align_to(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, int stages) {
@@ -168,7 +168,8 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, i
     s.obuf = (SP >= D) ? s.sc : align_to(red_end, 16);
     const int obuf_end = (SP >= D) ? red_end : s.obuf + MR * D * 4;
     s.rowoff = align_to(red_end > obuf_end ? red_end : obuf_end, 16);  // MR ints: partial row offsets
-    s.bar = align_to(s.rowoff + MR * 4, 16);
+    s.rowtab = align_to(s.rowoff + MR * 4, 16);  // 64 int2 per CTA: (mg / G, (mg % G) * R + mg / G)
+    s.bar = align_to(s.rowtab + 64 * 8, 16);
     s.total = s.bar + 16 * stages;
     return s;
 }
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     float *red = reinterpret_cast<float *>(smem + L.red);
     float *obuf = reinterpret_cast<float *>(smem + L.obuf);
     int *rowoff = reinterpret_cast<int *>(smem + L.rowoff);
+    int2 *rowtab = reinterpret_cast<int2 *>(smem + L.rowtab);
     const uint32_t bar0 = smem_u32(smem + L.bar);
     const int head_bytes = (int)p.geom.head_bytes;
 
@@ -222,6 +224,9 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     bool pending[2] = {false, false};      // a load into this stage is not consumed yet
     uint32_t pend_parity[2] = {0u, 0u};    // the phase that load completes
     for (int s = 0; s < S && u0 + s < u1; ++s) pending[s] = true;
+    // rows x heads m (< 64): x = its query row r = m / G, y = h_local * R + r with
+    // h_local = m % G; the partial of kv head g sits at row g * G * R + y
+    for (int m = threadIdx.x; m < 64; m += NTH) rowtab[m] = make_int2(m / G, (m % G) * R + m / G);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 16 * s));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -232,11 +237,15 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     __syncthreads();
 
     bool ok = true;
+    // unit u = (g * n_items + item) * T + tile, advanced incrementally
+    int tile = u0 % T, item = (u0 / T) % p.n_items, g = u0 / T / p.n_items;
     for (int u = u0, i = 0; u < u1; ++u, ++i) {
+        if (i > 0 && ++tile == T) {
+            tile = 0;
+            if (++item == p.n_items) item = 0, ++g;
+        }
         const int stage = i % S;
         const uint32_t parity = (uint32_t)((i / S) & 1);
-        const int tile = u % T, gi = u / T;
-        const int g = gi / p.n_items, item = gi - g * p.n_items;
         const int mo = tile * 8;  // first query row x head of this unit's tiles
         const uint32_t page = p.page[item];
         const uint8_t *hs = smem + L.stage + stage * head_bytes;  // this unit's page-head section
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 #pragma unroll
             for (int par = 0; par < 2; ++par) {
                 const int mg = mo + nt * 8 + 2 * tig + par;
-                const long long l = mg < rows ? p.pos0 + mg / G - kpos0 : -1;
+                const long long l = mg < rows ? p.pos0 - kpos0 + rowtab[mg].x : -1;
                 klim[nt][par] = l < -1 ? -1 : (l > P ? P : (int)l);
             }
         const int NKG = P / 16;
@@ -385,9 +394,9 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
             for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             const int mg = mo + m;
             if (lane == 0 && mg < rows) {
-                const int r = mg / G, h = g * G + (mg - r * G);
-                rowoff[m] = h * R + r;
-                float *ml = p.part_ml + (((int64_t)split * p.Hq + h) * R + r) * 2;
+                const int off = g * G * R + rowtab[mg].y;  // (h * R + r) of this row
+                rowoff[m] = off;
+                float *ml = p.part_ml + ((int64_t)split * p.Hq * R + off) * 2;
                 ml[0] = mx;
                 ml[1] = sum;
             }
