@@ -148,12 +148,19 @@ struct kvs_ctx {
         return host_dev + ((int64_t)layer * max_pages + page) * geom.page_bytes;
     }
     cudaStream_t stream(int s) const { return lanes[s]; }
-    // lane streams, then the library's own resident-page stream (id res_sid())
-    int n_streams() const { return 2 * n_lanes + 1; }
+    // lane streams, then the library's own resident-page stream (res_sid()) and
+    // the stream that reads lane 0's ring chunks (ring0_sid()), so that the
+    // caller's attention stream carries only the per-call work (Q prep, the
+    // combine, appends) and never waits behind ring refills
+    int n_streams() const { return 2 * n_lanes + 2; }
     int res_sid() const { return 2 * n_lanes; }
-    cudaStream_t res_stream = nullptr;  // created by kvs_create, lowest priority
+    int ring0_sid() const { return 2 * n_lanes + 1; }
+    int attn_sid_of_lane(int lane) const { return lane == 0 ? ring0_sid() : 2 * lane; }
+    cudaStream_t res_stream = nullptr;    // created by kvs_create, lowest priority
+    cudaStream_t ring0_stream = nullptr;  // created by kvs_create
     ~kvs_ctx() {
         if (res_stream) cudaStreamDestroy(res_stream);
+        if (ring0_stream) cudaStreamDestroy(ring0_stream);
     }
 };
 
@@ -232,7 +239,8 @@ kvs_status fork_lanes(kvs_ctx *c) {
         if (s == KVS_OK) s = join(c, kCopy, 2 * l + 1);
         if (s != KVS_OK) return s;
     }
-    return join(c, kAttn, c->res_sid());
+    kvs_status s = join(c, kAttn, c->res_sid());
+    return s != KVS_OK ? s : join(c, kAttn, c->ring0_sid());
 }
 
 // the other attention streams wait for the primary attention stream (inputs
@@ -242,7 +250,8 @@ kvs_status fork_attn_lanes(kvs_ctx *c) {
         kvs_status s = join(c, kAttn, 2 * l);
         if (s != KVS_OK) return s;
     }
-    return join(c, kAttn, c->res_sid());
+    kvs_status s = join(c, kAttn, c->res_sid());
+    return s != KVS_OK ? s : join(c, kAttn, c->ring0_sid());
 }
 
 // a publish (D2H of a completed tail page) was just enqueued on the copy
@@ -256,11 +265,11 @@ kvs_status mark_publish(kvs_ctx *c) {
 
 // the primary attention stream waits for the other attention streams
 kvs_status join_attn_lanes_into_attn(kvs_ctx *c) {
-    for (int sid = 2; sid < c->n_streams(); sid += 2) {
+    for (int sid = 2; sid <= c->res_sid(); sid += 2) {
         kvs_status s = join(c, sid, kAttn);
         if (s != KVS_OK) return s;
     }
-    return KVS_OK;
+    return join(c, c->ring0_sid(), kAttn);
 }
 
 // the primary attention stream waits for every other stream of every lane
@@ -808,6 +817,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         c->host_dev = static_cast<uint8_t *>(dp);
     }
     c->lanes.push_back(nullptr);  // the resident-page stream
+    c->lanes.push_back(nullptr);  // lane 0's ring-read stream
     if (!plan_only) {
         // resident pages of a layer that also reads ring chunks run beside
         // them at the lowest priority: ring reads gate the refills, resident
@@ -822,7 +832,16 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
             g_create_error = std::string("cudaStreamCreateWithPriority: ") + cudaGetErrorString(e);
             return KVS_ERR_CUDA;
         }
-        c->lanes.back() = c->res_stream;
+        c->lanes[c->res_sid()] = c->res_stream;
+        e = cudaStreamCreateWithFlags(&c->ring0_stream, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            c->ring0_stream = nullptr;
+            if (c->host_registered) cudaHostUnregister(cfg->host);
+            delete c;
+            g_create_error = std::string("cudaStreamCreateWithFlags: ") + cudaGetErrorString(e);
+            return KVS_ERR_CUDA;
+        }
+        c->lanes[c->ring0_sid()] = c->ring0_stream;
     }
     if (create_events(c) != KVS_OK) {
         g_create_error = c->err;
@@ -1401,6 +1420,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
         }
         // ring chunks in order: ready fence, read, consumed fence, refill
+        std::vector<int64_t> last_read(c->n_lanes, -1);  // per lane: last chunk read in this call
         while (!c->queue.empty() && c->queue.front().layer == layer) {
             Chunk &ch = c->queue.front();
             if (!ch.filled) {
@@ -1408,7 +1428,8 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
                 if (s != KVS_OK) return s;
                 if (!ch.filled) return fail(c, KVS_ERR_COVERAGE, "ring chunk could not be scheduled");
             }
-            const int sid = 2 * (int)(ch.id % (uint64_t)c->n_lanes);  // this chunk's attention lane
+            const int lane = (int)(ch.id % (uint64_t)c->n_lanes);
+            const int sid = c->attn_sid_of_lane(lane);  // this chunk's attention stream
             s = op_wait(c, sid, (int)(ch.id % c->ring_n));
             if (s != KVS_OK) return s;
             std::vector<int64_t> pg, sl;
@@ -1425,13 +1446,22 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             c->chunk_reader_sid[ch.id % c->ring_n] = sid;
             s = op_record(c, sid, (int)c->ring_n + (int)(ch.id % c->ring_n));
             if (s != KVS_OK) return s;
+            last_read[lane] = (int64_t)ch.id;
             c->attended = ch.id + 1;
             c->st.ring_chunks++;
             c->queue.pop_front();
             s = pump(c);
             if (s != KVS_OK) return s;
         }
-        s = join_attn_lanes_into_attn(c);
+        // The combine waits for this layer's reads only: each lane's last
+        // consumed event (recorded before any refill went onto that lane) and
+        // the resident-page stream; not for refills queued behind the reads.
+        for (int l = 0; l < c->n_lanes; ++l) {
+            if (last_read[l] < 0) continue;
+            s = op_wait(c, kAttn, (int)c->ring_n + (int)(last_read[l] % c->ring_n));
+            if (s != KVS_OK) return s;
+        }
+        s = join(c, c->res_sid(), kAttn);
         if (s != KVS_OK) return s;
     }
     c->announced.pop_front();
