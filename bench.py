@@ -56,8 +56,9 @@ WORKLOADS = {
         L=8, T=32768, R=1, ring=8, chunk=4, lanes=2, residency=("random", 0.5)),
     "verify163k": dict(
         desc=("span verify: 6 causal rows at positions 163840..163845, 64 layers, 24 q / 4 kv heads, D 256, "
-              "page 256, Q8_0 K / Q4_0 V; 400 resident pages per layer (prefix), the rest via an 8-slot ring"),
-        L=64, T=163840 + 6, R=6, ring=8, chunk=2, lanes=4, residency=("prefix_pages", 400)),
+              "page 256, Q8_0 K / Q4_0 V; 400 resident pages per layer (prefix), the rest via an 8-slot ring "
+              "(1-page chunks on 8 lanes)"),
+        L=64, T=163840 + 6, R=6, ring=8, chunk=1, lanes=8, residency=("prefix_pages", 400)),
     "prefill131k": dict(
         desc=("prefill chunk: 256 fp16 query rows appended at context 131072, causal, 24 q / 4 kv heads, D 256, "
               "page 256, Q8_0 K / Q4_0 V, tcgen05 tensor-core path"),
