@@ -170,7 +170,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, i
     s.rowoff = align_to(red_end > obuf_end ? red_end : obuf_end, 16);  // MR ints: partial row offsets
     s.rowtab = align_to(s.rowoff + MR * 4, 16);  // 64 int2 per CTA: (mg / G, (mg % G) * R + mg / G)
     s.bar = align_to(s.rowtab + 64 * 8, 16);
-    s.total = s.bar + 16 * stages;
+    s.total = s.bar + 32 * stages;  // per stage: K-piece and V-piece barriers
     return s;
 }
 
@@ -181,8 +181,10 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, i
 // Both shapes run the same arithmetic per row tile, for any warp count W.
 // Units are ordered head-major; CTA c takes units [c*U/C, (c+1)*U/C).
 // Page-head sections stream into `stages` shared-memory stages by bulk
-// asynchronous copies: while the warps work on one unit the next one is
-// already on its way.
+// asynchronous copies, in two pieces with a barrier each: the K piece (codes
+// and scales) and the V piece.  A stage's K piece is refilled with a later
+// unit as soon as the scores are done, its V piece once P.V is done, so the
+// copies of the next unit overlap the softmax, P.V and store of this one.
 template <int D, int NT, int W>
 __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -221,18 +223,28 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         const int gi = u / T, g = gi / p.n_items, item = gi - g * p.n_items;
         return p.arena + (int64_t)p.slot[item] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
     };
-    bool pending[2] = {false, false};      // a load into this stage is not consumed yet
-    uint32_t pend_parity[2] = {0u, 0u};    // the phase that load completes
-    for (int s = 0; s < S && u0 + s < u1; ++s) pending[s] = true;
+    // barrier 2s: K piece of stage s, 2s + 1: its V piece
+    const uint32_t kbytes = (uint32_t)p.geom.vq_off, vbytes = (uint32_t)head_bytes - kbytes;
+    auto load_piece = [&](int s, int unit, int v) {
+        const uint32_t off = v ? kbytes : 0u;
+        stage_load(smem_u32(smem + L.stage + s * head_bytes) + off, src_of(unit) + off, v ? vbytes : kbytes,
+                   bar0 + 16 * (2 * s + v));
+    };
+    // bit j of `pending`: a load on barrier j is not consumed yet; bit j of
+    // `pend_parity`: the phase that load completes
+    uint32_t pending = 0u, pend_parity = 0u;
+    for (int s = 0; s < S && u0 + s < u1; ++s) pending |= 3u << (2 * s);
     // rows x heads m (< 64): x = its query row r = m / G, y = h_local * R + r with
     // h_local = m % G; the partial of kv head g sits at row g * G * R + y
     for (int m = threadIdx.x; m < 64; m += NTH) rowtab[m] = make_int2(m / G, (m % G) * R + m / G);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 16 * s));
+        for (int s = 0; s < 2 * S; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 16 * s));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (int s = 0; s < S && u0 + s < u1; ++s)
-            stage_load(smem_u32(smem + L.stage + s * head_bytes), src_of(u0 + s), (uint32_t)head_bytes, bar0 + 16 * s);
+        for (int s = 0; s < S && u0 + s < u1; ++s) {
+            load_piece(s, u0 + s, 0);
+            load_piece(s, u0 + s, 1);
+        }
     }
     __syncthreads();
 
@@ -252,13 +264,9 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 
         // Q fragments of kv head g (built by qprep_kernel): qf[tile][ks][lane]
         const uint4 *qf = p.qf + ((int64_t)g * p.qtiles + tile) * KS * 32;
-        if (!mbar_wait(bar0 + 16 * stage, parity)) ok = false;
+        if (!mbar_wait(bar0 + 16 * (2 * stage), parity)) ok = false;
         if (!__syncthreads_and(ok)) break;
-        pending[stage] = false;
-        // every page section this CTA reads is now in shared memory: a refill
-        // of those slots launched as this grid's programmatic dependent may
-        // start (it begins once every CTA has signalled or exited)
-        if (u == u1 - 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        pending &= ~(1u << (2 * stage));
 
         // Scores: each warp takes KPW 16-key groups at a time as MMA row tiles.
         const long long kpos0 = (long long)page * P;
@@ -352,7 +360,15 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();  // scores written; the K piece is read
+        if (u + S < u1) {
+            pending |= 1u << (2 * stage);
+            pend_parity = (pend_parity & ~(1u << (2 * stage))) | ((parity ^ 1u) << (2 * stage));
+            if (threadIdx.x == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                load_piece(stage, u + S, 0);
+            }
+        }
 
         // Softmax over the page's keys, one row per warp at a time.  Each lane
         // owns 4-key groups (at most two: P <= 256) and rewrites a group's four
@@ -401,7 +417,13 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                 ml[1] = sum;
             }
         }
-        __syncthreads();
+        if (!mbar_wait(bar0 + 16 * (2 * stage + 1), parity)) ok = false;
+        if (!__syncthreads_and(ok)) break;
+        pending &= ~(2u << (2 * stage));
+        // every page section this CTA reads is now in shared memory: a refill
+        // of those slots launched as this grid's programmatic dependent may
+        // start (it begins once every CTA has signalled or exited)
+        if (u == u1 - 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
         // O^T = V^T P'^T over key parts: job j = (dim block j % NB, key part j / NB).
         // A warp owns every part of its block (kInReg) or one job.
@@ -488,12 +510,11 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         }
         __syncthreads();  // every read of this stage (and of sc) is done
         if (u + S < u1) {
-            pending[stage] = true;
-            pend_parity[stage] = parity ^ 1u;
+            pending |= 2u << (2 * stage);
+            pend_parity = (pend_parity & ~(2u << (2 * stage))) | ((parity ^ 1u) << (2 * stage + 1));
             if (threadIdx.x == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                stage_load(smem_u32(smem + L.stage + stage * head_bytes), src_of(u + S), (uint32_t)head_bytes,
-                           bar0 + 16 * stage);
+                load_piece(stage, u + S, 1);
             }
         }
         if (part0 == 0) {
@@ -539,8 +560,8 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         // a wait gave up: before the CTA exits, wait (bounded again) for every
         // stage load still in flight, so no copy lands in reassigned memory
         if (threadIdx.x == 0) {
-            for (int s = 0; s < S; ++s)
-                if (pending[s]) mbar_wait(bar0 + 16 * s, pend_parity[s]);
+            for (int s = 0; s < 2 * S; ++s)
+                if ((pending >> s) & 1u) mbar_wait(bar0 + 16 * s, (pend_parity >> s) & 1u);
             atomicExch(p.status, 1);
         }
         __syncthreads();
