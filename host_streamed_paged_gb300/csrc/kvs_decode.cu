@@ -569,16 +569,17 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 }
 
 // Q fragments for every kv head, once per attend: qf [Hk][NT][KS][32] uint4
-// = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand.
+// = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand.  One CTA per (kv head,
+// row tile): the kernel sits between two layers' reads, so its latency counts.
 template <int D, int NT>
 __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__ DecodeParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");            // q and the previous readers of qf
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // attention may be scheduled
     constexpr int KS = D / 16;
-    const int g = blockIdx.x, G = p.G, rows = G * p.R;
-    uint4 *qf = const_cast<uint4 *>(p.qf) + (int64_t)g * NT * KS * 32;
-    for (int e = threadIdx.x; e < NT * KS * 32; e += kThreads) {
-        const int ln = e & 31, ks = (e >> 5) % KS, nt = e / (KS * 32);
+    const int g = blockIdx.x, nt = blockIdx.y, G = p.G, rows = G * p.R;
+    uint4 *qf = const_cast<uint4 *>(p.qf) + ((int64_t)g * NT + nt) * KS * 32;
+    for (int e = threadIdx.x; e < KS * 32; e += kThreads) {
+        const int ln = e & 31, ks = e >> 5;
         const int m = nt * 8 + (ln >> 2);
         const int d0 = 32 * (ks >> 1) + 8 * (ln & 3) + 4 * (ks & 1);
         float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -627,7 +628,7 @@ template <int D, int NT, int W>
 cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     DecodeParams p = p_in;
     if (p.prep_q) {
-        cudaError_t e = launch_pdl(qprep_kernel<D, NT>, dim3(p.geom.Hk), dim3(kThreads), 0, s, p);
+        cudaError_t e = launch_pdl(qprep_kernel<D, NT>, dim3(p.geom.Hk, NT), dim3(kThreads), 0, s, p);
         if (e != cudaSuccess) return e;
         if (p.n_items == 0) return cudaSuccess;
     }
