@@ -683,24 +683,23 @@ cudaError_t launch_decode_d(const DecodeParams &p, int nt, cudaStream_t s) {
 
 // ------------------------------------------------------------------ combine
 
-// One CTA per (row, q head, 64-dim slice).  The largest split max M comes
-// first; then, block by block of splits, the weights w_s = 2^(m_s - M) go to
-// shared memory and each warp sums w_s * o_s over its splits s = warp,
-// warp + NW, ... with kCombineUnroll partial loads in flight; the warp sums
-// are added in warp order.  A fixed order: the result does not depend on
-// timing.
+// One CTA per (row, q head, 64-dim slice), in one pass over the splits.
+// Warp w takes splits w, w + NW, w + 2 NW, ... in that order, with
+// kCombineUnroll splits' (m, l) pairs and partial rows in flight, and keeps
+// a running max m_w: when a split's max exceeds it, the warp's sums are
+// rescaled by 2^(m_w - m) before the split is added with weight 2^(m_s - m_w).
+// The warps' (m_w, l_w, o_w) are then merged in warp order.  A fixed order:
+// the result does not depend on timing.
 constexpr int kCombineDims = 64;
 constexpr int kCombineThreads = 512;
-constexpr int kCombineBlock = 1024;  // splits per weight block
 constexpr int kCombineUnroll = 8;
 
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const CombineParams p) {
     constexpr int DS = D < kCombineDims ? D : kCombineDims;
     constexpr int VPL = DS / 32;  // dims per lane (2)
     constexpr int NW = kCombineThreads / 32;
-    __shared__ float wmax[NW], wl[NW];
-    __shared__ float wsm[kCombineBlock], lsm[kCombineBlock];
+    __shared__ float wm[NW], wl[NW];
     __shared__ float wo[NW][DS];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next call's Q prep may be scheduled
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
@@ -709,90 +708,63 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
     auto base_of = [&](int s) { return ((int64_t)s * p.Hq + h) * p.R + r; };
 
-    // (m, l) of the first weight block stay in registers for its weights
-    constexpr int kKeep = kCombineBlock / kCombineThreads;
-    float2 keep[kKeep];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < kKeep; ++q) {
-        const int s = threadIdx.x + q * kCombineThreads;
-        keep[q] = s < nsplit ? *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2) : make_float2(0.f, 0.f);
-        if (keep[q].y > 0.f) mx = fmaxf(mx, keep[q].x);
-    }
-    for (int s = threadIdx.x + kCombineBlock; s < nsplit; s += kCombineThreads) {
-        const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(s) * 2);
-        if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) wmax[warp] = mx;
-    __syncthreads();
-    float M = wmax[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) M = fmaxf(M, wmax[w]);
-
-    float o[VPL], Ls = 0.f;
+    float mw = -INFINITY, Lw = 0.f, o[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) o[i] = 0.f;
-    if (M != -INFINITY) {
-        for (int b0 = 0; b0 < nsplit; b0 += kCombineBlock) {
-            const int nb = nsplit - b0 < kCombineBlock ? nsplit - b0 : kCombineBlock;
-            __syncthreads();  // the previous block's weights are consumed
-            if (b0 == 0) {
+    for (int j0 = warp; j0 < nsplit; j0 += NW * kCombineUnroll) {
+        // lane u < kCombineUnroll holds the (m, l) pair of split j0 + u NW
+        float2 mlu = make_float2(0.f, 0.f);
+        if (lane < kCombineUnroll && j0 + lane * NW < nsplit)
+            mlu = *reinterpret_cast<const float2 *>(p.part_ml + base_of(j0 + lane * NW) * 2);
+        float v[kCombineUnroll][VPL];
 #pragma unroll
-                for (int q = 0; q < kKeep; ++q) {
-                    const int j = threadIdx.x + q * kCombineThreads;
-                    if (j >= nb) continue;
-                    const bool live = keep[q].y > 0.f;
-                    wsm[j] = live ? exp2f(keep[q].x - M) : 0.f;
-                    lsm[j] = live ? keep[q].y : 0.f;
-                }
-            } else {
-                for (int j = threadIdx.x; j < nb; j += kCombineThreads) {
-                    const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + base_of(b0 + j) * 2);
-                    const bool live = ml.y > 0.f;
-                    wsm[j] = live ? exp2f(ml.x - M) : 0.f;
-                    lsm[j] = live ? ml.y : 0.f;
-                }
-            }
-            __syncthreads();
-            for (int j0 = warp; j0 < nb; j0 += NW * kCombineUnroll) {
-                float v[kCombineUnroll][VPL];
-#pragma unroll
-                for (int u = 0; u < kCombineUnroll; ++u) {
-                    const int j = j0 + u * NW;
-                    v[u][0] = v[u][1] = 0.f;
-                    if (j < nb && wsm[j] > 0.f) {
-                        const float2 t =
-                            *reinterpret_cast<const float2 *>(p.part_o + base_of(b0 + j) * D + d0 + lane * VPL);
-                        v[u][0] = t.x;
-                        v[u][1] = t.y;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kCombineUnroll; ++u) {
-                    const int j = j0 + u * NW;
-                    if (j < nb && wsm[j] > 0.f) {
-                        o[0] = fmaf(wsm[j], v[u][0], o[0]);
-                        o[1] = fmaf(wsm[j], v[u][1], o[1]);
-                        Ls = fmaf(wsm[j], lsm[j], Ls);
-                    }
-                }
+        for (int u = 0; u < kCombineUnroll; ++u) {
+            const int j = j0 + u * NW;
+            v[u][0] = v[u][1] = 0.f;
+            if (j < nsplit) {
+                const float2 t = *reinterpret_cast<const float2 *>(p.part_o + base_of(j) * D + d0 + lane * VPL);
+                v[u][0] = t.x;
+                v[u][1] = t.y;
             }
         }
+#pragma unroll
+        for (int u = 0; u < kCombineUnroll; ++u) {
+            const float m = __shfl_sync(0xffffffffu, mlu.x, u), l = __shfl_sync(0xffffffffu, mlu.y, u);
+            if (!(l > 0.f)) continue;  // past the end, or a split with no visible key
+            if (m > mw) {
+                const float c = exp2f(mw - m);  // 0 while nothing has been added
+                Lw *= c;
+                o[0] *= c;
+                o[1] *= c;
+                mw = m;
+            }
+            const float w = exp2f(m - mw);
+            o[0] = fmaf(w, v[u][0], o[0]);
+            o[1] = fmaf(w, v[u][1], o[1]);
+            Lw = fmaf(w, l, Lw);
+        }
     }
-    if (lane == 0) wl[warp] = Ls;
+    if (lane == 0) {
+        wm[warp] = mw;
+        wl[warp] = Lw;
+    }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) wo[warp][lane * VPL + i] = o[i];
     __syncthreads();
     if (warp == 0) {
+        float M = -INFINITY;
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w]);
         float Lt = 0.f, ot[VPL];
 #pragma unroll
         for (int i = 0; i < VPL; ++i) ot[i] = 0.f;
-        for (int w = 0; w < NW; ++w) {
-            Lt += wl[w];
+        if (M != -INFINITY) {
+            for (int w = 0; w < NW; ++w) {
+                if (wm[w] == -INFINITY) continue;
+                const float c = exp2f(wm[w] - M);
+                Lt = fmaf(c, wl[w], Lt);
 #pragma unroll
-            for (int i = 0; i < VPL; ++i) ot[i] += wo[w][lane * VPL + i];
+                for (int i = 0; i < VPL; ++i) ot[i] = fmaf(c, wo[w][lane * VPL + i], ot[i]);
+            }
         }
         float *dst = p.out + ((int64_t)r * p.Hq + h) * D + d0 + lane * VPL;
         const float inv = (Lt > 0.f) ? 1.f / Lt : 0.f;
