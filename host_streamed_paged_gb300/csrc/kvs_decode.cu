@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     // bit j of `pending`: a load on barrier j is not consumed yet; bit j of
     // `pend_parity`: the phase that load completes
     uint32_t pending = 0u, pend_parity = 0u;
-    for (int s = 0; s < S && u0 + s < u1; ++s) pending |= 3u << (2 * s);
+    for (int s = 0; s < S && u0 + s < u1; ++s) pending |= 1u << (2 * s);
     // rows x heads m (< 64): x = its query row r = m / G, y = h_local * R + r with
     // h_local = m % G; the partial of kv head g sits at row g * G * R + y
     for (int m = threadIdx.x; m < 64; m += NTH) rowtab[m] = make_int2(m / G, (m % G) * R + m / G);
@@ -241,10 +241,9 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         for (int s = 0; s < 2 * S; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 16 * s));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (int s = 0; s < S && u0 + s < u1; ++s) {
-            load_piece(s, u0 + s, 0);
-            load_piece(s, u0 + s, 1);
-        }
+        // the first units' K pieces only: every CTA starts at once, and the
+        // scores can begin as soon as K is in; their V pieces follow below
+        for (int s = 0; s < S && u0 + s < u1; ++s) load_piece(s, u0 + s, 0);
     }
     __syncthreads();
 
@@ -267,6 +266,11 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         if (!mbar_wait(bar0 + 16 * (2 * stage), parity)) ok = false;
         if (!__syncthreads_and(ok)) break;
         pending &= ~(1u << (2 * stage));
+        if (i == 0) {  // the first units' V pieces, behind their K pieces
+            for (int s = 0; s < S && u0 + s < u1; ++s) pending |= 2u << (2 * s);
+            if (threadIdx.x == 0)
+                for (int s = 0; s < S && u0 + s < u1; ++s) load_piece(s, u0 + s, 1);
+        }
 
         // Scores: each warp takes KPW 16-key groups at a time as MMA row tiles.
         const long long kpos0 = (long long)page * P;
