@@ -79,7 +79,7 @@ GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 # DRAM bytes (read + write) per timed launch of the roofline kernel, from the ncu capture in
 # profiles/ named here; a workload missing from this table reports traffic as null
 TRAFFIC = {
-    "resident131k": (227.27e6, "profiles/decode_kernel_resident131k.md"),
+    "resident131k": (227.17e6, "profiles/decode_kernel_resident131k.md"),
 }
 
 
