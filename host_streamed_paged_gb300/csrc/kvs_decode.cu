@@ -3,9 +3,9 @@
 //
 // One work unit = one (page, kv head).  Every query head of the kv head's
 // group and every query row is served by the same unit, so each K/V byte is
-// read from memory once per step ("Q8_0 K and Q4_0 V are converted in
-// small tiles, not copied into another full FP16 cache", Adaptive KV
-// Streaming for llama.cpp V2, "Keep the stock attention order").
+// read from memory once per step.  The codes are dequantised tile by tile
+// in registers; no f16 copy of the cache is ever made (Adaptive KV Streaming
+// for llama.cpp V2, "Keep the stock attention order").
 //
 // Arithmetic.  Scores and P.V run on the tensor cores (mma.sync m16n8k16,
 // f16 operands, fp32 accumulation):

@@ -3,10 +3,10 @@
 // A prefill ubatch (up to 256 query rows, fp16 Q) attends causally over the
 // paged Q8_0-K / Q4_0-V history.  Here QK^T and PV are dense contractions
 // (1536 query rows per kv head at 6 query heads per kv head), so they run as
-// tcgen05.mma with fp32 accumulators in tensor memory; "each staged KV span is
-// consumed by all query tiles before its ring slot is released" (Adaptive KV
-// Streaming for llama.cpp, "Batch and micro-batch sizes") holds because one
-// launch covers every query tile of a key split.
+// tcgen05.mma with fp32 accumulators in tensor memory.  Every query tile
+// reads a staged span before its ring slot may be reused (Adaptive KV
+// Streaming for llama.cpp, "Batch and micro-batch sizes"): one launch covers
+// every query tile of a key split.
 //
 // CTA = (key split, kv head, 128-row tile of one query head); 64-key blocks
 // flow through a warp-specialised pipeline:

@@ -3,19 +3,18 @@
 // C ABI of include/kvs.h.
 //
 // Design source: "Adaptive KV Streaming for llama.cpp V2" --
-//   "KV data movement and attention": the complete history stays in host
-//     memory; the device holds resident pages plus ONE ring shared by every
-//     layer; the copy stream fills free slots for later layers while the
-//     attention stream computes; a ready fence keeps attention from reading
-//     an incomplete copy and a consumed fence keeps the copy stream from
-//     overwriting a slot still in use; physical budget = resident pages +
-//     ring slots.
+//   "KV data movement and attention": host memory keeps every layer's full
+//     history; on the device there are resident pages and a single ring
+//     that all layers share; refills for upcoming layers run on a copy
+//     stream during the current layer's attention; one event orders a read
+//     after its copy, another orders a refill after the last read of the
+//     slot; the device budget is the resident pages plus the ring slots.
 //   "Keep the stock attention order": one ordered history, resident pages
 //     and ring spans (at most two per wrap), then one final reduction.
 //   "Backend-neutral memory and streaming contracts": the span plan covers
 //     the history without gaps or overlaps.
 // and "Adaptive KV Streaming for llama.cpp", "Adaptive KV streaming":
-//   consumed ring slots are recycled immediately.
+//   a ring slot is reused as soon as its last read has run.
 //
 // Scheduling model.  Nonresident pages are grouped, layer by layer in the
 // order layers are announced, into chunks of up to chunk_pages pages.  Each

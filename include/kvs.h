@@ -3,7 +3,7 @@
  *
  * The complete KV history of every layer lives in host memory (pinned, or
  * registered by kvs_create).  A bounded device arena holds resident pages of
- * chosen layers plus ONE transfer ring shared by all layers; a copy stream
+ * chosen layers plus a single transfer ring that every layer uses; a copy stream
  * refills ring slots from host memory ahead of the attention stream, fenced
  * by a "ready" event (attention waits for the copy) and a "consumed" event
  * (the next copy into a slot waits for its last reader), and every layer
@@ -14,8 +14,8 @@
  * streaming": resident pages plus one shared ring, consumed slots recycled
  * immediately, the full history still attended).
  *
- * Cache types: K is Q8_0 and V is Q4_0 (32-element blocks, fp16 scale; the
- * pages' qualified pair "--cache-type-k q8_0 --cache-type-v q4_0").  Other
+ * Cache types: K uses Q8_0 and V uses Q4_0 (32-element blocks, fp16 scale), the
+ * one K/V pairing the pages qualify for streaming.  Other
  * types are refused (KVS_ERR_UNSUPPORTED), as the pages require a backend to
  * advertise only the K/V pairs it really supports.
  *
@@ -199,8 +199,9 @@ kvs_status kvs_query_sizes(const kvs_config *cfg, uint64_t *page_bytes, uint64_t
 /*
  * kvs_create -- validate cfg and build a context.  The arena is carved into
  * page slots: 2 * n_layers tail slots, then ring_slots ring slots, the rest
- * is the resident pool ("physical KV budget = resident pages across layers +
- * shared ring slots", V2 README, "KV data movement and attention").
+ * is the resident pool (the device KV budget is the resident pages of all
+ * layers plus the ring slots they share: V2 README, "KV data movement and
+ * attention").
  * Refusals: geometry outside the supported set or k/v types other than
  * Q8_0/Q4_0 -> KVS_ERR_UNSUPPORTED; arena or workspace below the minimum ->
  * KVS_ERR_ARENA (the pages refuse a too-small arena at start-up); host
@@ -218,7 +219,8 @@ kvs_status kvs_destroy(kvs_ctx *ctx);
  * (k_dev, v_dev: device fp32 [n_tokens][Hk][D]) into the layer's device tail
  * page(s) at positions T .. T+n_tokens-1 (K -> Q8_0, V -> Q4_0, on
  * attn_stream).  A page that becomes full is published device -> host on the
- * copy stream ("D2H publish changed tail when produced", V2 README); it stays
+ * copy stream as soon as it is written (the V2 README publishes a changed
+ * tail to host when it is produced); it stays
  * readable on the device until the page after next starts, and then moves to
  * the resident pool if the layer's residency mask asks for it and the pool
  * has room, else it is streamed from host like any other nonresident page.
@@ -260,9 +262,9 @@ kvs_status kvs_set_ring_slots(kvs_ctx *ctx, uint32_t n_slots, uint32_t chunk_pag
 /*
  * kvs_prefetch -- announce that `layer` is attended next (after any layer
  * already announced) and enqueue host -> ring copies of its nonresident pages
- * into ring slots whose previous reader has already been enqueued ("the copy
- * stream can fill free slots for later layers while the attention stream
- * computes the current layer", V2 README).  Non-blocking; copies that do not
+ * into ring slots whose previous reader has already been enqueued: copies
+ * for later layers proceed while the current layer is attended (V2 README,
+ * "KV data movement and attention").  Non-blocking; copies that do not
  * fit yet are issued by later kvs_attend calls as slots free up.  Layers must
  * then be attended in announcement order (KVS_ERR_STATE otherwise).
  */

@@ -9,8 +9,8 @@
  *
  * What is modelled, with the passage each part follows:
  *
- *  - "Every attention layer still processes its complete KV history; only
- *    physical residency and transfer scheduling change" (Adaptive KV
+ *  - Each layer attends over all of its history; streaming changes only
+ *    where pages live and when they are copied (Adaptive KV
  *    Streaming for llama.cpp, section "Adaptive KV streaming"; the V2 README,
  *    section "KV data movement and attention").  Streaming therefore does not
  *    enter the mathematics: the oracle is dense softmax attention over the
@@ -20,7 +20,7 @@
  *    written before they attend).  Query head h reads kv head h / (Hq / Hk).
  *
  *  - K is cached as Q8_0 and V as Q4_0 (V2 README, "Results and quick start"
- *    and the server example: --cache-type-k q8_0 --cache-type-v q4_0).  Both
+ *    and its server example's cache-type options).  Both
  *    are 32-element blocks with one fp16 scale.  Q8_0: d = max|x| / 127,
  *    code = round-half-away(x / d) as int8.  Q4_0: m = the element of largest
  *    magnitude (first one on ties) with its sign, d = m / -8,
@@ -31,8 +31,8 @@
  *    is taken; decoding is code * fp16(d) (Q8_0) and (code - 8) * fp16(d)
  *    (Q4_0), evaluated in fp64.
  *
- *  - The page layout (V2 README, "KV data movement and attention": a page
- *    holds 256 token positions and its K/V byte sizes follow the quant
+ *  - The page layout (V2 README, "KV data movement and attention": pages of
+ *    256 tokens each, whose K/V byte sizes follow the quant
  *    types).  The byte order inside a page is this library's own choice and
  *    is spelled out at kvs_oracle_encode_page; the oracle writes it from that
  *    definition only, to pin the bytes the device path stores.
