@@ -54,7 +54,7 @@ typedef struct kvs_ctx kvs_ctx;
 typedef enum {
     KVS_OK = 0,
     KVS_ERR_INVALID = -1,     /* bad argument or call order */
-    KVS_ERR_UNSUPPORTED = -2, /* geometry or type this build does not serve */
+    KVS_ERR_UNSUPPORTED = -2, /* geometry or type the library does not serve */
     KVS_ERR_ARENA = -3,       /* arena or workspace below the minimum */
     KVS_ERR_HOST = -4,        /* host history too small or cannot be registered */
     KVS_ERR_CUDA = -5,        /* a CUDA runtime call failed (message in last_error) */
