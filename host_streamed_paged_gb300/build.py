@@ -11,7 +11,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkvs.so")
-SOURCES = ["kvs_decode.cu", "kvs_prefill.cu", "kvs_copy.cu", "kvs_noalloc.cu", "kvs_runtime.cpp"]
+SOURCES = ["kvs_decode.cu", "kvs_prefill.cu", "kvs_copy.cu", "kvs_noalloc.cu", "kvs_runtime.cpp", "kvs_policy.cpp"]
 HEADERS = [os.path.join(CSRC, "kvs_internal.h"), os.path.join(ROOT, "include", "kvs.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

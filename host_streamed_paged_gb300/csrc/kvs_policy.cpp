@@ -1,0 +1,92 @@
+// Adaptive residency policy: proposes how a fixed budget of page slots is
+// split between resident pages and the shared ring.
+//
+// Design source: Adaptive KV Streaming for llama.cpp V2, "KV data movement
+// and attention" (the split follows readiness misses, ring occupancy and
+// copy-stream time, with hysteresis) and "Logical KV layout, policy, and
+// physical execution" (the policy derives resident/ring sizes from context
+// length and feedback and neither moves bytes nor launches kernels);
+// Adaptive KV Streaming for llama.cpp, "Adaptive KV streaming" (as the
+// context grows, resident space is kept as large as the budget allows and is
+// handed to a larger ring gradually).  The pages name the inputs but no
+// thresholds or step sizes; those come from kvs_policy_config.
+//
+// Pure host code: no context, no CUDA call, no allocation.
+#include <stdint.h>
+
+#include "kvs.h"
+
+namespace {
+
+bool fraction(float x) { return x >= 0.f && x <= 1.f; }  // false for NaN too
+
+uint32_t clamp_u32(uint64_t x, uint32_t lo, uint32_t hi) {
+    return x < lo ? lo : (x > hi ? hi : (uint32_t)x);
+}
+
+}  // namespace
+
+extern "C" kvs_status kvs_policy_step(const kvs_policy_config *cfg, const kvs_policy_state *prev,
+                                      const kvs_policy_observation *obs, kvs_policy_state *next,
+                                      kvs_policy_decision *out) {
+    if (!cfg || !prev || !obs || !next || !out) return KVS_ERR_INVALID;
+    if (cfg->page_tokens == 0 || cfg->n_layers == 0 || cfg->budget_slots == 0 || cfg->step_slots == 0 ||
+        cfg->hold_steps == 0)
+        return KVS_ERR_INVALID;
+    const uint32_t hi_cfg = cfg->max_ring_slots ? cfg->max_ring_slots : cfg->budget_slots;
+    const uint32_t hi = hi_cfg < cfg->budget_slots ? hi_cfg : cfg->budget_slots;
+    const uint32_t lo = cfg->min_ring_slots;
+    if (lo == 0 || lo > hi) return KVS_ERR_INVALID;
+    if (!fraction(cfg->miss_grow) || !fraction(cfg->copy_busy_max) || !fraction(cfg->occupancy_shrink) ||
+        !fraction(obs->ring_occupancy) || !fraction(obs->copy_busy) || obs->ready_misses > obs->streamed_reads)
+        return KVS_ERR_INVALID;
+
+    const uint64_t ppl = (obs->context_tokens + cfg->page_tokens - 1) / cfg->page_tokens;
+    const uint64_t need = ppl * cfg->n_layers;  // pages the whole history occupies
+
+    kvs_policy_state st = *prev;
+    st.steps = prev->steps + 1;
+    uint32_t ring;
+    uint32_t reason;
+    if (need <= (uint64_t)(cfg->budget_slots - lo)) {
+        // everything fits resident next to the smallest ring
+        ring = lo;
+        reason = KVS_POLICY_FITS;
+        st.grow_run = st.shrink_run = 0;
+    } else if (prev->ring_slots == 0) {
+        ring = lo;
+        reason = KVS_POLICY_INIT;
+        st.grow_run = st.shrink_run = 0;
+    } else {
+        const double miss_rate = obs->streamed_reads ? (double)obs->ready_misses / (double)obs->streamed_reads : 0.0;
+        const bool want_grow = miss_rate > cfg->miss_grow && obs->copy_busy < cfg->copy_busy_max;
+        const bool want_shrink = obs->ready_misses == 0 && obs->ring_occupancy < cfg->occupancy_shrink;
+        st.grow_run = want_grow ? prev->grow_run + 1 : 0;
+        st.shrink_run = want_shrink ? prev->shrink_run + 1 : 0;
+        ring = clamp_u32(prev->ring_slots, lo, hi);
+        reason = ring != prev->ring_slots ? KVS_POLICY_CLAMP : KVS_POLICY_HOLD;
+        // a change that a bound leaves without effect keeps its run counting
+        if (st.grow_run >= cfg->hold_steps && ring < hi) {
+            ring = clamp_u32((uint64_t)ring + cfg->step_slots, lo, hi);
+            reason = KVS_POLICY_GROW;
+            st.grow_run = st.shrink_run = 0;
+        } else if (st.shrink_run >= cfg->hold_steps && ring > lo) {
+            ring = clamp_u32(ring > cfg->step_slots ? ring - cfg->step_slots : 0, lo, hi);
+            reason = KVS_POLICY_SHRINK;
+            st.grow_run = st.shrink_run = 0;
+        }
+    }
+    st.ring_slots = ring;
+
+    kvs_policy_decision d;
+    d.ring_slots = ring;
+    d.resident_slots = cfg->budget_slots - ring;
+    const uint64_t per_layer = d.resident_slots / cfg->n_layers;
+    d.resident_pages_per_layer = ppl < per_layer ? ppl : per_layer;
+    d.pages_per_layer = ppl;
+    d.reason = reason;
+    d.changed = ring != prev->ring_slots;
+    *next = st;
+    *out = d;
+    return KVS_OK;
+}

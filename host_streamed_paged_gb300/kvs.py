@@ -85,6 +85,31 @@ class kvs_trace_op(ctypes.Structure):
                 ("c", ctypes.c_int64), ("d", ctypes.c_int64)]
 
 
+class kvs_policy_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint32) for n in (
+        "page_tokens", "n_layers", "budget_slots", "min_ring_slots", "max_ring_slots", "step_slots",
+        "hold_steps")] + [(n, ctypes.c_float) for n in ("miss_grow", "copy_busy_max", "occupancy_shrink")]
+
+
+class kvs_policy_state(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint32) for n in ("ring_slots", "grow_run", "shrink_run", "steps")]
+
+
+class kvs_policy_observation(ctypes.Structure):
+    _fields_ = [("context_tokens", ctypes.c_uint64), ("streamed_reads", ctypes.c_uint64),
+                ("ready_misses", ctypes.c_uint64), ("ring_occupancy", ctypes.c_float),
+                ("copy_busy", ctypes.c_float)]
+
+
+class kvs_policy_decision(ctypes.Structure):
+    _fields_ = [("ring_slots", ctypes.c_uint32), ("resident_slots", ctypes.c_uint32),
+                ("resident_pages_per_layer", ctypes.c_uint64), ("pages_per_layer", ctypes.c_uint64),
+                ("reason", ctypes.c_uint32), ("changed", ctypes.c_int32)]
+
+
+KVS_POLICY_INIT, KVS_POLICY_FITS, KVS_POLICY_HOLD, KVS_POLICY_GROW, KVS_POLICY_SHRINK, KVS_POLICY_CLAMP = range(1, 7)
+
+
 # every symbol include/kvs.h declares, with its ctypes signature
 _P, _U32, _U64, _I32, _I64, _F32 = (ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64,
                                     ctypes.c_int32, ctypes.c_int64, ctypes.c_float)
@@ -117,6 +142,7 @@ SIGNATURES = {
     "kvs_graph_destroy": ([_P], _I32),
     "kvs_attend_pages_noalloc": ([_P, _U64, _P, _U64, _U32, _U32, _U32, _P, _I32, _U32, _U32, _U64, _F32,
                                   _P, _P, _P], _I32),
+    "kvs_policy_step": ([_P, _P, _P, _P, _P], _I32),
 }
 KVS_TIME_RESIDENT = 1
 KVS_TIME_RING = 2
@@ -209,6 +235,17 @@ def kvs_set_residency(ctx, layer, mask) -> int:
 
 def kvs_set_ring_slots(ctx, n_slots, chunk_pages=0) -> int:
     return _check(ctx, load().kvs_set_ring_slots(ctx, n_slots, chunk_pages))
+
+
+def kvs_policy_step(config: kvs_policy_config, previous: kvs_policy_state,
+                    observation: kvs_policy_observation):
+    """One residency-policy decision: returns (next state, decision).  Pure host call."""
+    nxt, dec = kvs_policy_state(), kvs_policy_decision()
+    st = load().kvs_policy_step(ctypes.byref(config), ctypes.byref(previous), ctypes.byref(observation),
+                                ctypes.byref(nxt), ctypes.byref(dec))
+    if st != KVS_OK:
+        raise KVSError(st, "kvs_policy_step: invalid config, state or observation")
+    return nxt, dec
 
 
 def kvs_prefetch(ctx, layer) -> int:

@@ -260,6 +260,88 @@ kvs_status kvs_set_residency(kvs_ctx *ctx, uint32_t layer, const uint8_t *mask,
 kvs_status kvs_set_ring_slots(kvs_ctx *ctx, uint32_t n_slots, uint32_t chunk_pages);
 
 /*
+ * Adaptive residency policy (Adaptive KV Streaming for llama.cpp V2, "KV data
+ * movement and attention" and "Logical KV layout, policy, and physical
+ * execution"; Adaptive KV Streaming for llama.cpp, "Adaptive KV streaming").
+ * The pages' policy proposes the resident/ring split of a fixed slot budget
+ * from the active context length and from feedback: readiness misses, ring
+ * occupancy and copy-stream time, with hysteresis.  It moves no bytes and
+ * launches nothing; the caller applies a decision with kvs_set_ring_slots
+ * and kvs_set_residency.  The pages give no thresholds; these are the
+ * caller's, in kvs_policy_config.
+ */
+typedef struct {
+    uint32_t page_tokens;     /* tokens per page */
+    uint32_t n_layers;        /* attended layers sharing the budget */
+    uint32_t budget_slots;    /* page slots shared by resident pages and the ring */
+    uint32_t min_ring_slots;  /* ring lower bound (>= 1) */
+    uint32_t max_ring_slots;  /* ring upper bound (0: budget_slots) */
+    uint32_t step_slots;      /* slots moved between pool and ring per change (>= 1) */
+    uint32_t hold_steps;      /* consecutive agreeing observations before a change (>= 1) */
+    float miss_grow;          /* grow when ready_misses / streamed_reads exceeds this ... */
+    float copy_busy_max;      /* ... and the copy stream was busy less than this fraction */
+    float occupancy_shrink;   /* shrink when no read missed and the ring held prefetched
+                                 pages for less than this fraction of its slots */
+} kvs_policy_config;
+
+typedef struct {              /* zero-initialise before the first step */
+    uint32_t ring_slots;      /* the split in force (0: none yet) */
+    uint32_t grow_run;        /* consecutive observations asking for a larger ring */
+    uint32_t shrink_run;      /* consecutive observations asking for a smaller ring */
+    uint32_t steps;           /* observations taken */
+} kvs_policy_state;
+
+typedef struct {              /* one observation interval, e.g. one decode step */
+    uint64_t context_tokens;  /* active history length per layer */
+    uint64_t streamed_reads;  /* ring chunk reads in the interval */
+    uint64_t ready_misses;    /* of those, reads whose copy had not finished when issued */
+    float ring_occupancy;     /* mean fraction of ring slots holding a page not yet read */
+    float copy_busy;          /* fraction of the interval the copy stream was busy */
+} kvs_policy_observation;
+
+enum {
+    KVS_POLICY_INIT = 1,      /* first decision: smallest ring */
+    KVS_POLICY_FITS = 2,      /* the whole history fits resident: smallest ring */
+    KVS_POLICY_HOLD = 3,      /* no change */
+    KVS_POLICY_GROW = 4,      /* reads waited on copies while the link had room */
+    KVS_POLICY_SHRINK = 5,    /* the ring sat mostly empty and no read waited */
+    KVS_POLICY_CLAMP = 6      /* the split in force was outside the bounds */
+};
+
+typedef struct {
+    uint32_t ring_slots;               /* proposed ring size */
+    uint32_t resident_slots;           /* budget_slots - ring_slots */
+    uint64_t resident_pages_per_layer; /* min(pages per layer, resident_slots / n_layers) */
+    uint64_t pages_per_layer;          /* ceil(context_tokens / page_tokens) */
+    uint32_t reason;                   /* KVS_POLICY_* */
+    int32_t changed;                   /* ring_slots differs from the previous split */
+} kvs_policy_decision;
+
+/*
+ * kvs_policy_step -- one policy decision.  Pure host function (no context,
+ * no CUDA): reads config, previous state and observation; writes the next
+ * state and the decision.  Rules, in order:
+ *  1. The whole history (pages per layer x n_layers) fits in budget_slots
+ *     minus the smallest ring: smallest ring (FITS); resident space is kept
+ *     as large as the budget allows.
+ *  2. No split yet: smallest ring (INIT).
+ *  3. Otherwise an observation asks to grow when the miss rate exceeds
+ *     miss_grow while copy_busy < copy_busy_max (a deeper prefetch helps only
+ *     while the link has room), and to shrink when no read missed and
+ *     ring_occupancy < occupancy_shrink.  A change of step_slots is made
+ *     after hold_steps consecutive observations agree; any other observation
+ *     restarts the count (hysteresis), and a change restarts both counts.
+ *  4. The result is clamped to [min_ring_slots, max ring], where max ring =
+ *     min(max_ring_slots or budget_slots, budget_slots).
+ * KVS_ERR_INVALID (nothing written) for null pointers, page_tokens,
+ * n_layers, budget_slots, step_slots or hold_steps of 0, min_ring_slots of 0
+ * or above the max ring, or fractions outside [0, 1].
+ */
+kvs_status kvs_policy_step(const kvs_policy_config *config, const kvs_policy_state *previous,
+                           const kvs_policy_observation *observation, kvs_policy_state *next,
+                           kvs_policy_decision *decision);
+
+/*
  * kvs_prefetch -- announce that `layer` is attended next (after any layer
  * already announced) and enqueue host -> ring copies of its nonresident pages
  * into ring slots whose previous reader has already been enqueued: copies
