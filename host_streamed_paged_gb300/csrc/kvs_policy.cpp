@@ -2,10 +2,11 @@
 // split between resident pages and the shared ring.
 //
 // Design source: Adaptive KV Streaming for llama.cpp V2, "KV data movement
-// and attention" (the split follows readiness misses, ring occupancy and
-// copy-stream time, with hysteresis) and "Logical KV layout, policy, and
-// physical execution" (the policy derives resident/ring sizes from context
-// length and feedback and neither moves bytes nor launches kernels);
+// and attention" (the split reacts to reads that waited on copies, to how
+// full the ring runs and to how busy the copy stream is, and only after
+// consistent evidence) and "Logical KV layout, policy, and physical
+// execution" (a proposal computed from the context length and that
+// feedback; applying it is a separate step that moves the bytes);
 // Adaptive KV Streaming for llama.cpp, "Adaptive KV streaming" (as the
 // context grows, resident space is kept as large as the budget allows and is
 // handed to a larger ring gradually).  The pages name the inputs but no

@@ -27,9 +27,13 @@
  *    (PR "port adaptive KV streaming", review comments).
  *  - The library allocates no device or host memory: the caller owns the
  *    arena, the workspace, the host history, Q, out and lse, and keeps them
- *    alive until kvs_destroy.  It creates CUDA events only.
- *  - All device work is ordered on the caller's two streams (attn_stream,
- *    copy_stream).  Calls return once work is enqueued; results are valid
+ *    alive until kvs_destroy.  It creates CUDA events and two streams of its
+ *    own: one for reads of resident pages (lowest priority) and one for lane
+ *    0's ring reads.
+ *  - All device work is ordered with respect to the caller's streams
+ *    (attn_stream, copy_stream and the lanes' streams): the library's own
+ *    streams fork from them by events and join back into attn_stream before
+ *    the combine.  Calls return once work is enqueued; results are valid
  *    after the attention stream reaches that point (kvs_sync, or any later
  *    work on attn_stream).
  *  - A context serves one sequence and is not thread-safe.
@@ -264,8 +268,9 @@ kvs_status kvs_set_ring_slots(kvs_ctx *ctx, uint32_t n_slots, uint32_t chunk_pag
  * movement and attention" and "Logical KV layout, policy, and physical
  * execution"; Adaptive KV Streaming for llama.cpp, "Adaptive KV streaming").
  * The pages' policy proposes the resident/ring split of a fixed slot budget
- * from the active context length and from feedback: readiness misses, ring
- * occupancy and copy-stream time, with hysteresis.  It moves no bytes and
+ * from the active context length and from feedback (how many reads waited
+ * on a copy, how full the ring ran, how busy the copy stream was), and
+ * changes it only after consistent evidence (hysteresis).  It moves no bytes and
  * launches nothing; the caller applies a decision with kvs_set_ring_slots
  * and kvs_set_residency.  The pages give no thresholds; these are the
  * caller's, in kvs_policy_config.

@@ -3,8 +3,9 @@
 The pages (Adaptive KV Streaming for llama.cpp V2, "KV data movement and attention" and "Logical
 KV layout, policy, and physical execution"; Adaptive KV Streaming for llama.cpp, "Adaptive KV
 streaming") fix what the policy reads and what it may do: it proposes a resident/ring split of a
-fixed budget from the context length, readiness misses, ring occupancy and copy-stream time, with
-hysteresis, keeping resident space as large as the budget allows.  They give no thresholds, so the
+fixed budget from the context length and from feedback (reads that waited on copies, ring fill,
+copy-stream load), changes it only on consistent evidence, and keeps resident space as large as
+the budget allows.  They give no thresholds, so the
 tests check the rules the C header states, not particular numbers.
 """
 import numpy as np
