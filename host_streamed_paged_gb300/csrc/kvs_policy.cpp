@@ -42,15 +42,16 @@ extern "C" kvs_status kvs_policy_step(const kvs_policy_config *cfg, const kvs_po
         !fraction(obs->ring_occupancy) || !fraction(obs->copy_busy) || obs->ready_misses > obs->streamed_reads)
         return KVS_ERR_INVALID;
 
-    const uint64_t ppl = (obs->context_tokens + cfg->page_tokens - 1) / cfg->page_tokens;
-    const uint64_t need = ppl * cfg->n_layers;  // pages the whole history occupies
+    const uint64_t ppl = obs->context_tokens / cfg->page_tokens + (obs->context_tokens % cfg->page_tokens != 0);
+    // the whole history (ppl pages in each layer) fits next to the smallest
+    // ring: ppl * n_layers <= budget - lo, written without the product
+    const bool fits = ppl <= (uint64_t)(cfg->budget_slots - lo) / cfg->n_layers;
 
     kvs_policy_state st = *prev;
     st.steps = prev->steps + 1;
     uint32_t ring;
     uint32_t reason;
-    if (need <= (uint64_t)(cfg->budget_slots - lo)) {
-        // everything fits resident next to the smallest ring
+    if (fits) {
         ring = lo;
         reason = KVS_POLICY_FITS;
         st.grow_run = st.shrink_run = 0;

@@ -192,3 +192,8 @@ def test_random_feedback_keeps_every_invariant():
                 assert 0 < abs(d.ring_slots - prev) <= c.step_slots
             if d.reason == kvs.KVS_POLICY_HOLD:
                 assert d.ring_slots == prev
+
+
+def test_huge_context_does_not_overflow():
+    _, d = kvs.kvs_policy_step(cfg(), state(ring=8), obs(ctx=2**64 - 1))
+    assert d.pages_per_layer == (2**64 - 1) // P + 1 and d.reason == kvs.KVS_POLICY_HOLD
