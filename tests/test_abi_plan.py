@@ -123,8 +123,9 @@ class HB:
         return a is not b and a["vc"][s] <= b["vc"][s]
 
 
-def check_trace(st, n_q_head):
-    """Validate fences and coverage of every READ in a plan-only trace."""
+def check_trace(st, n_q_head, fixed_ring=True):
+    """Validate fences and coverage of every READ in a plan-only trace.  With fixed_ring, the
+    trace must not span a ring resize: reads from the final ring's slots must come from fills."""
     hb = HB(st.trace())
     ops = hb.ops
     first_ring, n_ring = st.ring_info()
@@ -152,7 +153,7 @@ def check_trace(st, n_q_head):
                 continue  # appending rows to the same page (same stream, ordered)
             assert HB.before(wj, ops[src]) or HB.before(o, wj), (
                 f"slot {slot} overwritten (op {j}) between its fill (op {src}) and read (op {i})")
-        if first_ring <= slot < first_ring + n_ring:
+        if fixed_ring and first_ring <= slot < first_ring + n_ring:
             assert ops[src]["op"] == kvs.KVS_OP_FILL
     # every ring fill of a published page is ordered after that publish
     pubs = {}

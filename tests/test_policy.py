@@ -197,3 +197,54 @@ def test_random_feedback_keeps_every_invariant():
 def test_huge_context_does_not_overflow():
     _, d = kvs.kvs_policy_step(cfg(), state(ring=8), obs(ctx=2**64 - 1))
     assert d.pages_per_layer == (2**64 - 1) // P + 1 and d.reason == kvs.KVS_POLICY_HOLD
+
+
+def test_policy_drives_a_plan_only_context():
+    """Closed loop on the host scheduler: as the context grows, each decision is applied with
+    kvs_set_residency / kvs_set_ring_slots; every read stays fenced and every attend covers its
+    whole history."""
+    from test_abi_plan import _plan_stream, _reads_of_attend, check_trace
+
+    Pg, Ln, Hk, budget = 64, 2, 1, 40
+    st = _plan_stream(Ln, Hk, Pg, Pg * 80, 2, 1, 2 * Ln + budget)
+    c = cfg(page_tokens=Pg, n_layers=Ln, budget_slots=budget, min_ring_slots=2, max_ring_slots=16,
+            step_slots=2, hold_steps=2)
+    s, T, rings = state(), 0, []
+    for l in range(Ln):
+        kvs.kvs_append(st.ctx, l, None, None, 10 * Pg)
+    T = 10 * Pg
+    for step in range(50):
+        for l in range(Ln):
+            kvs.kvs_append(st.ctx, l, None, None, Pg)
+        T += Pg
+        ring_now = st.stats()["ring_slots"]
+        ppl = -(-T // Pg)
+        streamed = max(0, ppl - (budget - ring_now) // Ln)
+        miss = 5 if streamed > 4 * ring_now else 0
+        s, d = kvs.kvs_policy_step(c, s, obs(ctx=T, reads=20, misses=miss, occ=0.9 if miss else 0.3,
+                                             busy=0.5))
+        rings.append(d.ring_slots)
+        n_mask = ppl - 2  # the two tail pages are device-readable without a pool slot
+        mask = np.zeros(n_mask, np.uint8)
+        mask[:min(d.resident_pages_per_layer, n_mask)] = 1
+        if d.ring_slots > ring_now:  # shrink residency first, then hand slots to the ring
+            for l in range(Ln):
+                st.set_residency(l, mask)
+            st.set_ring_slots(d.ring_slots)
+        else:
+            if d.ring_slots < ring_now:
+                st.set_ring_slots(d.ring_slots)
+            for l in range(Ln):
+                st.set_residency(l, mask)
+        n0 = len(st.trace())
+        st.prefetch(0)
+        for l in range(Ln):
+            if l + 1 < Ln:
+                st.prefetch(l + 1)
+            st.attend_plan(l, 1, 6 * Hk, T - 1)
+        new = st.trace()[n0:]
+        for l in range(Ln):
+            assert sorted(_reads_of_attend(new, l)) == [(p, 0) for p in range(ppl)]
+    check_trace(st, 6 * Hk, fixed_ring=False)  # the ring boundary moves during the trace
+    assert rings[0] == 2 and max(rings) > 2 and st.stats()["ring_slots"] == rings[-1]
+    st.close()
