@@ -270,6 +270,17 @@ def test_prefetch_order_enforced_and_state_errors():
     with pytest.raises(kvs.KVSError) as e:
         st.attend_plan(0, 1, 7, 0)  # more query heads than max_q_head
     assert e.value.status == kvs.KVS_ERR_INVALID
+    with pytest.raises(kvs.KVSError) as e:
+        st.attend_plan(0, 0, 6, 0)  # empty span
+    assert e.value.status == kvs.KVS_ERR_INVALID
+    with pytest.raises(kvs.KVSError) as e:
+        st.attend_plan(3, 1, 6, 0)  # layer out of range
+    assert e.value.status == kvs.KVS_ERR_INVALID
+    n_ops = len(st.trace())
+    for bad in ((0, 0, 6, 0), (3, 1, 6, 0), (0, 2, 6, 64 * 8 - 1)):
+        with pytest.raises(kvs.KVSError):
+            st.attend_plan(*bad)
+    assert len(st.trace()) == n_ops  # a refused call enqueues nothing
     check_trace(st, 6)
     st.close()
 
