@@ -1738,7 +1738,7 @@ kvs_status kvs_graph_destroy(kvs_ctx *c) {
 kvs_status kvs_debug_inject(kvs_ctx *c, uint32_t fault, uint64_t nth) {
     if (!c) return KVS_ERR_INVALID;
     if (fault > KVS_FAULT_SYNC_STALL) return fail(c, KVS_ERR_INVALID, "unknown fault kind");
-    c->fault = nth ? fault : KVS_FAULT_NONE;
+    c->fault = nth ? fault : (uint32_t)KVS_FAULT_NONE;
     c->fault_nth = nth;
     c->fault_count = 0;
     return KVS_OK;
