@@ -76,10 +76,14 @@ WORKLOADS = {
 }
 GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 
-# DRAM bytes (read + write) per timed launch of the roofline kernel, from the ncu capture in
-# profiles/ named here; a workload missing from this table reports traffic as null
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the roofline kernel,
+# from one ncu capture of that launch on a GB300.  resident131k: 218.21 MB read + 8.97 MB written,
+# captured with
+#   ncu --set full --clock-control none -k regex:decode_kernel -s 4 -c 1 -o <report> \
+#       python bench.py --workload resident131k --layers 1 --steps 1 --warmup 3 --no-cpu
+# A workload missing here, or a kernel changed since its capture, reports traffic as null.
 TRAFFIC = {
-    "resident131k": (227.17e6, "profiles/decode_kernel_resident131k.md"),
+    "resident131k": (227.17e6, "ncu capture of one decode_kernel launch (resident131k, 1 layer)"),
 }
 
 
@@ -490,7 +494,10 @@ def run_ours(args, wl):
             "cpu_baseline": cpu,
             "e2e": {"value": replicas.aggregate_rows_per_s(R, e2e_ms, world), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d_in,
-                    "d2h_bytes_per_step": d2h_out},
+                    "d2h_bytes_per_step": d2h_out,
+                    "how": ("every step: three pinned host -> device copies (all layers' Q, new K and new V "
+                            "rows), one replay of the captured step graph (kvs_graph_launch), one device -> "
+                            "pinned host copy of all layers' outputs, on the attention stream")},
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clk,
             "eager_ms_per_step": eager_ms,

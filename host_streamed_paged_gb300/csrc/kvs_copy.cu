@@ -2,6 +2,10 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "kvs_internal.h"
 
 namespace kvs {
@@ -163,6 +167,36 @@ cudaError_t launch_fill(const FillParams &p, cudaStream_t s, bool pdl) {
     cudaError_t e = cudaLaunchKernelEx(&cfg, fill_kernel, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+namespace {
+std::mutex g_dev_mutex;
+std::map<int, int> g_dev_sms;                        // device -> SM count
+std::map<std::pair<const void *, int>, int> g_smem;  // (kernel, device) -> dynamic smem limit set
+}  // namespace
+
+int current_device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    auto it = g_dev_sms.find(dev);
+    if (it != g_dev_sms.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_dev_sms[dev] = n;
+    return n;
+}
+
+cudaError_t ensure_smem_limit(const void *kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    int &have = g_smem[std::make_pair(kernel, dev)];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
 }
 
 }  // namespace kvs

@@ -112,9 +112,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)_
 
 constexpr uint32_t kSpinLimit = 1u << 26;
 
-// bounded wait for phase `parity` of an mbarrier; false on timeout
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// bounded wait for phase `parity` of an mbarrier; false after `limit` polls
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     __syncthreads();
 
     bool ok = true;
+    const uint32_t limit = p.give_up_waits ? 0u : kSpinLimit;
     // unit u = (g * n_items + item) * T + tile, advanced incrementally
     int tile = u0 % T, item = (u0 / T) % p.n_items, g = u0 / T / p.n_items;
     for (int u = u0, i = 0; u < u1; ++u, ++i) {
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 
         // Q fragments of kv head g (built by qprep_kernel): qf[tile][ks][lane]
         const uint4 *qf = p.qf + ((int64_t)g * p.qtiles + tile) * KS * 32;
-        if (!mbar_wait(bar0 + 16 * (2 * stage), parity)) ok = false;
+        if (!mbar_wait(bar0 + 16 * (2 * stage), parity, limit)) ok = false;
         if (!__syncthreads_and(ok)) break;
         pending &= ~(1u << (2 * stage));
         if (i == 0) {  // the first units' V pieces, behind their K pieces
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                 ml[1] = sum;
             }
         }
-        if (!mbar_wait(bar0 + 16 * (2 * stage + 1), parity)) ok = false;
+        if (!mbar_wait(bar0 + 16 * (2 * stage + 1), parity, limit)) ok = false;
         if (!__syncthreads_and(ok)) break;
         pending &= ~(2u << (2 * stage));
         // every page section this CTA reads is now in shared memory: a refill
@@ -607,8 +608,6 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
     }
 }
 
-int g_num_sms = 0;
-
 // Launch as a programmatic dependent of the previous kernel on `s`: the grid
 // may be scheduled once that kernel signals (griddepcontrol.launch_dependents)
 // and waits in griddepcontrol.wait for its completion before touching memory.
@@ -641,28 +640,20 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     // (the other CTA's copy overlaps this one's compute); otherwise one CTA
     // per SM with two stages
     int occ = (NT == 1 && W == 8) ? 2 : 1;
-    if (!g_num_sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (g_num_sms <= 0) g_num_sms = 1;
-    }
+    const int n_sms = current_device_sms();
     DecodeSmem L = decode_smem(D, NT, W, p.geom.P, occ == 2 ? 1 : 2);
     if (occ == 2 && 2 * (L.total + 1024) > 233472) occ = 1, L = decode_smem(D, NT, W, p.geom.P, 2);
     if (L.total > maxsm) L = decode_smem(D, NT, W, p.geom.P, 1);
     if (L.total > maxsm) return cudaErrorInvalidValue;
     p.stages = L.stages;
-    static int configured = 0;
-    if (configured < L.total) {
-        cudaError_t e =
-            cudaFuncSetAttribute(decode_kernel<D, NT, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+    {
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(decode_kernel<D, NT, W>), L.total);
         if (e != cudaSuccess) return e;
-        configured = L.total;
     }
     const int U = p.n_items * p.geom.Hk * (p.tile_mode ? p.run_tiles : 1);
-    int max_ctas = occ * g_num_sms;
+    int max_ctas = occ * n_sms;
     if (p.reserve_sms > 0) {  // leave reserve_sms SMs' worth of CTA slots free, at most a third
-        const int keep = g_num_sms - (p.reserve_sms < g_num_sms / 3 ? p.reserve_sms : g_num_sms / 3);
+        const int keep = n_sms - (p.reserve_sms < n_sms / 3 ? p.reserve_sms : n_sms / 3);
         max_ctas = occ * keep;
     }
     const int per_cta = (U + max_ctas - 1) / max_ctas;
@@ -709,6 +700,17 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const Combi
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
     const int d0 = blockIdx.y * DS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (p.status && *reinterpret_cast<const volatile int *>(p.status) != 0) {
+        // a bounded wait in an attention kernel gave up, so some partials were
+        // never written: make the whole output visibly invalid
+        if (warp == 0) {
+            float *dst = p.out + ((int64_t)r * p.Hq + h) * D + d0 + lane * VPL;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) dst[i] = __int_as_float(0x7fc00000);
+            if (p.lse && lane == 0 && blockIdx.y == 0) p.lse[(int64_t)r * p.Hq + h] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
     const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
     auto base_of = [&](int s) { return ((int64_t)s * p.Hq + h) * p.R + r; };
 

@@ -9,7 +9,7 @@
 
 namespace kvs {
 
-// Byte layout of one page (see kvs_query_sizes in include/kvs.h).  Inside a
+// Byte layout of one page (kvs_query_sizes in include/kvs.h states it).  Inside a
 // head section, K codes sit in 16-token groups of one 32-byte line per
 // (32-dim block, token) and V nibbles in 32-token chunks of one 32-byte line
 // per (block, byte row); every tensor-core fragment is then one conflict-free
@@ -27,8 +27,8 @@ struct PageGeom {
     int D;               // head dim
     int64_t head_bytes;  // P*D*13/8: one kv head's section
     int64_t page_bytes;  // Hk*head_bytes
-    int64_t ks_off;      // K scales  fp16 [P][D/32]
-    int64_t vq_off;      // V nibbles u8  [D/2][P]
+    int64_t ks_off;      // K scales  fp16 [P][D/32]   (K codes at 0, in kq_byte order)
+    int64_t vq_off;      // V nibbles u8, P*D/2 bytes in vq_byte order (32-token chunks)
     int64_t vs_off;      // V scales  fp16 [D/32][P]
 };
 
@@ -68,6 +68,8 @@ struct DecodeParams {
     int reserve_sms;       // leave this many SMs' worth of CTA slots free of this launch (at
                            // most a third of the GPU) for concurrent ring-chunk launches
     int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run
+    int give_up_waits;     // test hook: every pipeline wait gives up at once, as if its copy
+                           // never landed (the drain of copies in flight keeps its bound)
     int n_items;
     uint32_t page[kMaxItems];
     uint32_t slot[kMaxItems];
@@ -112,6 +114,7 @@ int prefill_smem_bytes();
 struct CombineParams {
     const float *part_o;
     const float *part_ml;
+    const int *status;  // nullable: when *status != 0 (a device wait gave up), every output is NaN
     float *out;   // [R][Hq][D]
     float *lse;   // [R][Hq] or null
     int R, Hq, D, P;
@@ -148,6 +151,12 @@ struct FillParams {
 // pdl: programmatic dependent launch (may start once the previous kernel on
 // `s` has signalled its dependents; see decode_kernel)
 cudaError_t launch_fill(const FillParams &p, cudaStream_t s, bool pdl = false);
+
+// Per device and thread-safe: the SM count of the current device, and a raise
+// of a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes` (made once per kernel and device).
+int current_device_sms();
+cudaError_t ensure_smem_limit(const void *kernel, int bytes);
 
 // Message returned by kvs_last_error(NULL) on this thread.
 void set_thread_error(const std::string &msg);

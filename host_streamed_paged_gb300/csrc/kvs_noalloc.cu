@@ -12,10 +12,13 @@
 // The array is a fixed kNoallocScratchBytes (32 MiB) on every GPU that loads
 // this library, held until the process exits.  Every call on a device shares
 // it and it keeps the previous call's contents.  Its first 256 bytes hold the
-// kernels' timeout flag, which starts at zero (a static device array is
-// zero-initialised) and is only ever set by a device wait that gave up; then
-// come the query fragments and the split partials, which need no clearing
-// because each call writes them before it reads them.  Calls whose work
+// kernels' timeout flag, which a bounded device wait sets when it gives up;
+// each call clears it on its stream (cudaMemsetAsync, which allocates
+// nothing) before its first kernel, and the combine kernel reads it: if any
+// wait of this call gave up, some partials were never written, and every
+// element of out (and lse) becomes NaN instead of a value built from an
+// earlier call's partials.  Then come the query fragments and the split
+// partials, which each call writes before it reads them.  Calls whose work
 // overlaps on the GPU (two streams, or two host threads) race on the array:
 // order them on one stream.
 #include <cuda_runtime.h>
@@ -97,32 +100,42 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
         kvs::set_thread_error("null pages, page table, q or out");
         return KVS_ERR_INVALID;
     }
+    if (pos0 > (uint64_t)INT64_MAX - n_rows) {  // the last row's position must not wrap
+        kvs::set_thread_error("pos0 + n_rows beyond the position range");
+        return KVS_ERR_INVALID;
+    }
     const uint64_t n_split = (pos0 + n_rows - 1) / P + 1;  // pages the rows can see
     if (n_split > n_pages) {
         kvs::set_thread_error("rows reach beyond the pages given");
         return KVS_ERR_CAPACITY;
     }
     const kvs::PageGeom geom = kvs::make_geom((int)P, (int)Hk, (int)D);
+    const uint64_t per_split = (uint64_t)n_q_head * n_rows;
+    const uint64_t qfrag = (uint64_t)kvs::qfrag_bytes((int)Hk, (int)D);
+    const uint64_t split_bytes = per_split * (D + 2) * sizeof(float);  // one page's partials
+    if (n_split > (kNoallocScratchBytes - kStatusBytes - qfrag) / split_bytes) {
+        kvs::set_thread_error("needs " + std::to_string(n_split) + " pages x " + std::to_string(split_bytes) +
+                              " bytes of split partials; the fixed scratch holds " +
+                              std::to_string(kNoallocScratchBytes) + " (use kvs_attend with a workspace instead)");
+        return KVS_ERR_CAPACITY;
+    }
     for (uint64_t i = 0; i < n_split; ++i) {
         if (((uint64_t)page_slots[i] + 1) * (uint64_t)geom.page_bytes > pages_bytes) {
             kvs::set_thread_error("a page slot lies outside pages_bytes");
             return KVS_ERR_INVALID;
         }
     }
-    const uint64_t per_split = (uint64_t)n_q_head * n_rows;
-    const uint64_t qfrag = (uint64_t)kvs::qfrag_bytes((int)Hk, (int)D);
-    const uint64_t need = kStatusBytes + qfrag + n_split * per_split * (D + 2) * sizeof(float);
-    if (need > kNoallocScratchBytes) {
-        kvs::set_thread_error("needs " + std::to_string(need) + " bytes of split partials; the fixed scratch "
-                              "holds " + std::to_string(kNoallocScratchBytes) +
-                              " (use kvs_attend with a workspace instead)");
-        return KVS_ERR_CAPACITY;
-    }
     void *scratch = nullptr;
     kvs_status s = scratch_on_current_device(&scratch);
     if (s != KVS_OK) return s;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the timeout flag must start at zero for this call
+    cudaError_t ce = cudaMemsetAsync(scratch, 0, sizeof(int), st);
+    if (ce != cudaSuccess) {
+        kvs::set_thread_error(std::string("clearing the timeout flag: ") + cudaGetErrorString(ce));
+        return KVS_ERR_CUDA;
+    }
     kvs::DecodeParams dp;
     memset(&dp, 0, offsetof(kvs::DecodeParams, page));
     dp.arena = static_cast<const uint8_t *>(pages_dev);
@@ -157,6 +170,7 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
     kvs::CombineParams cp;
     cp.part_o = dp.part_o;
     cp.part_ml = dp.part_ml;
+    cp.status = dp.status;
     cp.out = out_dev;
     cp.lse = lse_dev;
     cp.R = (int)n_rows;

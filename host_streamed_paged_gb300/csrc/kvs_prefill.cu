@@ -546,11 +546,9 @@ cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t s) {
     if (p.geom.D != kD || p.n_splits < 1 || p.n_splits > kMaxPrefillSplits || p.R < 1 || p.R > 256 ||
         p.geom.P % kBN != 0)
         return cudaErrorInvalidValue;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    {
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(prefill_kernel), kSmemBytes);
         if (e != cudaSuccess) return e;
-        configured = true;
     }
     const int rt = (p.R + kTileRows - 1) / kTileRows;
     dim3 grid(p.n_splits, p.geom.Hk * p.G * rt);

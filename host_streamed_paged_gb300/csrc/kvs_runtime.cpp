@@ -1032,6 +1032,58 @@ kvs_status kvs_truncate(kvs_ctx *c, uint32_t layer, uint64_t n_tokens) {
     return KVS_OK;
 }
 
+// Pre-encoded complete pages straight into the host history (the authoritative
+// copy of every page), extending a page-aligned layer.
+kvs_status kvs_load_host_pages(kvs_ctx *c, uint32_t layer, uint64_t first_page, uint64_t n_pages,
+                               const void *src) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "host page load while prefetches are pending");
+    if (n_pages == 0) return KVS_OK;
+    if (!src) return fail(c, KVS_ERR_INVALID, "null source pages");
+    if (!c->host) return fail(c, KVS_ERR_STATE, "no host history");
+    LayerState &L = c->layers[layer];
+    const uint64_t P = (uint64_t)c->geom.P;
+    if (L.T % P != 0 || first_page != L.T / P)
+        return fail(c, KVS_ERR_INVALID, "loaded pages must continue a page-aligned history (first_page = T / P)");
+    if (n_pages > (uint64_t)c->max_pages - first_page || (first_page + n_pages) * P > c->cfg.max_tokens)
+        return fail(c, KVS_ERR_CAPACITY, "loaded pages reach beyond max_tokens");
+    // a publish on the copy stream may still be writing the host history
+    kvs_status s = kvs_sync(c, 0);
+    if (s != KVS_OK) return s;
+    if (c->graph_exec) {  // its captured lengths no longer hold
+        release_graph(c);
+        c->graph_kernels = 0;
+    }
+    // the tail slots give up their (complete, published) pages: to the pool
+    // where the mask asks and there is room, else they are host-only
+    for (int i = 0; i < 2; ++i) {
+        const int64_t old = L.tail_page[i];
+        if (old < 0) continue;
+        if (evict_target(c, layer, old, c->pool_n - c->pool_used) == 1) {
+            const int64_t ps = pool_alloc(c, layer, old);
+            L.pool_slot[old] = ps;
+            if (c->plan_only) {
+                log_op(c, KVS_OP_MOVE, kAttn, layer, 0, old, ps);
+            } else {
+                cudaError_t e = cudaMemcpyAsync(c->slot_ptr(ps), c->slot_ptr(c->tail_slot(layer, old)),
+                                                (size_t)c->geom.page_bytes, cudaMemcpyDeviceToDevice, c->attn);
+                if (e != cudaSuccess) return cuda_fail(c, e, "tail -> pool move");
+            }
+        }
+        L.tail_page[i] = -1;
+    }
+    const uint8_t *from = static_cast<const uint8_t *>(src);
+    for (uint64_t i = 0; i < n_pages; ++i)
+        memcpy(c->host_page(layer, (int64_t)(first_page + i)), from + i * (uint64_t)c->geom.page_bytes,
+               (size_t)c->geom.page_bytes);
+    L.T = (first_page + n_pages) * P;
+    return KVS_OK;
+}
+
 kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, uint64_t n_pages) {
     if (!c) return KVS_ERR_INVALID;
     c->err.clear();
@@ -1382,6 +1434,8 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         dp.G = (int)G;
         dp.pos0 = (long long)pos0;
         dp.scale_log2 = scale * 1.4426950408889634f;
+        if (c->fault == KVS_FAULT_DEVICE_WAIT && c->fault_nth && ++c->fault_count == c->fault_nth)
+            dp.give_up_waits = 1;
 
         // Q fragments for every kv head, once per call (primary attention stream)
         c->st.kernel_launches++;
@@ -1472,6 +1526,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         kvs::CombineParams cp;
         cp.part_o = part_o;
         cp.part_ml = part_ml;
+        cp.status = static_cast<const int *>(c->cfg.workspace);
         cp.out = out_dev;
         cp.lse = lse_dev;
         cp.R = (int)n_rows;
@@ -1737,7 +1792,7 @@ kvs_status kvs_graph_destroy(kvs_ctx *c) {
 
 kvs_status kvs_debug_inject(kvs_ctx *c, uint32_t fault, uint64_t nth) {
     if (!c) return KVS_ERR_INVALID;
-    if (fault > KVS_FAULT_SYNC_STALL) return fail(c, KVS_ERR_INVALID, "unknown fault kind");
+    if (fault > KVS_FAULT_DEVICE_WAIT) return fail(c, KVS_ERR_INVALID, "unknown fault kind");
     c->fault = nth ? fault : (uint32_t)KVS_FAULT_NONE;
     c->fault_nth = nth;
     c->fault_count = 0;

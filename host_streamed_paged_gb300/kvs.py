@@ -37,7 +37,7 @@ KVS_FLAG_DMA_FILL = 2
 
 KVS_OP_RECORD, KVS_OP_WAIT, KVS_OP_FILL, KVS_OP_READ, KVS_OP_POOL_LOAD = 1, 2, 3, 4, 5
 KVS_OP_PUBLISH, KVS_OP_WRITE, KVS_OP_LAUNCH, KVS_OP_MOVE = 6, 7, 8, 9
-KVS_FAULT_NONE, KVS_FAULT_FILL_ENQUEUE, KVS_FAULT_SYNC_STALL = 0, 1, 2
+KVS_FAULT_NONE, KVS_FAULT_FILL_ENQUEUE, KVS_FAULT_SYNC_STALL, KVS_FAULT_DEVICE_WAIT = 0, 1, 2, 3
 
 
 class kvs_config(ctypes.Structure):
@@ -120,6 +120,7 @@ SIGNATURES = {
     "kvs_append": ([_P, _U32, _P, _P, _U32], _I32),
     "kvs_truncate": ([_P, _U32, _U64], _I32),
     "kvs_length": ([_P, _U32, _P], _I32),
+    "kvs_load_host_pages": ([_P, _U32, _U64, _U64, _P], _I32),
     "kvs_set_residency": ([_P, _U32, _P, _U64], _I32),
     "kvs_set_ring_slots": ([_P, _U32, _U32], _I32),
     "kvs_prefetch": ([_P, _U32], _I32),
@@ -226,6 +227,11 @@ def kvs_length(ctx, layer) -> int:
     n = ctypes.c_uint64()
     _check(ctx, load().kvs_length(ctx, layer, ctypes.byref(n)))
     return n.value
+
+
+def kvs_load_host_pages(ctx, layer, first_page, n_pages, src) -> int:
+    """Install n_pages encoded pages (host memory at src) into the host history of layer."""
+    return _check(ctx, load().kvs_load_host_pages(ctx, layer, first_page, n_pages, _ptr(src)))
 
 
 def kvs_set_residency(ctx, layer, mask) -> int:
@@ -373,8 +379,10 @@ class KVStream:
 
     ``arena_slots`` counts page slots (tails + pool + ring); default = tails +
     ring + one layer's pages of pool.  ``host`` may be given (numpy uint8 or a
-    pinned torch tensor); otherwise a pageable numpy buffer is allocated and
-    kvs_create registers it with CUDA.
+    pinned torch tensor); otherwise ``host_alloc`` chooses the buffer:
+    "pinned" (the default, CUDA-allocated pinned memory), "pageable" (numpy
+    memory that kvs_create registers with CUDA) or "hugepage".  A plan-only
+    context keeps ``host`` (if given) as a plain host buffer.
     """
 
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
@@ -400,8 +408,10 @@ class KVStream:
         if plan_only:
             cfg.flags |= KVS_FLAG_PLAN_ONLY
             cfg.arena, cfg.workspace = 1 << 20, 1 << 21  # never dereferenced
-            cfg.host = 0
-            self.arena = self.workspace = self.host = None
+            # host memory is plain memory: a plan-only context may keep a history
+            self.host = host
+            cfg.host = _ptr(host)
+            self.arena = self.workspace = None
         else:
             import torch
             # ring refills are the critical path of a streamed step: their copy
@@ -471,6 +481,13 @@ class KVStream:
 
     def length(self, layer):
         return kvs_length(self.ctx, layer)
+
+    def load_host_pages(self, layer, first_page, pages):
+        """pages: host uint8 array of whole pages (n_pages * page_bytes) in the library layout."""
+        src = np.ascontiguousarray(pages, dtype=np.uint8).reshape(-1)
+        if src.size % self.page_bytes:
+            raise ValueError("pages must hold a whole number of page_bytes")
+        return kvs_load_host_pages(self.ctx, layer, first_page, src.size // self.page_bytes, src)
 
     def set_residency(self, layer, mask):
         return kvs_set_residency(self.ctx, layer, mask)

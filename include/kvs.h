@@ -175,11 +175,19 @@ enum {
     KVS_OP_MOVE = 9       /* attention stream: device copy of page a into pool slot b */
 };
 
-/* kvs_debug_inject fault kinds (host-side only; no GPU fault is ever made). */
+/* kvs_debug_inject fault kinds.  None of them makes a GPU fault: each is made
+ * on the host, or (KVS_FAULT_DEVICE_WAIT) as a device-side wait that gives
+ * up by its own limit and reports a status. */
 enum {
     KVS_FAULT_NONE = 0,
     KVS_FAULT_FILL_ENQUEUE = 1, /* the nth ring refill enqueue fails */
-    KVS_FAULT_SYNC_STALL = 2    /* kvs_sync sees the GPU as busy until its deadline */
+    KVS_FAULT_SYNC_STALL = 2,   /* kvs_sync sees the GPU as busy until its deadline */
+    KVS_FAULT_DEVICE_WAIT = 3   /* in the split-K attention launches of the nth kvs_attend call,
+                                   every pipeline wait gives up at once, as if its copy never
+                                   landed: the CTAs drain the copies they issued (with the
+                                   normal bound), set the status word and exit.  That call's
+                                   outputs (and those of later calls until the next kvs_sync)
+                                   are NaN, and the next kvs_sync returns KVS_ERR_CUDA */
 };
 
 /*
@@ -190,12 +198,32 @@ enum {
  *   arena_bytes_min: minimum arena (2 tail slots per layer + ring_slots)
  *   workspace_bytes: minimum workspace (a 256-byte status word, then split
  *                    partials for max_rows rows)
- * Any output pointer may be NULL.  Page layout (one head section of
- * P*D*13/8 bytes per kv head, in kv-head order):
- *   Kq int8 [P][D] | Ks fp16 [P][D/32] | Vq u8 [D/2][P] | Vs fp16 [D/32][P]
- * Vq byte row b*16+c holds the Q4_0 codes of dims b*32+c (low nibble) and
- * b*32+c+16 (high nibble) for each token; this dim-major V order lets the
- * attention kernel load whole tensor-core fragments with one 32-bit load.
+ * Any output pointer may be NULL.  The page size follows the cache types:
+ * per token and kv head, Q8_0 K takes D + 2*D/32 bytes and Q4_0 V takes
+ * D/2 + 2*D/32 bytes (V2 README, "KV data movement and attention": page sizes
+ * follow the selected quants).
+ *
+ * Page layout.  A page is Hk head sections of S = P*D*13/8 bytes, kv head g at
+ * byte g*S.  With NB = D/32 blocks of 32 dims, token t (0 <= t < P) and dim d,
+ * a head section holds four sub-arrays:
+ *   Kq  offset 0,           P*D bytes:    the int8 Q8_0 code of (t, d) at byte
+ *                            ((t/16*NB + d/32)*16 + t%16)*32 + d%32
+ *                            (16-token groups; within a group block-major, then
+ *                            token, then the block's 32 codes)
+ *   Ks  offset P*D,         P*D/16 bytes: the fp16 Q8_0 scale of (t, block b)
+ *                            at fp16 element t*NB + b
+ *   Vq  offset P*D*17/16,   P*D/2 bytes:  byte row j (0 <= j < D/2) packs dims
+ *                            j/16*32 + j%16 (low nibble) and j/16*32 + j%16 + 16
+ *                            (high nibble); the byte of (t, j) is at
+ *                            ((t/32*NB + j/16)*16 + j%16)*32 + t%32
+ *                            (32-token chunks; within a chunk byte row, then
+ *                            the chunk's 32 tokens)
+ *   Vs  offset P*D*25/16,   P*D/16 bytes: the fp16 Q4_0 scale of (t, block b)
+ *                            at fp16 element b*P + t
+ * Values: K = code * scale; V = (nibble - 8) * scale (Q4_0 codes 0..15).
+ * fp16 scales are little-endian IEEE binary16.  These orders hand each
+ * tensor-core fragment of the attention kernel to one 8-byte load; the codes
+ * and scales themselves are exactly the Q8_0 / Q4_0 block contents.
  */
 kvs_status kvs_query_sizes(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
                            uint64_t *arena_bytes_min, uint64_t *workspace_bytes);
@@ -215,7 +243,10 @@ kvs_status kvs_query_sizes(const kvs_config *cfg, uint64_t *page_bytes, uint64_t
 kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out);
 
 /* kvs_destroy -- synchronise the context's streams, release events and any
- * host registration made by kvs_create.  Never frees caller memory. */
+ * host registration made by kvs_create.  Never frees caller memory (the
+ * caller owns the arena: V2 README, "Phase arena": one device-local parent
+ * allocation, lent out as bounded views).  Library API otherwise; the pages
+ * describe no such call. */
 kvs_status kvs_destroy(kvs_ctx *ctx);
 
 /*
@@ -234,19 +265,46 @@ kvs_status kvs_append(kvs_ctx *ctx, uint32_t layer, const float *k_dev, const fl
                       uint32_t n_tokens);
 
 /* kvs_truncate -- shorten layer `layer` to n_tokens (<= T), e.g. to drop a
- * rejected draft suffix.  Only the current tail page (and the page before it)
- * may be cut into; KVS_ERR_UNSUPPORTED for a cut further back.  KVS_ERR_STATE
- * while the layer has prefetched ring pages pending. */
+ * rejected draft suffix (V2 README, "MTP catch-up, prediction, and rollback":
+ * on rejection the rejected KV suffix is discarded and accepted work kept).
+ * Only the current tail page (and the page before it) may be cut into;
+ * KVS_ERR_UNSUPPORTED for a cut further back.  KVS_ERR_STATE while the layer
+ * has prefetched ring pages pending.  Rows appended afterwards overwrite the
+ * tail and publish it to host again once the page is full. */
 kvs_status kvs_truncate(kvs_ctx *ctx, uint32_t layer, uint64_t n_tokens);
 
-/* kvs_length -- tokens appended to layer `layer`. */
+/* kvs_length -- tokens appended to layer `layer`.  Library API; the pages
+ * describe no such call. */
 kvs_status kvs_length(const kvs_ctx *ctx, uint32_t layer, uint64_t *n_tokens);
+
+/*
+ * kvs_load_host_pages -- write n_pages complete, already encoded pages (src:
+ * host memory, n_pages * page_bytes, each in the page layout kvs_query_sizes
+ * gives) into the host history of `layer` as pages first_page ..
+ * first_page + n_pages - 1, and extend the layer to (first_page + n_pages) * P
+ * tokens.  The host history is the authoritative copy of every page (V2
+ * README, "KV data movement and attention"), so a history encoded elsewhere
+ * can be installed there without passing each row through the KV writer.
+ * first_page must equal T / P with T a multiple of P (KVS_ERR_INVALID
+ * otherwise), and the pages must fit max_tokens (KVS_ERR_CAPACITY).  The call
+ * first waits for the context's earlier device work (a publish may still be
+ * writing the host history), then copies on the host; it returns when the
+ * bytes are in place.  The loaded pages are host-only: they are streamed
+ * through the ring when attended, until a later kvs_set_residency makes some
+ * resident.  The tail slots keep the pages they held, so the next kvs_append
+ * starts a new page.  KVS_ERR_STATE while prefetches are pending or inside a
+ * step capture.
+ */
+kvs_status kvs_load_host_pages(kvs_ctx *ctx, uint32_t layer, uint64_t first_page, uint64_t n_pages,
+                               const void *src);
 
 /*
  * kvs_set_residency -- choose which pages of `layer` live in the resident
  * pool: mask[i] != 0 for page i (i < n_pages; pages >= n_pages are not
  * resident).  Newly resident pages are loaded host -> pool on the copy
- * stream; attention waits for the load before its next read.  The device
+ * stream; attention waits for the load before its next read (selected pages
+ * go host -> resident pool, and one layer may stay fully resident while
+ * others stream: V2 README, "KV data movement and attention").  The device
  * tail pages are always device-readable whatever the mask says.
  * KVS_ERR_CAPACITY if the pool has too few free slots (nothing changes);
  * KVS_ERR_STATE while any layer has prefetched ring pages pending.
@@ -257,6 +315,10 @@ kvs_status kvs_set_residency(kvs_ctx *ctx, uint32_t layer, const uint8_t *mask,
 /*
  * kvs_set_ring_slots -- re-split the arena between the resident pool and the
  * ring: ring = n_slots page slots (>= 1), chunk = chunk_pages (0: default).
+ * Under pressure the pages' policy trades resident pages for ring slots
+ * within one physical budget (V2 README, "KV data movement and attention");
+ * the runtime repartitions the pool only once a proposal is accepted ("Logical
+ * KV layout, policy, and physical execution").
  * KVS_ERR_CAPACITY if the pool would become smaller than the pages resident
  * now; KVS_ERR_STATE while prefetches are pending.  Waits for earlier ring
  * work on the device (stream-ordered) before slots change role.
@@ -386,13 +448,19 @@ kvs_status kvs_attend(kvs_ctx *ctx, uint32_t layer, const void *q_dev, int32_t q
                       uint32_t n_rows, uint32_t n_q_head, uint64_t pos0, float scale,
                       float *out_dev, float *lse_dev);
 
-/* kvs_sync -- wait until both streams have finished the context's work, or
- * return KVS_ERR_TIMEOUT after timeout_ms (0 = no limit).  Host-side polling
- * of CUDA events; no device-side wait is involved. */
+/* kvs_sync -- wait until every stream of the context has finished its work,
+ * or return KVS_ERR_TIMEOUT after timeout_ms (0 = no limit).  Host-side
+ * polling of CUDA events; no device-side wait is involved.  Then reads the
+ * workspace status word: a bounded device-side wait that gave up in an
+ * attention kernel since the last kvs_sync returns KVS_ERR_CUDA (and clears
+ * the word).  Failures are error returns, not aborts (PR "port adaptive KV
+ * streaming", review comments); the pages describe no call of this shape. */
 kvs_status kvs_sync(kvs_ctx *ctx, uint32_t timeout_ms);
 
 /* kvs_flush -- publish the partial tail page of `layer` (or of every layer if
- * layer == UINT32_MAX) to the host history. */
+ * layer == UINT32_MAX) to the host history, e.g. before saving it (the KV
+ * writer publishes a changed tail to host: V2 README, "KV data movement and
+ * attention"; full pages are published by kvs_append itself). */
 kvs_status kvs_flush(kvs_ctx *ctx, uint32_t layer);
 
 /*
@@ -400,20 +468,26 @@ kvs_status kvs_flush(kvs_ctx *ctx, uint32_t layer);
  * *kind = 0 host only, 1 tail slot, 2 resident pool; *slot = device slot id
  * (or -1).  kvs_read_slot copies device slot `slot` (page_bytes) to host_dst
  * synchronously; kvs_read_host_page copies the host history page.  Debug and
- * test helpers for bit-exact layout and indexing checks.
+ * test helpers for bit-exact layout and indexing checks; library API with no
+ * counterpart on the pages.
  */
 kvs_status kvs_page_location(const kvs_ctx *ctx, uint32_t layer, uint64_t page, int32_t *kind,
                              int64_t *slot);
 kvs_status kvs_read_slot(kvs_ctx *ctx, int64_t slot, void *host_dst);
 kvs_status kvs_read_host_page(kvs_ctx *ctx, uint32_t layer, uint64_t page, void *host_dst);
 
-/* kvs_ring_info -- first device slot id of the ring and its size. */
+/* kvs_ring_info -- first device slot id of the ring and its size.  Library
+ * API (test helper); no counterpart on the pages. */
 kvs_status kvs_ring_info(const kvs_ctx *ctx, int64_t *first_slot, uint32_t *n_slots);
 
-/* kvs_stats -- counters since create (or the last reset when reset != 0). */
+/* kvs_stats -- counters since create (or the last reset when reset != 0).
+ * They include the feedback the pages' policy samples (V2 README, "KV data
+ * movement and attention": readiness misses, ring occupancy, copy-stream
+ * time), in the form kvs_policy_observation takes. */
 kvs_status kvs_stats(kvs_ctx *ctx, kvs_stats_t *out, int reset);
 
-/* kvs_set_timing -- mask of KVS_TIME_* bits.  Each attention-kernel launch of
+/* kvs_set_timing -- library API for measurement (no counterpart on the
+ * pages): mask of KVS_TIME_* bits.  Each attention-kernel launch of
  * a selected kind is bracketed by CUDA events on attn_stream; its device time
  * and the page bytes it reads are added to kvs_stats_t.decode_ms /
  * decode_bytes once the events complete.  0 disables. */
@@ -435,28 +509,40 @@ kvs_status kvs_set_timing(kvs_ctx *ctx, int mask);
  * buffers (q, k, v, out, lse) whose addresses were captured.  Attention
  * timing (kvs_set_timing) is not recorded inside a capture.  kvs_set_residency
  * and kvs_set_ring_slots drop a captured graph (its slot schedule is baked in).
+ * A graph from an old layout is never reused (V2 README, "Backend-neutral
+ * memory and streaming contracts": captured graphs are invalidated at a layout
+ * change); the pages' step itself is host-issued, so this API has no direct
+ * counterpart there.
  */
 kvs_status kvs_graph_begin(kvs_ctx *ctx);
 kvs_status kvs_graph_end(kvs_ctx *ctx);
 kvs_status kvs_graph_launch(kvs_ctx *ctx);
 kvs_status kvs_graph_destroy(kvs_ctx *ctx);
 
-/* kvs_last_error -- message of the last failed call on ctx ("" if none);
+/* kvs_last_error -- library API (no counterpart on the pages): message of the
+ * last failed call on ctx ("" if none);
  * with ctx == NULL, the last failure of this thread in a call that takes no
  * context (kvs_query_sizes, kvs_create, kvs_attend_pages_noalloc). */
 const char *kvs_last_error(const kvs_ctx *ctx);
 
-/* kvs_debug_inject -- arm a host-side fault (KVS_FAULT_*) that fires on the
- * nth (1-based) matching event; nth = 0 disarms. */
+/* kvs_debug_inject -- arm a fault (KVS_FAULT_*) that fires on the nth
+ * (1-based) matching event; nth = 0 disarms.  Every fault is made on the host
+ * or as a shortened device-side wait limit: no GPU fault is ever made.  Test
+ * API; the pages describe no such call. */
 kvs_status kvs_debug_inject(kvs_ctx *ctx, uint32_t fault, uint64_t nth);
 
-/* kvs_trace_read -- copy up to max logged operations of a PLAN_ONLY context
+/* kvs_trace_read -- test API (no counterpart on the pages) for checking the
+ * span plan's coverage and fences (V2 README, "Backend-neutral memory and
+ * streaming contracts": a plan with gaps, overlaps or too little coverage is
+ * rejected): copy up to max logged operations of a PLAN_ONLY context
  * starting at index `first` into ops; *n_out = number copied, *n_total = log
  * length.  KVS_ERR_STATE for a context that is not PLAN_ONLY. */
 kvs_status kvs_trace_read(const kvs_ctx *ctx, uint64_t first, uint64_t max, kvs_trace_op *ops,
                           uint64_t *n_out, uint64_t *n_total);
 
-/* kvs_version -- KVS_ABI_VERSION of the loaded library. */
+/* kvs_version -- KVS_ABI_VERSION of the loaded library (library API; the
+ * pages' copy-ops table is versioned the same way: V2 README, "Logical KV
+ * layout, policy, and physical execution"). */
 int32_t kvs_version(void);
 
 /*
@@ -481,9 +567,15 @@ int32_t kvs_version(void);
  * KVS_ERR_CAPACITY before any work.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress); make that first call
  * before any stream capture on that device.  All calls on a device share the
- * array, which keeps the last call's contents (nothing in it needs clearing):
- * calls whose GPU work overlaps race, so order them on one stream.
- * Errors: kvs_last_error(NULL).
+ * array, which keeps the last call's contents: each call first clears the
+ * array's timeout flag on `stream` (cudaMemsetAsync, no allocation), and the
+ * partials are written before they are read.  Calls whose GPU work overlaps
+ * race, so order them on one stream.  A bounded device-side wait that gives
+ * up (a copy into shared memory that never completes) cannot be returned as
+ * a status, since the call returns before its kernels run: it makes every
+ * element of out_dev and lse_dev NaN instead.  pos0 + n_rows beyond INT64_MAX
+ * -> KVS_ERR_INVALID.  Works on any device of the process (the scratch address
+ * and launch limits are kept per device).  Errors: kvs_last_error(NULL).
  */
 kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t pages_bytes,
                                     const uint32_t *page_slots, uint64_t n_pages,

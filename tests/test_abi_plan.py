@@ -387,3 +387,88 @@ def test_prefill_scheduling_fences_and_split_coverage(seed):
         reads = sorted(p for p, g in _reads_of_attend(st.trace()[n0:], l))
         assert reads == list(range(math.ceil((T0 + R) / P)))
     check_trace(st, 6 * Hk)
+
+
+def test_load_host_pages_installs_pages_and_streams_them():
+    """Encoded pages written into the host history are attended like any streamed page."""
+    P, Hk, D, maxp = 64, 1, 128, 12
+    pb = Hk * P * D * 13 // 8
+    host = np.zeros(2 * maxp * pb, np.uint8)
+    st = kvs.KVStream(page_tokens=P, n_layers=2, n_kv_head=Hk, head_dim=D, max_q_head=6, max_rows=6,
+                      max_tokens=P * maxp, ring_slots=2, chunk_pages=1, arena_slots=4 + 2 + 12,
+                      plan_only=True, host=host)
+    assert st.page_bytes == pb
+    kvs.kvs_append(st.ctx, 0, None, None, 2 * P)  # pages 0, 1 sit in the tail slots
+    st.set_residency(0, np.array([1, 0], np.uint8))  # page 0 wanted resident
+    rng = np.random.default_rng(5)
+    pages = rng.integers(0, 256, size=3 * pb, dtype=np.uint8)
+    st.load_host_pages(0, 2, pages)
+    assert st.length(0) == 5 * P
+    for i in range(3):
+        assert np.array_equal(st.read_host_page(0, 2 + i), pages[i * pb:(i + 1) * pb])
+    # the tail slots gave up their pages: page 0 to the pool (mask), page 1 to the host
+    assert st.page_location(0, 0)[0] == 2
+    assert st.page_location(0, 1) == (0, -1)
+    for p in range(2, 5):
+        assert st.page_location(0, p) == (0, -1)
+    # refusals change nothing
+    for bad_first in (4, 6):
+        with pytest.raises(kvs.KVSError) as e:
+            st.load_host_pages(0, bad_first, pages[:pb])
+        assert e.value.status == kvs.KVS_ERR_INVALID
+    with pytest.raises(kvs.KVSError) as e:
+        st.load_host_pages(0, 5, np.zeros(8 * pb, np.uint8))  # 13 pages > 12
+    assert e.value.status == kvs.KVS_ERR_CAPACITY
+    st.prefetch(0)
+    with pytest.raises(kvs.KVSError) as e:
+        st.load_host_pages(1, 0, pages[:pb])
+    assert e.value.status == kvs.KVS_ERR_STATE
+    assert st.length(0) == 5 * P and st.length(1) == 0
+    # one new row starts page 5 in a tail slot; every page is read once, loaded ones through the ring
+    st.attend_plan(0, 1, 6, 5 * P - 1)
+    kvs.kvs_append(st.ctx, 0, None, None, 1)
+    st.attend_plan(0, 1, 6, 5 * P)
+    ops, _ = check_trace(st, 6)
+    fills = {o["a"] for o in ops if o["op"] == kvs.KVS_OP_FILL and o["layer"] == 0}
+    assert {1, 2, 3, 4} <= fills and 0 not in fills
+    reads = [o["a"] for o in ops if o["op"] == kvs.KVS_OP_READ]
+    assert sorted(reads) == sorted(list(range(5)) + list(range(6)))
+    # a history that is not page-aligned refuses a load
+    kvs.kvs_append(st.ctx, 1, None, None, 10)
+    with pytest.raises(kvs.KVSError) as e:
+        st.load_host_pages(1, 0, pages[:pb])
+    assert e.value.status == kvs.KVS_ERR_INVALID
+    st.close()
+
+
+def test_noalloc_refusals_come_before_any_device_work():
+    """Every refusal of kvs_attend_pages_noalloc is decided on the host from its
+    arguments (the pointers below are never dereferenced)."""
+    fake = 1 << 20
+    pb = 4 * 256 * 256 * 13 // 8
+    base = dict(pages=fake, pages_bytes=8 * pb, page_slots=np.arange(8, dtype=np.uint32), page_tokens=256,
+                n_kv_head=4, head_dim=256, q=fake, q_dtype=kvs.KVS_F32, n_rows=6, n_q_head=24,
+                pos0=256 * 8 - 6, scale=0.1, out=fake, lse=None, stream=0)
+    cases = [
+        (dict(page_tokens=48), kvs.KVS_ERR_UNSUPPORTED),
+        (dict(head_dim=96), kvs.KVS_ERR_UNSUPPORTED),
+        (dict(q_dtype=7), kvs.KVS_ERR_INVALID),
+        (dict(n_q_head=26), kvs.KVS_ERR_INVALID),
+        (dict(n_rows=0), kvs.KVS_ERR_INVALID),
+        (dict(n_rows=11, pos0=0), kvs.KVS_ERR_UNSUPPORTED),  # 6 heads x 11 rows > 64
+        (dict(q=None), kvs.KVS_ERR_INVALID),
+        (dict(out=None), kvs.KVS_ERR_INVALID),
+        (dict(pos0=2**63 - 3), kvs.KVS_ERR_INVALID),  # pos0 + n_rows wraps
+        (dict(pos0=2**64 - 6), kvs.KVS_ERR_INVALID),
+        (dict(pos0=256 * 8 - 5), kvs.KVS_ERR_CAPACITY),  # the last row reaches a ninth page
+        (dict(page_slots=np.r_[np.arange(7), 8].astype(np.uint32)), kvs.KVS_ERR_INVALID),  # slot 8 outside
+        (dict(page_slots=np.zeros(300, np.uint32), pos0=300 * 256 - 6), kvs.KVS_ERR_CAPACITY),  # > 32 MiB
+    ]
+    for over, want in cases:
+        a = dict(base, **over)
+        with pytest.raises(kvs.KVSError) as e:
+            kvs.kvs_attend_pages_noalloc(a["pages"], a["pages_bytes"], a["page_slots"], a["page_tokens"],
+                                         a["n_kv_head"], a["head_dim"], a["q"], a["q_dtype"], a["n_rows"],
+                                         a["n_q_head"], a["pos0"], a["scale"], a["out"], a["lse"], a["stream"])
+        assert e.value.status == want, (over, e.value)
+        assert kvs.kvs_last_error(None)

@@ -281,6 +281,60 @@ def test_sync_timeout_injection_on_gpu_context():
     st.sync(1000)
 
 
+def test_device_wait_that_gives_up_is_reported_and_recovered():
+    """A bounded pipeline wait in the attention kernel that gives up (made to
+    give up at once by the test hook) leaves NaN outputs, kvs_sync reports
+    KVS_ERR_CUDA, and the next attend is correct again."""
+    import torch
+    P, D, Hk, G, T = 64, 128, 2, 6, 64 * 9 + 13
+    st = make_stream(P, 1, Hk, D, G * Hk, 1, T, ring=2, chunk=1)
+    k, v = history(SEED, 0, T, Hk, D)
+    append_rows(st, 0, k, v)
+    mask = np.zeros(math.ceil(T / P), np.uint8)
+    mask[::2] = 1
+    st.set_residency(0, mask)
+    st.sync()
+    q = queries(SEED, 0, 1, G * Hk, D)
+    st.inject(kvs.KVS_FAULT_DEVICE_WAIT, 1)
+    qt = torch.from_numpy(q).cuda()
+    torch.cuda.synchronize()
+    out, lse = st.attend(0, qt, T - 1, 0.1)
+    with pytest.raises(kvs.KVSError) as e:
+        st.sync()
+    assert e.value.status == kvs.KVS_ERR_CUDA and "timed out" in str(e.value)
+    torch.cuda.synchronize()
+    assert np.isnan(out.cpu().numpy()).all() and np.isnan(lse.cpu().numpy()).all()
+    st.inject(kvs.KVS_FAULT_NONE, 0)
+    out, lse = attend(st, 0, q, T - 1, 0.1)
+    ro, rl = oracle_ref(k, v, q, T - 1, 0.1)
+    check_parity(out, lse, ro, rl)
+
+
+def test_loaded_host_pages_stream_and_match_the_oracle():
+    """Pages encoded elsewhere (here by the oracle, following the documented
+    layout) installed with kvs_load_host_pages, half of them made resident,
+    the rest streamed through a 2-slot ring."""
+    P, D, Hk, G = 256, 256, 4, 6
+    full, extra = 12, 70
+    T = full * P + extra
+    st = make_stream(P, 1, Hk, D, G * Hk, 2, T, ring=2, chunk=1)
+    k, v = history(SEED, 3, T, Hk, D)
+    ref = oracle.QuantKV(k[:full * P], v[:full * P])
+    pages = np.concatenate([ref.encode_page(P, i) for i in range(full)])
+    st.load_host_pages(0, 0, pages)
+    append_rows(st, 0, k[full * P:], v[full * P:])
+    for i in (0, 5, 11):
+        assert np.array_equal(st.read_host_page(0, i), pages[i * st.page_bytes:(i + 1) * st.page_bytes])
+    mask = np.zeros(full + 1, np.uint8)
+    mask[1::2] = 1
+    st.set_residency(0, mask)
+    q = queries(SEED, 3, 2, G * Hk, D)
+    out, lse = attend(st, 0, q, T - 2, 1.0 / math.sqrt(D))
+    ro, rl = oracle_ref(k, v, q, T - 2, 1.0 / math.sqrt(D))
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] >= full // 2
+
+
 # ------------------------------------------------------------ full-size samples
 
 @pytest.mark.parametrize("chunk,lanes", [(2, 1), (4, 2), (2, 3)])
