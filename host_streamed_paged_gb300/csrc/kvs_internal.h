@@ -91,6 +91,7 @@ inline int64_t qfrag_bytes(int Hk, int D) {
 // grid = (splits, Hk * G * row tiles).  Q is fp16; D must be 256.
 constexpr int kMaxPrefillSplits = 64;
 constexpr int kMaxPrefillItems = 1024;
+constexpr int kMaxPrefillSplitPages = 128;  // pages in one split of the tensor-core prefill path
 struct PrefillParams {
     const uint8_t *arena;
     PageGeom geom;

@@ -8,27 +8,34 @@
 // Streaming for llama.cpp, "Batch and micro-batch sizes"): one launch covers
 // every query tile of a key split.
 //
-// CTA = (key split, kv head, 128-row tile of one query head); 64-key blocks
-// flow through a warp-specialised pipeline:
-//   warps 4-7 (producers) dequantise block j's K (Q8_0) and V (Q4_0) into
-//     shared memory as f16 pairs hi + lo, in the 128-byte-swizzled K-major
-//     layout tcgen05 reads: hi = rn(d * x), lo = rn(d * x - hi) by one f16x2
-//     multiply and one fused multiply-add (d * x has at most 18 significant
-//     bits, so hi + lo is exact);
-//   warp 8 (one thread) issues S_j = Q K_j^T (hi + lo, M 128, N 64, K 256)
-//     into one of two TMEM score buffers, S_{j+1} before O += P_j V_j (hi + lo,
-//     M 128, N 256, K 64), so the tensor pipe has work while the softmax runs;
+// CTA pairs.  Two CTAs of a cluster share one M = 256 MMA (tcgen05
+// cta_group::2): each holds one 128-row query tile (a query head's rows) as
+// its half of A and keeps its own S and O accumulators in its tensor memory.
+// B is split along N between the pair: for S = Q K^T each CTA dequantises 64
+// of a block's 128 keys, for O += P V each CTA dequantises 128 of the 256
+// dims of V.  So a dequantised K/V block serves 256 query rows, and each SM
+// reads only half of every B operand from its shared memory (one M = 128 MMA
+// would read the whole of it, which saturates shared-memory bandwidth on its
+// own).  The grid puts a kv head's tile pairs fastest, so the pairs that read
+// one (split, kv head) run together and share its pages through L2.
+//
+// Roles, per CTA (the leader, cluster rank 0, issues every MMA of the pair):
+//   warps 4-7 (producers) dequantise their halves of block j's K (Q8_0) and V
+//     (Q4_0) into one of two shared-memory stages, as f16 in the 128-byte-
+//     swizzled K-major layouts tcgen05 reads: K[key][dim], V[dim][key], each
+//     value rn(d * x) (the pages' own tensor-core path also runs on f16
+//     dequantised values);
+//   warp 8, lane 0 of the leader, issues S_j (M 256, N 128, K 256) into one of
+//     two TMEM score buffers, then O += P_{j-1} V_{j-1} (M 256, N 256, K 128);
 //   warps 0-3 (one thread per row, TMEM lane = row) read S_j, scale, mask, run
-//     the online softmax and write P_j (f16) to shared memory; O in TMEM is
-//     rescaled only when a row's running max grows by more than 2^8 (the
-//     weights are then formed against the stale max, which is exact).
-// K, V and P are single-buffered: a block's K is rewritten once S_j is done,
-// its V and P once PV_j is done; the fences are mbarriers (producer and
-// softmax arrivals, tcgen05.commit for the MMAs).  At the end warps 0-3 write
-// the split's unnormalised partial (m, l, O) for the log-sum-exp combine
-// shared with the decode path.  Every wait is bounded; on a timeout the CTA
-// raises an abort flag that ends every role's loop, waits (bounded) for its
-// MMAs in flight and records a status code.
+//     the online softmax and write P_j (f16) to shared memory; O is rescaled
+//     only when a row's running max grows by more than 2^8 (the weights are
+//     then formed against the stale max, which is exact).
+// Fences are mbarriers in the leader (full barriers: arrivals from both CTAs)
+// and in both CTAs (empty barriers: multicast tcgen05.commit).  Every wait is
+// bounded; a timeout raises an abort flag in both CTAs that ends every role's
+// loop, and the CTA records a status code.  At the end each CTA writes its
+// tile's unnormalised partial (m, l, O) for the log-sum-exp combine.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -38,38 +45,44 @@ namespace kvs {
 namespace {
 
 constexpr int kPThreads = 288;    // 4 softmax warps, 4 producer warps, 1 MMA warp
-constexpr int kBN = 64;           // keys per block
-constexpr int kD = 256;           // head dim served by this kernel
-constexpr int kTileRows = 128;    // MMA M
+constexpr int kBN = 128;          // keys per block (S MMA N)
+constexpr int kHalfN = kBN / 2;   // keys of a block this CTA dequantises
+constexpr int kD = 256;           // head dim served by this kernel (PV MMA N)
+constexpr int kHalfD = kD / 2;    // dims of V this CTA dequantises
+constexpr int kNB = kD / 32;      // 32-dim scale blocks
+constexpr int kTileRows = 128;    // query rows per CTA (the pair's MMA M is 256)
 constexpr uint32_t kSpinLimit = 1u << 26;
 
 // shared-memory carve (bytes, 1024-aligned tiles for the 128B swizzle)
-constexpr int kQBytes = kTileRows * kD * 2;  // 64 KB: 4 atoms of 128 rows x 128 B
-constexpr int kKBytes = kBN * kD * 2;        // 32 KB: 4 atoms of 64 rows x 128 B
-constexpr int kVBytes = kD * kBN * 2;        // 32 KB: 1 atom of 256 rows x 128 B
-constexpr int kPBytes = kTileRows * kBN * 2; // 16 KB: 1 atom of 128 rows x 128 B
+constexpr int kQBytes = kTileRows * kD * 2;   // 64 KB: 4 atoms (64 dims) of 128 rows x 128 B
+constexpr int kKBytes = kHalfN * kD * 2;      // 32 KB per stage: 4 atoms (64 dims) of 64 key rows
+constexpr int kVBytes = kHalfD * kBN * 2;     // 32 KB per stage: 2 atoms (64 keys) of 128 dim rows
+constexpr int kPBytes = kTileRows * kBN * 2;  // 32 KB: 2 atoms (64 keys) of 128 rows x 128 B
 constexpr int kOffQ = 0;
-constexpr int kOffKh = kOffQ + kQBytes;
-constexpr int kOffKl = kOffKh + kKBytes;
-constexpr int kOffVh = kOffKl + kKBytes;
-constexpr int kOffVl = kOffVh + kVBytes;
-constexpr int kOffP = kOffVl + kVBytes;       // two P buffers
-constexpr int kOffBar = kOffP + 2 * kPBytes;  // mbarriers (kNumBars x 8 B)
-constexpr int kNumBars = 12;
+constexpr int kOffK = kOffQ + kQBytes;        // 2 stages
+constexpr int kOffV = kOffK + 2 * kKBytes;    // 2 stages
+constexpr int kOffP = kOffV + 2 * kVBytes;
+constexpr int kOffBar = kOffP + kPBytes;      // mbarriers (kNumBars x 8 B)
+constexpr int kNumBars = 16;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;  // TMEM base address written by tcgen05.alloc
 constexpr int kOffAbort = kOffTmem + 8;
-constexpr int kSmemBytes = kOffAbort + 8 + 1024;  // + slack to align the base to 1024
+constexpr int kOffSlots = kOffAbort + 8;          // device slot of each page of the split
+constexpr int kSmemBytes = kOffSlots + kMaxPrefillSplitPages * 4 + 1024;  // + slack to align the base
 
-constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 64) and [64, 128), O at [128, 384)
-constexpr uint32_t kColS = 0, kColO = 128;
-// barrier indices; a "+ buffer" barrier has one phase per use of that buffer,
-// so no waiter can fall two phases behind the barrier it waits on
-constexpr int kBarKFull = 0, kBarVFull = 1, kBarKEmpty = 2;
-constexpr int kBarPFull = 3;   // + P buffer (2)
-constexpr int kBarODone = 5;   // + P buffer (2): PV_j done, committed on buffer j & 1
-constexpr int kBarSFull = 7;   // + S buffer (2)
-constexpr int kBarSEmpty = 9;  // + S buffer (2)
-constexpr int kBarFinal = 11;
+constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 128) and [128, 256), O at [256, 512)
+constexpr uint32_t kColO = 256;
+// barrier indices.  "Full" barriers live in the leader and count arrivals
+// from both CTAs (4 warps each); the others are armed by multicast commits in
+// both CTAs.  Each completes one phase per use of what it guards.
+constexpr int kBarKFull = 0;   // + stage (2): producers wrote K_j
+constexpr int kBarVFull = 2;   // + stage (2): producers wrote V_j
+constexpr int kBarPFull = 4;   // softmax of both CTAs wrote P_j
+constexpr int kBarSEmpty = 5;  // + S buffer (2): softmax of both CTAs read S_j
+constexpr int kBarKEmpty = 7;  // + stage (2): S_j done, K stage free
+constexpr int kBarVEmpty = 9;  // + stage (2): PV_j done, V stage free
+constexpr int kBarODone = 11;  // PV_j done: P buffer free, O stable
+constexpr int kBarSFull = 12;  // + S buffer (2): S_j in TMEM
+constexpr int kBarFinal = 14;  // every MMA of the CTA pair finished
 
 // byte offset of element (row, k) in a 128B-swizzled K-major tile whose rows
 // are 128-byte lines of 64 f16 (one swizzle atom per 64 elements of k)
@@ -96,17 +109,31 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of local shared address `a` in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
 
-// bounded wait for phase `parity` of an mbarrier; false on timeout or once
-// another role of the CTA has raised *abort (which this wait also raises)
+// bounded wait (cluster-scope acquire) for phase `parity` of a local
+// mbarrier; false on timeout or once *abort is raised (a timeout raises it)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         uint32_t done;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
             : "r"(bar), "r"(parity)
             : "memory");
@@ -122,27 +149,36 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+// arrive (release, cluster scope) on an mbarrier given by its shared::cluster address
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D (TMEM of both CTAs) = A (smem of both) * B (smem of both, N split) [+ D]
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// arrive on barrier `bar` (same offset) of both CTAs once the pair's MMAs issued so far are done
+__device__ __forceinline__ void mma_commit_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void proxy_fence() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
-// 32 lanes x 32 columns of fp32 from TMEM (one row per thread)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+// 32 lanes x 32 columns of fp32 from TMEM (one row per thread), no wait
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float *v) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -152,12 +188,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -172,7 +208,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
-// 4 int8 (bytes of w) -> f16x2 (x0, x1), (x2, x3), exact (see kvs_decode.cu)
+// 4 int8 (bytes of w) -> f16x2 (x0, x1), (x2, x3), exact: the byte x + 128
+// under exponent 0x64 is 1024 + 128 + x, minus 1152 (exponent-bias
+// conversion, Kim et al. 2022, as in kvs_decode.cu)
 __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &a, uint32_t &b) {
     const uint32_t u = w ^ 0x80808080u;
     uint32_t bl, bh;
@@ -182,270 +220,345 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &a, uint32_t &b
     asm("sub.f16x2 %0, %1, %2;" : "=r"(b) : "r"(bh), "r"(0x64806480u));
 }
 
-// x * d -> (hi, lo) with hi = rn(x d), lo = rn(x d - hi) (exact remainder)
-__device__ __forceinline__ void mul_split(uint32_t x, uint32_t d, uint32_t &hi, uint32_t &lo) {
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(x), "r"(d));
-    const uint32_t nh = hi ^ 0x80008000u;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(x), "r"(d), "r"(nh));
+__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t d) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(d));
+    return r;
 }
 
-__global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+// Two packed Q4_0 bytes (keys k, k+1, bytes `sel` of w) -> f16x2 of the low
+// nibbles - 8 and of the high nibbles - 8.  Each nibble sits in the mantissa
+// under exponent 0x64: low = 1024 + n, high = 1024 + 16 n, and
+// (1024 + 16 n) / 16 - 72 = n - 8 exactly in one fused multiply-add.
+__device__ __forceinline__ void u4x2_pair(uint32_t w, uint32_t sel, uint32_t &lo, uint32_t &hi) {
+    uint32_t sp, tl, th;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sp) : "r"(w), "r"(0u), "r"(sel));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(tl) : "r"(sp), "r"(0x000f000fu), "r"(0x64006400u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(th) : "r"(sp), "r"(0x00f000f0u), "r"(0x64006400u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(tl), "r"(0x64086408u));                          // - 1032
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(th), "r"(0x2c002c00u), "r"(0xd480d480u));  // / 16 - 72
+}
+
+// 9 warps put 3 on one of the SM's four 16K-register partitions: 168 registers
+// per thread is the most that still launches
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const __grid_constant__ PrefillParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split_idx = blockIdx.x;
+    const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
+    const int split_idx = blockIdx.y;
     const int G = p.G, R = p.R, rt = (R + kTileRows - 1) / kTileRows;
-    const int g = blockIdx.y / (G * rt);
-    const int tile = blockIdx.y % (G * rt);
-    const int hl = tile / rt, r0 = (tile % rt) * kTileRows;
-    const int h = g * G + hl;
-    const int P = p.geom.P, bpp = P / kBN;  // blocks per page
+    const int ntiles = G * rt, npairs = (ntiles + 1) / 2;
+    const int g = blockIdx.x / (2 * npairs);
+    const int pair = (blockIdx.x % (2 * npairs)) >> 1;
+    // this CTA's tile and its partner's; a tile past the last is empty (no valid row)
+    auto tile_rows = [&](int t, int &h, int &r0, int &nrows) {
+        const int tt = t < ntiles ? t : 0;
+        h = g * G + tt / rt;
+        r0 = (tt % rt) * kTileRows;
+        nrows = t < ntiles ? ((R - r0) < kTileRows ? (R - r0) : kTileRows) : 0;
+    };
+    int h, r0, nrows, h_o, r0_o, nrows_o;
+    tile_rows(2 * pair + (int)rank, h, r0, nrows);
+    tile_rows(2 * pair + 1 - (int)rank, h_o, r0_o, nrows_o);
+    const int P = p.geom.P;
     const int it0 = p.split_begin[split_idx], it1 = p.split_begin[split_idx + 1];
     const int split = p.split_id[split_idx];
-    const long long last_pos = p.pos0 + ((r0 + kTileRows < R) ? (r0 + kTileRows) : R) - 1;  // tile's last row
+    const int n_keys = (it1 - it0) * P;                     // keys of this split
+    const long long key_pos0 = (long long)p.page[it0] * P;  // the split's pages are consecutive
 
     const uint32_t bar0 = smem_u32(smem + kOffBar);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const uint32_t lead_bar0 = peer_addr(bar0, 0);  // the leader's barriers, shared::cluster
+    auto lead_bar = [&](int i) { return lead_bar0 + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmem);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffAbort);
+    const uint32_t peer_abort = peer_addr(smem_u32(smem + kOffAbort), rank ^ 1u);
 
-    // blocks of this split the tile can see (pages ascend, so the first masked one ends the list)
-    int nblk = 0;
-    for (int j = 0; j < (it1 - it0) * bpp; ++j) {
-        const long long kpos0 = (long long)p.page[it0 + j / bpp] * P + (j % bpp) * kBN;
-        if (kpos0 > last_pos) break;
-        nblk = j + 1;
+    // 128-key blocks of this split the pair runs: enough for the later of the
+    // two tiles (the other tile's extra blocks are fully masked)
+    int nblk;
+    {
+        long long last = -1;
+        if (nrows > 0) last = p.pos0 + r0 + nrows - 1;
+        if (nrows_o > 0 && p.pos0 + r0_o + nrows_o - 1 > last) last = p.pos0 + r0_o + nrows_o - 1;
+        const long long vis = last - key_pos0 + 1;  // keys at or before the pair's last row
+        const int nv = vis <= 0 ? 0 : (int)((vis + kBN - 1) / kBN);
+        nblk = (n_keys + kBN - 1) / kBN;
+        if (nv < nblk) nblk = nv;
     }
-    auto page_base = [&](int j) {
-        return p.arena + (int64_t)p.slot[it0 + j / bpp] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
+    // page-head section holding split key `ks` (0 <= ks < n_keys); the split's
+    // slots are copied to shared memory once (indexing the parameter block at
+    // run time is slow)
+    const uint32_t *slots = reinterpret_cast<const uint32_t *>(smem + kOffSlots);
+    auto head_of = [&](int ks) {
+        return p.arena + (int64_t)slots[ks / P] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
+    };
+    auto raise_abort = [&]() {
+        *abort = 1;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
     };
 
     if (tid == 0) {
-        mbar_init(bar(kBarKFull), 4);
-        mbar_init(bar(kBarVFull), 4);
-        mbar_init(bar(kBarPFull), 4);
-        mbar_init(bar(kBarPFull + 1), 4);
-        mbar_init(bar(kBarKEmpty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(kBarKFull + s), 8);
+            mbar_init(bar(kBarVFull + s), 8);
+            mbar_init(bar(kBarSEmpty + s), 8);
+            mbar_init(bar(kBarKEmpty + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
+            mbar_init(bar(kBarSFull + s), 1);
+        }
+        mbar_init(bar(kBarPFull), 8);
         mbar_init(bar(kBarODone), 1);
-        mbar_init(bar(kBarODone + 1), 1);
-        mbar_init(bar(kBarSFull), 1);
-        mbar_init(bar(kBarSFull + 1), 1);
-        mbar_init(bar(kBarSEmpty), 4);
-        mbar_init(bar(kBarSEmpty + 1), 4);
         mbar_init(bar(kBarFinal), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+    for (int i = tid; i < it1 - it0; i += kPThreads) reinterpret_cast<uint32_t *>(smem + kOffSlots)[i] = p.slot[it0 + i];
+    if (warp == 0) {  // one warp of each CTA allocates the pair's tensor memory together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
     }
-    // Q tile -> shared memory (f16, swizzled); rows past R are zero
+    // Q tile -> shared memory (f16, swizzled); rows past the tile's are zero.
+    // All of a thread's loads are issued before its first store.
     {
+        constexpr int kQChunks = kTileRows * (kD / 8), kQPer = (kQChunks + kPThreads - 1) / kPThreads;
         const __half *q = reinterpret_cast<const __half *>(p.q);
-        for (int c = tid; c < kTileRows * (kD / 8); c += kPThreads) {
-            const int row = c / (kD / 8), k = (c % (kD / 8)) * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r0 + row < R) v = *reinterpret_cast<const uint4 *>(q + ((int64_t)(r0 + row) * p.Hq + h) * kD + k);
-            *reinterpret_cast<uint4 *>(smem + kOffQ + sw128(kTileRows, row, k)) = v;
+        uint4 v[kQPer];
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) {
+            const int c = tid + i * kPThreads, row = c / (kD / 8), k = (c % (kD / 8)) * 8;
+            v[i] = make_uint4(0, 0, 0, 0);
+            if (c < kQChunks && row < nrows)
+                v[i] = *reinterpret_cast<const uint4 *>(q + ((int64_t)(r0 + row) * p.Hq + h) * kD + k);
+        }
+#pragma unroll
+        for (int i = 0; i < kQPer; ++i) {
+            const int c = tid + i * kPThreads, row = c / (kD / 8), k = (c % (kD / 8)) * 8;
+            if (c < kQChunks) *reinterpret_cast<uint4 *>(smem + kOffQ + sw128(kTileRows, row, k)) = v[i];
         }
     }
     proxy_fence();
     tc_before_sync();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers and Q tiles are ready before any remote arrival or MMA
     tc_after_sync();
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= 4 && warp < 8) {
         // ------------------------------------------------------------ producers
-        // Raw bytes of block j+1 are loaded into registers before the wait
-        // for block j's slot, so their latency hides behind the pipeline.
+        // K: thread pt owns key row kr = pt % 64 of this CTA's half of the block
+        // (keys rank * 64 + kr) and dims blocks kb0 .. kb0 + 3, kb0 = (pt / 64) * 4.
+        // V: this CTA dequantises dims rank * 128 .. + 127, i.e. scale blocks
+        // rank * 4 .. + 3; thread pt owns 32-key chunk vc of block vb and its byte
+        // rows vq, vq + 8 (dims vb * 32 + row and + 16), so its 32 scales sit in
+        // its own registers; lanes differ in vq, which keeps every 16-byte store
+        // of a warp phase on its own banks under the swizzle.  Raw bytes of the
+        // next block are loaded into registers ahead of the waits for its stage.
         const int pt = tid - 128;  // 0..127
-        uint2 rk[16], rv[8];
-        __half sk[16];
-        uint4 sv[8];
+        const int kr = pt & 63, kb0 = (pt >> 6) * 4;
+        const int vbl = pt >> 5, vb = (int)rank * 4 + vbl, vc = (pt >> 3) & 3, vq = pt & 7;
+        uint4 rk[8], rv[4], sv[4];
+        uint2 sk;
         auto load_k = [&](int j) {
-            const uint8_t *hb = page_base(j);
-            const int kb = (j % bpp) * kBN;
-            const __half *ks = reinterpret_cast<const __half *>(hb + p.geom.ks_off);
+            const int ks = j * kBN + (int)rank * kHalfN + kr;
+            if (ks < n_keys) {
+                const uint8_t *hb = head_of(ks);
+                const int t = ks % P;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
-                rk[i] = *reinterpret_cast<const uint2 *>(hb + kq_byte(kb + key, k, kD / 32));
-                sk[i] = ks[(kb + key) * (kD / 32) + (k >> 5)];
+                for (int b = 0; b < 4; ++b) {
+                    const uint4 *line = reinterpret_cast<const uint4 *>(hb + kq_byte(t, (kb0 + b) * 32, kNB));
+                    rk[2 * b] = line[0];
+                    rk[2 * b + 1] = line[1];
+                }
+                sk = *reinterpret_cast<const uint2 *>(hb + p.geom.ks_off + ((int64_t)t * kNB + kb0) * 2);
+            } else {  // beyond the split: zero keys (masked by the softmax)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rk[i] = make_uint4(0, 0, 0, 0);
+                sk = make_uint2(0, 0);
             }
         };
         auto load_v = [&](int j) {
-            const uint8_t *hb = page_base(j);
-            const int kb = (j % bpp) * kBN;
-            const __half *vs = reinterpret_cast<const __half *>(hb + p.geom.vs_off);
+            const int ks = j * kBN + 32 * vc;  // a 32-key chunk never straddles a page (P % 64 == 0)
+            if (ks < n_keys) {
+                const uint8_t *hb = head_of(ks);
+                const uint8_t *line0 = hb + p.geom.vq_off + vq_byte(ks % P, vb * 16 + vq, kNB);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
-                rv[i] = *reinterpret_cast<const uint2 *>(hb + p.geom.vq_off + vq_byte(kb + k8, br, kD / 32));
-                sv[i] = *reinterpret_cast<const uint4 *>(vs + (br >> 4) * P + kb + k8);
-            }
-        };
-        // K of block j+1 needs only S_j finished, V of block j needs PV_{j-1}
-        // finished; S_j runs before PV_{j-1}, so K goes first.
-        auto write_k = [&](int j) {
-            const int kb = (j % bpp) * kBN;
-            (void)kb;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = pt + 128 * i, key = c >> 5, k = (c & 31) * 8;
-                const __half2 d2 = __halves2half2(sk[i], sk[i]);
-                const uint32_t d = *reinterpret_cast<const uint32_t *>(&d2);
-                uint32_t x[4], hi[4], lo[4];
-                i8x4_to_f16(rk[i].x, x[0], x[1]);
-                i8x4_to_f16(rk[i].y, x[2], x[3]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mul_split(x[e], d, hi[e], lo[e]);
-                const uint32_t off = sw128(kBN, key, k);
-                *reinterpret_cast<uint4 *>(smem + kOffKh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(smem + kOffKl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            proxy_fence();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarKFull));
-        };
-        // V: 128 byte rows (dim pairs) x 8 chunks of 8 keys -> [dim][key] tiles
-        auto write_v = [&]() {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int pc = pt + 128 * i, br = pc >> 3, k8 = (pc & 7) * 8;
-                const int dA = (br >> 4) * 32 + (br & 15), dB = dA + 16;
-                const uint32_t w[2] = {rv[i].x, rv[i].y};
-                const uint32_t dv[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};  // (k, k+1) scale pairs
-                uint32_t ah[4], al[4], bh[4], bl[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    // keys 2e, 2e+1: bytes 2(e%2), 2(e%2)+1 of w[e/2], one per f16 half
-                    uint32_t sp;
-                    const uint32_t sel = (e & 1) ? 0x7372u : 0x7170u;
-                    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(sp) : "r"(w[e >> 1]), "r"(0u), "r"(sel));
-                    uint32_t lo_n, hi_n, xa, xb;
-                    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(lo_n) : "r"(sp), "r"(0x000f000fu), "r"(0x64006400u));
-                    asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(hi_n) : "r"(sp >> 4), "r"(0x000f000fu), "r"(0x64006400u));
-                    asm("sub.f16x2 %0, %1, %2;" : "=r"(xa) : "r"(lo_n), "r"(0x64086408u));  // code - 8
-                    asm("sub.f16x2 %0, %1, %2;" : "=r"(xb) : "r"(hi_n), "r"(0x64086408u));
-                    mul_split(xa, dv[e], ah[e], al[e]);
-                    mul_split(xb, dv[e], bh[e], bl[e]);
+                for (int i = 0; i < 2; ++i) {  // byte rows vq + 8 i: lines 8 i apart
+                    rv[2 * i] = reinterpret_cast<const uint4 *>(line0 + i * 256)[0];
+                    rv[2 * i + 1] = reinterpret_cast<const uint4 *>(line0 + i * 256)[1];
                 }
-                const uint32_t oa = sw128(kD, dA, k8), ob = sw128(kD, dB, k8);
-                *reinterpret_cast<uint4 *>(smem + kOffVh + oa) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
-                *reinterpret_cast<uint4 *>(smem + kOffVl + oa) = make_uint4(al[0], al[1], al[2], al[3]);
-                *reinterpret_cast<uint4 *>(smem + kOffVh + ob) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-                *reinterpret_cast<uint4 *>(smem + kOffVl + ob) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+                const uint4 *sc = reinterpret_cast<const uint4 *>(hb + p.geom.vs_off + ((int64_t)vb * P + ks % P) * 2);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sv[i] = sc[i];
+            } else {  // beyond the split: code 8 = value 0
+#pragma unroll
+                for (int i = 0; i < 4; ++i) rv[i] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sv[i] = make_uint4(0, 0, 0, 0);
+            }
+        };
+        auto write_k = [&](int stage) {
+            uint8_t *kt = smem + kOffK + stage * kKBytes;
+            const uint32_t sc[2] = {sk.x, sk.y};  // scale pairs (blocks kb0 + 2i, kb0 + 2i + 1)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                uint32_t d;  // scale of block kb0 + b in both halves
+                asm("prmt.b32 %0, %1, %1, %2;" : "=r"(d) : "r"(sc[b >> 1]), "r"((b & 1) ? 0x3232u : 0x1010u));
+                const uint32_t w[8] = {rk[2 * b].x,     rk[2 * b].y,     rk[2 * b].z,     rk[2 * b].w,
+                                       rk[2 * b + 1].x, rk[2 * b + 1].y, rk[2 * b + 1].z, rk[2 * b + 1].w};
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t x0, x1;
+                    i8x4_to_f16(w[i], x0, x1);
+                    o[2 * i] = hmul2(x0, d);
+                    o[2 * i + 1] = hmul2(x1, d);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    *reinterpret_cast<uint4 *>(kt + sw128(kHalfN, kr, (kb0 + b) * 32 + 8 * m)) =
+                        make_uint4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
             }
             proxy_fence();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarVFull));
+            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarKFull + stage));
         };
+        auto write_v = [&](int stage) {
+            uint8_t *vt = smem + kOffV + stage * kVBytes;
+            const uint32_t d2[16] = {sv[0].x, sv[0].y, sv[0].z, sv[0].w, sv[1].x, sv[1].y, sv[1].z, sv[1].w,
+                                     sv[2].x, sv[2].y, sv[2].z, sv[2].w, sv[3].x, sv[3].y, sv[3].z, sv[3].w};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int rA = vbl * 32 + vq + 8 * i, rB = rA + 16;  // rows of this CTA's V tile (dims - rank * 128)
+                const uint32_t w[8] = {rv[2 * i].x,     rv[2 * i].y,     rv[2 * i].z,     rv[2 * i].w,
+                                       rv[2 * i + 1].x, rv[2 * i + 1].y, rv[2 * i + 1].z, rv[2 * i + 1].w};
+                uint32_t oa[16], ob[16];
+#pragma unroll
+                for (int k2 = 0; k2 < 16; ++k2) {  // keys 2 k2, 2 k2 + 1 of the chunk; d2[k2] holds their scales
+                    uint32_t lo, hi;
+                    u4x2_pair(w[k2 >> 1], (k2 & 1) ? 0x4342u : 0x4140u, lo, hi);
+                    oa[k2] = hmul2(lo, d2[k2]);
+                    ob[k2] = hmul2(hi, d2[k2]);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    *reinterpret_cast<uint4 *>(vt + sw128(kHalfD, rA, 32 * vc + 8 * m)) =
+                        make_uint4(oa[4 * m], oa[4 * m + 1], oa[4 * m + 2], oa[4 * m + 3]);
+                    *reinterpret_cast<uint4 *>(vt + sw128(kHalfD, rB, 32 * vc + 8 * m)) =
+                        make_uint4(ob[4 * m], ob[4 * m + 1], ob[4 * m + 2], ob[4 * m + 3]);
+                }
+            }
+            proxy_fence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarVFull + stage));
+        };
+        // block j goes to stage j & 1: K_j once S_{j-2} is done with that stage,
+        // V_j once PV_{j-2} is
         if (nblk > 0) {
             load_k(0);
             load_v(0);
-            write_k(0);
-            if (nblk > 1) load_k(1);
         }
         for (int j = 0; j < nblk; ++j) {  // every exit is a warp-uniform wait outcome
-            if (j + 1 < nblk) {
-                if (!mbar_wait_warp(bar(kBarKEmpty), (uint32_t)(j & 1), abort)) break;  // S_j done
-                write_k(j + 1);
-                if (j + 2 < nblk) load_k(j + 2);
-            }
-            if (j >= 1 && !mbar_wait_warp(bar(kBarODone + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort))
-                break;  // PV_{j-1} done
-            write_v();
+            const int st = j & 1;
+            if (j >= 2 && !mbar_wait_warp(bar(kBarKEmpty + st), (uint32_t)(((j - 2) >> 1) & 1), abort)) break;
+            write_k(st);
+            if (j + 1 < nblk) load_k(j + 1);
+            if (j >= 2 && !mbar_wait_warp(bar(kBarVEmpty + st), (uint32_t)(((j - 2) >> 1) & 1), abort)) break;
+            write_v(st);
             if (j + 1 < nblk) load_v(j + 1);
         }
     } else if (warp == 8) {
-        // ------------------------------------------------------------ MMA issue (one thread)
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issue (leader, one thread)
+        if (rank == 0 && lane == 0) {
             // descriptors of the tile bases; a k-step adds its byte offset / 16
-            const uint64_t dq = smem_desc(smem_u32(smem + kOffQ)), dkh = smem_desc(smem_u32(smem + kOffKh));
-            const uint64_t dkl = smem_desc(smem_u32(smem + kOffKl)), dvh = smem_desc(smem_u32(smem + kOffVh));
-            const uint64_t dvl = smem_desc(smem_u32(smem + kOffVl)), dp = smem_desc(smem_u32(smem + kOffP));
-            const uint32_t id_s = idesc_f16(kTileRows, kBN), id_o = idesc_f16(kTileRows, kD);
+            const uint64_t dq = smem_desc(smem_u32(smem + kOffQ)), dk = smem_desc(smem_u32(smem + kOffK));
+            const uint64_t dv = smem_desc(smem_u32(smem + kOffV)), dp = smem_desc(smem_u32(smem + kOffP));
+            const uint32_t id_s = idesc_f16(2 * kTileRows, kBN), id_o = idesc_f16(2 * kTileRows, kD);
             auto issue_s = [&](int j) {
-                const uint32_t ts = tmem + kColS + (uint32_t)((j & 1) * kBN);
+                const uint32_t ts = tmem + (uint32_t)((j & 1) * kBN);
+                const uint64_t dkj = dk + (uint64_t)(((j & 1) * kKBytes) >> 4);
 #pragma unroll
-                for (int s = 0; s < kD / 16; ++s) {
-                    const uint32_t ao = ((s >> 2) * (kTileRows * 128) + (s & 3) * 32) >> 4;
-                    const uint32_t bo = ((s >> 2) * (kBN * 128) + (s & 3) * 32) >> 4;
-                    mma_f16(ts, dq + ao, dkh + bo, id_s, s > 0);
-                    mma_f16(ts, dq + ao, dkl + bo, id_s, 1);
+                for (int s = 0; s < kD / 16; ++s) {  // 16 dims per k-step, 64 per swizzle atom
+                    const uint64_t aq = (uint64_t)(((s >> 2) * (kTileRows * 128) + (s & 3) * 32) >> 4);
+                    const uint64_t bk = (uint64_t)(((s >> 2) * (kHalfN * 128) + (s & 3) * 32) >> 4);
+                    mma_pair(ts, dq + aq, dkj + bk, id_s, s > 0);
                 }
-                mma_commit(bar(kBarSFull + (j & 1)));
-                mma_commit(bar(kBarKEmpty));
+                mma_commit_both(bar(kBarSFull + (j & 1)));
+                mma_commit_both(bar(kBarKEmpty + (j & 1)));
+            };
+            auto issue_pv = [&](int j) {
+                const uint64_t dvj = dv + (uint64_t)(((j & 1) * kVBytes) >> 4);
+#pragma unroll
+                for (int s = 0; s < kBN / 16; ++s) {  // 16 keys per k-step, 64 per swizzle atom
+                    const uint64_t ap = (uint64_t)(((s >> 2) * (kTileRows * 128) + (s & 3) * 32) >> 4);
+                    const uint64_t bv = (uint64_t)(((s >> 2) * (kHalfD * 128) + (s & 3) * 32) >> 4);
+                    mma_pair(tmem + kColO, dp + ap, dvj + bv, id_o, (j > 0 || s > 0) ? 1u : 0u);
+                }
+                mma_commit_both(bar(kBarVEmpty + (j & 1)));
+                mma_commit_both(bar(kBarODone));
             };
             bool ok = true;
-            if (nblk > 0) {
-                ok = mbar_wait(bar(kBarKFull), 0u, abort);
-                if (ok) {
-                    tc_after_sync();
-                    issue_s(0);
-                }
-            }
             for (int j = 0; j < nblk && ok; ++j) {
-                if (j + 1 < nblk) {
-                    ok = mbar_wait(bar(kBarKFull), (uint32_t)((j + 1) & 1), abort);
-                    if (ok && j + 1 >= 2) ok = mbar_wait(bar(kBarSEmpty + ((j + 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
-                    if (!ok) break;
-                    tc_after_sync();
-                    issue_s(j + 1);
-                }
-                ok = mbar_wait(bar(kBarPFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort) &&
-                     mbar_wait(bar(kBarVFull), (uint32_t)(j & 1), abort);
+                ok = mbar_wait(bar(kBarKFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort);
+                if (ok && j >= 2) ok = mbar_wait(bar(kBarSEmpty + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort);
                 if (!ok) break;
                 tc_after_sync();
-                const uint64_t dpj = dp + (uint64_t)(((j & 1) * kPBytes) >> 4);
-#pragma unroll
-                for (int s = 0; s < kBN / 16; ++s) {
-                    mma_f16(tmem + kColO, dpj + (s * 32 >> 4), dvh + (s * 32 >> 4), id_o, (j > 0 || s > 0) ? 1u : 0u);
-                    mma_f16(tmem + kColO, dpj + (s * 32 >> 4), dvl + (s * 32 >> 4), id_o, 1);
+                issue_s(j);
+                if (j >= 1) {
+                    ok = mbar_wait(bar(kBarPFull), (uint32_t)((j - 1) & 1), abort) &&
+                         mbar_wait(bar(kBarVFull + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
+                    if (!ok) break;
+                    tc_after_sync();
+                    issue_pv(j - 1);
                 }
-                mma_commit(bar(kBarODone + (j & 1)));
             }
-            // every MMA this thread issued has finished before TMEM is read or freed
-            mma_commit(bar(kBarFinal));
-            volatile int no_abort = 0;
-            mbar_wait(bar(kBarFinal), 0u, &no_abort);
+            if (ok && nblk > 0) {
+                ok = mbar_wait(bar(kBarPFull), (uint32_t)((nblk - 1) & 1), abort) &&
+                     mbar_wait(bar(kBarVFull + ((nblk - 1) & 1)), (uint32_t)(((nblk - 1) >> 1) & 1), abort);
+                if (ok) {
+                    tc_after_sync();
+                    issue_pv(nblk - 1);
+                }
+            }
+            if (!ok) raise_abort();
+            // every MMA of the pair has finished before either CTA reads or frees TMEM
+            mma_commit_both(bar(kBarFinal));
         }
     } else {
         // ------------------------------------------------------------ softmax rows (warps 0-3)
         const int row = tid;
         const long long qpos = p.pos0 + r0 + row;
-        const bool row_valid = r0 + row < R;
+        const bool row_valid = row < nrows;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         float m_used = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < nblk && ok; ++j) {
-            const long long kpos0 = (long long)p.page[it0 + j / bpp] * P + (j % bpp) * kBN;
             ok = mbar_wait_warp(bar(kBarSFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort);
             if (!ok) break;
             tc_after_sync();
             float s[kBN];
             {
-                float t32[32];
-                const uint32_t ta = lane_base + kColS + (uint32_t)((j & 1) * kBN);
-                tmem_ld32(ta, t32);
+                const uint32_t ta = lane_base + (uint32_t)((j & 1) * kBN);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[i] = t32[i];
-                tmem_ld32(ta + 32, t32);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[32 + i] = t32[i];
+                for (int c = 0; c < kBN; c += 32) tmem_ld32_nowait(ta + c, s + c);
+                tmem_wait_ld();
             }
             tc_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarSEmpty + (j & 1)));
-            // causal mask only where the block reaches past this row (keys i > lim)
-            const long long lim64 = row_valid ? qpos - kpos0 : -1;
-            if (lim64 < kBN - 1) {
-                const int lim = (int)(lim64 < -1 ? -1 : lim64);
+            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarSEmpty + (j & 1)));
+            // keys i > lim are masked: after this row's position, or beyond the split
+            {
+                const long long kpos = key_pos0 + (long long)j * kBN;
+                long long lim64 = row_valid ? qpos - kpos : -1;
+                const int in_split = n_keys - j * kBN - 1;
+                if (lim64 > in_split) lim64 = in_split;
+                if (lim64 < kBN - 1) {
+                    const int lim = (int)(lim64 < -1 ? -1 : lim64);
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
+                    for (int i = 0; i < kBN; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
+                }
             }
             // raw-score max in four independent chains; scale > 0 keeps the order
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -476,16 +589,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                 pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
             }
             l_sum += (b4[0] + b4[1]) + (b4[2] + b4[3]);
-            // a rescale of O needs PV_{j-1} done; P buffer j & 1 needs PV_{j-2} done
-            if (j >= 1 && __any_sync(0xffffffffu, need_rescale)) {
-                ok = mbar_wait_warp(bar(kBarODone + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
+            // PV_{j-1} done: the P buffer is free and O may be rescaled
+            if (j >= 1) {
+                ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort);
                 if (!ok) break;
                 tc_after_sync();
-                {
+                if (__any_sync(0xffffffffu, need_rescale)) {
                     const uint32_t ta = lane_base + kColO;
+#pragma unroll 1
                     for (int c = 0; c < kD; c += 32) {
                         float v[32];
-                        tmem_ld32(ta + c, v);
+                        tmem_ld32_nowait(ta + c, v);
+                        tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] *= alpha;
                         tmem_st32(ta + c, v);
@@ -493,11 +608,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
             }
-            if (j >= 2) {
-                ok = mbar_wait_warp(bar(kBarODone + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort);
-                if (!ok) break;
-            }
-            uint8_t *pbuf = smem + kOffP + (j & 1) * kPBytes;
+            uint8_t *pbuf = smem + kOffP;
 #pragma unroll
             for (int c8 = 0; c8 < kBN / 8; ++c8)
                 *reinterpret_cast<uint4 *>(pbuf + sw128(kTileRows, row, c8 * 8)) =
@@ -505,18 +616,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             proxy_fence();
             tc_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBarPFull + (j & 1)));
+            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarPFull));
         }
         // the last PV, then the partial: unnormalised O, m (log2 units), l
-        if (ok && nblk > 0)
-            ok = mbar_wait_warp(bar(kBarODone + ((nblk - 1) & 1)), (uint32_t)(((nblk - 1) >> 1) & 1), abort);
+        if (ok && nblk > 0) ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((nblk - 1) & 1), abort);
         if (ok) {
             tc_after_sync();
             const uint32_t ta = lane_base + kColO;
             const int64_t base = (((int64_t)split * p.Hq + h) * R + (r0 + row));
             float v[32];
+#pragma unroll 1
             for (int c = 0; c < kD; c += 32) {
-                if (nblk > 0) tmem_ld32(ta + c, v);
+                if (nblk > 0) {
+                    tmem_ld32_nowait(ta + c, v);
+                    tmem_wait_ld();
+                }
                 if (row_valid) {
                     float *dst = p.part_o + base * kD + c;
 #pragma unroll
@@ -531,11 +645,22 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_kernel(const __grid_cons
             }
         }
     }
+    // A role that gave up tells the peer CTA, so that its waits end too.
+    if (lane == 0 && *abort) raise_abort();
+    // Both CTAs wait for the pair's last MMA before either may exit or free
+    // tensor memory: an MMA in flight reads both CTAs' shared memory.  The
+    // leader commits Final on every path, so this wait (bounded, and not cut
+    // short by an abort) always ends.
+    if (tid == 0) {
+        volatile int no_abort = 0;
+        if (!mbar_wait(bar(kBarFinal), 0u, &no_abort)) *abort = 1;
+    }
     tc_before_sync();
     __syncthreads();
+    cluster_sync();
     tc_after_sync();
     if (tid == 0 && *abort) atomicExch(p.status, 1);
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
 }  // namespace
@@ -544,14 +669,17 @@ int prefill_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t s) {
     if (p.geom.D != kD || p.n_splits < 1 || p.n_splits > kMaxPrefillSplits || p.R < 1 || p.R > 256 ||
-        p.geom.P % kBN != 0)
+        p.geom.P % 64 != 0)
         return cudaErrorInvalidValue;
+    for (int i = 0; i < p.n_splits; ++i)
+        if (p.split_begin[i + 1] - p.split_begin[i] > kMaxPrefillSplitPages) return cudaErrorInvalidValue;
     {
         cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(prefill_kernel), kSmemBytes);
         if (e != cudaSuccess) return e;
     }
     const int rt = (p.R + kTileRows - 1) / kTileRows;
-    dim3 grid(p.n_splits, p.geom.Hk * p.G * rt);
+    const int npairs = (p.G * rt + 1) / 2;
+    dim3 grid(p.geom.Hk * 2 * npairs, p.n_splits);  // clusters of 2 along x
     prefill_kernel<<<grid, kPThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -619,6 +619,7 @@ constexpr uint64_t kStatusBytes = 256;  // device status word at the start of th
 
 uint64_t prefill_split_of(const kvs_config *cfg) {
     uint64_t sp = cfg->prefill_split_pages ? cfg->prefill_split_pages : 8;
+    sp = std::min<uint64_t>(sp, (uint64_t)kvs::kMaxPrefillSplitPages);
     const uint64_t ring = cfg->ring_slots ? cfg->ring_slots : 1;
     return std::max<uint64_t>(1, std::min(sp, ring));
 }

@@ -122,8 +122,9 @@ typedef struct {
     void *lane_attn_streams[7];  /* cudaStream_t of attention lanes 1 .. n_lanes-1 */
     void *lane_copy_streams[7];  /* cudaStream_t of copy lanes 1 .. n_lanes-1 */
     uint32_t prefill_split_pages; /* pages per split of the tensor-core prefill path (0 = 8,
-                                     at most ring_slots); when max_q_head * max_rows allows
-                                     that path, ring chunks never cross a split */
+                                     at most ring_slots and at most 128); when max_q_head *
+                                     max_rows allows that path, ring chunks never cross a
+                                     split */
 } kvs_config;
 
 typedef struct {

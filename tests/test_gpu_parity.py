@@ -478,9 +478,9 @@ def test_step_graph_replay_matches_eager_bitwise():
 
 # ------------------------------------------------------------ tensor-core prefill
 
-def _prefill_case(R, T, mask_fn=None, ring=8, chunk=2, lanes=1, split=8, seed=SEED):
+def _prefill_case(R, T, mask_fn=None, ring=8, chunk=2, lanes=1, split=8, seed=SEED, P=256):
     import torch
-    P, Hk, G, D = 256, 4, 6, 256
+    Hk, G, D = 4, 6, 256
     Hq = G * Hk
     st = kvs.KVStream(page_tokens=P, n_layers=1, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
                       max_tokens=T, ring_slots=ring, chunk_pages=chunk, lanes=lanes,
@@ -500,6 +500,19 @@ def test_prefill_tensor_core_parity(R, T):
     ro, rl = oracle_ref(k, v, q, T - R, 1 / 16)
     check_parity(out, lse, ro, rl)
     assert st.stats()["h2d_pages"] == 0
+
+
+@pytest.mark.parametrize("P,R,T,split,ring", [(64, 256, 64 * 13 + 17, 3, 4), (64, 200, 64 * 9, 2, 2),
+                                               (128, 130, 128 * 7 + 50, 2, 4)])
+def test_prefill_small_pages_and_ragged_splits(P, R, T, split, ring):
+    """Pages of 64 and 128 tokens: a 128-key block of the tensor-core kernel
+    spans two pages, and with an odd number of 64-token pages per split it
+    runs past the split's end (those keys are masked); half the pages stream."""
+    st, k, v, q, out, lse = _prefill_case(R, T, mask_fn=lambda n: (np.arange(n) % 2 == 0).astype(np.uint8),
+                                          ring=ring, chunk=1, split=split, P=P)
+    ro, rl = oracle_ref(k, v, q, T - R, 1 / 16)
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] > 0
 
 
 def test_prefill_streamed_equals_resident_bitwise():
