@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     const int head_bytes = (int)p.geom.head_bytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    const int G = p.G, R = p.R, rows = G * R;
+    // this launch serves query rows row0 .. row0 + Rg - 1 of the call's R rows
+    const int G = p.G, R = p.R, rows = G * p.Rg, row0 = p.row0;
     const int T = p.tile_mode ? p.run_tiles : 1;
     const int U = p.n_items * p.geom.Hk * T;
     const int u0 = (int)((int64_t)blockIdx.x * U / gridDim.x), u1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
@@ -234,9 +235,9 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     // `pend_parity`: the phase that load completes
     uint32_t pending = 0u, pend_parity = 0u;
     for (int s = 0; s < S && u0 + s < u1; ++s) pending |= 1u << (2 * s);
-    // rows x heads m (< 64): x = its query row r = m / G, y = h_local * R + r with
-    // h_local = m % G; the partial of kv head g sits at row g * G * R + y
-    for (int m = threadIdx.x; m < 64; m += NTH) rowtab[m] = make_int2(m / G, (m % G) * R + m / G);
+    // rows x heads m (< 64): x = its query row r = row0 + m / G, y = h_local * R + r
+    // with h_local = m % G; the partial of kv head g sits at row g * G * R + y
+    for (int m = threadIdx.x; m < 64; m += NTH) rowtab[m] = make_int2(row0 + m / G, (m % G) * R + row0 + m / G);
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2 * S; ++s) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 16 * s));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -581,7 +582,7 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
     asm volatile("griddepcontrol.wait;" ::: "memory");            // q and the previous readers of qf
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // attention may be scheduled
     constexpr int KS = D / 16;
-    const int g = blockIdx.x, nt = blockIdx.y, G = p.G, rows = G * p.R;
+    const int g = blockIdx.x, nt = blockIdx.y, G = p.G, rows = G * p.Rg;
     uint4 *qf = const_cast<uint4 *>(p.qf) + ((int64_t)g * NT + nt) * KS * 32;
     for (int e = threadIdx.x; e < KS * 32; e += kThreads) {
         const int ln = e & 31, ks = e >> 5;
@@ -589,7 +590,7 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
         const int d0 = 32 * (ks >> 1) + 8 * (ln & 3) + 4 * (ks & 1);
         float x[4] = {0.f, 0.f, 0.f, 0.f};
         if (m < rows) {
-            const int r = m / G, h = g * G + (m - r * G);
+            const int rl = m / G, r = p.row0 + rl, h = g * G + (m - rl * G);
             const int64_t off = ((int64_t)r * p.Hq + h) * D + d0;
             if (p.q_f16) {
                 const uint2 raw = *reinterpret_cast<const uint2 *>(reinterpret_cast<const __half *>(p.q) + off);
@@ -786,8 +787,8 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const Combi
 int decode_max_mma_rows() { return 64; }
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s) {
-    const int rows = p.G * p.R;
-    if (rows < 1 || rows > 64 || (p.n_items < 1 && !p.prep_q) || p.n_items > kMaxItems) return cudaErrorInvalidValue;
+    const int rows = p.G * p.Rg;
+    if (rows < 1 || rows > 64 || p.row0 < 0 || p.row0 + p.Rg > p.R || (p.n_items < 1 && !p.prep_q) || p.n_items > kMaxItems) return cudaErrorInvalidValue;
     if (p.tile_mode && p.prep_q) return cudaErrorInvalidValue;
     const int nt = (rows + 7) / 8;
     DecodeParams q = p;

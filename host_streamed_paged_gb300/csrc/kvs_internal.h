@@ -58,7 +58,9 @@ struct DecodeParams {
     float *part_o;         // [split][Hq][R][D]   split = logical page
     float *part_ml;        // [split][Hq][R][2]   (max in log2 units, sum)
     int *status;           // set to 1 if a bounded device wait timed out
-    int R, Hq, G;
+    int R, Hq, G;          // R: query rows of the call (the partials' row stride)
+    int row0, Rg;          // this launch's row group: query rows row0 .. row0 + Rg - 1
+                           // (G * Rg <= 64 MMA rows; a call wider than that runs as groups)
     long long pos0;
     float scale_log2;      // scale * log2(e)
     int stages;            // shared-memory stages (set by launch_decode)

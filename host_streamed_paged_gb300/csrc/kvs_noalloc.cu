@@ -148,6 +148,8 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
     dp.part_o = reinterpret_cast<float *>(qf_area + qfrag);
     dp.part_ml = dp.part_o + n_split * per_split * D;
     dp.R = (int)n_rows;
+    dp.row0 = 0;
+    dp.Rg = (int)n_rows;  // one row group: G * n_rows <= 64
     dp.Hq = (int)n_q_head;
     dp.G = (int)(n_q_head / Hk);
     dp.pos0 = (long long)pos0;

@@ -92,6 +92,8 @@ struct kvs_ctx {
     int64_t max_pages = 0;
     int64_t prefill_split = 8;  // pages per tensor-core prefill split
     bool split_chunks = false;  // ring chunks stop at prefill split boundaries (prefill-capable context)
+    uint32_t verify_rows = 1;   // widest split-K call (row groups beyond 64 rows x heads)
+    int64_t qfrag_groups = 1;   // query-fragment areas in the workspace (one per row group)
     bool check_status = false;  // a kernel with bounded device waits ran since the last kvs_sync
     std::vector<LayerState> layers;
 
@@ -617,6 +619,21 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
 
 constexpr uint64_t kStatusBytes = 256;  // device status word at the start of the workspace
 
+// the tensor-core prefill path serves fp16 queries at head_dim 256 with pages
+// of a multiple of 64 tokens
+bool prefill_geometry(uint32_t D, uint32_t P) { return D == 256 && P % 64 == 0; }
+
+// query rows per split-K row group (its MMA tile holds 64 rows x heads)
+uint32_t rows_per_group(uint32_t G) { return std::max<uint32_t>(1, (uint32_t)kvs::decode_max_mma_rows() / G); }
+
+// widest call the split-K kernel serves, as row groups (kvs_config.max_verify_rows)
+uint64_t verify_rows_of(const kvs_config *cfg) {
+    const uint32_t G = cfg->max_q_head / std::max<uint32_t>(1, cfg->n_kv_head);
+    if (cfg->max_verify_rows) return std::min<uint64_t>(cfg->max_verify_rows, cfg->max_rows);
+    if (prefill_geometry(cfg->head_dim, cfg->page_tokens)) return std::min<uint64_t>(cfg->max_rows, rows_per_group(G));
+    return cfg->max_rows;
+}
+
 uint64_t prefill_split_of(const kvs_config *cfg) {
     uint64_t sp = cfg->prefill_split_pages ? cfg->prefill_split_pages : 8;
     sp = std::min<uint64_t>(sp, (uint64_t)kvs::kMaxPrefillSplitPages);
@@ -642,14 +659,8 @@ bool geometry_ok(const kvs_config *cfg, std::string *why) {
         *why = "max_q_head must be a positive multiple of n_kv_head";
         return false;
     }
-    const uint32_t G = cfg->max_q_head / cfg->n_kv_head;
     if (cfg->max_rows < 1 || cfg->max_rows > 256) {
         *why = "max_rows must be in 1..256";
-        return false;
-    }
-    if (G * cfg->max_rows > (uint32_t)kvs::decode_max_mma_rows() && (D != 256 || P % 64 != 0)) {
-        *why = "more than 64 query rows per kv head (the tensor-core prefill path) needs head_dim 256 "
-               "and page_tokens a multiple of 64";
         return false;
     }
     if (cfg->k_type != KVS_TYPE_Q8_0 || cfg->v_type != KVS_TYPE_Q4_0) {
@@ -668,18 +679,26 @@ void sizes_of(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
     if (host_bytes) *host_bytes = (uint64_t)cfg->n_layers * max_pages * (uint64_t)g.page_bytes;
     if (arena_min) *arena_min = (2ull * cfg->n_layers + ring) * (uint64_t)g.page_bytes;
     if (ws_min) {
-        // decode / verify: one partial per page for Hq * R <= 64 * Hk query rows
-        const uint64_t dec_rows = std::min<uint64_t>((uint64_t)cfg->max_q_head * cfg->max_rows,
-                                                     64ull * cfg->n_kv_head);
+        // split-K (decode, verify, wide verify as row groups): one partial per page
+        // for every (row, head) of a call of up to max_verify_rows rows
+        // (any call within 64 rows x heads per kv head, and any row-group call)
+        const uint64_t vrows = verify_rows_of(cfg);
+        const uint64_t dec_rows = std::max<uint64_t>(
+            std::min<uint64_t>((uint64_t)cfg->max_q_head * cfg->max_rows, 64ull * cfg->n_kv_head),
+            (uint64_t)cfg->max_q_head * vrows);
         uint64_t need = max_pages * dec_rows * (uint64_t)(cfg->head_dim + 2) * 4ull;
         // prefill: one partial per split
-        if ((uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head) {
+        if ((uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head &&
+            prefill_geometry(cfg->head_dim, cfg->page_tokens)) {
             const uint64_t sp = prefill_split_of(cfg);
             const uint64_t splits = (max_pages + sp - 1) / sp;
             need = std::max<uint64_t>(need, splits * cfg->max_q_head * cfg->max_rows *
                                                 (uint64_t)(cfg->head_dim + 2) * 4ull);
         }
-        *ws_min = kStatusBytes + (uint64_t)kvs::qfrag_bytes((int)cfg->n_kv_head, (int)cfg->head_dim) + need;
+        // query fragments of every row group of the widest split-K call
+        const uint32_t G = cfg->max_q_head / cfg->n_kv_head;
+        const uint64_t groups = (vrows + rows_per_group(G) - 1) / rows_per_group(G);
+        *ws_min = kStatusBytes + groups * (uint64_t)kvs::qfrag_bytes((int)cfg->n_kv_head, (int)cfg->head_dim) + need;
     }
 }
 
@@ -768,7 +787,13 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
     }
     c->max_pages = (int64_t)((cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens);
     c->prefill_split = (int64_t)prefill_split_of(cfg);
-    c->split_chunks = (uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head;
+    c->split_chunks = (uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head &&
+                      prefill_geometry(cfg->head_dim, cfg->page_tokens);
+    c->verify_rows = (uint32_t)verify_rows_of(cfg);
+    {
+        const uint32_t G = cfg->max_q_head / cfg->n_kv_head;
+        c->qfrag_groups = (int64_t)((c->verify_rows + rows_per_group(G) - 1) / rows_per_group(G));
+    }
     c->layers.resize(cfg->n_layers);
     for (auto &L : c->layers) L.pool_slot.assign(c->max_pages, -1);
     c->n_slots = (int64_t)(cfg->arena_bytes / (uint64_t)c->geom.page_bytes);
@@ -1369,11 +1394,16 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         return fail(c, KVS_ERR_INVALID, "n_q_head must be a multiple of n_kv_head and <= max_q_head");
     const uint32_t G = n_q_head / c->geom.Hk;
     if (n_rows > c->cfg.max_rows) return fail(c, KVS_ERR_UNSUPPORTED, "n_rows beyond max_rows");
-    const bool prefill = G * n_rows > (uint32_t)kvs::decode_max_mma_rows();
-    if (prefill && (q_dtype != KVS_F16 || c->geom.D != 256 || c->geom.P % 64 != 0))
+    // more than 64 (row x head) per kv head: fp16 queries on a prefill-capable
+    // geometry take the tensor-core path; any other call runs on the split-K
+    // kernel as consecutive row groups, each group reading every staged span
+    // before its ring slots are released
+    const bool wide = G * n_rows > (uint32_t)kvs::decode_max_mma_rows();
+    const bool prefill = wide && q_dtype == KVS_F16 && prefill_geometry(c->geom.D, c->geom.P);
+    if (wide && !prefill && n_rows > c->verify_rows)
         return fail(c, KVS_ERR_UNSUPPORTED,
-                    "more than 64 query rows per kv head run on the tensor-core prefill path, which needs fp16 "
-                    "queries, head_dim 256 and page_tokens a multiple of 64");
+                    "a split-K call wider than 64 rows x heads per kv head needs n_rows <= max_verify_rows "
+                    "(the workspace is sized for that many rows)");
     LayerState &L = c->layers[layer];
     if (pos0 + n_rows > L.T) return fail(c, KVS_ERR_CAPACITY, "rows beyond the appended length");
     if (!c->plan_only && (!q_dev || !out_dev)) return fail(c, KVS_ERR_INVALID, "null q or out");
@@ -1411,7 +1441,8 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
 
     const size_t per_split = (size_t)n_q_head * n_rows;
     uint8_t *qfrag = static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes;
-    float *part_o = reinterpret_cast<float *>(qfrag + kvs::qfrag_bytes(c->geom.Hk, c->geom.D));
+    const int64_t qf_bytes = kvs::qfrag_bytes(c->geom.Hk, c->geom.D);
+    float *part_o = reinterpret_cast<float *>(qfrag + c->qfrag_groups * qf_bytes);
     const int64_t n_partials = prefill ? (c->max_pages + c->prefill_split - 1) / c->prefill_split : c->max_pages;
     float *part_ml = part_o + (size_t)n_partials * per_split * c->geom.D;
     c->st.attend_calls++;
@@ -1437,17 +1468,30 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         dp.scale_log2 = scale * 1.4426950408889634f;
         if (c->fault == KVS_FAULT_DEVICE_WAIT && c->fault_nth && ++c->fault_count == c->fault_nth)
             dp.give_up_waits = 1;
+        // row groups: query rows row0 .. row0 + Rg - 1, G * Rg <= 64, each with its
+        // own query fragments
+        const uint32_t rpg = rows_per_group(G);
+        std::vector<kvs::DecodeParams> groups;
+        for (uint32_t r0 = 0; r0 < n_rows; r0 += rpg) {
+            kvs::DecodeParams gp = dp;
+            gp.row0 = (int)r0;
+            gp.Rg = (int)std::min(rpg, n_rows - r0);
+            gp.qf = reinterpret_cast<const uint4 *>(qfrag + (int64_t)groups.size() * qf_bytes);
+            groups.push_back(gp);
+        }
 
-        // Q fragments for every kv head, once per call (primary attention stream)
-        c->st.kernel_launches++;
-        if (c->plan_only) {
-            log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 4, c->geom.Hk);
-        } else {
-            dp.prep_q = 1;
-            dp.n_items = 0;
-            cudaError_t e = kvs::launch_decode(dp, c->attn);
-            if (e != cudaSuccess) return cuda_fail(c, e, "query fragment launch");
-            dp.prep_q = 0;
+        // Q fragments for every kv head and row group, once per call (primary attention stream)
+        for (kvs::DecodeParams &gp : groups) {
+            c->st.kernel_launches++;
+            if (c->plan_only) {
+                log_op(c, KVS_OP_LAUNCH, kAttn, layer, 0, 4, c->geom.Hk);
+            } else {
+                gp.prep_q = 1;
+                gp.n_items = 0;
+                cudaError_t e = kvs::launch_decode(gp, c->attn);
+                if (e != cudaSuccess) return cuda_fail(c, e, "query fragment launch");
+                gp.prep_q = 0;
+            }
         }
         // other lanes start after this call's inputs (Q and its fragments, the
         // previous combine's reads of the partials, published pages) are in place
@@ -1468,9 +1512,13 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
                     (int64_t)c->n_lanes * c->chunk_pages * c->geom.Hk * ((G * n_rows + 7) / 8);
                 dp.reserve_sms = (int)std::min<int64_t>(1 << 20, (ring_ctas + 1) / 2);
             }
-            s = launch_items(c, layer, res_pages, res_slots, dp, KVS_TIME_RESIDENT, sid);
+            for (kvs::DecodeParams &gp : groups) {
+                gp.reserve_sms = dp.reserve_sms;
+                s = launch_items(c, layer, res_pages, res_slots, gp, KVS_TIME_RESIDENT, sid);
+                gp.reserve_sms = 0;
+                if (s != KVS_OK) return s;
+            }
             dp.reserve_sms = 0;
-            if (s != KVS_OK) return s;
             c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
         }
         // ring chunks in order: ready fence, read, consumed fence, refill
@@ -1493,8 +1541,11 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
                 sl.push_back(c->ring_slot_id(ch.seq0 + i));
             }
             if (!pg.empty()) {
-                s = launch_items(c, layer, pg, sl, dp, KVS_TIME_RING, sid);
-                if (s != KVS_OK) return s;
+                // every row group reads the chunk before its consumed fence
+                for (kvs::DecodeParams &gp : groups) {
+                    s = launch_items(c, layer, pg, sl, gp, KVS_TIME_RING, sid);
+                    if (s != KVS_OK) return s;
+                }
                 c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
             }
             c->chunk_reader_sid[ch.id % c->ring_n] = sid;

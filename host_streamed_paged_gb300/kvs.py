@@ -66,6 +66,7 @@ class kvs_config(ctypes.Structure):
         ("lane_attn_streams", ctypes.c_void_p * 7),
         ("lane_copy_streams", ctypes.c_void_p * 7),
         ("prefill_split_pages", ctypes.c_uint32),
+        ("max_verify_rows", ctypes.c_uint32),
     ]
 
 
@@ -388,7 +389,7 @@ class KVStream:
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
                  max_tokens, ring_slots=8, chunk_pages=0, arena_slots=None, arena_bytes=None,
                  plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None,
-                 prefill_split_pages=0, dma_fill=False, host_alloc="pinned"):
+                 prefill_split_pages=0, dma_fill=False, host_alloc="pinned", max_verify_rows=0):
         cfg = kvs_config()
         cfg.page_tokens, cfg.n_layers, cfg.n_kv_head, cfg.head_dim = page_tokens, n_layers, n_kv_head, head_dim
         cfg.max_q_head, cfg.max_rows, cfg.max_tokens = max_q_head, max_rows, max_tokens
@@ -396,6 +397,7 @@ class KVStream:
         cfg.ring_slots, cfg.chunk_pages = ring_slots, chunk_pages
         cfg.n_lanes = lanes
         cfg.prefill_split_pages = prefill_split_pages
+        cfg.max_verify_rows = max_verify_rows
         cfg.flags = KVS_FLAG_DMA_FILL if dma_fill else 0
         self.page_bytes, host_bytes, arena_min, ws_bytes = kvs_query_sizes(cfg)
         self.max_pages = math.ceil(max_tokens / page_tokens)

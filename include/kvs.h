@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define KVS_ABI_VERSION 2
+#define KVS_ABI_VERSION 3
 
 typedef struct kvs_ctx kvs_ctx;
 
@@ -125,6 +125,11 @@ typedef struct {
                                      at most ring_slots and at most 128); when max_q_head *
                                      max_rows allows that path, ring chunks never cross a
                                      split */
+    uint32_t max_verify_rows;     /* widest kvs_attend (query rows) served on the split-K
+                                     kernel; calls beyond 64 rows x heads per kv head run as
+                                     row groups and need workspace for every row: 0 = max_rows
+                                     when the geometry has no tensor-core prefill path, else
+                                     64 / (max_q_head / n_kv_head) rows (no row groups) */
 } kvs_config;
 
 typedef struct {
@@ -437,12 +442,16 @@ kvs_status kvs_prefetch(kvs_ctx *ctx, uint32_t layer);
  * attention order", V2 README).
  * Rows: 1 (decode) up to floor(64 / (Hq/Hk)) (span verify, e.g. 2..6 draft
  * rows with 6 query heads per kv head) run on the split-K kernel with one
- * partial per page.  More rows (a prefill chunk, up to 256 rows) run on the
+ * partial per page.  Wider calls with fp16 queries at head_dim 256 and
+ * page_tokens a multiple of 64 (a prefill chunk, up to 256 rows) run on the
  * tcgen05 tensor-core kernel with one partial per prefill split (a fixed
  * group of prefill_split_pages pages, so the result is again independent of
- * residency and ring size); that path needs q_dtype KVS_F16, head_dim 256 and
- * page_tokens a multiple of 64 (KVS_ERR_UNSUPPORTED otherwise).  A timed-out
- * device-side wait in that kernel is reported by the next kvs_sync as
+ * residency and ring size).  Any other wider call (e.g. an fp32 ngram verify
+ * of 49 rows) runs on the split-K kernel as consecutive row groups of at most
+ * 64 rows x heads per kv head, every group reading each staged ring span
+ * before its slots are released, with one partial per (page, row, head):
+ * n_rows must be <= max_verify_rows (KVS_ERR_UNSUPPORTED otherwise).  A
+ * timed-out device-side wait is reported by the next kvs_sync as
  * KVS_ERR_CUDA.
  */
 kvs_status kvs_attend(kvs_ctx *ctx, uint32_t layer, const void *q_dev, int32_t q_dtype,

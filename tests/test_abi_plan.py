@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     for name in sorted(declared):
         assert hasattr(lib, name), name
     assert declared <= set(kvs.SIGNATURES), declared - set(kvs.SIGNATURES)
-    assert kvs.kvs_version() == 2
+    assert kvs.kvs_version() == 3
 
 
 def _cfg(**kw):
@@ -57,7 +57,7 @@ def test_query_sizes_formulas():
 
 @pytest.mark.parametrize("kw", [dict(page_tokens=48), dict(head_dim=96), dict(k_type=kvs.KVS_TYPE_Q4_0),
                                 dict(v_type=kvs.KVS_TYPE_Q8_0), dict(max_q_head=6), dict(max_rows=257),
-                                dict(max_q_head=0), dict(max_rows=11, head_dim=128), dict(max_rows=11, page_tokens=32)])
+                                dict(max_q_head=0)])
 def test_unsupported_configs_refused(kw):
     with pytest.raises(kvs.KVSError) as e:
         kvs.kvs_query_sizes(_cfg(**kw))
@@ -73,6 +73,22 @@ def _plan_cfg(arena_slots, host_bytes=None, ws=None, **kw):
     c.workspace_bytes = wmin if ws is None else ws
     c.host_bytes = hb if host_bytes is None else host_bytes
     return c
+
+
+@pytest.mark.parametrize("kw", [dict(max_rows=11, head_dim=128), dict(max_rows=11, page_tokens=32),
+                                dict(max_rows=49, max_verify_rows=49)])
+def test_wide_split_k_calls_size_the_workspace_for_every_row(kw):
+    """More than 64 rows x heads per kv head without the tensor-core path (another
+    head dim or page size, or fp32 queries): row groups on the split-K kernel, with
+    one partial per (page, row, head) and one query-fragment area per row group."""
+    cfg = _cfg(**kw)
+    pb, hb, amin, wmin = kvs.kvs_query_sizes(cfg)
+    D, Hk, Hq = cfg.head_dim, cfg.n_kv_head, cfg.max_q_head
+    pages = -(-cfg.max_tokens // cfg.page_tokens)
+    rows = cfg.max_verify_rows or cfg.max_rows
+    groups = -(-rows // (64 // (Hq // Hk)))
+    qfrag = Hk * 8 * (D // 16) * 32 * 16
+    assert wmin >= 256 + groups * qfrag + pages * Hq * rows * (D + 2) * 4
 
 
 def test_create_refusals():
@@ -472,3 +488,37 @@ def test_noalloc_refusals_come_before_any_device_work():
                                          a["n_q_head"], a["pos0"], a["scale"], a["out"], a["lse"], a["stream"])
         assert e.value.status == want, (over, e.value)
         assert kvs.kvs_last_error(None)
+
+
+@pytest.mark.parametrize("R,G,lanes", [(20, 6, 1), (49, 6, 2), (9, 8, 1)])
+def test_wide_split_k_row_groups_read_every_chunk_before_release(R, G, lanes):
+    """A call wider than 64 rows x heads per kv head on the split-K kernel: every
+    row group reads each ring chunk after its fill and before any refill of its
+    slots (the fence model), and each (page, kv head) is read once per group."""
+    P, Hk, T = 64, 2, 64 * 11 + 30
+    st = kvs.KVStream(page_tokens=P, n_layers=2, n_kv_head=Hk, head_dim=128, max_q_head=G * Hk, max_rows=R,
+                      max_tokens=T, ring_slots=2, chunk_pages=1, arena_slots=4 + 2 + 24, plan_only=True,
+                      lanes=lanes, max_verify_rows=R)
+    for l in range(2):
+        kvs.kvs_append(st.ctx, l, None, None, T)
+        mask = np.zeros(12, np.uint8)
+        mask[l::2] = 1
+        st.set_residency(l, mask)
+    st.prefetch(0)
+    st.prefetch(1)
+    for l in range(2):
+        st.attend_plan(l, R, G * Hk, T - R)
+    ops, _ = check_trace(st, G * Hk)
+    groups = -(-R // (64 // G))
+    for l in range(2):
+        reads = _reads_of_attend(ops, l)
+        assert sorted(set(reads)) == [(p, g) for p in range(12) for g in range(Hk)]
+        assert all(reads.count(x) == groups for x in set(reads)), l
+    # the split-K kernel is not used beyond max_verify_rows
+    with pytest.raises(kvs.KVSError) as e:
+        small = kvs.KVStream(page_tokens=P, n_layers=1, n_kv_head=Hk, head_dim=128, max_q_head=G * Hk, max_rows=R,
+                             max_tokens=T, ring_slots=2, chunk_pages=1, arena_slots=2 + 2 + 12, plan_only=True,
+                             max_verify_rows=max(1, R // 2))
+        kvs.kvs_append(small.ctx, 0, None, None, T)
+        small.attend_plan(0, R, G * Hk, T - R)
+    assert e.value.status == kvs.KVS_ERR_UNSUPPORTED

@@ -335,6 +335,53 @@ def test_loaded_host_pages_stream_and_match_the_oracle():
     assert st.stats()["h2d_pages"] >= full // 2
 
 
+def _wide_case(R, T, mask_fn, ring=8, chunk=2, lanes=1, seed=SEED, P=256, D=256, Hk=4, G=6):
+    st = kvs.KVStream(page_tokens=P, n_layers=1, n_kv_head=Hk, head_dim=D, max_q_head=G * Hk, max_rows=R,
+                      max_tokens=T, ring_slots=ring, chunk_pages=chunk, lanes=lanes,
+                      arena_slots=2 + ring + math.ceil(T / P), max_verify_rows=R)
+    (k, v), = _fill(st, 1, T, Hk, D, seed=seed)
+    st.set_residency(0, mask_fn(math.ceil(T / P)))
+    q = queries(seed, 0, R, G * Hk, D)
+    out, lse = attend(st, 0, q, T - R, 1.0 / math.sqrt(D))
+    return st, k, v, q, out, lse
+
+
+@pytest.mark.parametrize("R,T,P,D", [(49, 256 * 12 + 70, 256, 256), (20, 128 * 9 + 5, 128, 128)])
+def test_wide_fp32_verify_row_groups_match_the_oracle(R, T, P, D):
+    """An fp32 span of R causal rows (49 at 6 query heads per kv head: 294 rows x
+    heads) runs on the split-K kernel as row groups of 10 rows; half the pages
+    stream through the ring, every group reading each chunk before its release."""
+    st, k, v, q, out, lse = _wide_case(R, T, lambda n: (np.arange(n) % 2 == 1).astype(np.uint8), P=P, D=D)
+    ro, rl = oracle_ref(k, v, q, T - R, 1.0 / math.sqrt(D))
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] > 0
+
+
+def test_wide_fp32_verify_streamed_equals_resident_bitwise():
+    R, T = 49, 256 * 16 + 3
+    base = _wide_case(R, T, lambda n: np.ones(n, np.uint8))
+    rng = np.random.default_rng(11)
+    for ring, chunk, lanes in [(8, 2, 1), (6, 3, 2)]:
+        st, _, _, _, out, lse = _wide_case(R, T, lambda n: (rng.random(n) < 0.5).astype(np.uint8),
+                                           ring=ring, chunk=chunk, lanes=lanes)
+        assert st.stats()["h2d_pages"] > 0
+        assert np.array_equal(out, base[4]) and np.array_equal(lse, base[5]), (ring, chunk, lanes)
+        st.close()
+
+
+def test_wide_fp32_verify_full_size_sampled_rows():
+    """49 fp32 rows at context 163840 (the span-verify stack's geometry), 400
+    resident pages, the rest through an 8-slot ring; six sampled rows."""
+    R, P = 49, 256
+    T = 163840 + R
+    st, k, v, q, out, lse = _wide_case(R, T, lambda n: (np.arange(n) < 400).astype(np.uint8), chunk=1, lanes=4)
+    qkv = oracle.QuantKV(k, v)
+    for r in (0, 9, 10, 30, 47, 48):
+        ro, rl = qkv.attend(q[r:r + 1], T - R + r, 1.0 / 16)
+        check_parity(out[r:r + 1], lse[r:r + 1], ro, rl)
+    assert st.stats()["h2d_pages"] > 0
+
+
 # ------------------------------------------------------------ full-size samples
 
 @pytest.mark.parametrize("chunk,lanes", [(2, 1), (4, 2), (2, 3)])
