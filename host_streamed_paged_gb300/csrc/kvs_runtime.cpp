@@ -93,6 +93,11 @@ struct kvs_ctx {
     int64_t prefill_split = 8;  // pages per tensor-core prefill split
     bool split_chunks = false;  // ring chunks stop at prefill split boundaries (prefill-capable context)
     uint32_t verify_rows = 1;   // widest split-K call (row groups beyond 64 rows x heads)
+    // complete-layer lease: slots [ring_first + ring_n, ring_first + lease_ring_full)
+    // are taken out of the ring and hold the leased layer's nonresident pages
+    int64_t lease_layer = -1;
+    uint32_t lease_ring_full = 0;       // ring size before the lease
+    std::vector<int64_t> lease_spare;   // leased slots not holding a page yet
     int64_t qfrag_groups = 1;   // query-fragment areas in the workspace (one per row group)
     bool check_status = false;  // a kernel with bounded device waits ran since the last kvs_sync
     std::vector<LayerState> layers;
@@ -450,6 +455,11 @@ void pool_free(kvs_ctx *c, int64_t slot) {
         c->pool_page[i] = -1;
         c->pool_used--;
     }
+}
+
+bool is_lease_slot(const kvs_ctx *c, int64_t slot) {
+    return c->lease_layer >= 0 && slot >= c->ring_first + (int64_t)c->ring_n &&
+           slot < c->ring_first + (int64_t)c->lease_ring_full;
 }
 
 bool layer_has_plan(const kvs_ctx *c, uint32_t layer) {
@@ -928,10 +938,15 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
     // Pre-check every eviction this append causes, so a refusal changes nothing.
     {
         int64_t free_pool = c->pool_n - c->pool_used;
+        int64_t lease_free = c->lease_layer == (int64_t)layer ? (int64_t)c->lease_spare.size() : 0;
         for (uint64_t t = L.T; t < L.T + n_tokens; t = (t / P + 1) * P) {
             if (t % P != 0) continue;
             const int64_t q = (int64_t)(t / P), old = q - 2;
             if (old < 0 || L.tail_page[q & 1] != old) continue;
+            if (evict_target(c, layer, old, free_pool) != 1 && lease_free > 0) {
+                lease_free--;
+                continue;
+            }
             if (evict_target(c, layer, old, free_pool) < 0)
                 return fail(c, KVS_ERR_STATE,
                             "append would move a page out of its tail slot while the layer has a pending "
@@ -956,8 +971,21 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
             // page q starts in tail slot q % 2: evict its previous page
             const int64_t old = L.tail_page[q & 1];
             if (old >= 0 && old != q) {
-                const int target = evict_target(c, layer, old, c->pool_n - c->pool_used);
-                if (target == 1) {
+                int target = evict_target(c, layer, old, c->pool_n - c->pool_used);
+                // a page leaving a leased layer's tail extends the lease while it has spare slots
+                if (target != 1 && c->lease_layer == (int64_t)layer && !c->lease_spare.empty()) target = 3;
+                if (target == 3) {
+                    const int64_t ls = c->lease_spare.back();
+                    c->lease_spare.pop_back();
+                    L.pool_slot[old] = ls;
+                    if (c->plan_only) {
+                        log_op(c, KVS_OP_MOVE, kAttn, layer, 0, old, ls);
+                    } else {
+                        cudaError_t e = cudaMemcpyAsync(c->slot_ptr(ls), c->slot_ptr(tslot), (size_t)c->geom.page_bytes,
+                                                        cudaMemcpyDeviceToDevice, c->attn);
+                        if (e != cudaSuccess) return cuda_fail(c, e, "tail -> lease move");
+                    }
+                } else if (target == 1) {
                     const int64_t ps = pool_alloc(c, layer, old);
                     L.pool_slot[old] = ps;
                     if (c->plan_only) {
@@ -1044,6 +1072,7 @@ kvs_status kvs_truncate(kvs_ctx *c, uint32_t layer, uint64_t n_tokens) {
     for (int64_t p = new_last + 1; p <= cur_last; ++p) {
         if (L.tail_page[p & 1] == p) L.tail_page[p & 1] = -1;
         if (p < (int64_t)L.pool_slot.size() && L.pool_slot[p] >= 0) {
+            if (is_lease_slot(c, L.pool_slot[p])) c->lease_spare.push_back(L.pool_slot[p]);
             pool_free(c, L.pool_slot[p]);
             L.pool_slot[p] = -1;
         }
@@ -1068,6 +1097,7 @@ kvs_status kvs_load_host_pages(kvs_ctx *c, uint32_t layer, uint64_t first_page, 
     if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
     if (!c->queue.empty() || !c->announced.empty())
         return fail(c, KVS_ERR_STATE, "host page load while prefetches are pending");
+    if (c->lease_layer >= 0) return fail(c, KVS_ERR_STATE, "host page load while a lease is held");
     if (n_pages == 0) return KVS_OK;
     if (!src) return fail(c, KVS_ERR_INVALID, "null source pages");
     if (!c->host) return fail(c, KVS_ERR_STATE, "no host history");
@@ -1119,6 +1149,7 @@ kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, ui
     if (n_pages && !mask) return fail(c, KVS_ERR_INVALID, "null mask");
     if (!c->queue.empty() || !c->announced.empty())
         return fail(c, KVS_ERR_STATE, "residency change while prefetches are pending");
+    if (c->lease_layer >= 0) return fail(c, KVS_ERR_STATE, "residency change while a lease is held");
     LayerState &L = c->layers[layer];
     const int64_t complete = (int64_t)(L.T / c->geom.P);  // pages 0..complete-1 are full
     if (c->graph_exec) {  // its baked slot schedule no longer holds
@@ -1177,6 +1208,7 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     if (n_slots < 1) return fail(c, KVS_ERR_INVALID, "ring needs at least one slot");
     if (!c->queue.empty() || !c->announced.empty())
         return fail(c, KVS_ERR_STATE, "ring change while prefetches are pending");
+    if (c->lease_layer >= 0) return fail(c, KVS_ERR_STATE, "ring change while a lease is held");
     const int64_t base = 2 * (int64_t)c->cfg.n_layers;
     const int64_t new_pool = c->n_slots - base - (int64_t)n_slots;
     if (new_pool < 0) return fail(c, KVS_ERR_CAPACITY, "arena too small for that ring");
@@ -1233,6 +1265,102 @@ kvs_status kvs_set_ring_slots(kvs_ctx *c, uint32_t n_slots, uint32_t chunk_pages
     c->st.chunk_pages = c->chunk_pages;
     c->st.pool_slots = (uint64_t)c->pool_n;
     return create_events(c);
+}
+
+// Give the ring a new size at the same first slot (slots above it leave or
+// rejoin the ring), after every earlier device use of the ring slots.
+kvs_status resize_ring(kvs_ctx *c, uint32_t n_slots) {
+    kvs_status s = join_all_into_attn(c);
+    if (s != KVS_OK) return s;
+    s = join_attn_into_copy(c);
+    if (s != KVS_OK) return s;
+    s = join_copy_into_attn(c);
+    if (s != KVS_OK) return s;
+    if (!c->plan_only)
+        for (cudaStream_t st : c->lanes) cudaStreamSynchronize(st);
+    release_graph(c);
+    c->graph_kernels = 0;
+    destroy_events(c);
+    c->ring_n = n_slots;
+    c->chunk_pages = std::min(c->chunk_pages, n_slots);
+    c->slot_last_chunk.assign(c->ring_n, -1);
+    c->chunk_reader_sid.assign(c->ring_n, -1);
+    c->ring_seq = 0;
+    c->st.ring_slots = c->ring_n;
+    c->st.chunk_pages = c->chunk_pages;
+    return create_events(c);
+}
+
+// Complete-layer lease: the layer's nonresident pages are loaded once into
+// slots taken off the top of the ring (plus spare slots for pages that leave
+// its tail while the lease is held); attention then reads them like resident
+// pages, and the other layers stream through the smaller ring, so no refill
+// can overwrite a leased slot until kvs_lease_release gives them back.
+kvs_status kvs_lease_acquire(kvs_ctx *c, uint32_t layer, uint32_t extra_slots) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (layer >= c->cfg.n_layers) return fail(c, KVS_ERR_INVALID, "layer out of range");
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
+    if (c->lease_layer >= 0) return fail(c, KVS_ERR_STATE, "a lease is already held");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "lease while prefetches are pending");
+    LayerState &L = c->layers[layer];
+    std::vector<int64_t> pages;
+    for (int64_t p = 0; p < n_pages_of(c, layer); ++p) {
+        int64_t sl;
+        if (locate(c, layer, p, &sl) == 0) pages.push_back(p);
+    }
+    const uint64_t k = pages.size() + (uint64_t)extra_slots;
+    if (k >= c->ring_n)
+        return fail(c, KVS_ERR_CAPACITY, "the lease needs " + std::to_string(k) + " ring slots and the ring (" +
+                                             std::to_string(c->ring_n) + ") must keep at least one");
+    const uint32_t full = c->ring_n;
+    kvs_status s = resize_ring(c, full - (uint32_t)k);
+    if (s != KVS_OK) return s;
+    c->lease_layer = layer;
+    c->lease_ring_full = full;
+    std::vector<int64_t> slots;
+    for (uint64_t i = 0; i < k; ++i) {
+        const int64_t slot = c->ring_first + (int64_t)c->ring_n + (int64_t)i;
+        if (i < pages.size()) {
+            slots.push_back(slot);
+            L.pool_slot[pages[i]] = slot;
+        } else {
+            c->lease_spare.push_back(slot);
+        }
+    }
+    if (!pages.empty()) {
+        s = op_copy_pages(c, layer, pages, slots, KVS_OP_POOL_LOAD, nullptr);
+        if (s != KVS_OK) return s;
+        c->st.pool_load_bytes += pages.size() * (uint64_t)c->geom.page_bytes;
+        s = join_copy_into_attn(c);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_lease_release(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
+    if (c->lease_layer < 0) return fail(c, KVS_ERR_STATE, "no lease is held");
+    if (!c->queue.empty() || !c->announced.empty())
+        return fail(c, KVS_ERR_STATE, "lease release while prefetches are pending");
+    LayerState &L = c->layers[c->lease_layer];
+    for (int64_t &sl : L.pool_slot)  // the host history keeps every leased page
+        if (sl >= 0 && is_lease_slot(c, sl)) sl = -1;
+    const uint32_t full = c->lease_ring_full;
+    c->lease_layer = -1;
+    c->lease_spare.clear();
+    return resize_ring(c, full);
+}
+
+kvs_status kvs_lease_info(const kvs_ctx *c, int64_t *layer, uint32_t *leased_slots, uint32_t *spare_slots) {
+    if (!c) return KVS_ERR_INVALID;
+    if (layer) *layer = c->lease_layer;
+    if (leased_slots) *leased_slots = c->lease_layer >= 0 ? c->lease_ring_full - c->ring_n : 0;
+    if (spare_slots) *spare_slots = (uint32_t)c->lease_spare.size();
+    return KVS_OK;
 }
 
 kvs_status kvs_prefetch(kvs_ctx *c, uint32_t layer) {
@@ -1675,9 +1803,9 @@ kvs_status kvs_flush(kvs_ctx *c, uint32_t layer) {
 }
 
 kvs_status kvs_page_location(const kvs_ctx *c, uint32_t layer, uint64_t page, int32_t *kind, int64_t *slot) {
-    if (!c || !kind || !slot || layer >= c->cfg.n_layers || page >= (uint64_t)c->max_pages)
-        return KVS_ERR_INVALID;
+    if (!c || !kind || !slot || layer >= c->cfg.n_layers || page >= (uint64_t)c->max_pages) return KVS_ERR_INVALID;
     *kind = locate(c, layer, (int64_t)page, slot);
+    if (*kind == 2 && is_lease_slot(c, *slot)) *kind = 3;
     return KVS_OK;
 }
 

@@ -125,6 +125,9 @@ SIGNATURES = {
     "kvs_set_residency": ([_P, _U32, _P, _U64], _I32),
     "kvs_set_ring_slots": ([_P, _U32, _U32], _I32),
     "kvs_prefetch": ([_P, _U32], _I32),
+    "kvs_lease_acquire": ([_P, _U32, _U32], _I32),
+    "kvs_lease_release": ([_P], _I32),
+    "kvs_lease_info": ([_P, _P, _P, _P], _I32),
     "kvs_attend": ([_P, _U32, _P, _I32, _U32, _U32, _U64, _F32, _P, _P], _I32),
     "kvs_sync": ([_P, _U32], _I32),
     "kvs_flush": ([_P, _U32], _I32),
@@ -253,6 +256,21 @@ def kvs_policy_step(config: kvs_policy_config, previous: kvs_policy_state,
     if st != KVS_OK:
         raise KVSError(st, "kvs_policy_step: invalid config, state or observation")
     return nxt, dec
+
+
+def kvs_lease_acquire(ctx, layer, extra_slots=0) -> int:
+    return _check(ctx, load().kvs_lease_acquire(ctx, layer, extra_slots))
+
+
+def kvs_lease_release(ctx) -> int:
+    return _check(ctx, load().kvs_lease_release(ctx))
+
+
+def kvs_lease_info(ctx):
+    """(leased layer or -1, leased slots, spare slots)"""
+    layer, held, spare = ctypes.c_int64(), ctypes.c_uint32(), ctypes.c_uint32()
+    _check(ctx, load().kvs_lease_info(ctx, ctypes.byref(layer), ctypes.byref(held), ctypes.byref(spare)))
+    return layer.value, held.value, spare.value
 
 
 def kvs_prefetch(ctx, layer) -> int:
@@ -499,6 +517,15 @@ class KVStream:
 
     def prefetch(self, layer):
         return kvs_prefetch(self.ctx, layer)
+
+    def lease_acquire(self, layer, extra_slots=0):
+        return kvs_lease_acquire(self.ctx, layer, extra_slots)
+
+    def lease_release(self):
+        return kvs_lease_release(self.ctx)
+
+    def lease_info(self):
+        return kvs_lease_info(self.ctx)
 
     def sync(self, timeout_ms=0):
         return kvs_sync(self.ctx, timeout_ms)

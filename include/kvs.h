@@ -415,6 +415,38 @@ kvs_status kvs_policy_step(const kvs_policy_config *config, const kvs_policy_sta
                            kvs_policy_decision *decision);
 
 /*
+ * Complete-layer lease and ring guard (V2 README, "MTP catch-up, prediction,
+ * and rollback": an attached layer with its own host history borrows the
+ * resident/ring pool, loads its nonresident suffix into the ring once for a
+ * catch-up and draft phase, and gives the whole ring back afterwards; and
+ * "Backend-neutral memory and streaming contracts": the lease holder keeps the
+ * ring protected from the other layers' lookahead, and committed tail rows
+ * extend the retained lease).
+ *
+ * kvs_lease_acquire -- take 1 slot per nonresident page of `layer` (pages in
+ * neither the pool nor a tail slot), plus extra_slots spare slots, off the top
+ * of the ring, and load those pages into them on the copy stream (attention
+ * waits for the load).  While the lease is held: attends of `layer` read every
+ * page from the device (no ring chunks); the other layers stream through the
+ * remaining ring slots, so no refill ever writes a leased slot; a page leaving
+ * `layer`'s tail slots moves into a spare slot (while spares remain, else it
+ * is treated as usual); a truncation that drops leased pages returns their
+ * slots to the spares.  kvs_page_location reports leased pages as kind 3.
+ * kvs_set_residency, kvs_set_ring_slots and kvs_load_host_pages are refused
+ * (KVS_ERR_STATE) while a lease is held.  Refusals: a lease already held or
+ * prefetches pending -> KVS_ERR_STATE; the ring would keep no slot ->
+ * KVS_ERR_CAPACITY.  Acquire and release wait for earlier ring work on the
+ * device (stream-ordered) and drop a captured step graph.
+ *
+ * kvs_lease_release -- give every leased slot back to the ring; the pages are
+ * host-only again (the host history holds them unchanged).  kvs_lease_info
+ * reports the leased layer (-1 if none), the slots it holds and its spares.
+ */
+kvs_status kvs_lease_acquire(kvs_ctx *ctx, uint32_t layer, uint32_t extra_slots);
+kvs_status kvs_lease_release(kvs_ctx *ctx);
+kvs_status kvs_lease_info(const kvs_ctx *ctx, int64_t *layer, uint32_t *leased_slots, uint32_t *spare_slots);
+
+/*
  * kvs_prefetch -- announce that `layer` is attended next (after any layer
  * already announced) and enqueue host -> ring copies of its nonresident pages
  * into ring slots whose previous reader has already been enqueued: copies
@@ -475,7 +507,8 @@ kvs_status kvs_flush(kvs_ctx *ctx, uint32_t layer);
 
 /*
  * kvs_page_location -- where page `page` of `layer` is device-readable now:
- * *kind = 0 host only, 1 tail slot, 2 resident pool; *slot = device slot id
+ * *kind = 0 host only, 1 tail slot, 2 resident pool, 3 leased ring slot
+ * (kvs_lease_acquire); *slot = device slot id
  * (or -1).  kvs_read_slot copies device slot `slot` (page_bytes) to host_dst
  * synchronously; kvs_read_host_page copies the host history page.  Debug and
  * test helpers for bit-exact layout and indexing checks; library API with no

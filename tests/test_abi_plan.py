@@ -522,3 +522,54 @@ def test_wide_split_k_row_groups_read_every_chunk_before_release(R, G, lanes):
         kvs.kvs_append(small.ctx, 0, None, None, T)
         small.attend_plan(0, R, G * Hk, T - R)
     assert e.value.status == kvs.KVS_ERR_UNSUPPORTED
+
+
+def test_lease_holds_a_layers_pages_and_guards_the_ring():
+    """A complete-layer lease: the layer's nonresident pages are loaded once into
+    slots taken off the ring, its attends read no ring chunk, the other layers'
+    refills never write a leased slot, a page leaving its tail fills a spare
+    leased slot, and release gives the whole ring back."""
+    P = 64
+    st = _plan_stream(3, 1, P, P * 14, 8, 2, 6 + 8 + 6)  # 6 tail slots, pool of 6, ring of 8
+    for l in range(3):
+        kvs.kvs_append(st.ctx, l, None, None, P * 10 + 5)  # pages 0..10, tail pages 9, 10
+    st.set_residency(2, np.array([1, 1, 1], np.uint8))
+    first, n = st.ring_info()
+    with pytest.raises(kvs.KVSError) as e:
+        st.lease_acquire(2, 2)  # 6 nonresident pages + 2 spares = the whole ring
+    assert e.value.status == kvs.KVS_ERR_CAPACITY
+    st.lease_acquire(2, 1)  # pages 3..8 + one spare: 7 slots, the ring keeps 1
+    assert st.lease_info() == (2, 7, 1) and st.ring_info() == (first, 1)
+    leased = set(range(first + 1, first + 8))
+    for p in range(3, 9):
+        kind, slot = st.page_location(2, p)
+        assert kind == 3 and slot in leased
+    for call in (lambda: st.lease_acquire(0), lambda: st.set_residency(0, np.ones(2, np.uint8)),
+                 lambda: st.set_ring_slots(4)):
+        with pytest.raises(kvs.KVSError) as e:
+            call()
+        assert e.value.status == kvs.KVS_ERR_STATE
+    n0 = len(st.trace())
+    for _ in range(2):  # a catch-up / draft phase of the leased layer, the others streaming
+        for l in (2, 0, 1):
+            st.attend_plan(l, 1, 6, P * 10 + 4)
+    # page 11 starts: page 9 leaves its tail slot into the spare; page 12: page 10 goes to the host
+    kvs.kvs_append(st.ctx, 2, None, None, 2 * P)
+    assert st.page_location(2, 9)[0] == 3 and st.page_location(2, 10) == (0, -1)
+    assert st.lease_info() == (2, 7, 0)
+    st.attend_plan(2, 1, 6, P * 12 + 4)
+    ops = st.trace()[n0:]
+    fills = [o for o in ops if o["op"] == kvs.KVS_OP_FILL]
+    assert fills and not any(o["b"] in leased for o in fills)
+    assert {o["a"] for o in fills if o["layer"] == 2} == {10}  # only the page the lease could not hold
+    st.lease_release()
+    assert st.lease_info() == (-1, 0, 0) and st.ring_info() == (first, 8)
+    assert st.page_location(2, 5) == (0, -1)
+    with pytest.raises(kvs.KVSError) as e:
+        st.lease_release()
+    assert e.value.status == kvs.KVS_ERR_STATE
+    st.attend_plan(2, 1, 6, P * 12 + 4)
+    ops, n_reads = check_trace(st, 6, fixed_ring=False)
+    late = [o["a"] for o in st.trace()[n0:] if o["op"] == kvs.KVS_OP_FILL and o["layer"] == 2]
+    assert set(range(3, 11)) <= set(late)  # after release the layer streams again
+    st.close()

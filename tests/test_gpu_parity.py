@@ -382,6 +382,61 @@ def test_wide_fp32_verify_full_size_sampled_rows():
     assert st.stats()["h2d_pages"] > 0
 
 
+def test_lease_draft_phase_matches_the_oracle_and_resident_bitwise():
+    """Layer 1 is a second history (an attached draft layer) leased into the ring:
+    it appends and attends three draft rows while layer 0 keeps streaming through
+    the rest of the ring; every output matches the oracle, and matches the same
+    calls on an all-resident context bitwise."""
+    import torch
+    P, D, Hk, G = 64, 128, 2, 6
+    Hq = G * Hk
+    T0, T1 = 64 * 20 + 7, 64 * 6 + 10
+    k0, v0 = history(SEED, 0, T0, Hk, D)
+    k1, v1 = history(SEED, 1, T1 + 3, Hk, D)
+    kinds = []
+
+    def run(leased):
+        st = make_stream(P, 2, Hk, D, Hq, 1, T0 + 64, ring=8, chunk=1, pool_pages=None if not leased else 4)
+        append_rows(st, 0, k0, v0)
+        append_rows(st, 1, k1[:T1], v1[:T1])
+        if not leased:
+            st.set_residency(0, np.ones(21, np.uint8))
+            st.set_residency(1, np.ones(8, np.uint8))
+        else:
+            st.lease_acquire(1, 1)  # pages 0..4 of layer 1 + one spare
+            kinds.append([st.page_location(1, p)[0] for p in range(7)])
+        outs = []
+        for i in range(3):
+            kn = torch.from_numpy(np.ascontiguousarray(k1[T1 + i:T1 + i + 1])).cuda()
+            vn = torch.from_numpy(np.ascontiguousarray(v1[T1 + i:T1 + i + 1])).cuda()
+            torch.cuda.synchronize()
+            st.append(1, kn, vn)
+            q = queries(SEED, 10 + i, 1, Hq, D)
+            outs.append(attend(st, 1, q, T1 + i, 0.1))
+            q0 = queries(SEED, 20 + i, 1, Hq, D)
+            outs.append(attend(st, 0, q0, T0 - 1, 0.1))
+        stats = st.stats()
+        if leased:
+            st.lease_release()
+            outs.append(attend(st, 1, queries(SEED, 30, 1, Hq, D), T1 + 2, 0.1))
+        st.close()
+        return outs, stats
+
+    base, _ = run(False)
+    got, stats = run(True)
+    assert kinds[0][:5] == [3] * 5 and kinds[0][5:] == [1, 1]
+    assert stats["h2d_pages"] > 0  # layer 0 streamed through the smaller ring
+    for i in range(3):
+        ro, rl = oracle_ref(k1[:T1 + i + 1], v1[:T1 + i + 1], queries(SEED, 10 + i, 1, Hq, D), T1 + i, 0.1)
+        check_parity(*got[2 * i], ro, rl)
+        ro, rl = oracle_ref(k0, v0, queries(SEED, 20 + i, 1, Hq, D), T0 - 1, 0.1)
+        check_parity(*got[2 * i + 1], ro, rl)
+    for g, b in zip(got, base):
+        assert np.array_equal(g[0], b[0]) and np.array_equal(g[1], b[1])
+    ro, rl = oracle_ref(k1[:T1 + 3], v1[:T1 + 3], queries(SEED, 30, 1, Hq, D), T1 + 2, 0.1)
+    check_parity(*got[6], ro, rl)
+
+
 # ------------------------------------------------------------ full-size samples
 
 @pytest.mark.parametrize("chunk,lanes", [(2, 1), (4, 2), (2, 3)])
