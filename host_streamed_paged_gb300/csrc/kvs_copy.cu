@@ -101,7 +101,14 @@ constexpr int kFillThreads = 512;
 constexpr int kFillUnroll = 4;
 constexpr int kFillMaxCtas = 64;
 
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 __global__ void __launch_bounds__(kFillThreads) fill_kernel(const __grid_constant__ FillParams p) {
+    if (p.rec && threadIdx.x == 0) atomicMax(&p.rec[0], ~global_ns());  // earliest start, complemented
     const uint32_t upp = (uint32_t)(p.page_bytes / 16);  // 16-byte units per page
     const uint32_t n = upp * (uint32_t)p.n;
     const uint32_t stride = gridDim.x * blockDim.x;
@@ -123,6 +130,10 @@ __global__ void __launch_bounds__(kFillThreads) fill_kernel(const __grid_constan
                 reinterpret_cast<uint4 *>(p.dst[pg])[i - pg * upp] = v[u];
             }
         }
+    }
+    if (p.rec) {  // latest end: after every thread of this CTA has issued its stores
+        __syncthreads();
+        if (threadIdx.x == 0) atomicMax(&p.rec[1], global_ns());
     }
 }
 

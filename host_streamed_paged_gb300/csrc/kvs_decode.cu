@@ -192,6 +192,25 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     // launched as a programmatic dependent: nothing is read before the grids
     // this launch depends on have completed and their writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.rec && blockIdx.x == 0 && threadIdx.x == 0) {
+        // a ring chunk's read: account its wait for the copy and clear the record
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        volatile unsigned long long *rc = p.rec;
+        const unsigned long long fs = ~rc[0], fe = rc[1];
+        if (fe != 0 && rc[0] != 0) {
+            const unsigned long long wait = t > fe ? t - fe : 0ull;
+            ObsAccumulator *a = reinterpret_cast<ObsAccumulator *>(p.acc);
+            atomicAdd(&a->reads, 1ull);
+            if (wait < kMissNs) atomicAdd(&a->misses, 1ull);
+            atomicAdd(&a->occupancy_page_ns, wait * (unsigned long long)p.rec_pages);
+            atomicAdd(&a->fill_busy_ns, fe > fs ? fe - fs : 0ull);
+            atomicMax(&a->first_fill_neg, ~fs);
+            atomicMax(&a->last_read, t);
+        }
+        rc[0] = 0ull;
+        rc[1] = 0ull;
+    }
     constexpr int NB = D / 32;  // 32-dim scale blocks
     constexpr int KS = D / 16;  // QK k-steps
     constexpr int MR = NT * 8;  // MMA rows (query rows x heads, padded to 8)

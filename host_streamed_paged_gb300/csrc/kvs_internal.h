@@ -72,6 +72,9 @@ struct DecodeParams {
     int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run
     int give_up_waits;     // test hook: every pipeline wait gives up at once, as if its copy
                            // never landed (the drain of copies in flight keeps its bound)
+    unsigned long long *rec;  // ring-chunk read: the chunk's fill record (nullable, see FillParams)
+    unsigned long long *acc;  // observation accumulator the first CTA adds the read to
+    int rec_pages;            // pages of the chunk
     int n_items;
     uint32_t page[kMaxItems];
     uint32_t slot[kMaxItems];
@@ -145,7 +148,21 @@ cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStre
 // Copy whole pages host -> device with SM loads (pinned host memory is
 // directly addressable by the GPU).  One launch per ring chunk.
 constexpr int kMaxFillPages = 64;
+// Observation records.  A ring refill stamps its record {~start, end} (ns, by
+// atomic max, from zero); the first CTA of the read of that chunk turns the
+// record into counts in the accumulator and clears it.  A read that starts
+// within kMissNs of its copy's end waited for the copy (a readiness miss).
+constexpr int kObsRecords = 1024;               // records, indexed by chunk id
+constexpr unsigned long long kMissNs = 4000;
+struct ObsAccumulator {  // all fields start at zero
+    unsigned long long reads, misses;
+    unsigned long long occupancy_page_ns;  // sum of pages x (read start - fill end)
+    unsigned long long fill_busy_ns;       // sum of fill durations
+    unsigned long long first_fill_neg;     // ~(earliest fill start), by atomic max
+    unsigned long long last_read;          // latest read start
+};
 struct FillParams {
+    unsigned long long *rec;  // this refill's record (nullable)
     int n;
     int64_t page_bytes;
     const uint8_t *src[kMaxFillPages];

@@ -95,6 +95,7 @@ struct kvs_ctx {
     uint32_t verify_rows = 1;   // widest split-K call (row groups beyond 64 rows x heads)
     // complete-layer lease: slots [ring_first + ring_n, ring_first + lease_ring_full)
     // are taken out of the ring and hold the leased layer's nonresident pages
+    kvs_policy_observation last_obs = {};  // the last kvs_observe result
     int64_t lease_layer = -1;
     uint32_t lease_ring_full = 0;       // ring size before the lease
     std::vector<int64_t> lease_spare;   // leased slots not holding a page yet
@@ -288,9 +289,14 @@ kvs_status join_all_into_attn(kvs_ctx *c) {
 }
 
 // host pages -> device slots on the copy stream (ring fill or pool load)
+// observation record of ring chunk `id` in the workspace (null in plan-only mode)
+unsigned long long *obs_record(kvs_ctx *c, uint64_t id);
+unsigned long long *obs_accumulator(kvs_ctx *c);
+
 kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
                          const std::vector<int64_t> &slots, uint32_t kind,
-                         const std::vector<uint64_t> *seqs, int sid = kCopy, bool pdl = false) {
+                         const std::vector<uint64_t> *seqs, int sid = kCopy, bool pdl = false,
+                         unsigned long long *rec = nullptr) {
     if (!(c->cfg.flags & KVS_FLAG_DMA_FILL))
         c->st.kernel_launches += (pages.size() + kvs::kMaxFillPages - 1) / kvs::kMaxFillPages;
     if (c->plan_only) {
@@ -312,6 +318,7 @@ kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> 
     }
     for (size_t i0 = 0; i0 < pages.size(); i0 += kvs::kMaxFillPages) {
         kvs::FillParams fp;
+        fp.rec = rec;
         fp.n = (int)std::min<size_t>(kvs::kMaxFillPages, pages.size() - i0);
         fp.page_bytes = c->geom.page_bytes;
         for (int j = 0; j < fp.n; ++j) {
@@ -563,7 +570,7 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
         seqs[i] = ch.seq0 + i;
         slots[i] = c->ring_slot_id(ch.seq0 + i);
     }
-    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs, sid, follow);
+    s = op_copy_pages(c, ch.layer, ch.pages, slots, KVS_OP_FILL, &seqs, sid, follow, obs_record(c, ch.id));
     if (s != KVS_OK) return s;
     s = op_record(c, sid, (int)(ch.id % c->ring_n));
     if (s != KVS_OK) return s;
@@ -618,6 +625,7 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
         cudaEvent_t t0;
         kvs_status s = timed_begin(c, kind, &t0, sid);
         if (s != KVS_OK) return s;
+        if (i0 > 0) dp.rec = nullptr;  // one record per chunk
         cudaError_t e = kvs::launch_decode(dp, c->stream(sid));
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel launch");
         c->check_status = true;
@@ -627,7 +635,21 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
     return KVS_OK;
 }
 
-constexpr uint64_t kStatusBytes = 256;  // device status word at the start of the workspace
+// workspace: [status word at 0, observation accumulator at 64 | 256 B]
+// [observation records | kObsRecords x 16 B][query fragments][partials]
+constexpr uint64_t kStatusBytes = 256;
+constexpr uint64_t kAccOffset = 64;
+constexpr uint64_t kObsBytes = (uint64_t)kvs::kObsRecords * 16;
+
+unsigned long long *obs_record(kvs_ctx *c, uint64_t id) {
+    if (c->plan_only) return nullptr;
+    return reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes) +
+           2 * (id % (uint64_t)kvs::kObsRecords);
+}
+unsigned long long *obs_accumulator(kvs_ctx *c) {
+    if (c->plan_only) return nullptr;
+    return reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(c->cfg.workspace) + kAccOffset);
+}
 
 // the tensor-core prefill path serves fp16 queries at head_dim 256 with pages
 // of a multiple of 64 tokens
@@ -708,7 +730,8 @@ void sizes_of(const kvs_config *cfg, uint64_t *page_bytes, uint64_t *host_bytes,
         // query fragments of every row group of the widest split-K call
         const uint32_t G = cfg->max_q_head / cfg->n_kv_head;
         const uint64_t groups = (vrows + rows_per_group(G) - 1) / rows_per_group(G);
-        *ws_min = kStatusBytes + groups * (uint64_t)kvs::qfrag_bytes((int)cfg->n_kv_head, (int)cfg->head_dim) + need;
+        *ws_min = kStatusBytes + kObsBytes + groups * (uint64_t)kvs::qfrag_bytes((int)cfg->n_kv_head, (int)cfg->head_dim) +
+                  need;
     }
 }
 
@@ -886,7 +909,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         return KVS_ERR_CUDA;
     }
     if (!plan_only) {
-        cudaError_t e = cudaMemset(cfg->workspace, 0, kStatusBytes);
+        cudaError_t e = cudaMemset(cfg->workspace, 0, kStatusBytes + kObsBytes);
         if (e != cudaSuccess) {
             g_create_error = std::string("workspace status clear: ") + cudaGetErrorString(e);
             destroy_events(c);
@@ -1568,7 +1591,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
     }
 
     const size_t per_split = (size_t)n_q_head * n_rows;
-    uint8_t *qfrag = static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes;
+    uint8_t *qfrag = static_cast<uint8_t *>(c->cfg.workspace) + kStatusBytes + kObsBytes;
     const int64_t qf_bytes = kvs::qfrag_bytes(c->geom.Hk, c->geom.D);
     float *part_o = reinterpret_cast<float *>(qfrag + c->qfrag_groups * qf_bytes);
     const int64_t n_partials = prefill ? (c->max_pages + c->prefill_split - 1) / c->prefill_split : c->max_pages;
@@ -1669,9 +1692,18 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
                 sl.push_back(c->ring_slot_id(ch.seq0 + i));
             }
             if (!pg.empty()) {
-                // every row group reads the chunk before its consumed fence
-                for (kvs::DecodeParams &gp : groups) {
+                // every row group reads the chunk before its consumed fence; the
+                // first accounts the chunk's wait for its copy
+                for (size_t gi = 0; gi < groups.size(); ++gi) {
+                    kvs::DecodeParams &gp = groups[gi];
+                    if (gi == 0) {
+                        gp.rec = obs_record(c, ch.id);
+                        gp.acc = obs_accumulator(c);
+                        gp.rec_pages = (int)pg.size();
+                    }
                     s = launch_items(c, layer, pg, sl, gp, KVS_TIME_RING, sid);
+                    gp.rec = nullptr;
+                    gp.acc = nullptr;
                     if (s != KVS_OK) return s;
                 }
                 c->st.ring_pages_read += pg.size() * (uint64_t)c->geom.Hk;
@@ -1844,6 +1876,10 @@ kvs_status kvs_stats(kvs_ctx *c, kvs_stats_t *out, int reset) {
     c->st.chunk_pages = c->chunk_pages;
     c->st.pool_slots = (uint64_t)c->pool_n;
     c->st.pool_used = (uint64_t)c->pool_used;
+    c->st.observed_reads = c->last_obs.streamed_reads;
+    c->st.ready_misses = c->last_obs.ready_misses;
+    c->st.ring_occupancy = c->last_obs.ring_occupancy;
+    c->st.copy_busy = c->last_obs.copy_busy;
     *out = c->st;
     if (reset) {
         const uint64_t rs = c->st.ring_slots, ps = c->st.pool_slots, pu = c->st.pool_used;
@@ -1851,6 +1887,34 @@ kvs_status kvs_stats(kvs_ctx *c, kvs_stats_t *out, int reset) {
         c->st.ring_slots = rs;
         c->st.pool_slots = ps;
         c->st.pool_used = pu;
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_observe(kvs_ctx *c, kvs_policy_observation *out, int reset) {
+    if (!c || !out) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (c->capturing) return fail(c, KVS_ERR_STATE, "not allowed inside a step capture");
+    memset(out, 0, sizeof(*out));
+    for (const LayerState &L : c->layers) out->context_tokens = std::max<uint64_t>(out->context_tokens, L.T);
+    if (c->plan_only) return KVS_OK;
+    kvs_status s = kvs_sync(c, 0);
+    if (s != KVS_OK) return s;
+    kvs::ObsAccumulator a;
+    cudaError_t e = cudaMemcpy(&a, obs_accumulator(c), sizeof(a), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(c, e, "observation read");
+    out->streamed_reads = a.reads;
+    out->ready_misses = a.misses;
+    const unsigned long long first = ~a.first_fill_neg;
+    if (a.reads && a.last_read > first) {
+        const double span = (double)(a.last_read - first);
+        out->ring_occupancy = (float)std::min(1.0, (double)a.occupancy_page_ns / (span * (double)c->ring_n));
+        out->copy_busy = (float)std::min(1.0, (double)a.fill_busy_ns / span);
+    }
+    c->last_obs = *out;
+    if (reset) {
+        e = cudaMemset(obs_accumulator(c), 0, sizeof(a));
+        if (e != cudaSuccess) return cuda_fail(c, e, "observation reset");
     }
     return KVS_OK;
 }

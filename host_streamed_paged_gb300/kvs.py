@@ -77,7 +77,8 @@ class kvs_stats_t(ctypes.Structure):
         "kernel_launches", "decode_launches")] + [("decode_ms", ctypes.c_double)] + [
         (n, ctypes.c_uint64) for n in ("decode_timed", "decode_bytes", "ring_slots", "pool_slots",
                                        "pool_used", "graph_launches", "graph_kernels",
-                                       "chunk_pages")]
+                                       "chunk_pages", "observed_reads", "ready_misses")] + [
+        (n, ctypes.c_double) for n in ("ring_occupancy", "copy_busy")]
 
 
 class kvs_trace_op(ctypes.Structure):
@@ -125,6 +126,7 @@ SIGNATURES = {
     "kvs_set_residency": ([_P, _U32, _P, _U64], _I32),
     "kvs_set_ring_slots": ([_P, _U32, _U32], _I32),
     "kvs_prefetch": ([_P, _U32], _I32),
+    "kvs_observe": ([_P, _P, ctypes.c_int], _I32),
     "kvs_lease_acquire": ([_P, _U32, _U32], _I32),
     "kvs_lease_release": ([_P], _I32),
     "kvs_lease_info": ([_P, _P, _P, _P], _I32),
@@ -256,6 +258,13 @@ def kvs_policy_step(config: kvs_policy_config, previous: kvs_policy_state,
     if st != KVS_OK:
         raise KVSError(st, "kvs_policy_step: invalid config, state or observation")
     return nxt, dec
+
+
+def kvs_observe(ctx, reset=False) -> "kvs_policy_observation":
+    """The policy's feedback measured on the device since the last reset."""
+    obs = kvs_policy_observation()
+    _check(ctx, load().kvs_observe(ctx, ctypes.byref(obs), 1 if reset else 0))
+    return obs
 
 
 def kvs_lease_acquire(ctx, layer, extra_slots=0) -> int:
@@ -517,6 +526,9 @@ class KVStream:
 
     def prefetch(self, layer):
         return kvs_prefetch(self.ctx, layer)
+
+    def observe(self, reset=False):
+        return kvs_observe(self.ctx, reset)
 
     def lease_acquire(self, layer, extra_slots=0):
         return kvs_lease_acquire(self.ctx, layer, extra_slots)

@@ -155,6 +155,11 @@ typedef struct {
     uint64_t graph_launches;   /* kvs_graph_launch calls */
     uint64_t graph_kernels;    /* kernels in the captured step graph */
     uint64_t chunk_pages;      /* current ring chunk size, pages */
+    /* the policy's feedback as the last kvs_observe measured it (see there) */
+    uint64_t observed_reads;   /* ring chunk reads accounted */
+    uint64_t ready_misses;     /* of those, reads that waited for their copy */
+    double ring_occupancy;     /* mean fraction of ring slots holding a page not yet read */
+    double copy_busy;          /* fraction of the interval the refills were running */
 } kvs_stats_t;
 
 /* One logged operation of a KVS_FLAG_PLAN_ONLY context (see kvs_trace_read). */
@@ -445,6 +450,26 @@ kvs_status kvs_policy_step(const kvs_policy_config *config, const kvs_policy_sta
 kvs_status kvs_lease_acquire(kvs_ctx *ctx, uint32_t layer, uint32_t extra_slots);
 kvs_status kvs_lease_release(kvs_ctx *ctx);
 kvs_status kvs_lease_info(const kvs_ctx *ctx, int64_t *layer, uint32_t *leased_slots, uint32_t *spare_slots);
+
+/*
+ * kvs_observe -- the feedback the residency policy samples (V2 README, "KV
+ * data movement and attention": readiness misses, ring occupancy and
+ * copy-stream time), measured on the device since the last reset, as a
+ * kvs_policy_observation: every ring refill by the SM fill kernel stamps its
+ * start and end (%globaltimer), and the read of that chunk accounts, at its
+ * start, whether it waited for the copy (it started within 4 us of the copy's
+ * end: a readiness miss) and how long the chunk's pages sat in the ring
+ * unread.  context_tokens = the longest layer; streamed_reads, ready_misses =
+ * chunk reads accounted and missed; ring_occupancy = sum over reads of
+ * pages x (read start - copy end) / (interval x ring_slots); copy_busy = sum
+ * of copy durations / interval (at most 1), the interval running from the
+ * first copy's start to the last read's start.  Refills by the copy engines
+ * (KVS_FLAG_DMA_FILL) are not stamped and not accounted.  Waits for the
+ * context's device work first (kvs_sync); reset != 0 starts a new interval.
+ * The counters also accumulate across step-graph replays.  The values are
+ * copied into kvs_stats_t.  Library API (the pages give the inputs, not a call).
+ */
+kvs_status kvs_observe(kvs_ctx *ctx, kvs_policy_observation *out, int reset);
 
 /*
  * kvs_prefetch -- announce that `layer` is attended next (after any layer

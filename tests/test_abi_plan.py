@@ -50,7 +50,8 @@ def test_query_sizes_formulas():
     assert hb == 4 * 128 * pb
     assert amin == (2 * 4 + 8) * pb
     qfrag = 4 * 8 * 16 * 32 * 16  # query fragments of 4 kv heads (already 256-aligned)
-    assert wmin == 256 + qfrag + 128 * 24 * 6 * (256 + 2) * 4  # status word + fragments + one partial per page
+    obs = 1024 * 16  # observation records (one per ring chunk id modulo 1024)
+    assert wmin == 256 + obs + qfrag + 128 * 24 * 6 * (256 + 2) * 4  # status, records, fragments, one partial per page
     pb2, *_ = kvs.kvs_query_sizes(_cfg(page_tokens=256, n_kv_head=2, head_dim=128, max_q_head=8))
     assert pb2 == 2 * 256 * 128 * 13 // 8 == 106496  # 104 KiB
 
@@ -573,3 +574,14 @@ def test_lease_holds_a_layers_pages_and_guards_the_ring():
     late = [o["a"] for o in st.trace()[n0:] if o["op"] == kvs.KVS_OP_FILL and o["layer"] == 2]
     assert set(range(3, 11)) <= set(late)  # after release the layer streams again
     st.close()
+
+
+def test_observe_on_a_plan_only_context_reports_only_the_context_length():
+    st = _plan_stream(2, 1, 64, 64 * 10, 2, 1, 4 + 2 + 4)
+    kvs.kvs_append(st.ctx, 0, None, None, 200)
+    kvs.kvs_append(st.ctx, 1, None, None, 333)
+    st.attend_plan(1, 1, 6, 332)
+    o = st.observe(reset=True)
+    assert (o.context_tokens, o.streamed_reads, o.ready_misses, o.ring_occupancy, o.copy_busy) == (333, 0, 0, 0.0, 0.0)
+    s = st.stats()
+    assert s["observed_reads"] == 0 and s["copy_busy"] == 0.0

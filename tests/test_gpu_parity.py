@@ -437,6 +437,96 @@ def test_lease_draft_phase_matches_the_oracle_and_resident_bitwise():
     check_parity(*got[6], ro, rl)
 
 
+def test_observation_counts_every_streamed_read_and_stays_in_range():
+    P, D, Hk, G, T = 256, 256, 4, 6, 256 * 24 + 9
+    st = make_stream(P, 2, Hk, D, G * Hk, 1, T, ring=8, chunk=2, pool_pages=8)
+    for l in range(2):
+        k, v = history(SEED, l, T, Hk, D)
+        append_rows(st, l, k, v)
+    st.set_residency(0, (np.arange(25) < 4).astype(np.uint8))
+    st.sync()
+    st.observe(reset=True)
+    st.stats(reset=True)
+    q = queries(SEED, 0, 1, G * Hk, D)
+    for l in range(2):
+        attend(st, l, q, T - 1, 1 / 16)
+    o = st.observe(reset=False)
+    chunks = st.stats()["ring_chunks"]
+    assert o.streamed_reads == chunks > 0 and o.ready_misses <= o.streamed_reads
+    assert 0.0 <= o.ring_occupancy <= 1.0 and 0.0 < o.copy_busy <= 1.0
+    assert o.context_tokens == T
+    s = st.stats()
+    assert s["observed_reads"] == chunks and s["copy_busy"] == o.copy_busy
+    # counters accumulate until a reset, also over a step graph's replays
+    import torch
+    q_t = torch.from_numpy(q).cuda()
+    bufs = [(torch.empty((1, G * Hk, D), device="cuda"), torch.empty((1, G * Hk), device="cuda")) for _ in range(2)]
+    torch.cuda.synchronize()
+    st.graph_begin()
+    st.prefetch(0)
+    st.prefetch(1)
+    for l in range(2):
+        st.attend(l, q_t, T - 1, 1 / 16, out=bufs[l][0], lse=bufs[l][1])
+    st.graph_end()
+    st.graph_launch()
+    st.graph_launch()
+    o2 = st.observe(reset=True)
+    assert o2.streamed_reads == 3 * chunks
+    assert st.observe().streamed_reads == 0
+
+
+def test_residency_policy_drives_a_streamed_stack_in_closed_loop():
+    """kvs_policy_step chooses the resident/ring split of a fixed 96-slot budget
+    from the library's own observations (kvs_observe), step after step, and the
+    decisions are applied with kvs_set_ring_slots / kvs_set_residency; the
+    outputs match the oracle on sampled layers after every change."""
+    import torch
+    P, D, Hk, G, L, T = 256, 256, 4, 6, 4, 256 * 64
+    Hq = G * Hk
+    budget = 96
+    npages = T // P
+    st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=1,
+                      max_tokens=T, ring_slots=8, chunk_pages=2, lanes=2, arena_slots=2 * L + budget)
+    hist = _fill(st, L, T, Hk, D)
+    cfg = kvs.kvs_policy_config(page_tokens=P, n_layers=L, budget_slots=budget, min_ring_slots=8,
+                                max_ring_slots=64, step_slots=8, hold_steps=2, miss_grow=0.25,
+                                copy_busy_max=0.98, occupancy_shrink=0.05)
+    state = kvs.kvs_policy_state()
+    qs = [queries(SEED, 50 + l, 1, Hq, D) for l in range(L)]
+    q_dev = [torch.from_numpy(q).cuda() for q in qs]
+    torch.cuda.synchronize()
+    applied = []
+    for step in range(6):
+        st.prefetch(0)
+        outs = []
+        for l in range(L):
+            if l + 1 < L:
+                st.prefetch(l + 1)
+            outs.append(st.attend(l, q_dev[l], T - 1, 1 / 16))
+        st.sync()
+        obs = st.observe(reset=True)
+        assert obs.streamed_reads > 0 and obs.ready_misses <= obs.streamed_reads
+        if step in (0, 5) or applied and applied[-1][0] == step - 1:
+            for l in (0, L - 1):
+                ro, rl = oracle_ref(*hist[l], qs[l], T - 1, 1 / 16)
+                check_parity(outs[l][0].cpu().numpy(), outs[l][1].cpu().numpy(), ro, rl)
+        state, dec = kvs.kvs_policy_step(cfg, state, obs)
+        assert 8 <= dec.ring_slots <= 64 and dec.resident_slots == budget - dec.ring_slots
+        if dec.changed or step == 0:
+            per = min(npages - 2, dec.resident_pages_per_layer)
+            for l in range(L):
+                st.set_residency(l, np.zeros(npages, np.uint8))
+            st.set_ring_slots(dec.ring_slots, max(1, dec.ring_slots // 4))
+            for l in range(L):
+                m = np.zeros(npages, np.uint8)
+                m[:per] = 1
+                st.set_residency(l, m)
+            st.sync()
+            applied.append((step, dec.ring_slots, dec.reason))
+            assert st.stats()["ring_slots"] == dec.ring_slots
+    assert applied and applied[0][2] == kvs.KVS_POLICY_INIT
+
+
 # ------------------------------------------------------------ full-size samples
 
 @pytest.mark.parametrize("chunk,lanes", [(2, 1), (4, 2), (2, 3)])
