@@ -287,7 +287,7 @@ def run_ours(args, wl):
     st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
                       max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"], arena_slots=arena_slots,
                       device=dev, lanes=wl.get("lanes", 1), dma_fill=wl.get("dma", False),
-                      host_alloc=args.host_alloc)
+                      host_alloc=args.host_alloc, f16_operands=args.operands == "f16")
     ceiling = h2d_ceiling(torch, dev)
 
     # history: seeded rows appended through the KV writer
@@ -483,6 +483,9 @@ def run_ours(args, wl):
                        "chunk_pages": chunk_eff, "lanes": wl.get("lanes", 1),
                        "fill": "copy engines" if wl.get("dma") else "SM fill kernel",
                        "host_alloc": args.host_alloc,
+                       "operands": ("single f16 (query and softmax weight x V scale rounded to f16; K/V codes exact; "
+                                    "fp32 accumulation)" if args.operands == "f16" else
+                                    "f16 hi + lo pairs (query and softmax weight x V scale); fp32 accumulation"),
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {kv_bytes_step / 1e9:.2f} GB of KV pages read per step",
                        "step": "per layer: append rows, prefetch next layer, attend, truncate; one CUDA graph replay"},
@@ -532,6 +535,9 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="long262k: sweep the resident fraction 0..100%%")
     ap.add_argument("--host-alloc", choices=["pageable", "pinned", "hugepage"], default="pinned",
                     help="host history buffer: registered numpy memory, CUDA pinned, or huge-page advised")
+    ap.add_argument("--operands", choices=["split", "f16"], default="f16",
+                    help="split-K attention operands: single f16 values (Q and P' rounded once), or f16 "
+                         "hi + lo pairs (about 22 significant bits)")
     ap.add_argument("--fill", choices=["default", "sm", "dma"], default="default",
                     help="ring refills by the SM fill kernel or the copy engines (default: the workload's)")
     args = ap.parse_args()

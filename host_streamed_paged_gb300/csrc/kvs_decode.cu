@@ -149,7 +149,7 @@ __host__ __device__ inline int pv_parts(int D, int P) {
     return parts < 1 ? 1 : parts;
 }
 
-// Shared-memory carve of decode_kernel<D, NT, W> (bytes; page size P, S stages).
+// Shared-memory carve of decode_kernel<D, NT, W, SPL> (bytes; page size P, S stages).
 struct DecodeSmem {
     int stage, sc, red, obuf, rowoff, rowtab, bar, total, stages;
 };
@@ -185,7 +185,7 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, i
 // and scales) and the V piece.  A stage's K piece is refilled with a later
 // unit as soon as the scores are done, its V piece once P.V is done, so the
 // copies of the next unit overlap the softmax, P.V and store of this one.
-template <int D, int NT, int W>
+template <int D, int NT, int W, bool SPL>
 __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 
         // Q fragments of kv head g (built by qprep_kernel): qf[tile][ks][lane]
         const uint4 *qf = p.qf + ((int64_t)g * p.qtiles + tile) * KS * 32;
+        const uint2 *qf2 = reinterpret_cast<const uint2 *>(p.qf) + ((int64_t)g * p.qtiles + tile) * KS * 32;
         if (!mbar_wait(bar0 + 16 * (2 * stage), parity, limit)) ok = false;
         if (!__syncthreads_and(ok)) break;
         pending &= ~(1u << (2 * stage));
@@ -350,11 +351,17 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const uint4 qv = qf[(nt * KS + 2 * b + s) * 32 + lane];
+                        if (SPL) {
+                            const uint4 qv = qf[(nt * KS + 2 * b + s) * 32 + lane];
 #pragma unroll
-                        for (int q = 0; q < KPW; ++q) {
-                            mma16816(cb[q][nt], a[q], qv.x, qv.y);
-                            mma16816(cb[q][nt], a[q], qv.z, qv.w);
+                            for (int q = 0; q < KPW; ++q) {
+                                mma16816(cb[q][nt], a[q], qv.x, qv.y);
+                                mma16816(cb[q][nt], a[q], qv.z, qv.w);
+                            }
+                        } else {
+                            const uint2 qv = qf2[(nt * KS + 2 * b + s) * 32 + lane];
+#pragma unroll
+                            for (int q = 0; q < KPW; ++q) mma16816(cb[q][nt], a[q], qv.x, qv.y);
                         }
                     }
                 }
@@ -426,10 +433,16 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                     e[3] = exp2f(sg[q].w - mx);
                 }
                 sum += (e[0] + e[1]) + (e[2] + e[3]);
-                uint32_t h02, l02, h13, l13;
-                split_f16(e[0], e[2], h02, l02);
-                split_f16(e[1], e[3], h13, l13);
-                *reinterpret_cast<uint4 *>(sc + m * SP + k4) = make_uint4(h02, h13, l02, l13);
+                if (SPL) {
+                    uint32_t h02, l02, h13, l13;
+                    split_f16(e[0], e[2], h02, l02);
+                    split_f16(e[1], e[3], h13, l13);
+                    *reinterpret_cast<uint4 *>(sc + m * SP + k4) = make_uint4(h02, h13, l02, l13);
+                } else {
+                    const __half2 h02 = __floats2half2_rn(e[0], e[2]), h13 = __floats2half2_rn(e[1], e[3]);
+                    *reinterpret_cast<uint2 *>(sc + m * SP + k4) =
+                        make_uint2(*reinterpret_cast<const uint32_t *>(&h02), *reinterpret_cast<const uint32_t *>(&h13));
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -497,16 +510,26 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                         asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d13) : "r"(dlo), "r"(dhi));
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint4 pr =
-                                *reinterpret_cast<const uint4 *>(sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s);
-                            // P' = (hi + lo) * d: hi * d rounded, its exact remainder, plus lo * d
-                            uint32_t bh0, bl0, bh1, bl1;
-                            scale_split(pr.x, pr.z, d02, bh0, bl0);  // keys +0, +2
-                            scale_split(pr.y, pr.w, d13, bh1, bl1);  // keys +1, +3
-                            mma16816(acc[pp][0][nt], a0, bh0, bh1);
-                            mma16816(acc[pp][1][nt], a1, bh0, bh1);
-                            mma16816(acc[pp][0][nt], a0, bl0, bl1);
-                            mma16816(acc[pp][1][nt], a1, bl0, bl1);
+                            const float *rec = sc + (nt * 8 + gid) * SP + kb + 8 * tig + 4 * s;
+                            if (SPL) {
+                                const uint4 pr = *reinterpret_cast<const uint4 *>(rec);
+                                // P' = (hi + lo) * d: hi * d rounded, its exact remainder, plus lo * d
+                                uint32_t bh0, bl0, bh1, bl1;
+                                scale_split(pr.x, pr.z, d02, bh0, bl0);  // keys +0, +2
+                                scale_split(pr.y, pr.w, d13, bh1, bl1);  // keys +1, +3
+                                mma16816(acc[pp][0][nt], a0, bh0, bh1);
+                                mma16816(acc[pp][1][nt], a1, bh0, bh1);
+                                mma16816(acc[pp][0][nt], a0, bl0, bl1);
+                                mma16816(acc[pp][1][nt], a1, bl0, bl1);
+                            } else {
+                                // P' = rn(p * d), p already rounded to f16
+                                const uint2 pr = *reinterpret_cast<const uint2 *>(rec);
+                                uint32_t b0, b1;
+                                asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(b0) : "r"(pr.x), "r"(d02));
+                                asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(b1) : "r"(pr.y), "r"(d13));
+                                mma16816(acc[pp][0][nt], a0, b0, b1);
+                                mma16816(acc[pp][1][nt], a1, b0, b1);
+                            }
                         }
                     }
                 }
@@ -596,13 +619,14 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
 // Q fragments for every kv head, once per attend: qf [Hk][NT][KS][32] uint4
 // = {b0_hi, b1_hi, b0_lo, b1_lo} of the QK B operand.  One CTA per (kv head,
 // row tile): the kernel sits between two layers' reads, so its latency counts.
-template <int D, int NT>
+template <int D, int NT, bool SPL>
 __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__ DecodeParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");            // q and the previous readers of qf
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // attention may be scheduled
     constexpr int KS = D / 16;
     const int g = blockIdx.x, nt = blockIdx.y, G = p.G, rows = G * p.Rg;
     uint4 *qf = const_cast<uint4 *>(p.qf) + ((int64_t)g * NT + nt) * KS * 32;
+    uint2 *qf2 = reinterpret_cast<uint2 *>(const_cast<uint4 *>(p.qf)) + ((int64_t)g * NT + nt) * KS * 32;
     for (int e = threadIdx.x; e < KS * 32; e += kThreads) {
         const int ln = e & 31, ks = e >> 5;
         const int m = nt * 8 + (ln >> 2);
@@ -624,7 +648,10 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
         uint32_t h0, l0, h1, l1;
         split_f16(x[0], x[1], h0, l0);
         split_f16(x[2], x[3], h1, l1);
-        qf[e] = make_uint4(h0, h1, l0, l1);
+        if (SPL)
+            qf[e] = make_uint4(h0, h1, l0, l1);
+        else
+            qf2[e] = make_uint2(h0, h1);
     }
 }
 
@@ -647,11 +674,11 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, int smem, cudaStream_t s
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int D, int NT, int W>
+template <int D, int NT, int W, bool SPL>
 cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     DecodeParams p = p_in;
     if (p.prep_q) {
-        cudaError_t e = launch_pdl(qprep_kernel<D, NT>, dim3(p.geom.Hk, NT), dim3(kThreads), 0, s, p);
+        cudaError_t e = launch_pdl(qprep_kernel<D, NT, SPL>, dim3(p.geom.Hk, NT), dim3(kThreads), 0, s, p);
         if (e != cudaSuccess) return e;
         if (p.n_items == 0) return cudaSuccess;
     }
@@ -667,7 +694,7 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     if (L.total > maxsm) return cudaErrorInvalidValue;
     p.stages = L.stages;
     {
-        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(decode_kernel<D, NT, W>), L.total);
+        cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(decode_kernel<D, NT, W, SPL>), L.total);
         if (e != cudaSuccess) return e;
     }
     const int U = p.n_items * p.geom.Hk * (p.tile_mode ? p.run_tiles : 1);
@@ -678,22 +705,26 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     }
     const int per_cta = (U + max_ctas - 1) / max_ctas;
     const int grid = (U + per_cta - 1) / per_cta;
-    return launch_pdl(decode_kernel<D, NT, W>, dim3(grid), dim3(W * 32), L.total, s, p);
+    return launch_pdl(decode_kernel<D, NT, W, SPL>, dim3(grid), dim3(W * 32), L.total, s, p);
 }
 
-template <int D>
-cudaError_t launch_decode_d(const DecodeParams &p, int nt, cudaStream_t s) {
-    if (p.tile_mode) return launch_decode_t<D, 1, 8>(p, s);
+template <int D, bool SPL>
+cudaError_t launch_decode_m(const DecodeParams &p, int nt, cudaStream_t s) {
+    if (p.tile_mode) return launch_decode_t<D, 1, 8, SPL>(p, s);
     switch (nt) {
-        case 1: return launch_decode_t<D, 1, 8>(p, s);
-        case 2: return launch_decode_t<D, 2, 8>(p, s);
-        case 3: return launch_decode_t<D, 3, 8>(p, s);
-        case 4: return launch_decode_t<D, 4, 8>(p, s);
-        case 5: return launch_decode_t<D, 5, 8>(p, s);
-        case 6: return launch_decode_t<D, 6, 8>(p, s);
-        case 8: return launch_decode_t<D, 8, 8>(p, s);
+        case 1: return launch_decode_t<D, 1, 8, SPL>(p, s);
+        case 2: return launch_decode_t<D, 2, 8, SPL>(p, s);
+        case 3: return launch_decode_t<D, 3, 8, SPL>(p, s);
+        case 4: return launch_decode_t<D, 4, 8, SPL>(p, s);
+        case 5: return launch_decode_t<D, 5, 8, SPL>(p, s);
+        case 6: return launch_decode_t<D, 6, 8, SPL>(p, s);
+        case 8: return launch_decode_t<D, 8, 8, SPL>(p, s);
         default: return cudaErrorInvalidValue;
     }
+}
+template <int D>
+cudaError_t launch_decode_d(const DecodeParams &p, int nt, cudaStream_t s) {
+    return p.single_f16 ? launch_decode_m<D, false>(p, nt, s) : launch_decode_m<D, true>(p, nt, s);
 }
 
 // ------------------------------------------------------------------ combine

@@ -70,6 +70,7 @@ struct DecodeParams {
     int reserve_sms;       // leave this many SMs' worth of CTA slots free of this launch (at
                            // most a third of the GPU) for concurrent ring-chunk launches
     int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run
+    int single_f16;        // Q and P' as single f16 operands (else f16 hi + lo pairs)
     int give_up_waits;     // test hook: every pipeline wait gives up at once, as if its copy
                            // never landed (the drain of copies in flight keeps its bound)
     unsigned long long *rec;  // ring-chunk read: the chunk's fill record (nullable, see FillParams)

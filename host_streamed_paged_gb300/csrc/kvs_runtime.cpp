@@ -1617,6 +1617,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         dp.G = (int)G;
         dp.pos0 = (long long)pos0;
         dp.scale_log2 = scale * 1.4426950408889634f;
+        dp.single_f16 = (c->cfg.flags & KVS_FLAG_F16_OPERANDS) ? 1 : 0;
         if (c->fault == KVS_FAULT_DEVICE_WAIT && c->fault_nth && ++c->fault_count == c->fault_nth)
             dp.give_up_waits = 1;
         // row groups: query rows row0 .. row0 + Rg - 1, G * Rg <= 64, each with its

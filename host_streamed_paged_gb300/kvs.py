@@ -34,6 +34,7 @@ KVS_F32 = 0
 KVS_F16 = 1
 KVS_FLAG_PLAN_ONLY = 1
 KVS_FLAG_DMA_FILL = 2
+KVS_FLAG_F16_OPERANDS = 4
 
 KVS_OP_RECORD, KVS_OP_WAIT, KVS_OP_FILL, KVS_OP_READ, KVS_OP_POOL_LOAD = 1, 2, 3, 4, 5
 KVS_OP_PUBLISH, KVS_OP_WRITE, KVS_OP_LAUNCH, KVS_OP_MOVE = 6, 7, 8, 9
@@ -416,7 +417,8 @@ class KVStream:
     def __init__(self, *, page_tokens, n_layers, n_kv_head, head_dim, max_q_head, max_rows,
                  max_tokens, ring_slots=8, chunk_pages=0, arena_slots=None, arena_bytes=None,
                  plan_only=False, host=None, device="cuda", lanes=1, copy_priority=None,
-                 prefill_split_pages=0, dma_fill=False, host_alloc="pinned", max_verify_rows=0):
+                 prefill_split_pages=0, dma_fill=False, host_alloc="pinned", max_verify_rows=0,
+                 f16_operands=False):
         cfg = kvs_config()
         cfg.page_tokens, cfg.n_layers, cfg.n_kv_head, cfg.head_dim = page_tokens, n_layers, n_kv_head, head_dim
         cfg.max_q_head, cfg.max_rows, cfg.max_tokens = max_q_head, max_rows, max_tokens
@@ -425,7 +427,7 @@ class KVStream:
         cfg.n_lanes = lanes
         cfg.prefill_split_pages = prefill_split_pages
         cfg.max_verify_rows = max_verify_rows
-        cfg.flags = KVS_FLAG_DMA_FILL if dma_fill else 0
+        cfg.flags = (KVS_FLAG_DMA_FILL if dma_fill else 0) | (KVS_FLAG_F16_OPERANDS if f16_operands else 0)
         self.page_bytes, host_bytes, arena_min, ws_bytes = kvs_query_sizes(cfg)
         self.max_pages = math.ceil(max_tokens / page_tokens)
         if arena_bytes is None:

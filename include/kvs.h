@@ -85,6 +85,13 @@ typedef enum { KVS_F32 = 0, KVS_F16 = 1 } kvs_dtype;
                                  consecutive in both host and device memory)
                                  instead of the SM-driven fill kernel: no SM
                                  time, a fixed cost per copy */
+#define KVS_FLAG_F16_OPERANDS 4u /* split-K attention (decode, span verify) feeds the
+                                 tensor cores the query and the softmax weights
+                                 times the V scale as single f16 values (about 11
+                                 significant bits) instead of f16 hi + lo pairs
+                                 (about 22): half the MMAs, measured relative
+                                 error ~5e-4 instead of ~1e-6 against the fp64
+                                 oracle; accumulation stays fp32 */
 
 typedef struct {
     uint32_t page_tokens;  /* P: token positions per page; 32, 64, 128 or 256 */
