@@ -186,6 +186,75 @@ def h2d_ceiling(torch, dev):
     return n / (best * 1e-3) / 1e9
 
 
+def _union(iv):
+    """Total length of the union of intervals [(a, b)]."""
+    tot, cur_a, cur_b = 0, None, None
+    for a, b in sorted(iv):
+        if cur_b is None or a > cur_b:
+            if cur_b is not None:
+                tot += cur_b - cur_a
+            cur_a, cur_b = a, b
+        else:
+            cur_b = max(cur_b, b)
+    return tot + ((cur_b - cur_a) if cur_b is not None else 0)
+
+
+def _clip(iv, lo, hi):
+    return [(max(a, lo), min(b, hi)) for a, b in iv if b > lo and a < hi]
+
+
+def timeline_summary(recs, L):
+    """Per-step summary of one replayed step's launch timeline (device %globaltimer stamps).
+
+    Link: the union of ring-refill launches is the time the host link is being
+    read.  Layer boundary: from the end of layer l's last page read to the start
+    of layer l+1's first page read; the kernels on that chain (combine of l,
+    truncate clear of l, append of l+1, query fragments of l+1) are listed with
+    their median durations, and the refill time inside the boundary shows
+    whether the link idles there."""
+    ran = [r for r in recs if r["start_ns"] and r["end_ns"]]
+    if not ran:
+        return None
+    t0 = min(r["start_ns"] for r in ran)
+    t1 = max(r["end_ns"] for r in ran)
+    fills = [(r["start_ns"], r["end_ns"]) for r in ran if r["kind"] == "fill"]
+    reads = {}
+    for r in ran:
+        if r["kind"] in ("read_resident", "read_ring", "prefill"):
+            reads.setdefault(r["layer"], []).append((r["start_ns"], r["end_ns"]))
+    bounds, fill_in, chain = [], [], {}
+    for l in range(L - 1):
+        if l not in reads or l + 1 not in reads:
+            continue
+        a = max(b for _, b in reads[l])
+        b = min(x for x, _ in reads[l + 1])
+        bounds.append(max(0, b - a))
+        fill_in.append(_union(_clip(fills, a, b)) if b > a else 0)
+        for r in ran:
+            key = None
+            if r["layer"] == l and r["kind"] in ("combine", "clear"):
+                key = r["kind"] + " (layer l)"
+            elif r["layer"] == l + 1 and r["kind"] in ("append", "qprep", "clear"):
+                key = r["kind"] + " (layer l+1)"
+            if key and a - 5000 <= r["start_ns"] <= b + 5000:
+                chain.setdefault(key, []).append(r["end_ns"] - r["start_ns"])
+    med = lambda v: statistics.median(v) / 1e3 if v else None  # noqa: E731
+    span = t1 - t0
+    busy = _union(fills)
+    return {
+        "step_us": span / 1e3,
+        "refill_busy_us": busy / 1e3,
+        "refill_busy_frac": busy / span if span else None,
+        "refill_launches": len(fills),
+        "boundary_us_median": med(bounds),
+        "boundary_us_total": sum(bounds) / 1e3,
+        "refill_busy_in_boundaries_frac": (sum(fill_in) / sum(bounds)) if sum(bounds) else None,
+        "boundary_kernels_us_median": {k: med(v) for k, v in sorted(chain.items())},
+        "how": ("one replay of the captured step with every launch stamped (first CTA start, last CTA end, "
+                "%globaltimer); refill = SM fill kernels reading pinned host memory"),
+    }
+
+
 def alg_flops_per_layer(wl):
     """QK^T and PV multiply-adds, 2 flops each, over the keys each row sees."""
     T, R, Hq, D = wl["T"], wl["R"], wl["Hq"], wl["D"]
@@ -452,6 +521,36 @@ def run_ours(args, wl):
                     "ms_per_launch": r_ms / max(r_n, 1), "peak_source": peak_src + " hbm_gbs",
                     "timed_region": f"{n_eager} host-issued steps ({ms_timed_eager:.2f} ms/step)"}
 
+        # timeline leg: the same step captured with every launch stamped, one replay read back
+        st.graph_destroy()
+        timeline = None
+        if not args.no_timeline:
+            st.timeline_begin(1 << 16)
+            st.graph_begin()
+            step()
+            st.graph_end()
+            st.timeline_end()
+            for _ in range(args.warmup):
+                st.timeline_zero()
+                st.graph_launch()
+            st.timeline_zero()
+            st.graph_launch()
+            st.sync()
+            recs, dropped = st.timeline_read()
+            st.graph_destroy()
+            timeline = timeline_summary(recs, L)
+            if timeline is not None:
+                timeline["launches"] = len(recs)
+                timeline["dropped"] = dropped
+            if args.timeline_out and rank == 0:
+                with open(args.timeline_out, "w") as f:
+                    f.write("kind,layer,stream,pages,start_us,end_us\n")
+                    base = min((r["start_ns"] for r in recs if r["start_ns"]), default=0)
+                    for r in recs:
+                        f.write(f"{r['kind']},{r['layer']},{r['stream']},{r['pages']},"
+                                f"{(r['start_ns'] - base) / 1e3 if r['start_ns'] else ''},"
+                                f"{(r['end_ns'] - base) / 1e3 if r['end_ns'] else ''}\n")
+
         # CPU baseline (rank 0): the oracle on sampled layers/rows, scaled to the step
         cpu = parity = None
         if rank == 0 and cpu_layers and frac in (None, fracs[0]):
@@ -503,6 +602,7 @@ def run_ours(args, wl):
                             "pinned host copy of all layers' outputs, on the attention stream")},
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clk,
+            "timeline": timeline,
             "eager_ms_per_step": eager_ms,
             "parity": parity,
             "prep_s": prep_s,
@@ -538,6 +638,8 @@ def main():
     ap.add_argument("--operands", choices=["split", "f16"], default="f16",
                     help="split-K attention operands: single f16 values (Q and P' rounded once), or f16 "
                          "hi + lo pairs (about 22 significant bits)")
+    ap.add_argument("--no-timeline", action="store_true", help="skip the stamped-timeline replay")
+    ap.add_argument("--timeline-out", default="", help="write the stamped launches of one step as CSV")
     ap.add_argument("--fill", choices=["default", "sm", "dma"], default="default",
                     help="ring refills by the SM fill kernel or the copy engines (default: the workload's)")
     args = ap.parse_args()

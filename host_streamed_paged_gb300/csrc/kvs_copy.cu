@@ -21,9 +21,14 @@ namespace {
 // PR "port adaptive KV streaming") writes encoded rows at the page's token
 // slot; here the slot is t0 + token.
 __global__ void __launch_bounds__(256) quantize_kernel(const QuantizeParams p) {
+    // a programmatic dependent launch: the rows and the page are touched only
+    // once the kernels this launch depends on have completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int D = p.geom.D, NB = D / 32, Hk = p.geom.Hk, P = p.geom.P;
     const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    tl_begin(p.tl);
     if (wid >= (int64_t)p.n * Hk * NB) return;
     const int b = (int)(wid % NB);
     const int g = (int)((wid / NB) % Hk);
@@ -65,10 +70,12 @@ __global__ void __launch_bounds__(256) quantize_kernel(const QuantizeParams p) {
     const int chi = __shfl_down_sync(0xffffffffu, c, 16);
     if (lane < 16) hb[p.geom.vq_off + vq_byte(t, b * 16 + lane, NB)] = (uint8_t)(c | (chi << 4));
     if (lane == 0) reinterpret_cast<__half *>(hb + p.geom.vs_off)[(int64_t)b * P + t] = __float2half_rn(dv);
+    if (p.tl && lane == 0) atomicMax(&p.tl[1], tl_now());
 }
 
 // Zero token slots [t0, P) of every section of every head of one page.
-__global__ void clear_tail_kernel(uint8_t *page, PageGeom g, int t0) {
+__global__ void clear_tail_kernel(uint8_t *page, PageGeom g, int t0, unsigned long long *tl) {
+    tl_begin(tl);
     const int64_t n = g.page_bytes;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -80,6 +87,10 @@ __global__ void clear_tail_kernel(uint8_t *page, PageGeom g, int t0) {
         else if (off < g.vs_off) tok = (off - g.vq_off) / (NB * 512) * 32 + (off - g.vq_off) % 32;  // V lines
         else tok = ((off - g.vs_off) / 2) % g.P;                                          // V scales
         if (tok >= t0) page[i] = 0;
+    }
+    if (tl) {
+        __syncthreads();
+        tl_finish(tl);
     }
 }
 
@@ -109,6 +120,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 __global__ void __launch_bounds__(kFillThreads) fill_kernel(const __grid_constant__ FillParams p) {
     if (p.rec && threadIdx.x == 0) atomicMax(&p.rec[0], ~global_ns());  // earliest start, complemented
+    tl_begin(p.tl);
     const uint32_t upp = (uint32_t)(p.page_bytes / 16);  // 16-byte units per page
     const uint32_t n = upp * (uint32_t)p.n;
     const uint32_t stride = gridDim.x * blockDim.x;
@@ -131,9 +143,10 @@ __global__ void __launch_bounds__(kFillThreads) fill_kernel(const __grid_constan
             }
         }
     }
-    if (p.rec) {  // latest end: after every thread of this CTA has issued its stores
+    if (p.rec || p.tl) {  // latest end: after every thread of this CTA has issued its stores
         __syncthreads();
-        if (threadIdx.x == 0) atomicMax(&p.rec[1], global_ns());
+        if (p.rec && threadIdx.x == 0) atomicMax(&p.rec[1], global_ns());
+        tl_finish(p.tl);
     }
 }
 
@@ -143,14 +156,24 @@ cudaError_t launch_quantize(const QuantizeParams &p, cudaStream_t s) {
     if (p.n <= 0) return cudaSuccess;
     const int64_t warps = (int64_t)p.n * p.geom.Hk * (p.geom.D / 32);
     const int64_t blocks = (warps * 32 + 255) / 256;
-    quantize_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_kernel, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStream_t s) {
-    if (t0 <= 0) return cudaMemsetAsync(page, 0, (size_t)g.page_bytes, s);
+cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStream_t s,
+                              unsigned long long *tl) {
+    if (t0 <= 0 && !tl) return cudaMemsetAsync(page, 0, (size_t)g.page_bytes, s);
     if (t0 >= g.P) return cudaSuccess;
-    clear_tail_kernel<<<152, 256, 0, s>>>(page, g, t0);
+    clear_tail_kernel<<<152, 256, 0, s>>>(page, g, t0 < 0 ? 0 : t0, tl);
     return cudaGetLastError();
 }
 

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         rc[0] = 0ull;
         rc[1] = 0ull;
     }
+    tl_begin(p.tl);
     constexpr int NB = D / 32;  // 32-dim scale blocks
     constexpr int KS = D / 16;  // QK k-steps
     constexpr int MR = NT * 8;  // MMA rows (query rows x heads, padded to 8)
@@ -236,7 +237,10 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     const int T = p.tile_mode ? p.run_tiles : 1;
     const int U = p.n_items * p.geom.Hk * T;
     const int u0 = (int)((int64_t)blockIdx.x * U / gridDim.x), u1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
-    if (u0 >= u1) return;
+    if (u0 >= u1) {
+        tl_finish(p.tl);
+        return;
+    }
     const int S = L.stages;
 
     auto src_of = [&](int u) {
@@ -614,6 +618,10 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         }
         __syncthreads();
     }
+    if (p.tl) {
+        __syncthreads();
+        tl_finish(p.tl);
+    }
 }
 
 // Q fragments for every kv head, once per attend: qf [Hk][NT][KS][32] uint4
@@ -623,6 +631,7 @@ template <int D, int NT, bool SPL>
 __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__ DecodeParams p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");            // q and the previous readers of qf
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // attention may be scheduled
+    tl_begin(p.tl_prep);
     constexpr int KS = D / 16;
     const int g = blockIdx.x, nt = blockIdx.y, G = p.G, rows = G * p.Rg;
     uint4 *qf = const_cast<uint4 *>(p.qf) + ((int64_t)g * NT + nt) * KS * 32;
@@ -652,6 +661,10 @@ __global__ void __launch_bounds__(kThreads) qprep_kernel(const __grid_constant__
             qf[e] = make_uint4(h0, h1, l0, l1);
         else
             qf2[e] = make_uint2(h0, h1);
+    }
+    if (p.tl_prep) {
+        __syncthreads();
+        tl_finish(p.tl_prep);
     }
 }
 
@@ -699,10 +712,7 @@ cudaError_t launch_decode_t(const DecodeParams &p_in, cudaStream_t s) {
     }
     const int U = p.n_items * p.geom.Hk * (p.tile_mode ? p.run_tiles : 1);
     int max_ctas = occ * n_sms;
-    if (p.reserve_sms > 0) {  // leave reserve_sms SMs' worth of CTA slots free, at most a third
-        const int keep = n_sms - (p.reserve_sms < n_sms / 3 ? p.reserve_sms : n_sms / 3);
-        max_ctas = occ * keep;
-    }
+    if (p.max_sms > 0 && p.max_sms < n_sms) max_ctas = occ * p.max_sms;
     const int per_cta = (U + max_ctas - 1) / max_ctas;
     const int grid = (U + per_cta - 1) / per_cta;
     return launch_pdl(decode_kernel<D, NT, W, SPL>, dim3(grid), dim3(W * 32), L.total, s, p);
@@ -747,7 +757,11 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const Combi
     constexpr int NW = kCombineThreads / 32;
     __shared__ float wm[NW], wl[NW];
     __shared__ float wo[NW][DS];
+    // launched as a programmatic dependent of the layer's last read: nothing is
+    // read before that grid (and every earlier dependency) has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next call's Q prep may be scheduled
+    tl_begin(p.tl);
     const int rh = blockIdx.x, r = rh / p.Hq, h = rh - r * p.Hq;
     const int d0 = blockIdx.y * DS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -760,6 +774,7 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const Combi
             for (int i = 0; i < VPL; ++i) dst[i] = __int_as_float(0x7fc00000);
             if (p.lse && lane == 0 && blockIdx.y == 0) p.lse[(int64_t)r * p.Hq + h] = __int_as_float(0x7fc00000);
         }
+        tl_finish(p.tl);
         return;
     }
     const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
@@ -829,6 +844,7 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const Combi
         for (int i = 0; i < VPL; ++i) dst[i] = ot[i] * inv;
         if (p.lse && lane == 0 && blockIdx.y == 0)
             p.lse[(int64_t)r * p.Hq + h] = (Lt > 0.f) ? (M + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+        tl_finish(p.tl);
     }
 }
 
@@ -857,12 +873,11 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t s) {
     if (blocks < 1) return cudaSuccess;
     const dim3 grid(blocks, p.D > kCombineDims ? p.D / kCombineDims : 1);
     switch (p.D) {
-        case 64: combine_kernel<64><<<grid, kCombineThreads, 0, s>>>(p); break;
-        case 128: combine_kernel<128><<<grid, kCombineThreads, 0, s>>>(p); break;
-        case 256: combine_kernel<256><<<grid, kCombineThreads, 0, s>>>(p); break;
+        case 64: return launch_pdl(combine_kernel<64>, grid, dim3(kCombineThreads), 0, s, p);
+        case 128: return launch_pdl(combine_kernel<128>, grid, dim3(kCombineThreads), 0, s, p);
+        case 256: return launch_pdl(combine_kernel<256>, grid, dim3(kCombineThreads), 0, s, p);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace kvs

@@ -21,6 +21,25 @@ __host__ __device__ inline int64_t vq_byte(int64_t t, int row, int NB) {
     return ((t / 32 * NB + row / 16) * 16 + row % 16) * 32 + t % 32;
 }
 
+// Launch timeline (kvs_timeline_begin): a record is two words {~first CTA
+// start, last CTA end} of %globaltimer (ns), each by atomic max from zero; a
+// kernel given a null record pointer stamps nothing.
+#ifdef __CUDACC__
+__device__ __forceinline__ unsigned long long tl_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// called by every CTA (thread 0 stamps)
+__device__ __forceinline__ void tl_begin(unsigned long long *tl) {
+    if (tl && threadIdx.x == 0) atomicMax(&tl[0], ~tl_now());
+}
+// called by thread 0 once the CTA's work is done
+__device__ __forceinline__ void tl_finish(unsigned long long *tl) {
+    if (tl && threadIdx.x == 0) atomicMax(&tl[1], tl_now());
+}
+#endif
+
 struct PageGeom {
     int P;               // tokens per page
     int Hk;              // kv heads
@@ -67,8 +86,8 @@ struct DecodeParams {
     const uint4 *qf;       // Q fragments [Hk][NT][D/16][32] (written by the Q prep kernel)
     int prep_q;            // launch_decode first (re)builds qf/qs from q
     int tile_mode;         // one CTA per (page, kv head, row tile) (ring chunks)
-    int reserve_sms;       // leave this many SMs' worth of CTA slots free of this launch (at
-                           // most a third of the GPU) for concurrent ring-chunk launches
+    int max_sms;           // > 0: use at most this many SMs' worth of CTA slots (resident reads
+                           // beside ring-chunk reads and refills); 0: every SM
     int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run
     int single_f16;        // Q and P' as single f16 operands (else f16 hi + lo pairs)
     int give_up_waits;     // test hook: every pipeline wait gives up at once, as if its copy
@@ -76,6 +95,8 @@ struct DecodeParams {
     unsigned long long *rec;  // ring-chunk read: the chunk's fill record (nullable, see FillParams)
     unsigned long long *acc;  // observation accumulator the first CTA adds the read to
     int rec_pages;            // pages of the chunk
+    unsigned long long *tl;       // timeline record of the attention launch (nullable)
+    unsigned long long *tl_prep;  // timeline record of the query-fragment launch (nullable)
     int n_items;
     uint32_t page[kMaxItems];
     uint32_t slot[kMaxItems];
@@ -108,6 +129,7 @@ struct PrefillParams {
     int R, Hq, G;
     long long pos0;
     float scale_log2;
+    unsigned long long *tl;  // timeline record (nullable)
     int n_splits;
     int split_begin[kMaxPrefillSplits + 1];  // item range of each split
     int split_id[kMaxPrefillSplits];         // logical split index (partials row)
@@ -127,6 +149,7 @@ struct CombineParams {
     int R, Hq, D, P;
     int split_pages;  // pages per split (1 for decode, the prefill split otherwise)
     long long pos0;
+    unsigned long long *tl;  // timeline record (nullable)
 };
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s);
 
@@ -139,11 +162,13 @@ struct QuantizeParams {
     uint8_t *page;  // device page base
     PageGeom geom;
     int t0, n;
+    unsigned long long *tl;  // timeline record (nullable)
 };
 cudaError_t launch_quantize(const QuantizeParams &p, cudaStream_t s);
 
 // Zero token slots [t0, P) of one device page (all sections of all heads).
-cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStream_t s);
+cudaError_t launch_clear_tail(uint8_t *page, const PageGeom &g, int t0, cudaStream_t s,
+                              unsigned long long *tl = nullptr);
 
 // ---------------------------------------------------------------- ring fill
 // Copy whole pages host -> device with SM loads (pinned host memory is
@@ -164,6 +189,7 @@ struct ObsAccumulator {  // all fields start at zero
 };
 struct FillParams {
     unsigned long long *rec;  // this refill's record (nullable)
+    unsigned long long *tl;   // timeline record (nullable)
     int n;
     int64_t page_bytes;
     const uint8_t *src[kMaxFillPages];

@@ -181,6 +181,7 @@ extern "C" kvs_status kvs_attend_pages_noalloc(const void *pages_dev, uint64_t p
     cp.P = (int)P;
     cp.split_pages = 1;
     cp.pos0 = (long long)pos0;
+    cp.tl = nullptr;
     cudaError_t e = kvs::launch_combine(cp, st);
     if (e != cudaSuccess) {
         kvs::set_thread_error(std::string("combine launch: ") + cudaGetErrorString(e));

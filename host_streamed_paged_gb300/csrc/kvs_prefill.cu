@@ -245,6 +245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    tl_begin(p.tl);
     const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
     const int split_idx = blockIdx.y;
     const int G = p.G, R = p.R, rt = (R + kTileRows - 1) / kTileRows;
@@ -660,6 +661,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
     cluster_sync();
     tc_after_sync();
     if (tid == 0 && *abort) atomicExch(p.status, 1);
+    tl_finish(p.tl);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 

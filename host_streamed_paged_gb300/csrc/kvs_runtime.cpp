@@ -116,9 +116,13 @@ struct kvs_ctx {
     // events: [0, R) ready, [R, 2R) consumed, 2R attn mark, 2R+1 copy mark,
     // one publish event per tail slot, then one mark per lane stream
     std::vector<cudaEvent_t> events;
-    int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0, ev_lane0 = 0, ev_pub_last = 0;
+    int ev_attn_mark = 0, ev_copy_mark = 0, ev_pub0 = 0, ev_lane0 = 0, ev_pub_last = 0, ev_clear0 = 0;
+    // per layer: a truncate's tail clear is queued on the resident-page stream and
+    // the attention stream has not waited for it yet (settle_clear)
+    std::vector<uint8_t> clear_pending;
     uint64_t pub_generation = 0;        // publishes recorded on the copy stream
     std::vector<uint64_t> lane_pub_seen;  // per stream: pub_generation it has waited for
+    std::vector<uint64_t> page_pub_gen;   // per (layer, page): pub_generation of its last publish
     std::vector<int> chunk_reader_sid;    // per chunk id % ring_n: stream its attention read ran on
 
     // timing of attention kernels (mask of KVS_TIME_*)
@@ -163,6 +167,11 @@ struct kvs_ctx {
     int res_sid() const { return 2 * n_lanes; }
     int ring0_sid() const { return 2 * n_lanes + 1; }
     int attn_sid_of_lane(int lane) const { return lane == 0 ? ring0_sid() : 2 * lane; }
+    // launch timeline (kvs_timeline_begin): the caller's device records and per-record meta
+    unsigned long long *tl_buf = nullptr;
+    uint32_t tl_max = 0, tl_dropped = 0;
+    bool tl_on = false;
+    std::vector<kvs_timeline_record> tl_meta;
     cudaStream_t res_stream = nullptr;    // created by kvs_create, lowest priority
     cudaStream_t ring0_stream = nullptr;  // created by kvs_create
     ~kvs_ctx() {
@@ -262,10 +271,11 @@ kvs_status fork_attn_lanes(kvs_ctx *c) {
 }
 
 // a publish (D2H of a completed tail page) was just enqueued on the copy
-// stream: copy lanes that later refill from host wait for it once
-kvs_status mark_publish(kvs_ctx *c) {
+// stream: a copy lane that later refills that page from host waits for it once
+kvs_status mark_publish(kvs_ctx *c, uint32_t layer, int64_t page) {
     kvs_status s = op_record(c, kCopy, c->ev_pub_last);
     if (s == KVS_OK) c->pub_generation++;
+    c->page_pub_gen[(size_t)layer * (size_t)c->max_pages + (size_t)page] = c->pub_generation;
     c->lane_pub_seen[kCopy] = c->pub_generation;  // the copy stream itself
     return s;
 }
@@ -285,7 +295,45 @@ kvs_status join_all_into_attn(kvs_ctx *c) {
         kvs_status s = join(c, sid, kAttn);
         if (s != KVS_OK) return s;
     }
+    std::fill(c->clear_pending.begin(), c->clear_pending.end(), 0);  // the resident-page stream joined
     return KVS_OK;
+}
+
+// A truncate zeroes the dropped token slots of the tail page on the
+// resident-page stream, so the clear is not a link of the attention stream's
+// layer-to-layer chain.  Work on the attention stream that touches that
+// layer's tail slots waits for it first (everything ordered after the
+// attention stream then is too); resident reads on the resident-page stream
+// follow it in stream order.
+kvs_status settle_clear(kvs_ctx *c, uint32_t layer) {
+    if (layer >= c->clear_pending.size() || !c->clear_pending[layer]) return KVS_OK;
+    kvs_status s = op_wait(c, kAttn, c->ev_clear0 + (int)layer);
+    if (s == KVS_OK) c->clear_pending[layer] = 0;
+    return s;
+}
+
+kvs_status settle_clears(kvs_ctx *c, uint32_t l0, uint32_t l1) {
+    for (uint32_t l = l0; l < l1 && l < c->clear_pending.size(); ++l) {
+        kvs_status s = settle_clear(c, l);
+        if (s != KVS_OK) return s;
+    }
+    return KVS_OK;
+}
+
+// the next timeline record for a launch (null when the timeline is off or full)
+unsigned long long *tl_take(kvs_ctx *c, uint32_t kind, uint32_t layer, int sid, uint32_t pages = 0) {
+    if (!c->tl_on || c->plan_only) return nullptr;
+    if (c->tl_meta.size() >= c->tl_max) {
+        c->tl_dropped++;
+        return nullptr;
+    }
+    kvs_timeline_record r = {};
+    r.kind = kind;
+    r.layer = layer;
+    r.stream = sid;
+    r.pages = pages;
+    c->tl_meta.push_back(r);
+    return c->tl_buf + 2 * (c->tl_meta.size() - 1);
 }
 
 // host pages -> device slots on the copy stream (ring fill or pool load)
@@ -320,6 +368,7 @@ kvs_status op_copy_pages(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> 
         kvs::FillParams fp;
         fp.rec = rec;
         fp.n = (int)std::min<size_t>(kvs::kMaxFillPages, pages.size() - i0);
+        fp.tl = tl_take(c, kind == KVS_OP_FILL ? KVS_TL_FILL : KVS_TL_POOL_LOAD, layer, sid, (uint32_t)fp.n);
         fp.page_bytes = c->geom.page_bytes;
         for (int j = 0; j < fp.n; ++j) {
             fp.src[j] = c->host_page_dev(layer, pages[i0 + j]);
@@ -394,12 +443,14 @@ void destroy_events(kvs_ctx *c) {
 
 kvs_status create_events(kvs_ctx *c) {
     const int R = (int)c->ring_n;
-    const int n = 2 * R + 2 + 2 * (int)c->cfg.n_layers + c->n_streams() + 1;
+    const int n = 2 * R + 2 + 2 * (int)c->cfg.n_layers + c->n_streams() + 1 + (int)c->cfg.n_layers;
     c->ev_attn_mark = 2 * R;
     c->ev_copy_mark = 2 * R + 1;
     c->ev_pub0 = 2 * R + 2;
     c->ev_lane0 = c->ev_pub0 + 2 * (int)c->cfg.n_layers;
     c->ev_pub_last = c->ev_lane0 + c->n_streams();
+    c->ev_clear0 = c->ev_pub_last + 1;
+    c->clear_pending.assign(c->cfg.n_layers, 0);
     c->pub_generation = 0;
     c->lane_pub_seen.assign(c->n_streams(), 0);
     c->events.assign(n, nullptr);
@@ -550,6 +601,9 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
     bool follow = !prev.empty();
     const int rsid = follow ? c->chunk_reader_sid[prev[0] % c->ring_n] : -1;
     for (int64_t p : prev) follow = follow && rsid >= 0 && c->chunk_reader_sid[p % c->ring_n] == rsid;
+    // a refill never follows a read on the caller's attention stream, where it
+    // would hold up the combine and the next call's work
+    if (rsid == kAttn) follow = false;
     kvs_status s;
     if (follow) {
         sid = rsid;
@@ -559,7 +613,12 @@ kvs_status fill_chunk(kvs_ctx *c, Chunk &ch) {
             if (s != KVS_OK) return s;
         }
     }
-    if (c->lane_pub_seen[sid] < c->pub_generation) {  // host pages published since: wait for them
+    // a page of this chunk published since this lane last waited: wait for the
+    // publishes (the copy stream runs them in order, so the last one covers all)
+    uint64_t need = 0;
+    for (int64_t p : ch.pages)
+        need = std::max(need, c->page_pub_gen[(size_t)ch.layer * (size_t)c->max_pages + (size_t)p]);
+    if (c->lane_pub_seen[sid] < need) {
         s = op_wait(c, sid, c->ev_pub_last);
         if (s != KVS_OK) return s;
         c->lane_pub_seen[sid] = c->pub_generation;
@@ -600,6 +659,29 @@ kvs_status pump(kvs_ctx *c) {
 
 // ---- attention launches
 
+// SMs a launch over resident pages may take while the layer also reads ring
+// chunks.  Those reads and the refills that follow them set the step's pace
+// (the host link is the bound); the resident reads only need to finish within
+// the layer.  Budget: enough SMs to read the resident units in about half the
+// time the layer's ring pages take over the link, at least an eighth of the
+// GPU, and never the SMs the ring chunks in flight need (two chunk-read CTAs
+// per SM, at most a third of the GPU).  Rates: ~200 GB/s host link on GB300,
+// and ~3.6 us of SM time per (page, kv head) unit and row tile of the
+// split-K kernel (measured, one row tile).
+int resident_sm_budget(const kvs_ctx *c, int64_t res_units_per_head, int row_tiles, int64_t ring_pages,
+                       int rows_x_heads) {
+    const int n_sms = kvs::current_device_sms();
+    const int64_t ring_ctas = (int64_t)c->n_lanes * c->chunk_pages * c->geom.Hk * ((rows_x_heads + 7) / 8);
+    const int ring_keep = (int)std::min<int64_t>((ring_ctas + 1) / 2, n_sms / 3);
+    const double link_bytes_per_us = 2.0e5;
+    const double stream_us = (double)ring_pages * (double)c->geom.page_bytes / link_bytes_per_us;
+    const double unit_sm_us = 3.6 * std::pow((double)row_tiles, 1.1);
+    const double res_sm_us = (double)res_units_per_head * c->geom.Hk * unit_sm_us;
+    int want = stream_us > 0 ? (int)std::ceil(res_sm_us / (0.5 * stream_us)) : n_sms;
+    want = std::max(want, n_sms / 8);
+    return std::max(1, std::min(want, n_sms - ring_keep));
+}
+
 kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
                         const std::vector<int64_t> &slots, kvs::DecodeParams &dp, uint32_t kind,
                         int sid = kAttn) {
@@ -626,6 +708,7 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
         kvs_status s = timed_begin(c, kind, &t0, sid);
         if (s != KVS_OK) return s;
         if (i0 > 0) dp.rec = nullptr;  // one record per chunk
+        dp.tl = tl_take(c, kind == KVS_TIME_RING ? KVS_TL_READ_RING : KVS_TL_READ_RESIDENT, layer, sid, (uint32_t)n);
         cudaError_t e = kvs::launch_decode(dp, c->stream(sid));
         if (e != cudaSuccess) return cuda_fail(c, e, "attention kernel launch");
         c->check_status = true;
@@ -819,6 +902,7 @@ kvs_status kvs_create(const kvs_config *cfg, kvs_ctx **out) {
         c->lanes[2 * l + 1] = static_cast<cudaStream_t>(cfg->lane_copy_streams[l - 1]);
     }
     c->max_pages = (int64_t)((cfg->max_tokens + cfg->page_tokens - 1) / cfg->page_tokens);
+    c->page_pub_gen.assign((size_t)cfg->n_layers * (size_t)c->max_pages, 0);
     c->prefill_split = (int64_t)prefill_split_of(cfg);
     c->split_chunks = (uint64_t)cfg->max_q_head * cfg->max_rows > 64ull * cfg->n_kv_head &&
                       prefill_geometry(cfg->head_dim, cfg->page_tokens);
@@ -957,6 +1041,10 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
     if (!c->plan_only && (!k_dev || !v_dev)) return fail(c, KVS_ERR_INVALID, "null K/V rows");
     LayerState &L = c->layers[layer];
     if (L.T + n_tokens > c->cfg.max_tokens) return fail(c, KVS_ERR_CAPACITY, "append beyond max_tokens");
+    {
+        kvs_status s0 = settle_clear(c, layer);
+        if (s0 != KVS_OK) return s0;
+    }
     const int P = c->geom.P;
     // Pre-check every eviction this append causes, so a refusal changes nothing.
     {
@@ -1033,7 +1121,8 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
             if (c->plan_only) {
                 c->st.kernel_launches++;
             } else {
-                cudaError_t e = kvs::launch_clear_tail(c->slot_ptr(tslot), c->geom, t0, c->attn);
+                cudaError_t e = kvs::launch_clear_tail(c->slot_ptr(tslot), c->geom, t0, c->attn,
+                                                       tl_take(c, KVS_TL_CLEAR, layer, kAttn));
                 if (e != cudaSuccess) return cuda_fail(c, e, "tail page clear");
                 c->st.kernel_launches++;
             }
@@ -1049,6 +1138,7 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
             qp.geom = c->geom;
             qp.t0 = t0;
             qp.n = (int)n;
+            qp.tl = tl_take(c, KVS_TL_APPEND, layer, kAttn);
             cudaError_t e = kvs::launch_quantize(qp, c->attn);
             if (e != cudaSuccess) return cuda_fail(c, e, "quantise/append launch");
         }
@@ -1069,7 +1159,7 @@ kvs_status kvs_append(kvs_ctx *c, uint32_t layer, const float *k_dev, const floa
             }
             s = op_record(c, kCopy, c->ev_pub0 + (int)tslot);
             if (s != KVS_OK) return s;
-            s = mark_publish(c);
+            s = mark_publish(c, layer, q);
             if (s != KVS_OK) return s;
             c->st.d2h_pages++;
             c->st.d2h_bytes += (uint64_t)c->geom.page_bytes;
@@ -1101,10 +1191,20 @@ kvs_status kvs_truncate(kvs_ctx *c, uint32_t layer, uint64_t n_tokens) {
         }
     }
     if (n_tokens % P != 0 && !c->plan_only) {
-        cudaError_t e = kvs::launch_clear_tail(c->slot_ptr(c->tail_slot(layer, new_last)), c->geom,
-                                               (int)(n_tokens % P), c->attn);
+        // on the resident-page stream, after everything enqueued on the
+        // attention stream (this layer's reads) and after a publish of the slot
+        const int rs = c->res_sid();
+        const int64_t ts = c->tail_slot(layer, new_last);
+        kvs_status s = join(c, kAttn, rs);
+        if (s == KVS_OK) s = op_wait(c, rs, c->ev_pub0 + (int)ts);
+        if (s != KVS_OK) return s;
+        cudaError_t e = kvs::launch_clear_tail(c->slot_ptr(ts), c->geom, (int)(n_tokens % P), c->stream(rs),
+                                               tl_take(c, KVS_TL_CLEAR, layer, rs));
         if (e != cudaSuccess) return cuda_fail(c, e, "truncate clear");
         c->st.kernel_launches++;
+        s = op_record(c, rs, c->ev_clear0 + (int)layer);
+        if (s != KVS_OK) return s;
+        c->clear_pending[layer] = 1;
     }
     L.T = n_tokens;
     return KVS_OK;
@@ -1175,6 +1275,10 @@ kvs_status kvs_set_residency(kvs_ctx *c, uint32_t layer, const uint8_t *mask, ui
     if (c->lease_layer >= 0) return fail(c, KVS_ERR_STATE, "residency change while a lease is held");
     LayerState &L = c->layers[layer];
     const int64_t complete = (int64_t)(L.T / c->geom.P);  // pages 0..complete-1 are full
+    {
+        kvs_status s0 = settle_clear(c, layer);
+        if (s0 != KVS_OK) return s0;
+    }
     if (c->graph_exec) {  // its baked slot schedule no longer holds
         if (!c->plan_only) cudaStreamSynchronize(c->attn);
         release_graph(c);
@@ -1327,6 +1431,10 @@ kvs_status kvs_lease_acquire(kvs_ctx *c, uint32_t layer, uint32_t extra_slots) {
     if (c->lease_layer >= 0) return fail(c, KVS_ERR_STATE, "a lease is already held");
     if (!c->queue.empty() || !c->announced.empty())
         return fail(c, KVS_ERR_STATE, "lease while prefetches are pending");
+    {
+        kvs_status s0 = settle_clear(c, layer);
+        if (s0 != KVS_OK) return s0;
+    }
     LayerState &L = c->layers[layer];
     std::vector<int64_t> pages;
     for (int64_t p = 0; p < n_pages_of(c, layer); ++p) {
@@ -1455,6 +1563,7 @@ kvs_status attend_prefill(kvs_ctx *c, uint32_t layer, const void *q_dev, uint32_
         cudaEvent_t t0;
         kvs_status ts = timed_begin(c, kind, &t0, kAttn);
         if (ts != KVS_OK) return ts;
+        pp.tl = tl_take(c, KVS_TL_PREFILL, layer, kAttn, (uint32_t)it);
         cudaError_t e = kvs::launch_prefill(pp, c->attn);
         if (e != cudaSuccess) return cuda_fail(c, e, "prefill kernel launch");
         c->check_status = true;
@@ -1561,6 +1670,10 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
     if (!c->announced.empty() && c->announced.front() != layer)
         return fail(c, KVS_ERR_STATE, "layers must be attended in the order they were prefetched");
     if (c->announced.empty()) plan_layer(c, layer);
+    {
+        kvs_status s0 = settle_clear(c, layer);
+        if (s0 != KVS_OK) return s0;
+    }
 
     const int P = c->geom.P;
     const int64_t last = (int64_t)((pos0 + n_rows - 1) / P);
@@ -1640,7 +1753,9 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             } else {
                 gp.prep_q = 1;
                 gp.n_items = 0;
+                gp.tl_prep = tl_take(c, KVS_TL_QPREP, layer, kAttn);
                 cudaError_t e = kvs::launch_decode(gp, c->attn);
+                gp.tl_prep = nullptr;
                 if (e != cudaSuccess) return cuda_fail(c, e, "query fragment launch");
                 gp.prep_q = 0;
             }
@@ -1658,23 +1773,23 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         if (!res_pages.empty()) {
             const bool ring_too = !c->queue.empty() && c->queue.front().layer == layer;
             int sid = kAttn;
+            int max_sms = 0;
             if (ring_too) {
                 sid = c->res_sid();
-                const int64_t ring_ctas =
-                    (int64_t)c->n_lanes * c->chunk_pages * c->geom.Hk * ((G * n_rows + 7) / 8);
-                dp.reserve_sms = (int)std::min<int64_t>(1 << 20, (ring_ctas + 1) / 2);
+                max_sms = resident_sm_budget(c, (int64_t)res_pages.size() * (int64_t)groups.size(),
+                                             (G * rpg + 7) / 8, (int64_t)streamed.size(), G * n_rows);
             }
             for (kvs::DecodeParams &gp : groups) {
-                gp.reserve_sms = dp.reserve_sms;
+                gp.max_sms = max_sms;
                 s = launch_items(c, layer, res_pages, res_slots, gp, KVS_TIME_RESIDENT, sid);
-                gp.reserve_sms = 0;
+                gp.max_sms = 0;
                 if (s != KVS_OK) return s;
             }
-            dp.reserve_sms = 0;
             c->st.resident_pages_read += res_pages.size() * (uint64_t)c->geom.Hk;
         }
         // ring chunks in order: ready fence, read, consumed fence, refill
         std::vector<int64_t> last_read(c->n_lanes, -1);  // per lane: last chunk read in this call
+        int chunk_in_layer = 0;
         while (!c->queue.empty() && c->queue.front().layer == layer) {
             Chunk &ch = c->queue.front();
             if (!ch.filled) {
@@ -1686,6 +1801,17 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             const int sid = c->attn_sid_of_lane(lane);  // this chunk's attention stream
             s = op_wait(c, sid, (int)(ch.id % c->ring_n));
             if (s != KVS_OK) return s;
+            // Stagger the lanes: the layer's first chunks are all in the ring when
+            // it starts; read at once, their refills would run side by side and
+            // the lanes would stay in phase (every lane reading while the link
+            // idles, then every lane refilling at a share of the link).  Each of
+            // the first n_lanes - 1 later chunks waits for the read before it, so a
+            // lane reads while the previous lane's refill has the link.
+            if (chunk_in_layer > 0 && chunk_in_layer < c->n_lanes) {
+                s = op_wait(c, sid, (int)c->ring_n + (int)((ch.id - 1) % c->ring_n));
+                if (s != KVS_OK) return s;
+            }
+            ++chunk_in_layer;
             std::vector<int64_t> pg, sl;
             for (size_t i = 0; i < ch.pages.size(); ++i) {
                 if (ch.pages[i] > last) continue;
@@ -1748,6 +1874,7 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
         cp.P = P;
         cp.split_pages = prefill ? (int)c->prefill_split : 1;
         cp.pos0 = (long long)pos0;
+        cp.tl = tl_take(c, KVS_TL_COMBINE, layer, kAttn);
         cudaError_t e = kvs::launch_combine(cp, c->attn);
         if (e != cudaSuccess) return cuda_fail(c, e, "combine launch");
     }
@@ -1788,6 +1915,7 @@ kvs_status kvs_sync(kvs_ctx *c, uint32_t timeout_ms) {
         std::this_thread::sleep_for(std::chrono::microseconds(20));
     }
     harvest_timers(c);
+    std::fill(c->clear_pending.begin(), c->clear_pending.end(), 0);  // every stream has drained
     if (c->check_status) {
         c->check_status = false;
         int status = 0;
@@ -1811,7 +1939,8 @@ kvs_status kvs_flush(kvs_ctx *c, uint32_t layer) {
     } else if (layer >= c->cfg.n_layers) {
         return fail(c, KVS_ERR_INVALID, "layer out of range");
     }
-    kvs_status s = join_attn_into_copy(c);
+    kvs_status s = settle_clears(c, l0, l1);
+    if (s == KVS_OK) s = join_attn_into_copy(c);
     if (s != KVS_OK) return s;
     for (uint32_t l = l0; l < l1; ++l) {
         const LayerState &L = c->layers[l];
@@ -1827,7 +1956,7 @@ kvs_status kvs_flush(kvs_ctx *c, uint32_t layer) {
         }
         s = op_record(c, kCopy, c->ev_pub0 + (int)ts);
         if (s != KVS_OK) return s;
-        s = mark_publish(c);
+        s = mark_publish(c, l, q);
         if (s != KVS_OK) return s;
         c->st.d2h_pages++;
         c->st.d2h_bytes += (uint64_t)c->geom.page_bytes;
@@ -1916,6 +2045,49 @@ kvs_status kvs_observe(kvs_ctx *c, kvs_policy_observation *out, int reset) {
     if (reset) {
         e = cudaMemset(obs_accumulator(c), 0, sizeof(a));
         if (e != cudaSuccess) return cuda_fail(c, e, "observation reset");
+    }
+    return KVS_OK;
+}
+
+kvs_status kvs_timeline_begin(kvs_ctx *c, void *records_dev, uint32_t max_records) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    if (!c->plan_only && max_records > 0 && (!records_dev || (reinterpret_cast<uintptr_t>(records_dev) & 7u)))
+        return fail(c, KVS_ERR_INVALID, "timeline records must be a non-null, 8-byte aligned device buffer");
+    c->tl_buf = static_cast<unsigned long long *>(records_dev);
+    c->tl_max = max_records;
+    c->tl_dropped = 0;
+    c->tl_meta.clear();
+    c->tl_on = true;
+    return KVS_OK;
+}
+
+kvs_status kvs_timeline_end(kvs_ctx *c) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    c->tl_on = false;
+    return KVS_OK;
+}
+
+kvs_status kvs_timeline_read(kvs_ctx *c, kvs_timeline_record *out, uint32_t max_out, uint32_t *n_out,
+                             uint32_t *n_dropped) {
+    if (!c) return KVS_ERR_INVALID;
+    c->err.clear();
+    const uint32_t n = (uint32_t)std::min<size_t>(max_out, c->tl_meta.size());
+    if (n_out) *n_out = n;
+    if (n_dropped) *n_dropped = c->tl_dropped;
+    if (n == 0) return KVS_OK;
+    if (!out) return fail(c, KVS_ERR_INVALID, "null output records");
+    std::vector<unsigned long long> raw(2 * (size_t)n, 0ull);
+    if (!c->plan_only) {
+        cudaError_t e = cudaMemcpy(raw.data(), c->tl_buf, raw.size() * sizeof(unsigned long long),
+                                   cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(c, e, "timeline read");
+    }
+    for (uint32_t i = 0; i < n; ++i) {
+        out[i] = c->tl_meta[i];
+        out[i].start_ns = raw[2 * i] ? ~raw[2 * i] : 0ull;
+        out[i].end_ns = raw[2 * i + 1];
     }
     return KVS_OK;
 }

@@ -88,6 +88,15 @@ class kvs_trace_op(ctypes.Structure):
                 ("c", ctypes.c_int64), ("d", ctypes.c_int64)]
 
 
+class kvs_timeline_record(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_uint32), ("layer", ctypes.c_uint32), ("stream", ctypes.c_int32),
+                ("pages", ctypes.c_uint32), ("start_ns", ctypes.c_uint64), ("end_ns", ctypes.c_uint64)]
+
+
+KVS_TL_KINDS = {1: "append", 2: "clear", 3: "qprep", 4: "read_resident", 5: "read_ring", 6: "combine",
+                7: "fill", 8: "pool_load", 9: "prefill"}
+
+
 class kvs_policy_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint32) for n in (
         "page_tokens", "n_layers", "budget_slots", "min_ring_slots", "max_ring_slots", "step_slots",
@@ -140,6 +149,9 @@ SIGNATURES = {
     "kvs_ring_info": ([_P, _P, _P], _I32),
     "kvs_stats": ([_P, _P, ctypes.c_int], _I32),
     "kvs_set_timing": ([_P, ctypes.c_int], _I32),
+    "kvs_timeline_begin": ([_P, _P, _U32], _I32),
+    "kvs_timeline_end": ([_P], _I32),
+    "kvs_timeline_read": ([_P, _P, _U32, _P, _P], _I32),
     "kvs_last_error": ([_P], ctypes.c_char_p),
     "kvs_debug_inject": ([_P, _U32, _U64], _I32),
     "kvs_trace_read": ([_P, _U64, _U64, _P, _P, _P], _I32),
@@ -328,6 +340,27 @@ def kvs_stats(ctx, reset=False) -> dict:
 
 def kvs_set_timing(ctx, mask=KVS_TIME_RESIDENT | KVS_TIME_RING) -> int:
     return _check(ctx, load().kvs_set_timing(ctx, int(mask)))
+
+
+def kvs_timeline_begin(ctx, records, max_records) -> int:
+    return _check(ctx, load().kvs_timeline_begin(ctx, _ptr(records), int(max_records)))
+
+
+def kvs_timeline_end(ctx) -> int:
+    return _check(ctx, load().kvs_timeline_end(ctx))
+
+
+def kvs_timeline_read(ctx, max_out):
+    """(list of per-launch dicts with kind names, dropped launches)."""
+    buf = (kvs_timeline_record * max(int(max_out), 1))()
+    n, dropped = ctypes.c_uint32(), ctypes.c_uint32()
+    _check(ctx, load().kvs_timeline_read(ctx, buf, int(max_out), ctypes.byref(n), ctypes.byref(dropped)))
+    out = []
+    for i in range(n.value):
+        r = {f: getattr(buf[i], f) for f, _ in kvs_timeline_record._fields_}
+        r["kind"] = KVS_TL_KINDS.get(r["kind"], str(r["kind"]))
+        out.append(r)
+    return out, dropped.value
 
 
 def kvs_attend_pages_noalloc(pages, pages_bytes, page_slots, page_tokens, n_kv_head, head_dim, q, q_dtype,
@@ -568,6 +601,24 @@ class KVStream:
 
     def set_timing(self, mask=KVS_TIME_RESIDENT | KVS_TIME_RING):
         return kvs_set_timing(self.ctx, mask)
+
+    def timeline_begin(self, max_records=1 << 16):
+        """Stamp every following launch (until timeline_end) into a device buffer of max_records."""
+        import torch
+        self._tl = torch.zeros(2 * max_records, dtype=torch.int64, device=self.arena.device)
+        return kvs_timeline_begin(self.ctx, self._tl, max_records)
+
+    def timeline_zero(self):
+        """Zero the records on the attention stream (before the stamped launches run again)."""
+        import torch
+        with torch.cuda.stream(self.attn_stream):
+            self._tl.zero_()
+
+    def timeline_end(self):
+        return kvs_timeline_end(self.ctx)
+
+    def timeline_read(self):
+        return kvs_timeline_read(self.ctx, self._tl.numel() // 2)
 
     def graph_begin(self):
         return kvs_graph_begin(self.ctx)

@@ -571,6 +571,48 @@ kvs_status kvs_stats(kvs_ctx *ctx, kvs_stats_t *out, int reset);
 kvs_status kvs_set_timing(kvs_ctx *ctx, int mask);
 
 /*
+ * Launch timeline -- library API for measurement (no counterpart on the
+ * pages; it shows what the V2 README, "KV data movement and attention",
+ * describes: refills for upcoming layers running while the current layer is
+ * attended).  Between kvs_timeline_begin and kvs_timeline_end every kernel
+ * the context launches takes the next of `max_records` records in the
+ * caller's device buffer `records_dev` (16 bytes each, 8-byte aligned): the
+ * kernel's first CTA start (stored complemented) and its last CTA end, in
+ * %globaltimer nanoseconds, each written by atomic max.  The caller zeroes
+ * the records before the launches run (cudaMemsetAsync on attn_stream) --
+ * also before each replay of a step graph captured inside the window, whose
+ * launches keep the records they were captured with.  Copy-engine refills
+ * (KVS_FLAG_DMA_FILL) are not kernels and take no record.  Launches beyond
+ * max_records are counted in kvs_timeline_read's *n_dropped and not stamped.
+ * kvs_timeline_read (after kvs_sync) copies the records back and returns, per
+ * launch, its kind, layer, stream and pages with the two times (0 when the
+ * launch has not run).  A new kvs_timeline_begin restarts at record 0.
+ */
+#define KVS_TL_APPEND 1u      /* quantise rows into the tail page (kvs_append) */
+#define KVS_TL_CLEAR 2u       /* zero the tail page's unused token slots */
+#define KVS_TL_QPREP 3u       /* query fragments (kvs_attend) */
+#define KVS_TL_READ_RESIDENT 4u /* attention over tail and resident-pool pages */
+#define KVS_TL_READ_RING 5u   /* attention over one ring chunk */
+#define KVS_TL_COMBINE 6u     /* log-sum-exp combine (kvs_attend) */
+#define KVS_TL_FILL 7u        /* ring refill: host pages into ring slots */
+#define KVS_TL_POOL_LOAD 8u   /* host pages into the resident pool (kvs_set_residency) */
+#define KVS_TL_PREFILL 9u     /* tensor-core prefill over one batch of splits */
+typedef struct {
+    uint32_t kind;      /* KVS_TL_* */
+    uint32_t layer;
+    int32_t stream;     /* 0 attn_stream, 1 copy_stream, 2k / 2k + 1 lane k's attention /
+                           copy stream, 2 n_lanes the resident-page stream, 2 n_lanes + 1
+                           lane 0's ring-read stream */
+    uint32_t pages;     /* pages the launch reads or moves (0 for other kinds) */
+    uint64_t start_ns;  /* first CTA start, %globaltimer */
+    uint64_t end_ns;    /* last CTA end */
+} kvs_timeline_record;
+kvs_status kvs_timeline_begin(kvs_ctx *ctx, void *records_dev, uint32_t max_records);
+kvs_status kvs_timeline_end(kvs_ctx *ctx);
+kvs_status kvs_timeline_read(kvs_ctx *ctx, kvs_timeline_record *out, uint32_t max_out, uint32_t *n_out,
+                             uint32_t *n_dropped);
+
+/*
  * Step graphs.  One decode (or verify) step issues many small launches and
  * ready/consumed handshakes; capturing the step once as a CUDA graph and
  * replaying it removes the host cost of issuing them.  kvs_graph_begin starts

@@ -585,3 +585,16 @@ def test_observe_on_a_plan_only_context_reports_only_the_context_length():
     assert (o.context_tokens, o.streamed_reads, o.ready_misses, o.ring_occupancy, o.copy_busy) == (333, 0, 0, 0.0, 0.0)
     s = st.stats()
     assert s["observed_reads"] == 0 and s["copy_busy"] == 0.0
+
+
+def test_timeline_in_a_plan_only_context_stamps_nothing():
+    st = _plan_stream(2, 2, 64, 64 * 6, 2, 1, 2 * 2 + 2 + 12)
+    for l in range(2):
+        kvs.kvs_append(st.ctx, l, None, None, 64 * 6)
+    assert kvs.kvs_timeline_begin(st.ctx, None, 16) == kvs.KVS_OK
+    st.prefetch(0)
+    st.attend_plan(0, 1, 12, 64 * 6 - 1)
+    assert kvs.kvs_timeline_end(st.ctx) == kvs.KVS_OK
+    recs, dropped = kvs.kvs_timeline_read(st.ctx, 16)
+    assert recs == [] and dropped == 0
+    st.close()

@@ -719,3 +719,44 @@ def test_prefill_streamed_equals_resident_bitwise():
         assert st.stats()["h2d_pages"] > 0
         assert np.array_equal(out, base[4]) and np.array_equal(lse, base[5]), (ring, chunk, lanes)
         st.close()
+
+
+def test_timeline_records_every_launch_and_reads_follow_their_copies():
+    """The launch timeline of a streamed decode step: every stamped launch ran
+    (start <= end), the kinds match the step's work, and the k-th ring-chunk
+    read starts only after the k-th ring refill has ended (the ready fence,
+    observed on the device clock)."""
+    P, Hk, G, D, L = 64, 2, 6, 128, 2
+    T = 64 * 12 + 5
+    Hq = G * Hk
+    st = make_stream(P, L, Hk, D, Hq, 1, T + 1, ring=4, chunk=1, pool_pages=L * 4, lanes=2)
+    hist = _fill(st, L, T, Hk, D)
+    npages = math.ceil(T / P)
+    for l in range(L):
+        mask = np.zeros(npages, np.uint8)
+        mask[[1, 4, 7]] = 1
+        st.set_residency(l, mask)
+    st.sync()
+    st.timeline_begin(4096)
+    st.prefetch(0)
+    outs = []
+    for l in range(L):
+        if l + 1 < L:
+            st.prefetch(l + 1)
+        q = queries(SEED, l, 1, Hq, D)
+        outs.append((q, attend(st, l, q, T - 1, 0.09)))
+    st.timeline_end()
+    recs, dropped = st.timeline_read()
+    assert dropped == 0 and recs
+    for r in recs:
+        assert 0 < r["start_ns"] <= r["end_ns"], r
+    kinds = [r["kind"] for r in recs]
+    assert kinds.count("combine") == L and kinds.count("qprep") == L
+    fills = [r for r in recs if r["kind"] == "fill"]
+    reads = [r for r in recs if r["kind"] == "read_ring"]
+    assert len(fills) == len(reads) == st.stats()["ring_chunks"] > 0
+    for f, r in zip(fills, reads):
+        assert (f["layer"], f["pages"]) == (r["layer"], r["pages"])
+        assert r["start_ns"] >= f["end_ns"], (f, r)
+    for l, (q, (o, lse)) in enumerate(outs):
+        check_parity(o, lse, *oracle_ref(*hist[l], q, T - 1, 0.09))
