@@ -51,6 +51,11 @@ WORKLOADS = {
               "Q8_0 K / Q4_0 V, 50% of pages resident (seeded), rest streamed via an 8-slot ring "
               "with next-layer prefetch (4-page chunks on 2 lanes)"),
         L=64, T=32768, R=1, ring=8, chunk=4, lanes=2, residency=("random", 0.5)),
+    "single4k": dict(
+        desc=("single layer decode: 1 query row, context 4096, 8 q / 2 kv heads (GQA), head_dim 128, page 256, "
+              "all 16 pages resident, Q8_0 K / Q4_0 V from seeded N(0,1)"),
+        L=1, T=4096, R=1, ring=2, chunk=1, lanes=1, residency=("prefix_frac", 1.0),
+        geom=dict(Hq=8, Hk=2, D=128, P=256)),
     "decode32k_small": dict(  # a reduced copy for quick checks and profiling captures
         desc="decode stack, 8 layers, otherwise as decode32k",
         L=8, T=32768, R=1, ring=8, chunk=4, lanes=2, residency=("random", 0.5)),
@@ -329,6 +334,48 @@ def run_reference(args, wl):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# The other configurations' headline numbers, carried on the default line: each
+# runs as its own process (its history is built from scratch and freed after),
+# with a short timed region and the oracle on one sampled layer for parity.
+EXTRAS = [
+    ("single4k", []),
+    ("verify163k", []),
+    ("prefill131k_1layer", ["--workload", "prefill131k", "--layers", "1"]),
+    ("prefill131k", []),
+    ("long262k_1row", ["--workload", "long262k"]),
+    ("long262k_4rows", ["--workload", "long262k", "--rows", "4"]),
+    ("resident131k", []),
+]
+
+
+def run_extras(args):
+    out = {}
+    for name, extra in EXTRAS:
+        cmd = [sys.executable, os.path.abspath(__file__), "--steps", "5", "--warmup", "3", "--cpu-layers", "1",
+               "--no-extras", "--no-timeline", "--operands", args.operands]
+        cmd += extra if extra else ["--workload", name]
+        t0 = time.perf_counter()
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=600)
+            d = json.loads([x for x in r.stdout.strip().splitlines() if x.startswith("{")][-1])
+        except Exception as e:  # noqa: BLE001 - reported, never fatal to the main line
+            out[name] = {"error": f"{type(e).__name__}: {str(e)[:200]}"}
+            continue
+        roof = d.get("roofline") or {}
+        out[name] = {
+            "config": d["config"]["workload"], "layers": d["config"]["layers"], "rows": d["config"]["rows"],
+            "tokens_per_s": d["value"], "ms_per_step": d["ms_per_step"], "e2e_tokens_per_s": d["e2e"]["value"],
+            "kv_gbs": d["kv_gbs"], "h2d_frac": d["h2d"]["frac"] if d["h2d"]["bytes_per_step"] else None,
+            "roofline": {k: roof.get(k) for k in ("bound", "achieved", "peak", "unit", "frac", "ms_per_launch")},
+            "tflops": d.get("tflops"),
+            "parity_max_rel_err": (d.get("parity") or {}).get("max_rel_err"),
+            "clocks_sm_mhz": (d.get("clocks") or {}).get("sm_mhz"),
+            "throttle_reasons": (d.get("clocks") or {}).get("reasons"),
+            "steps": d["steps"], "wall_s": time.perf_counter() - t0,
+        }
+    return out
 
 
 def run_ours(args, wl):
@@ -610,6 +657,11 @@ def run_ours(args, wl):
         if prefill:
             line["tflops"] = alg_flops_per_layer(wl) * L / (ms_step * 1e-3) / 1e12
         if rank == 0:
+            if args.extras and world == 1 and frac is None and args.workload == "decode32k" and not args.overridden:
+                st.close()
+                torch.cuda.synchronize(dev)
+                torch.cuda.empty_cache()
+                line["workloads"] = run_extras(args)
             print(json.dumps(line), flush=True)
     st.close()
     if dist:
@@ -639,13 +691,15 @@ def main():
                     help="split-K attention operands: single f16 values (Q and P' rounded once), or f16 "
                          "hi + lo pairs (about 22 significant bits)")
     ap.add_argument("--no-timeline", action="store_true", help="skip the stamped-timeline replay")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="do not run the other configurations after the default one")
     ap.add_argument("--timeline-out", default="", help="write the stamped launches of one step as CSV")
     ap.add_argument("--fill", choices=["default", "sm", "dma"], default="default",
                     help="ring refills by the SM fill kernel or the copy engines (default: the workload's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(WORKLOADS[args.workload])
-    wl.update(GEOM)
+    wl.update(wl.pop("geom", GEOM))
     for key, name in (("ring", "ring"), ("chunk", "chunk"), ("layers", "L"), ("lanes", "lanes")):
         v = getattr(args, key)
         if v:
@@ -662,6 +716,8 @@ def main():
         kind = "arena_frac" if wl["residency"][0] == "arena_frac" else "prefix_frac"
         wl["residency"] = (kind, args.resident)
         wl["desc"] += f" [resident override: {args.resident}]"
+    args.overridden = any((args.ring, args.chunk, args.layers, args.lanes, args.rows, args.resident >= 0,
+                           args.fill != "default", args.sweep))
     if args.impl == "reference":
         run_reference(args, wl)
     else:
