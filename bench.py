@@ -82,13 +82,20 @@ WORKLOADS = {
 GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the roofline kernel,
-# from one ncu capture of that launch on a GB300.  resident131k: 218.21 MB read + 8.97 MB written,
-# captured with
+# from one ncu capture of that launch on a GB300 (a workload missing here, or a kernel changed since
+# its capture, reports traffic as null).
+# resident131k, single-f16 operand mode: 218.19 MB read + 9.16 MB written, captured with
 #   ncu --set full --clock-control none -k regex:decode_kernel -s 4 -c 1 -o <report> \
-#       python bench.py --workload resident131k --layers 1 --steps 1 --warmup 3 --no-cpu
-# A workload missing here, or a kernel changed since its capture, reports traffic as null.
+#       python bench.py --workload resident131k --layers 1 --steps 1 --warmup 3 --no-cpu --no-timeline
+# decode32k: the resident-page launch of a layer (64 pages x 4 kv heads, 27.26 MB algorithmic):
+# 27.33 MB read, 0 written (the 1.5 MB of partials stay in L2), the same in every layer, captured on
+# a 2-layer copy of the workload with
+#   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum,launch__grid_size \
+#       --clock-control none -k regex:decode_kernel -c 60 --csv \
+#       python bench.py --no-cpu --no-extras --no-timeline --layers 2 --steps 1 --warmup 3
 TRAFFIC = {
-    "resident131k": (227.17e6, "ncu capture of one decode_kernel launch (resident131k, 1 layer)"),
+    "resident131k": (227.35e6, "ncu capture of one decode_kernel launch (resident131k, 1 layer)"),
+    "decode32k": (27.33e6, "ncu capture of the resident decode_kernel launches (decode32k, 2 layers)"),
 }
 
 

@@ -33,7 +33,6 @@
 #include <algorithm>
 #include <climits>
 #include <chrono>
-#include <cmath>
 #include <deque>
 #include <string>
 #include <thread>
@@ -658,29 +657,6 @@ kvs_status pump(kvs_ctx *c) {
 }
 
 // ---- attention launches
-
-// SMs a launch over resident pages may take while the layer also reads ring
-// chunks.  Those reads and the refills that follow them set the step's pace
-// (the host link is the bound); the resident reads only need to finish within
-// the layer.  Budget: enough SMs to read the resident units in about half the
-// time the layer's ring pages take over the link, at least an eighth of the
-// GPU, and never the SMs the ring chunks in flight need (two chunk-read CTAs
-// per SM, at most a third of the GPU).  Rates: ~200 GB/s host link on GB300,
-// and ~3.6 us of SM time per (page, kv head) unit and row tile of the
-// split-K kernel (measured, one row tile).
-int resident_sm_budget(const kvs_ctx *c, int64_t res_units_per_head, int row_tiles, int64_t ring_pages,
-                       int rows_x_heads) {
-    const int n_sms = kvs::current_device_sms();
-    const int64_t ring_ctas = (int64_t)c->n_lanes * c->chunk_pages * c->geom.Hk * ((rows_x_heads + 7) / 8);
-    const int ring_keep = (int)std::min<int64_t>((ring_ctas + 1) / 2, n_sms / 3);
-    const double link_bytes_per_us = 2.0e5;
-    const double stream_us = (double)ring_pages * (double)c->geom.page_bytes / link_bytes_per_us;
-    const double unit_sm_us = 3.6 * std::pow((double)row_tiles, 1.1);
-    const double res_sm_us = (double)res_units_per_head * c->geom.Hk * unit_sm_us;
-    int want = stream_us > 0 ? (int)std::ceil(res_sm_us / (0.5 * stream_us)) : n_sms;
-    want = std::max(want, n_sms / 8);
-    return std::max(1, std::min(want, n_sms - ring_keep));
-}
 
 kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &pages,
                         const std::vector<int64_t> &slots, kvs::DecodeParams &dp, uint32_t kind,
@@ -1776,8 +1752,10 @@ kvs_status kvs_attend(kvs_ctx *c, uint32_t layer, const void *q_dev, int32_t q_d
             int max_sms = 0;
             if (ring_too) {
                 sid = c->res_sid();
-                max_sms = resident_sm_budget(c, (int64_t)res_pages.size() * (int64_t)groups.size(),
-                                             (G * rpg + 7) / 8, (int64_t)streamed.size(), G * n_rows);
+                const int n_sms = kvs::current_device_sms();
+                const int64_t ring_ctas =
+                    (int64_t)c->n_lanes * c->chunk_pages * c->geom.Hk * ((G * std::min(rpg, n_rows) + 7) / 8);
+                max_sms = n_sms - (int)std::min<int64_t>((ring_ctas + 1) / 2, n_sms / 3);
             }
             for (kvs::DecodeParams &gp : groups) {
                 gp.max_sms = max_sms;
