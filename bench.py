@@ -67,7 +67,7 @@ WORKLOADS = {
     "prefill131k": dict(
         desc=("prefill chunk: 256 fp16 query rows appended at context 131072, causal, 24 q / 4 kv heads, D 256, "
               "page 256, Q8_0 K / Q4_0 V, tcgen05 tensor-core path"),
-        L=64, T=131072 + 256, R=256, ring=8, chunk=2, lanes=2, residency=("prefix_frac", 1.0), q_f16=True),
+        L=64, T=131072 + 256, R=256, ring=16, chunk=2, lanes=2, residency=("prefix_frac", 1.0), q_f16=True),
     "long262k": dict(
         desc=("long-context decode: 64 layers, context 262144, 24 q / 4 kv heads, D 256, page 256, Q8_0 K / "
               "Q4_0 V, fixed 2048 MiB arena split between resident pages (per-layer prefixes) and the ring "
@@ -410,7 +410,8 @@ def run_ours(args, wl):
     st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=D, max_q_head=Hq, max_rows=R,
                       max_tokens=T, ring_slots=wl["ring"], chunk_pages=wl["chunk"], arena_slots=arena_slots,
                       device=dev, lanes=wl.get("lanes", 1), dma_fill=wl.get("dma", False),
-                      host_alloc=args.host_alloc, f16_operands=args.operands == "f16")
+                      host_alloc=args.host_alloc, f16_operands=args.operands == "f16",
+                      prefill_split_pages=wl.get("split", 0))
     ceiling = h2d_ceiling(torch, dev)
 
     # history: seeded rows appended through the KV writer
@@ -719,13 +720,14 @@ def main():
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="do not run the other configurations after the default one")
     ap.add_argument("--timeline-out", default="", help="write the stamped launches of one step as CSV")
+    ap.add_argument("--split", type=int, default=0, help="override the tensor-core prefill split (pages)")
     ap.add_argument("--fill", choices=["default", "sm", "dma"], default="default",
                     help="ring refills by the SM fill kernel or the copy engines (default: the workload's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = dict(WORKLOADS[args.workload])
     wl.update(wl.pop("geom", GEOM))
-    for key, name in (("ring", "ring"), ("chunk", "chunk"), ("layers", "L"), ("lanes", "lanes")):
+    for key, name in (("ring", "ring"), ("chunk", "chunk"), ("layers", "L"), ("lanes", "lanes"), ("split", "split")):
         v = getattr(args, key)
         if v:
             wl[name] = v
@@ -741,7 +743,7 @@ def main():
         kind = "arena_frac" if wl["residency"][0] == "arena_frac" else "prefix_frac"
         wl["residency"] = (kind, args.resident)
         wl["desc"] += f" [resident override: {args.resident}]"
-    args.overridden = any((args.ring, args.chunk, args.layers, args.lanes, args.rows, args.resident >= 0,
+    args.overridden = any((args.ring, args.chunk, args.layers, args.lanes, args.rows, args.split, args.resident >= 0,
                            args.fill != "default", args.sweep))
     if args.impl == "reference":
         run_reference(args, wl)
