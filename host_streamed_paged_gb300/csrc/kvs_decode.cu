@@ -151,7 +151,7 @@ __host__ __device__ inline int pv_parts(int D, int P) {
 
 // Shared-memory carve of decode_kernel<D, NT, W, SPL> (bytes; page size P, S stages).
 struct DecodeSmem {
-    int stage, sc, red, obuf, rowoff, rowtab, bar, total, stages;
+    int stage, sc, red, obuf, obs, rowoff, rowtab, bar, total, stages;  // obs: output row stride (floats)
 };
 __host__ __device__ inline int align_to(int x, int a) { return (x + a - 1) / a * a; }
 __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, int stages) {
@@ -164,9 +164,11 @@ __host__ __device__ inline DecodeSmem decode_smem(int D, int NT, int W, int P, i
     s.sc = align_to(stages * head, 128);
     s.red = align_to(s.sc + MR * SP * 4, 16);
     const int red_end = s.red + (in_reg ? 0 : (pv_parts(D, P) - 1) * MR * D * 4);
-    // the output tile reuses the score buffer when it fits there
-    s.obuf = (SP >= D) ? s.sc : align_to(red_end, 16);
-    const int obuf_end = (SP >= D) ? red_end : s.obuf + MR * D * 4;
+    // the output tile reuses the score buffer when it fits there; its row stride
+    // is 4 mod 32 floats, so a warp's fragment writes fall on distinct banks
+    s.obs = (SP >= D + 4) ? SP : D + 4;
+    s.obuf = (SP >= D + 4) ? s.sc : align_to(red_end, 16);
+    const int obuf_end = (SP >= D + 4) ? red_end : s.obuf + MR * s.obs * 4;
     s.rowoff = align_to(red_end > obuf_end ? red_end : obuf_end, 16);  // MR ints: partial row offsets
     s.rowtab = align_to(s.rowoff + MR * 4, 16);  // 64 int2 per CTA: (mg / G, (mg % G) * R + mg / G)
     s.bar = align_to(s.rowtab + 64 * 8, 16);
@@ -585,7 +587,11 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                             }
                 }
             }
-            // rows gid + 8 (high-nibble dims) carried 16 * (code - 8)
+            // This warp owns dims 32 b .. 32 b + 31 of every row: it stages them in its
+            // own columns of the output tile and stores them itself, 128 contiguous
+            // bytes per row, so no CTA barrier separates staging and store.  Rows
+            // gid + 8 (high-nibble dims) carried 16 * (code - 8).
+            const int OS = L.obs;
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -594,17 +600,16 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                     for (int e = 0; e < 4; ++e) {
                         const int dim = 32 * b + mt * 8 + gid + ((e >= 2) ? 16 : 0);
                         const int m = nt * 8 + 2 * tig + (e & 1);
-                        obuf[m * D + dim] = (e >= 2) ? acc[0][mt][nt][e] * 0.0625f : acc[0][mt][nt][e];
+                        obuf[m * OS + dim] = (e >= 2) ? acc[0][mt][nt][e] * 0.0625f : acc[0][mt][nt][e];
                     }
-        }
-        __syncthreads();
-        // coalesced partial store of the valid rows (row offsets from the table)
-        const int urows = rows - mo < MR ? rows - mo : MR;
-        const int64_t split_base = (int64_t)split * p.Hq * R;
-        for (int c = threadIdx.x; c < urows * (D / 4); c += NTH) {
-            const int m = c / (D / 4), d4 = (c % (D / 4)) * 4;
-            *reinterpret_cast<float4 *>(p.part_o + (split_base + rowoff[m]) * D + d4) =
-                *reinterpret_cast<const float4 *>(obuf + m * D + d4);
+            __syncwarp();
+            // the valid rows, at their partial rows (offsets from the table)
+            const int urows = rows - mo < MR ? rows - mo : MR;
+            const int64_t split_base = (int64_t)split * p.Hq * R;
+            const int d4 = 32 * b + 4 * (lane & 7);
+            for (int m = lane >> 3; m < urows; m += 4)
+                *reinterpret_cast<float4 *>(p.part_o + (split_base + rowoff[m]) * D + d4) =
+                    *reinterpret_cast<const float4 *>(obuf + m * OS + d4);
         }
         __syncthreads();  // obuf / sc free for the next unit
     }
