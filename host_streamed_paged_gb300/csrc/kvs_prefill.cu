@@ -57,19 +57,18 @@ constexpr uint32_t kSpinLimit = 1u << 26;
 constexpr int kQBytes = kTileRows * kD * 2;   // 64 KB: 4 atoms (64 dims) of 128 rows x 128 B
 constexpr int kKBytes = kHalfN * kD * 2;      // 32 KB per stage: 4 atoms (64 dims) of 64 key rows
 constexpr int kVBytes = kHalfD * kBN * 2;     // 32 KB per stage: 2 atoms (64 keys) of 128 dim rows
-constexpr int kPBytes = kTileRows * kBN * 2;  // 32 KB: 2 atoms (64 keys) of 128 rows x 128 B
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;        // 2 stages
 constexpr int kOffV = kOffK + 2 * kKBytes;    // 2 stages
-constexpr int kOffP = kOffV + 2 * kVBytes;
-constexpr int kOffBar = kOffP + kPBytes;      // mbarriers (kNumBars x 8 B)
+constexpr int kOffBar = kOffV + 2 * kVBytes;  // mbarriers (kNumBars x 8 B)
 constexpr int kNumBars = 16;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;  // TMEM base address written by tcgen05.alloc
 constexpr int kOffAbort = kOffTmem + 8;
 constexpr int kOffSlots = kOffAbort + 8;          // device slot of each page of the split
 constexpr int kSmemBytes = kOffSlots + kMaxPrefillSplitPages * 4 + 1024;  // + slack to align the base
 
-constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 128) and [128, 256), O at [256, 512)
+constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 128) and [128, 256), O at [256, 512);
+                                     // P_j (f16 pairs, 64 columns) overwrites S_j's first half
 constexpr uint32_t kColO = 256;
 // barrier indices.  "Full" barriers live in the leader and count arrivals
 // from both CTAs (4 warps each); the others are armed by multicast commits in
@@ -160,6 +159,16 @@ __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// D (TMEM of both CTAs) = A (TMEM of both: each CTA's 128 rows, f16 pairs per
+// column) * B (smem of both, N split) [+ D]
+__device__ __forceinline__ void mma_pair_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
 // arrive on barrier `bar` (same offset) of both CTAs once the pair's MMAs issued so far are done
@@ -475,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
         if (rank == 0 && lane == 0) {
             // descriptors of the tile bases; a k-step adds its byte offset / 16
             const uint64_t dq = smem_desc(smem_u32(smem + kOffQ)), dk = smem_desc(smem_u32(smem + kOffK));
-            const uint64_t dv = smem_desc(smem_u32(smem + kOffV)), dp = smem_desc(smem_u32(smem + kOffP));
+            const uint64_t dv = smem_desc(smem_u32(smem + kOffV));
             const uint32_t id_s = idesc_f16(2 * kTileRows, kBN), id_o = idesc_f16(2 * kTileRows, kD);
             auto issue_s = [&](int j) {
                 const uint32_t ts = tmem + (uint32_t)((j & 1) * kBN);
@@ -492,10 +501,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
             auto issue_pv = [&](int j) {
                 const uint64_t dvj = dv + (uint64_t)(((j & 1) * kVBytes) >> 4);
 #pragma unroll
-                for (int s = 0; s < kBN / 16; ++s) {  // 16 keys per k-step, 64 per swizzle atom
-                    const uint64_t ap = (uint64_t)(((s >> 2) * (kTileRows * 128) + (s & 3) * 32) >> 4);
+                // A = P_j in TMEM over S_j's buffer: 16 keys per k-step = 8 columns.  S_{j+2},
+                // which overwrites that buffer, is issued after this in program order, and
+                // the tensor pipe runs one thread's MMAs in order
+                const uint32_t tp = tmem + (uint32_t)((j & 1) * kBN);
+                for (int s = 0; s < kBN / 16; ++s) {  // 16 keys per k-step, 64 per swizzle atom of V
                     const uint64_t bv = (uint64_t)(((s >> 2) * (kHalfD * 128) + (s & 3) * 32) >> 4);
-                    mma_pair(tmem + kColO, dp + ap, dvj + bv, id_o, (j > 0 || s > 0) ? 1u : 0u);
+                    mma_pair_ta(tmem + kColO, tp + (uint32_t)(8 * s), dvj + bv, id_o, (j > 0 || s > 0) ? 1u : 0u);
                 }
                 mma_commit_both(bar(kBarVEmpty + (j & 1)));
                 mma_commit_both(bar(kBarODone));
@@ -590,7 +602,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                 pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
             }
             l_sum += (b4[0] + b4[1]) + (b4[2] + b4[3]);
-            // PV_{j-1} done: the P buffer is free and O may be rescaled
+            // PV_{j-1} done: O may be rescaled
             if (j >= 1) {
                 ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort);
                 if (!ok) break;
@@ -609,12 +621,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 }
             }
-            uint8_t *pbuf = smem + kOffP;
-#pragma unroll
-            for (int c8 = 0; c8 < kBN / 8; ++c8)
-                *reinterpret_cast<uint4 *>(pbuf + sw128(kTileRows, row, c8 * 8)) =
-                    make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-            proxy_fence();
+            // P_j as f16 pairs into the first 64 columns of S_j's buffer (this
+            // thread's row was read out of it above)
+            {
+                const uint32_t tp = lane_base + (uint32_t)((j & 1) * kBN);
+                tmem_st32(tp, reinterpret_cast<const float *>(pk));
+                tmem_st32(tp + 32, reinterpret_cast<const float *>(pk + 32));
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
             tc_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(lead_bar(kBarPFull));
