@@ -500,11 +500,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
             };
             auto issue_pv = [&](int j) {
                 const uint64_t dvj = dv + (uint64_t)(((j & 1) * kVBytes) >> 4);
-#pragma unroll
                 // A = P_j in TMEM over S_j's buffer: 16 keys per k-step = 8 columns.  S_{j+2},
                 // which overwrites that buffer, is issued after this in program order, and
                 // the tensor pipe runs one thread's MMAs in order
                 const uint32_t tp = tmem + (uint32_t)((j & 1) * kBN);
+#pragma unroll
                 for (int s = 0; s < kBN / 16; ++s) {  // 16 keys per k-step, 64 per swizzle atom of V
                     const uint64_t bv = (uint64_t)(((s >> 2) * (kHalfD * 128) + (s & 3) * 32) >> 4);
                     mma_pair_ta(tmem + kColO, tp + (uint32_t)(8 * s), dvj + bv, id_o, (j > 0 || s > 0) ? 1u : 0u);
