@@ -377,6 +377,7 @@ def run_extras(args):
             "kv_gbs": d["kv_gbs"], "h2d_frac": d["h2d"]["frac"] if d["h2d"]["bytes_per_step"] else None,
             "roofline": {k: roof.get(k) for k in ("bound", "achieved", "peak", "unit", "frac", "ms_per_launch")},
             "tflops": d.get("tflops"),
+            "policy": d.get("policy"),
             "parity_max_rel_err": (d.get("parity") or {}).get("max_rel_err"),
             "clocks_sm_mhz": (d.get("clocks") or {}).get("sm_mhz"),
             "throttle_reasons": (d.get("clocks") or {}).get("reasons"),
@@ -483,6 +484,60 @@ def run_ours(args, wl):
     fracs = [None]
     if args.sweep and wl["residency"][0] == "arena_frac":
         fracs = [i / 10 for i in range(11)]
+
+    def set_split(ring_slots, per_layer):
+        # a fixed arena: resident prefixes of per_layer pages, the ring gets the rest
+        for l in range(L):
+            st.set_residency(l, np.zeros(npages, np.uint8))
+        st.set_ring_slots(ring_slots, wl["chunk"])
+        m = np.zeros(npages, np.uint8)
+        m[:per_layer] = 1
+        for l in range(L):
+            st.set_residency(l, m)
+        st.sync()
+
+    # Closed loop (fixed arena): the residency policy chooses the resident / ring
+    # split from the device-measured observation of the steps run at the split in
+    # force (readiness misses, ring occupancy, copy-busy fraction); the line is
+    # then measured at its last decision
+    policy_trace, forced = None, None
+    if args.policy and fixed_arena:
+        pcfg = kvs.kvs_policy_config(page_tokens=P, n_layers=L, budget_slots=free, min_ring_slots=8,
+                                     max_ring_slots=free - L, step_slots=max(8, free // 16), hold_steps=1,
+                                     miss_grow=0.25, copy_busy_max=0.98, occupancy_shrink=0.05)
+        pstate = kvs.kvs_policy_state()
+        f0 = wl["residency"][1]
+        per0 = min(npages, int(round(f0 * (free - 8))) // L)
+        ring_now, per_now = free - per0 * L, per0
+        policy_trace = []
+        for k in range(args.policy):
+            set_split(ring_now, per_now)
+            st.graph_begin()
+            step()
+            st.graph_end()
+            st.graph_launch()
+            st.sync()
+            st.observe(reset=True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st.attn_stream)
+            for _ in range(2):
+                st.graph_launch()
+            e1.record(st.attn_stream)
+            st.sync()
+            ms = e0.elapsed_time(e1) / 2
+            obs = st.observe(reset=True)
+            st.graph_destroy()
+            pstate, dec = kvs.kvs_policy_step(pcfg, pstate, obs)
+            policy_trace.append({
+                "ring_slots": ring_now, "resident_pages_per_layer": per_now, "tokens_per_s": R / (ms * 1e-3),
+                "streamed_reads": obs.streamed_reads, "ready_misses": obs.ready_misses,
+                "ring_occupancy": obs.ring_occupancy, "copy_busy": obs.copy_busy,
+                "decision": {"ring_slots": dec.ring_slots, "resident_pages_per_layer": dec.resident_pages_per_layer,
+                             "reason": ["", "init", "fits", "hold", "grow", "shrink", "clamp"][dec.reason]}})
+            ring_now = dec.ring_slots
+            per_now = min(npages, int(dec.resident_pages_per_layer))
+        forced = (ring_now, per_now)
+
     for frac in fracs:
         # residency (and, in a fixed arena, the ring gets every slot the pool does not)
         if fixed_arena:
@@ -490,6 +545,8 @@ def run_ours(args, wl):
             pool_slots = int(round(f * (free - 8)))
             per_layer = min(npages, pool_slots // L)
             ring = free - per_layer * L
+            if forced is not None:
+                ring, per_layer = forced
             masks = []
             for _ in range(L):
                 m = np.zeros(npages, np.uint8)
@@ -676,6 +733,7 @@ def run_ours(args, wl):
             "gpu_launches": kernels_per_step * args.steps,
             "clocks": clk,
             "timeline": timeline,
+            "policy": policy_trace,
             "eager_ms_per_step": eager_ms,
             "parity": parity,
             "prep_s": prep_s,
@@ -711,6 +769,8 @@ def main():
     ap.add_argument("--resident", type=float, default=-1.0,
                     help="override the resident fraction (prefix of each layer; for long262k of the arena)")
     ap.add_argument("--sweep", action="store_true", help="long262k: sweep the resident fraction 0..100%%")
+    ap.add_argument("--policy", type=int, default=0,
+                    help="long262k: this many closed-loop steps of the residency policy choose the split first")
     ap.add_argument("--host-alloc", choices=["pageable", "pinned", "hugepage"], default="pinned",
                     help="host history buffer: registered numpy memory, CUDA pinned, or huge-page advised")
     ap.add_argument("--operands", choices=["split", "f16"], default="f16",
@@ -743,7 +803,8 @@ def main():
         kind = "arena_frac" if wl["residency"][0] == "arena_frac" else "prefix_frac"
         wl["residency"] = (kind, args.resident)
         wl["desc"] += f" [resident override: {args.resident}]"
-    args.overridden = any((args.ring, args.chunk, args.layers, args.lanes, args.rows, args.split, args.resident >= 0,
+    args.overridden = any((args.ring, args.chunk, args.layers, args.lanes, args.rows, args.split, args.policy,
+                           args.resident >= 0,
                            args.fill != "default", args.sweep))
     if args.impl == "reference":
         run_reference(args, wl)
