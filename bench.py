@@ -353,6 +353,7 @@ EXTRAS = [
     ("prefill131k", []),
     ("long262k_1row", ["--workload", "long262k"]),
     ("long262k_4rows", ["--workload", "long262k", "--rows", "4"]),
+    ("long262k_policy", ["--workload", "long262k", "--policy", "6"]),
     ("resident131k", []),
 ]
 
@@ -502,13 +503,16 @@ def run_ours(args, wl):
     # then measured at its last decision
     policy_trace, forced = None, None
     if args.policy and fixed_arena:
+        # the link has room while refills run below 90% of the pinned-copy ceiling
+        # measured in this run
         pcfg = kvs.kvs_policy_config(page_tokens=P, n_layers=L, budget_slots=free, min_ring_slots=8,
                                      max_ring_slots=free - L, step_slots=max(8, free // 16), hold_steps=1,
-                                     miss_grow=0.25, copy_busy_max=0.98, occupancy_shrink=0.05)
-        pstate = kvs.kvs_policy_state()
-        f0 = wl["residency"][1]
-        per0 = min(npages, int(round(f0 * (free - 8))) // L)
-        ring_now, per_now = free - per0 * L, per0
+                                     miss_grow=0.25, copy_busy_max=0.9, occupancy_shrink=0.05,
+                                     link_gbs=ceiling)
+        # first decision from the context length alone
+        pstate, dec = kvs.kvs_policy_step(pcfg, kvs.kvs_policy_state(),
+                                          kvs.kvs_policy_observation(context_tokens=T))
+        ring_now, per_now = dec.ring_slots, min(npages, int(dec.resident_pages_per_layer))
         policy_trace = []
         for k in range(args.policy):
             set_split(ring_now, per_now)
@@ -532,6 +536,7 @@ def run_ours(args, wl):
                 "ring_slots": ring_now, "resident_pages_per_layer": per_now, "tokens_per_s": R / (ms * 1e-3),
                 "streamed_reads": obs.streamed_reads, "ready_misses": obs.ready_misses,
                 "ring_occupancy": obs.ring_occupancy, "copy_busy": obs.copy_busy,
+                "refill_gbs": obs.copy_bytes / obs.interval_ns if obs.interval_ns else None,
                 "decision": {"ring_slots": dec.ring_slots, "resident_pages_per_layer": dec.resident_pages_per_layer,
                              "reason": ["", "init", "fits", "hold", "grow", "shrink", "clamp"][dec.reason]}})
             ring_now = dec.ring_slots

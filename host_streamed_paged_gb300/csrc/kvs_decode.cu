@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
             if (wait < kMissNs) atomicAdd(&a->misses, 1ull);
             atomicAdd(&a->occupancy_page_ns, wait * (unsigned long long)p.rec_pages);
             atomicAdd(&a->fill_busy_ns, fe > fs ? fe - fs : 0ull);
+            atomicAdd(&a->fill_bytes, (unsigned long long)p.rec_pages * (unsigned long long)p.geom.page_bytes);
             atomicMax(&a->first_fill_neg, ~fs);
             atomicMax(&a->last_read, t);
         }

@@ -186,6 +186,7 @@ struct ObsAccumulator {  // all fields start at zero
     unsigned long long fill_busy_ns;       // sum of fill durations
     unsigned long long first_fill_neg;     // ~(earliest fill start), by atomic max
     unsigned long long last_read;          // latest read start
+    unsigned long long fill_bytes;         // page bytes of the accounted refills
 };
 struct FillParams {
     unsigned long long *rec;  // this refill's record (nullable)

@@ -39,7 +39,8 @@ extern "C" kvs_status kvs_policy_step(const kvs_policy_config *cfg, const kvs_po
     const uint32_t lo = cfg->min_ring_slots;
     if (lo == 0 || lo > hi) return KVS_ERR_INVALID;
     if (!fraction(cfg->miss_grow) || !fraction(cfg->copy_busy_max) || !fraction(cfg->occupancy_shrink) ||
-        !fraction(obs->ring_occupancy) || !fraction(obs->copy_busy) || obs->ready_misses > obs->streamed_reads)
+        !fraction(obs->ring_occupancy) || !fraction(obs->copy_busy) || obs->ready_misses > obs->streamed_reads ||
+        !(cfg->link_gbs >= 0.f && cfg->link_gbs < 1e9f))
         return KVS_ERR_INVALID;
 
     const uint64_t ppl = obs->context_tokens / cfg->page_tokens + (obs->context_tokens % cfg->page_tokens != 0);
@@ -61,7 +62,17 @@ extern "C" kvs_status kvs_policy_step(const kvs_policy_config *cfg, const kvs_po
         st.grow_run = st.shrink_run = 0;
     } else {
         const double miss_rate = obs->streamed_reads ? (double)obs->ready_misses / (double)obs->streamed_reads : 0.0;
-        const bool want_grow = miss_rate > cfg->miss_grow && obs->copy_busy < cfg->copy_busy_max;
+        // the link has room: its measured rate against the caller's ceiling when both
+        // are known (refills of several lanes overlap, so busy time alone saturates
+        // before the link does), else the copy stream's busy fraction
+        bool room;
+        if (cfg->link_gbs > 0.f && obs->interval_ns > 0) {
+            const double gbs = (double)obs->copy_bytes / (double)obs->interval_ns;  // bytes per ns = GB/s
+            room = gbs < (double)cfg->copy_busy_max * (double)cfg->link_gbs;
+        } else {
+            room = obs->copy_busy < cfg->copy_busy_max;
+        }
+        const bool want_grow = miss_rate > cfg->miss_grow && room;
         const bool want_shrink = obs->ready_misses == 0 && obs->ring_occupancy < cfg->occupancy_shrink;
         st.grow_run = want_grow ? prev->grow_run + 1 : 0;
         st.shrink_run = want_shrink ? prev->shrink_run + 1 : 0;

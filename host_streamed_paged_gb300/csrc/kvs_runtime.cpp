@@ -2018,6 +2018,8 @@ kvs_status kvs_observe(kvs_ctx *c, kvs_policy_observation *out, int reset) {
         const double span = (double)(a.last_read - first);
         out->ring_occupancy = (float)std::min(1.0, (double)a.occupancy_page_ns / (span * (double)c->ring_n));
         out->copy_busy = (float)std::min(1.0, (double)a.fill_busy_ns / span);
+        out->copy_bytes = a.fill_bytes;
+        out->interval_ns = a.last_read - first;
     }
     c->last_obs = *out;
     if (reset) {

@@ -100,7 +100,8 @@ KVS_TL_KINDS = {1: "append", 2: "clear", 3: "qprep", 4: "read_resident", 5: "rea
 class kvs_policy_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint32) for n in (
         "page_tokens", "n_layers", "budget_slots", "min_ring_slots", "max_ring_slots", "step_slots",
-        "hold_steps")] + [(n, ctypes.c_float) for n in ("miss_grow", "copy_busy_max", "occupancy_shrink")]
+        "hold_steps")] + [(n, ctypes.c_float) for n in ("miss_grow", "copy_busy_max", "occupancy_shrink",
+                                                      "link_gbs")]
 
 
 class kvs_policy_state(ctypes.Structure):
@@ -110,7 +111,7 @@ class kvs_policy_state(ctypes.Structure):
 class kvs_policy_observation(ctypes.Structure):
     _fields_ = [("context_tokens", ctypes.c_uint64), ("streamed_reads", ctypes.c_uint64),
                 ("ready_misses", ctypes.c_uint64), ("ring_occupancy", ctypes.c_float),
-                ("copy_busy", ctypes.c_float)]
+                ("copy_busy", ctypes.c_float), ("copy_bytes", ctypes.c_uint64), ("interval_ns", ctypes.c_uint64)]
 
 
 class kvs_policy_decision(ctypes.Structure):

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define KVS_ABI_VERSION 3
+#define KVS_ABI_VERSION 4
 
 typedef struct kvs_ctx kvs_ctx;
 
@@ -368,6 +368,10 @@ typedef struct {
     float copy_busy_max;      /* ... and the copy stream was busy less than this fraction */
     float occupancy_shrink;   /* shrink when no read missed and the ring held prefetched
                                  pages for less than this fraction of its slots */
+    float link_gbs;           /* > 0: the host link's measured copy rate (GB/s); the link
+                                 then has room while the observed refill rate
+                                 (copy_bytes / interval_ns) is below copy_busy_max times
+                                 it, instead of while copy_busy is below copy_busy_max */
 } kvs_policy_config;
 
 typedef struct {              /* zero-initialise before the first step */
@@ -383,6 +387,8 @@ typedef struct {              /* one observation interval, e.g. one decode step 
     uint64_t ready_misses;    /* of those, reads whose copy had not finished when issued */
     float ring_occupancy;     /* mean fraction of ring slots holding a page not yet read */
     float copy_busy;          /* fraction of the interval the copy stream was busy */
+    uint64_t copy_bytes;      /* bytes the interval's refills moved (0: not measured) */
+    uint64_t interval_ns;     /* length of the interval (0: not measured) */
 } kvs_policy_observation;
 
 enum {
@@ -412,8 +418,10 @@ typedef struct {
  *     as large as the budget allows.
  *  2. No split yet: smallest ring (INIT).
  *  3. Otherwise an observation asks to grow when the miss rate exceeds
- *     miss_grow while copy_busy < copy_busy_max (a deeper prefetch helps only
- *     while the link has room), and to shrink when no read missed and
+ *     miss_grow while the link has room (a deeper prefetch helps only then):
+ *     with link_gbs > 0 and a measured interval, while copy_bytes /
+ *     interval_ns < copy_busy_max x link_gbs, else while copy_busy <
+ *     copy_busy_max; and to shrink when no read missed and
  *     ring_occupancy < occupancy_shrink.  A change of step_slots is made
  *     after hold_steps consecutive observations agree; any other observation
  *     restarts the count (hysteresis), and a change restarts both counts.
@@ -470,8 +478,10 @@ kvs_status kvs_lease_info(const kvs_ctx *ctx, int64_t *layer, uint32_t *leased_s
  * unread.  context_tokens = the longest layer; streamed_reads, ready_misses =
  * chunk reads accounted and missed; ring_occupancy = sum over reads of
  * pages x (read start - copy end) / (interval x ring_slots); copy_busy = sum
- * of copy durations / interval (at most 1), the interval running from the
- * first copy's start to the last read's start.  Refills by the copy engines
+ * of copy durations / interval (at most 1; refills of several lanes that
+ * overlap each count), the interval running from the first copy's start to
+ * the last read's start; copy_bytes = page bytes of the accounted refills;
+ * interval_ns = that interval.  Refills by the copy engines
  * (KVS_FLAG_DMA_FILL) are not stamped and not accounted.  Waits for the
  * context's device work first (kvs_sync); reset != 0 starts a new interval.
  * The counters also accumulate across step-graph replays.  The values are

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
     for name in sorted(declared):
         assert hasattr(lib, name), name
     assert declared <= set(kvs.SIGNATURES), declared - set(kvs.SIGNATURES)
-    assert kvs.kvs_version() == 3
+    assert kvs.kvs_version() == 4
 
 
 def _cfg(**kw):

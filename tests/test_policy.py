@@ -248,3 +248,34 @@ def test_policy_drives_a_plan_only_context():
     check_trace(st, 6 * Hk, fixed_ring=False)  # the ring boundary moves during the trace
     assert rings[0] == 2 and max(rings) > 2 and st.stats()["ring_slots"] == rings[-1]
     st.close()
+
+
+def test_link_rate_decides_room_when_the_ceiling_is_given():
+    """With link_gbs set, room on the link is the observed refill rate against
+    copy_busy_max x link_gbs; copy_busy (which saturates at 1 when refills of
+    several lanes overlap) is then not consulted."""
+    c = cfg(hold_steps=1, copy_busy_max=0.9, link_gbs=200.0)
+    miss = dict(reads=100, misses=90, occ=0.9, busy=1.0)
+    slow = kvs.kvs_policy_observation(context_tokens=262144, streamed_reads=100, ready_misses=90,
+                                      ring_occupancy=0.9, copy_busy=1.0,
+                                      copy_bytes=120 * 10**6, interval_ns=10**6)   # 120 GB/s
+    fast = kvs.kvs_policy_observation(context_tokens=262144, streamed_reads=100, ready_misses=90,
+                                      ring_occupancy=0.9, copy_busy=1.0,
+                                      copy_bytes=185 * 10**6, interval_ns=10**6)   # 185 GB/s >= 0.9 x 200
+    _, d = kvs.kvs_policy_step(c, state(ring=64), slow)
+    assert (d.ring_slots, d.reason) == (72, kvs.KVS_POLICY_GROW)
+    _, d = kvs.kvs_policy_step(c, state(ring=64), fast)
+    assert (d.ring_slots, d.reason) == (64, kvs.KVS_POLICY_HOLD)
+    # without the ceiling the busy fraction decides: 1.0 is never below 0.9
+    _, d = kvs.kvs_policy_step(cfg(hold_steps=1, copy_busy_max=0.9), state(ring=64), slow)
+    assert d.reason == kvs.KVS_POLICY_HOLD
+    # with the ceiling but no measured interval, the busy fraction decides too
+    _, d = kvs.kvs_policy_step(c, state(ring=64), obs(**miss))
+    assert d.reason == kvs.KVS_POLICY_HOLD
+
+
+@pytest.mark.parametrize("bad", [-1.0, float("nan"), float("inf")])
+def test_link_rate_must_be_a_finite_nonnegative_number(bad):
+    o = obs()
+    with pytest.raises(kvs.KVSError):
+        kvs.kvs_policy_step(cfg(link_gbs=bad), state(ring=64), o)
