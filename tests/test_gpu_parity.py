@@ -475,11 +475,14 @@ def test_observation_counts_every_streamed_read_and_stays_in_range():
     assert st.observe().streamed_reads == 0
 
 
-def test_residency_policy_drives_a_streamed_stack_in_closed_loop():
+@pytest.mark.parametrize("link_gbs", [0.0, 1e4])
+def test_residency_policy_drives_a_streamed_stack_in_closed_loop(link_gbs):
     """kvs_policy_step chooses the resident/ring split of a fixed 96-slot budget
     from the library's own observations (kvs_observe), step after step, and the
     decisions are applied with kvs_set_ring_slots / kvs_set_residency; the
-    outputs match the oracle on sampled layers after every change."""
+    outputs match the oracle on sampled layers after every change.  With a link
+    ceiling (link_gbs, here far above any refill rate) the observation's refill
+    bytes and interval are measured and the link always has room."""
     import torch
     P, D, Hk, G, L, T = 256, 256, 4, 6, 4, 256 * 64
     Hq = G * Hk
@@ -490,7 +493,7 @@ def test_residency_policy_drives_a_streamed_stack_in_closed_loop():
     hist = _fill(st, L, T, Hk, D)
     cfg = kvs.kvs_policy_config(page_tokens=P, n_layers=L, budget_slots=budget, min_ring_slots=8,
                                 max_ring_slots=64, step_slots=8, hold_steps=2, miss_grow=0.25,
-                                copy_busy_max=0.98, occupancy_shrink=0.05)
+                                copy_busy_max=0.98, occupancy_shrink=0.05, link_gbs=link_gbs)
     state = kvs.kvs_policy_state()
     qs = [queries(SEED, 50 + l, 1, Hq, D) for l in range(L)]
     q_dev = [torch.from_numpy(q).cuda() for q in qs]
@@ -506,6 +509,8 @@ def test_residency_policy_drives_a_streamed_stack_in_closed_loop():
         st.sync()
         obs = st.observe(reset=True)
         assert obs.streamed_reads > 0 and obs.ready_misses <= obs.streamed_reads
+        # every accounted read's chunk moved whole pages, within a measured interval
+        assert obs.interval_ns > 0 and obs.copy_bytes > 0 and obs.copy_bytes % st.page_bytes == 0
         if step in (0, 5) or applied and applied[-1][0] == step - 1:
             for l in (0, L - 1):
                 ro, rl = oracle_ref(*hist[l], qs[l], T - 1, 1 / 16)
