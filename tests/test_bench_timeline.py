@@ -36,7 +36,7 @@ def test_summary_of_two_layers():
     ]
     t = bench.timeline_summary(recs, 2)
     assert t["step_us"] == 50
-    assert t["refill_busy_us"] == 34 and t["refill_launches"] == 3   # union of [0,22] and [24,34]
+    assert t["refill_busy_us"] == 30 and t["refill_launches"] == 3   # [0,10], [12,22], [24,34]
     # boundary: layer 0's last read ends at 27, layer 1's first read starts at 40
     assert t["boundary_us_median"] == 13 and t["boundary_us_total"] == 13
     # refills run 27..34 of that boundary's 13 us
