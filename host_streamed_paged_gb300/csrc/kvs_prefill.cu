@@ -20,8 +20,9 @@
 // one (split, kv head) run together and share its pages through L2.
 //
 // Roles, per CTA (the leader, cluster rank 0, issues every MMA of the pair):
-//   warps 4-7 (producers) dequantise their halves of block j's K (Q8_0) and V
-//     (Q4_0) into one of two shared-memory stages, as f16 in the 128-byte-
+//   warps 4-7 (producers) dequantise their halves of block j's K (Q8_0) and
+//     block j-1's V (Q4_0) into shared-memory stages (two each) and publish
+//     both under one proxy fence, as f16 in the 128-byte-
 //     swizzled K-major layouts tcgen05 reads: K[key][dim], V[dim][key], each
 //     value rn(d * x) (the pages' own tensor-core path also runs on f16
 //     dequantised values);
@@ -44,7 +45,7 @@
 namespace kvs {
 namespace {
 
-constexpr int kPThreads = 288;    // 4 softmax warps, 4 producer warps, 1 MMA warp
+constexpr int kPThreads = 320;    // 4 softmax warps, 4 producer warps, MMA issue / relay warps 8-9
 constexpr int kBN = 128;          // keys per block (S MMA N)
 constexpr int kHalfN = kBN / 2;   // keys of a block this CTA dequantises
 constexpr int kD = 256;           // head dim served by this kernel (PV MMA N)
@@ -70,18 +71,26 @@ constexpr int kSmemBytes = kOffSlots + kMaxPrefillSplitPages * 4 + 1024;  // + s
 constexpr uint32_t kTmemCols = 512;  // S buffers at [0, 128) and [128, 256), O at [256, 512);
                                      // P_j (f16 pairs, 64 columns) overwrites S_j's first half
 constexpr uint32_t kColO = 256;
-// barrier indices.  "Full" barriers live in the leader and count arrivals
-// from both CTAs (4 warps each); the others are armed by multicast commits in
-// both CTAs.  Each completes one phase per use of what it guards.
-constexpr int kBarKFull = 0;   // + stage (2): producers wrote K_j
-constexpr int kBarVFull = 2;   // + stage (2): producers wrote V_j
-constexpr int kBarPFull = 4;   // softmax of both CTAs wrote P_j
-constexpr int kBarSEmpty = 5;  // + S buffer (2): softmax of both CTAs read S_j
+// barrier indices.  Producers and softmax warps arrive on their own CTA's
+// "Full" barriers with a CTA-scope release; in the peer, relay threads (warps
+// 8 and 9) wait for those and pass each phase on to the leader's barrier with
+// one cluster-scope release, so the leader's Full barriers count 4 local warps
+// and 1 relay.  A cluster-scope release costs the arriving warp about a
+// microsecond; the relays take it off the producers' and the softmax's paths.
+// The other barriers are armed by multicast commits in both CTAs.  Each
+// completes one phase per use of what it guards.
+constexpr int kBarKVFull = 0;  // + j & 1 (2): producers wrote K_j (stage j & 1) and V_{j-1}
+constexpr int kBarPFull = 4;   // + j & 1 (2): softmax wrote P_j (which also means S_j was read)
+// Two barriers per Full kind (by the parity of j) keep a relay's wait from
+// aliasing: the next phase of the barrier it waits on (j + 2) cannot complete
+// before the leader has consumed phase j, which needs the relay's arrival.
 constexpr int kBarKEmpty = 7;  // + stage (2): S_j done, K stage free
 constexpr int kBarVEmpty = 9;  // + stage (2): PV_j done, V stage free
-constexpr int kBarODone = 11;  // PV_j done: P buffer free, O stable
+constexpr int kBarFinal = 11;  // every MMA of the CTA pair finished
 constexpr int kBarSFull = 12;  // + S buffer (2): S_j in TMEM
-constexpr int kBarFinal = 14;  // every MMA of the CTA pair finished
+constexpr int kBarODone = 14;  // + j & 1 (2): PV_j done, O stable (one barrier per parity of
+                               // j, so a wait for PV_j may be skipped: the barrier's next
+                               // phase, PV_{j+2}, needs P_{j+2}, which is not written yet)
 
 // byte offset of element (row, k) in a 128B-swizzled K-major tile whose rows
 // are 128-byte lines of 64 f16 (one swizzle atom per 64 elements of k)
@@ -151,6 +160,11 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 // arrive (release, cluster scope) on an mbarrier given by its shared::cluster address
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
+// arrive (release, CTA scope) on an mbarrier of this CTA
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // D (TMEM of both CTAs) = A (smem of both) * B (smem of both, N split) [+ D]
@@ -227,6 +241,12 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &a, uint32_t &b
     asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(bh) : "r"(u), "r"(0x64646464u));
     asm("sub.f16x2 %0, %1, %2;" : "=r"(a) : "r"(bl), "r"(0x64806480u));
     asm("sub.f16x2 %0, %1, %2;" : "=r"(b) : "r"(bh), "r"(0x64806480u));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t d) {
@@ -311,15 +331,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(kBarKFull + s), 8);
-            mbar_init(bar(kBarVFull + s), 8);
-            mbar_init(bar(kBarSEmpty + s), 8);
+            mbar_init(bar(kBarKVFull + s), rank == 0 ? 5 : 4);
             mbar_init(bar(kBarKEmpty + s), 1);
             mbar_init(bar(kBarVEmpty + s), 1);
             mbar_init(bar(kBarSFull + s), 1);
         }
-        mbar_init(bar(kBarPFull), 8);
+        mbar_init(bar(kBarPFull), rank == 0 ? 5 : 4);
+        mbar_init(bar(kBarPFull + 1), rank == 0 ? 5 : 4);
         mbar_init(bar(kBarODone), 1);
+        mbar_init(bar(kBarODone + 1), 1);
         mbar_init(bar(kBarFinal), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -431,9 +451,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                     *reinterpret_cast<uint4 *>(kt + sw128(kHalfN, kr, (kb0 + b) * 32 + 8 * m)) =
                         make_uint4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
             }
-            proxy_fence();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarKFull + stage));
         };
         auto write_v = [&](int stage) {
             uint8_t *vt = smem + kOffV + stage * kVBytes;
@@ -460,28 +477,41 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                         make_uint4(ob[4 * m], ob[4 * m + 1], ob[4 * m + 2], ob[4 * m + 3]);
                 }
             }
+        };
+        // Iteration j publishes K_j (stage j & 1, free once S_{j-2} is done) and
+        // V_{j-1} (stage (j-1) & 1, free once PV_{j-3} is done) under one proxy
+        // fence: the MMA thread issues PV_{j-1} right after S_j, so both are
+        // wanted at the same time, and the fence costs about as much as the
+        // dequantisation of a whole K tile.
+        if (nblk > 0) load_k(0);
+        for (int j = 0; j <= nblk; ++j) {  // every exit is a warp-uniform wait outcome
+            const bool wk = j < nblk, wv = j >= 1;
+            if (wk && j >= 2 && !mbar_wait_warp(bar(kBarKEmpty + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort)) break;
+            if (wv && j >= 3 &&
+                !mbar_wait_warp(bar(kBarVEmpty + ((j - 1) & 1)), (uint32_t)(((j - 3) >> 1) & 1), abort))
+                break;
+            if (wk) write_k(j & 1);
+            if (wv) write_v((j - 1) & 1);
             proxy_fence();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarVFull + stage));
-        };
-        // block j goes to stage j & 1: K_j once S_{j-2} is done with that stage,
-        // V_j once PV_{j-2} is
-        if (nblk > 0) {
-            load_k(0);
-            load_v(0);
-        }
-        for (int j = 0; j < nblk; ++j) {  // every exit is a warp-uniform wait outcome
-            const int st = j & 1;
-            if (j >= 2 && !mbar_wait_warp(bar(kBarKEmpty + st), (uint32_t)(((j - 2) >> 1) & 1), abort)) break;
-            write_k(st);
+            if (lane == 0) mbar_arrive_local(bar(kBarKVFull + (j & 1)));
             if (j + 1 < nblk) load_k(j + 1);
-            if (j >= 2 && !mbar_wait_warp(bar(kBarVEmpty + st), (uint32_t)(((j - 2) >> 1) & 1), abort)) break;
-            write_v(st);
-            if (j + 1 < nblk) load_v(j + 1);
+            if (j < nblk) load_v(j);
         }
-    } else if (warp == 8) {
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ relays (peer, one thread each)
+        if (rank == 1 && lane == 0) {
+            // warp 8 passes on the producers' phases (nblk + 1 of them), warp 9 the softmax's
+            const int nph = warp == 8 ? nblk + 1 : nblk;
+            bool ok = true;
+            for (int j = 0; j < nph && ok; ++j) {
+                const int b = (warp == 8 ? kBarKVFull : kBarPFull) + (j & 1);
+                ok = mbar_wait(bar(b), (uint32_t)((j >> 1) & 1), abort);
+                if (ok) mbar_arrive_cluster(lead_bar(b));
+            }
+        }
         // ------------------------------------------------------------ MMA issue (leader, one thread)
-        if (rank == 0 && lane == 0) {
+        if (rank == 0 && warp == 8 && lane == 0) {
             // descriptors of the tile bases; a k-step adds its byte offset / 16
             const uint64_t dq = smem_desc(smem_u32(smem + kOffQ)), dk = smem_desc(smem_u32(smem + kOffK));
             const uint64_t dv = smem_desc(smem_u32(smem + kOffV));
@@ -510,26 +540,26 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                     mma_pair_ta(tmem + kColO, tp + (uint32_t)(8 * s), dvj + bv, id_o, (j > 0 || s > 0) ? 1u : 0u);
                 }
                 mma_commit_both(bar(kBarVEmpty + (j & 1)));
-                mma_commit_both(bar(kBarODone));
+                mma_commit_both(bar(kBarODone + (j & 1)));
             };
             bool ok = true;
+            // S_j overwrites the buffer of S_{j-2} and P_{j-2}: P_{j-2} written means
+            // S_{j-2} was read, and PV_{j-2} was issued before S_j
             for (int j = 0; j < nblk && ok; ++j) {
-                ok = mbar_wait(bar(kBarKFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort);
-                if (ok && j >= 2) ok = mbar_wait(bar(kBarSEmpty + (j & 1)), (uint32_t)(((j - 2) >> 1) & 1), abort);
+                ok = mbar_wait(bar(kBarKVFull + (j & 1)), (uint32_t)((j >> 1) & 1), abort);  // K_j, V_{j-1}
                 if (!ok) break;
                 tc_after_sync();
                 issue_s(j);
                 if (j >= 1) {
-                    ok = mbar_wait(bar(kBarPFull), (uint32_t)((j - 1) & 1), abort) &&
-                         mbar_wait(bar(kBarVFull + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
+                    ok = mbar_wait(bar(kBarPFull + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
                     if (!ok) break;
                     tc_after_sync();
                     issue_pv(j - 1);
                 }
             }
             if (ok && nblk > 0) {
-                ok = mbar_wait(bar(kBarPFull), (uint32_t)((nblk - 1) & 1), abort) &&
-                     mbar_wait(bar(kBarVFull + ((nblk - 1) & 1)), (uint32_t)(((nblk - 1) >> 1) & 1), abort);
+                ok = mbar_wait(bar(kBarPFull + ((nblk - 1) & 1)), (uint32_t)(((nblk - 1) >> 1) & 1), abort) &&
+                     mbar_wait(bar(kBarKVFull + (nblk & 1)), (uint32_t)((nblk >> 1) & 1), abort);  // V_{nblk-1}
                 if (ok) {
                     tc_after_sync();
                     issue_pv(nblk - 1);
@@ -558,9 +588,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                 for (int c = 0; c < kBN; c += 32) tmem_ld32_nowait(ta + c, s + c);
                 tmem_wait_ld();
             }
-            tc_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarSEmpty + (j & 1)));
             // keys i > lim are masked: after this row's position, or beyond the split
             {
                 const long long kpos = key_pos0 + (long long)j * kBN;
@@ -573,10 +600,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
                     for (int i = 0; i < kBN; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
                 }
             }
-            // raw-score max in four independent chains; scale > 0 keeps the order
+            // raw-score max in four independent chains of three-input maxima; scale > 0
+            // keeps the order
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) m4[i & 3] = fmaxf(m4[i & 3], s[i]);
+            for (int i = 0; i < kBN; i += 2) m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], s[i], s[i + 1]);
             const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
             int need_rescale = 0;
             float alpha = 1.f;
@@ -590,51 +618,54 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
             const float mneg = (m_used == -INFINITY) ? 0.f : -m_used;
             float b4[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[kBN / 2];
+            // P_j as f16 pairs into the first 64 columns of S_j's buffer (this
+            // thread's row was read out of it above), each half stored as soon
+            // as it is formed
+            const uint32_t tp = lane_base + (uint32_t)((j & 1) * kBN);
 #pragma unroll
-            for (int i = 0; i < kBN; i += 2) {
-                float e0, e1;
-                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fmaf(s[i], p.scale_log2, mneg)));
-                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fmaf(s[i + 1], p.scale_log2, mneg)));
-                const __half2 hp = __floats2half2_rn(e0, e1);
-                // l sums the fp32 weights; their f16 roundings (<= 2^-12 relative,
-                // independent per key) average out far below the tolerance
-                b4[(i >> 1) & 3] += e0 + e1;
-                pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int i = half * (kBN / 2); i < (half + 1) * (kBN / 2); i += 2) {
+                    float e0, e1;
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(fmaf(s[i], p.scale_log2, mneg)));
+                    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(fmaf(s[i + 1], p.scale_log2, mneg)));
+                    const __half2 hp = __floats2half2_rn(e0, e1);
+                    // l sums the fp32 weights; their f16 roundings (<= 2^-12 relative,
+                    // independent per key) average out far below the tolerance
+                    b4[(i >> 1) & 3] += e0 + e1;
+                    pk[i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
+                tmem_st32(tp + 32 * half, reinterpret_cast<const float *>(pk + 32 * half));
             }
             l_sum += (b4[0] + b4[1]) + (b4[2] + b4[3]);
-            // PV_{j-1} done: O may be rescaled
-            if (j >= 1) {
-                ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((j - 1) & 1), abort);
-                if (!ok) break;
-                tc_after_sync();
-                if (__any_sync(0xffffffffu, need_rescale)) {
-                    const uint32_t ta = lane_base + kColO;
-#pragma unroll 1
-                    for (int c = 0; c < kD; c += 32) {
-                        float v[32];
-                        tmem_ld32_nowait(ta + c, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                        tmem_st32(ta + c, v);
-                    }
+            // O is rescaled once PV_{j-1} is done (P_j's buffer is not the one PV_{j-1}
+            // reads, so only a rescale waits for it)
+            if (j >= 1 && __any_sync(0xffffffffu, need_rescale)) {
+                ok = mbar_wait_warp(bar(kBarODone + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort);
+                if (!ok) {
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    break;
+                }
+                tc_after_sync();
+                const uint32_t ta = lane_base + kColO;
+#pragma unroll 1
+                for (int c = 0; c < kD; c += 32) {
+                    float v[32];
+                    tmem_ld32_nowait(ta + c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                    tmem_st32(ta + c, v);
                 }
             }
-            // P_j as f16 pairs into the first 64 columns of S_j's buffer (this
-            // thread's row was read out of it above)
-            {
-                const uint32_t tp = lane_base + (uint32_t)((j & 1) * kBN);
-                tmem_st32(tp, reinterpret_cast<const float *>(pk));
-                tmem_st32(tp + 32, reinterpret_cast<const float *>(pk + 32));
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");  // P_j (and O) stored
             tc_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead_bar(kBarPFull));
+            if (lane == 0) mbar_arrive_local(bar(kBarPFull + (j & 1)));
         }
         // the last PV, then the partial: unnormalised O, m (log2 units), l
-        if (ok && nblk > 0) ok = mbar_wait_warp(bar(kBarODone), (uint32_t)((nblk - 1) & 1), abort);
+        if (ok && nblk > 0)
+            ok = mbar_wait_warp(bar(kBarODone + ((nblk - 1) & 1)), (uint32_t)(((nblk - 1) >> 1) & 1), abort);
         if (ok) {
             tc_after_sync();
             const uint32_t ta = lane_base + kColO;
