@@ -321,8 +321,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
     // slots are copied to shared memory once (indexing the parameter block at
     // run time is slow)
     const uint32_t *slots = reinterpret_cast<const uint32_t *>(smem + kOffSlots);
+    const int lgP = __ffs(P) - 1;  // P is a power of two
+    const uint8_t *arena_g = p.arena + (int64_t)g * p.geom.head_bytes;
     auto head_of = [&](int ks) {
-        return p.arena + (int64_t)slots[ks / P] * p.geom.page_bytes + (int64_t)g * p.geom.head_bytes;
+        return arena_g + (int64_t)slots[ks >> lgP] * p.geom.page_bytes;
     };
     auto raise_abort = [&]() {
         *abort = 1;
@@ -395,14 +397,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
             const int ks = j * kBN + (int)rank * kHalfN + kr;
             if (ks < n_keys) {
                 const uint8_t *hb = head_of(ks);
-                const int t = ks % P;
+                const int t = ks & (P - 1);
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
-                    const uint4 *line = reinterpret_cast<const uint4 *>(hb + kq_byte(t, (kb0 + b) * 32, kNB));
+                    // kq_byte in 32 bits: 16-token group, 32-dim block, token in the group
+                    const uint4 *line =
+                        reinterpret_cast<const uint4 *>(hb + (((t >> 4) * kNB + kb0 + b) * 16 + (t & 15)) * 32);
                     rk[2 * b] = line[0];
                     rk[2 * b + 1] = line[1];
                 }
-                sk = *reinterpret_cast<const uint2 *>(hb + p.geom.ks_off + ((int64_t)t * kNB + kb0) * 2);
+                sk = *reinterpret_cast<const uint2 *>(hb + p.geom.ks_off + (t * kNB + kb0) * 2);
             } else {  // beyond the split: zero keys (masked by the softmax)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) rk[i] = make_uint4(0, 0, 0, 0);
@@ -413,13 +417,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
             const int ks = j * kBN + 32 * vc;  // a 32-key chunk never straddles a page (P % 64 == 0)
             if (ks < n_keys) {
                 const uint8_t *hb = head_of(ks);
-                const uint8_t *line0 = hb + p.geom.vq_off + vq_byte(ks % P, vb * 16 + vq, kNB);
+                const int t = ks & (P - 1);
+                // vq_byte in 32 bits: 32-token chunk, byte row, token in the chunk
+                const uint8_t *line0 = hb + p.geom.vq_off + (((t >> 5) * kNB + vb) * 16 + vq) * 32 + (t & 31);
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {  // byte rows vq + 8 i: lines 8 i apart
                     rv[2 * i] = reinterpret_cast<const uint4 *>(line0 + i * 256)[0];
                     rv[2 * i + 1] = reinterpret_cast<const uint4 *>(line0 + i * 256)[1];
                 }
-                const uint4 *sc = reinterpret_cast<const uint4 *>(hb + p.geom.vs_off + ((int64_t)vb * P + ks % P) * 2);
+                const uint4 *sc = reinterpret_cast<const uint4 *>(hb + p.geom.vs_off + (vb * P + t) * 2);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) sv[i] = sc[i];
             } else {  // beyond the split: code 8 = value 0
