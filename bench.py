@@ -67,7 +67,7 @@ WORKLOADS = {
     "prefill131k": dict(
         desc=("prefill chunk: 256 fp16 query rows appended at context 131072, causal, 24 q / 4 kv heads, D 256, "
               "page 256, Q8_0 K / Q4_0 V, tcgen05 tensor-core path"),
-        L=64, T=131072 + 256, R=256, ring=16, chunk=2, lanes=2, residency=("prefix_frac", 1.0), q_f16=True),
+        L=64, T=131072 + 256, R=256, ring=24, chunk=2, lanes=2, residency=("prefix_frac", 1.0), q_f16=True),
     "long262k": dict(
         desc=("long-context decode: 64 layers, context 262144, 24 q / 4 kv heads, D 256, page 256, Q8_0 K / "
               "Q4_0 V, fixed 2048 MiB arena split between resident pages (per-layer prefixes) and the ring "

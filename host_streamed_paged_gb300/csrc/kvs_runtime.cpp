@@ -89,7 +89,7 @@ struct kvs_ctx {
     int64_t pool_used = 0;
 
     int64_t max_pages = 0;
-    int64_t prefill_split = 16;  // pages per tensor-core prefill split
+    int64_t prefill_split = 24;  // pages per tensor-core prefill split
     bool split_chunks = false;  // ring chunks stop at prefill split boundaries (prefill-capable context)
     uint32_t verify_rows = 1;   // widest split-K call (row groups beyond 64 rows x heads)
     // complete-layer lease: slots [ring_first + ring_n, ring_first + lease_ring_full)
@@ -726,7 +726,7 @@ uint64_t verify_rows_of(const kvs_config *cfg) {
 }
 
 uint64_t prefill_split_of(const kvs_config *cfg) {
-    uint64_t sp = cfg->prefill_split_pages ? cfg->prefill_split_pages : 16;
+    uint64_t sp = cfg->prefill_split_pages ? cfg->prefill_split_pages : 24;
     sp = std::min<uint64_t>(sp, (uint64_t)kvs::kMaxPrefillSplitPages);
     const uint64_t ring = cfg->ring_slots ? cfg->ring_slots : 1;
     return std::max<uint64_t>(1, std::min(sp, ring));

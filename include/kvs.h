@@ -128,7 +128,7 @@ typedef struct {
                               (attn_stream, copy_stream) */
     void *lane_attn_streams[7];  /* cudaStream_t of attention lanes 1 .. n_lanes-1 */
     void *lane_copy_streams[7];  /* cudaStream_t of copy lanes 1 .. n_lanes-1 */
-    uint32_t prefill_split_pages; /* pages per split of the tensor-core prefill path (0 = 16,
+    uint32_t prefill_split_pages; /* pages per split of the tensor-core prefill path (0 = 24,
                                      at most ring_slots and at most 128); when max_q_head *
                                      max_rows allows that path, ring chunks never cross a
                                      split.  Longer splits write fewer partials and spend
