@@ -93,9 +93,13 @@ GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 #   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum,launch__grid_size \
 #       --clock-control none -k regex:decode_kernel -c 60 --csv \
 #       python bench.py --no-cpu --no-extras --no-timeline --layers 2 --steps 1 --warmup 3
+# prefill131k, default 24-page splits: 223.76 MB read + 103.55 MB written (split partials), captured with
+#   ncu --set full --clock-control none -k regex:prefill_kernel -s 1 -c 1 -o <report> \
+#       python bench.py --workload prefill131k --layers 1 --steps 1 --warmup 3 --no-cpu --no-timeline --no-extras
 TRAFFIC = {
     "resident131k": (227.35e6, "ncu capture of one decode_kernel launch (resident131k, 1 layer)"),
     "decode32k": (27.33e6, "ncu capture of the resident decode_kernel launches (decode32k, 2 layers)"),
+    "prefill131k": (327.30e6, "ncu capture of one prefill_kernel launch (prefill131k, 1 layer, 24-page splits)"),
 }
 
 
@@ -620,8 +624,10 @@ def run_ours(args, wl):
         if prefill:  # tensor-core prefill: algorithmic flops over the timed launches
             flops_step = alg_flops_per_layer(wl) * L
             achieved = flops_step * n_eager / (r_ms * 1e-3) / 1e12 if r_ms > 0 else 0.0
+            tr = TRAFFIC.get(args.workload) if args.split in (0, 24) and args.ring in (0, 24) else None
             roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": achieved / tc_peak, "traffic": None,
+                    "frac": achieved / tc_peak, "traffic": tr[0] if tr else None,
+                    "traffic_source": tr[1] if tr else None,
                     "kernel": "prefill_kernel (tcgen05 kind::f16, M128 x N64/N256, TMEM accumulators)",
                     "flops_per_step_algorithmic": flops_step, "launches_timed": r_n,
                     "ms_per_launch": r_ms / max(r_n, 1),
