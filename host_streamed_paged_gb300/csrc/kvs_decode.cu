@@ -862,6 +862,104 @@ __global__ void __launch_bounds__(kCombineThreads, 3) combine_kernel(const Combi
     }
 }
 
+// Combine for calls with many (row, head) pairs and few splits (the prefill
+// chunk: 6144 pairs over about 22 splits): one warp per (row, q head), each
+// lane holding D / 32 dims, merging the splits in split order with a running
+// max (a split whose max exceeds it rescales the sums by 2^(m_w - m) first).
+// The split-strided form above would give each pair 4 CTAs of 512 threads
+// with one or two splits per warp; here a pair is 32 threads.  A fixed order:
+// the result depends on the call's shape only.
+constexpr int kRowsCombineThreads = 256;
+constexpr int kRowsCombineUnroll = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kRowsCombineThreads) combine_rows_kernel(const CombineParams p) {
+    constexpr int VPL = D / 32;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tl_begin(p.tl);
+    const int lane = threadIdx.x & 31;
+    const int rh = blockIdx.x * (kRowsCombineThreads / 32) + (threadIdx.x >> 5);
+    if (rh < p.R * p.Hq) {
+        const int r = rh / p.Hq, h = rh - r * p.Hq;
+        float *dst = p.out + (int64_t)rh * D + lane * VPL;
+        if (p.status && *reinterpret_cast<const volatile int *>(p.status) != 0) {
+            // a bounded wait in an attention kernel gave up: the output is invalid
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) dst[i] = __int_as_float(0x7fc00000);
+            if (p.lse && lane == 0) p.lse[rh] = __int_as_float(0x7fc00000);
+        } else {
+            const int nsplit = (int)((p.pos0 + r) / ((long long)p.P * p.split_pages)) + 1;
+            auto base_of = [&](int s) { return ((int64_t)s * p.Hq + h) * p.R + r; };
+            float mw = -INFINITY, Lw = 0.f, o[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) o[i] = 0.f;
+            for (int j0 = 0; j0 < nsplit; j0 += kRowsCombineUnroll) {
+                float2 ml[kRowsCombineUnroll];
+                float v[kRowsCombineUnroll][VPL];
+#pragma unroll
+                for (int u = 0; u < kRowsCombineUnroll; ++u) {
+                    ml[u] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) v[u][i] = 0.f;
+                    if (j0 + u < nsplit) {
+                        const int64_t b = base_of(j0 + u);
+                        ml[u] = *reinterpret_cast<const float2 *>(p.part_ml + b * 2);
+                        const float *src = p.part_o + b * D + lane * VPL;
+                        if (VPL % 4 == 0) {
+#pragma unroll
+                            for (int i = 0; i < VPL; i += 4) {
+                                const float4 t = *reinterpret_cast<const float4 *>(src + i);
+                                v[u][i] = t.x;
+                                v[u][i + 1] = t.y;
+                                v[u][i + 2] = t.z;
+                                v[u][i + 3] = t.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < VPL; i += 2) {
+                                const float2 t = *reinterpret_cast<const float2 *>(src + i);
+                                v[u][i] = t.x;
+                                v[u][i + 1] = t.y;
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kRowsCombineUnroll; ++u) {
+                    const float m = ml[u].x, l = ml[u].y;
+                    if (!(l > 0.f)) continue;  // past the end, or a split with no visible key
+                    if (m > mw) {
+                        const float c = exp2f(mw - m);  // 0 while nothing has been added
+                        Lw *= c;
+#pragma unroll
+                        for (int i = 0; i < VPL; ++i) o[i] *= c;
+                        mw = m;
+                    }
+                    const float w = exp2f(m - mw);
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) o[i] = fmaf(w, v[u][i], o[i]);
+                    Lw = fmaf(w, l, Lw);
+                }
+            }
+            const float inv = (Lw > 0.f) ? 1.f / Lw : 0.f;
+            if (VPL % 4 == 0) {
+#pragma unroll
+                for (int i = 0; i < VPL; i += 4)
+                    *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+            } else {
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) dst[i] = o[i] * inv;
+            }
+            if (p.lse && lane == 0) p.lse[rh] = (Lw > 0.f) ? (mw + log2f(Lw)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+    if (p.tl) {
+        __syncthreads();
+        tl_finish(p.tl);
+    }
+}
+
 }  // namespace
 
 int decode_max_mma_rows() { return 64; }
@@ -885,6 +983,18 @@ cudaError_t launch_decode(const DecodeParams &p, cudaStream_t s) {
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s) {
     const int blocks = p.R * p.Hq;
     if (blocks < 1) return cudaSuccess;
+    // many (row, head) pairs over few splits: a warp per pair (chosen from the
+    // call's shape alone, so any residency gives the same arithmetic)
+    const long long max_split = (p.pos0 + p.R - 1) / ((long long)p.P * p.split_pages) + 1;
+    if (blocks >= 512 && max_split <= 64) {
+        const dim3 rgrid((blocks + kRowsCombineThreads / 32 - 1) / (kRowsCombineThreads / 32));
+        switch (p.D) {
+            case 64: return launch_pdl(combine_rows_kernel<64>, rgrid, dim3(kRowsCombineThreads), 0, s, p);
+            case 128: return launch_pdl(combine_rows_kernel<128>, rgrid, dim3(kRowsCombineThreads), 0, s, p);
+            case 256: return launch_pdl(combine_rows_kernel<256>, rgrid, dim3(kRowsCombineThreads), 0, s, p);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     const dim3 grid(blocks, p.D > kCombineDims ? p.D / kCombineDims : 1);
     switch (p.D) {
         case 64: return launch_pdl(combine_kernel<64>, grid, dim3(kCombineThreads), 0, s, p);
