@@ -119,6 +119,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
 constexpr uint32_t kSpinLimit = 1u << 26;
 
 // bounded wait for phase `parity` of an mbarrier; false after `limit` polls
+// one non-blocking test: has the phase of this parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = kSpinLimit) {
     for (uint32_t i = 0; i < limit; ++i) {
         uint32_t done;
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
     }
     __syncthreads();
 
-    bool ok = true;
+    bool ok = true, triggered = false;
     const uint32_t limit = p.give_up_waits ? 0u : kSpinLimit;
     // unit u = (g * n_items + item) * T + tile, advanced incrementally
     int tile = u0 % T, item = (u0 / T) % p.n_items, g = u0 / T / p.n_items;
@@ -405,7 +417,16 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
                 }
             }
         }
-        __syncthreads();  // scores written; the K piece is read
+        // scores written; the K piece is read.  On the last unit, if its V piece
+        // has landed too, every page section this CTA reads is in shared memory:
+        // a refill of those slots launched as this grid's programmatic dependent
+        // may be scheduled now rather than after the softmax (when the launch asks)
+        bool v_in = false;
+        if (p.early_dependents && u == u1 - 1 && threadIdx.x == 0) v_in = mbar_test(bar0 + 16 * (2 * stage + 1), parity);
+        if (__syncthreads_or(v_in)) {
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            triggered = true;
+        }
         if (u + S < u1) {
             pending |= 1u << (2 * stage);
             pend_parity = (pend_parity & ~(1u << (2 * stage))) | ((parity ^ 1u) << (2 * stage));
@@ -476,7 +497,7 @@ __global__ void __launch_bounds__(W * 32, (NT == 1 && W == 8) ? 2 : 1)
         // every page section this CTA reads is now in shared memory: a refill
         // of those slots launched as this grid's programmatic dependent may
         // start (it begins once every CTA has signalled or exited)
-        if (u == u1 - 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (u == u1 - 1 && !triggered) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
         // O^T = V^T P'^T over key parts: job j = (dim block j % NB, key part j / NB).
         // A warp owns every part of its block (kInReg) or one job.

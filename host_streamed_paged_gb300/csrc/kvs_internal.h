@@ -86,6 +86,8 @@ struct DecodeParams {
     const uint4 *qf;       // Q fragments [Hk][NT][D/16][32] (written by the Q prep kernel)
     int prep_q;            // launch_decode first (re)builds qf/qs from q
     int tile_mode;         // one CTA per (page, kv head, row tile) (ring chunks)
+    int early_dependents;  // signal programmatic dependents (the chunk's refill) as soon as the
+                           // page sections are in shared memory, before the softmax
     int max_sms;           // > 0: use at most this many SMs' worth of CTA slots (resident reads
                            // beside ring-chunk reads and refills); 0: every SM
     int qtiles, run_tiles; // set by launch_decode: fragment-layout row tiles, tiles to run

@@ -676,6 +676,11 @@ kvs_status launch_items(kvs_ctx *c, uint32_t layer, const std::vector<int64_t> &
         // ring chunks: one CTA per (page, kv head, row tile), so the chunk's
         // slots are read (and can be refilled) as soon as possible
         dp.tile_mode = kind == KVS_TIME_RING ? 1 : 0;
+        // a small chunk read's signal sits on its refill's path (decode32k: 16 CTAs
+        // per read, refills 1.5 us sooner, +1.5%); with large chunks (long262k:
+        // 128 CTAs per read) the sooner refills overlapped more and the link ran
+        // a few percent slower, so those signal after the softmax
+        dp.early_dependents = dp.tile_mode && n * c->geom.Hk * (int)((dp.G * dp.Rg + 7) / 8) <= 64;
         for (int j = 0; j < n; ++j) {
             dp.page[j] = (uint32_t)pages[i0 + j];
             dp.slot[j] = (uint32_t)slots[i0 + j];
