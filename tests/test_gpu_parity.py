@@ -357,6 +357,17 @@ def test_wide_fp32_verify_row_groups_match_the_oracle(R, T, P, D):
     assert st.stats()["h2d_pages"] > 0
 
 
+@pytest.mark.parametrize("R,T,P,D", [(32, 128 * 9 + 5, 128, 128), (32, 64 * 20 + 3, 64, 64)])
+def test_wide_fp32_verify_warp_per_pair_combine(R, T, P, D):
+    """32 rows x 24 query heads = 768 (row, head) pairs over at most 21 one-page
+    splits: the log-sum-exp combine runs one warp per pair (its D 256 form is
+    reached by the 49-row case above); a third of the pages stream."""
+    st, k, v, q, out, lse = _wide_case(R, T, lambda n: (np.arange(n) % 3 == 1).astype(np.uint8), P=P, D=D)
+    ro, rl = oracle_ref(k, v, q, T - R, 1.0 / math.sqrt(D))
+    check_parity(out, lse, ro, rl)
+    assert st.stats()["h2d_pages"] > 0
+
+
 def test_wide_fp32_verify_streamed_equals_resident_bitwise():
     R, T = 49, 256 * 16 + 3
     base = _wide_case(R, T, lambda n: np.ones(n, np.uint8))
