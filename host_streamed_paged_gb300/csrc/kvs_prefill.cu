@@ -486,9 +486,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168) prefill_kernel(const 
         };
         // Iteration j publishes K_j (stage j & 1, free once S_{j-2} is done) and
         // V_{j-1} (stage (j-1) & 1, free once PV_{j-3} is done) under one proxy
-        // fence: the MMA thread issues PV_{j-1} right after S_j, so both are
-        // wanted at the same time, and the fence costs about as much as the
-        // dequantisation of a whole K tile.
+        // fence and one arrival: the MMA thread issues PV_{j-1} right after S_j,
+        // so both are wanted at the same time (separate K and V publishes, with
+        // a third relay in the peer, measured slower).
         if (nblk > 0) load_k(0);
         for (int j = 0; j <= nblk; ++j) {  // every exit is a warp-uniform wait outcome
             const bool wk = j < nblk, wv = j >= 1;
