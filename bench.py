@@ -84,9 +84,10 @@ GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the roofline kernel,
 # from one ncu capture of that launch on a GB300 (a workload missing here, or a kernel changed since
 # its capture, reports traffic as null).
-# resident131k, single-f16 operand mode: 218.19 MB read + 9.16 MB written, captured with
-#   ncu --set full --clock-control none -k regex:decode_kernel -s 4 -c 1 -o <report> \
-#       python bench.py --workload resident131k --layers 1 --steps 1 --warmup 3 --no-cpu --no-timeline
+# resident131k, single-f16 operand mode: 218.19 MB read + 8.63 MB written, captured with
+#   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum,launch__grid_size \
+#       --clock-control none -k regex:decode_kernel -s 4 -c 1 --csv \
+#       python bench.py --workload resident131k --layers 1 --steps 1 --warmup 3 --no-cpu --no-timeline --no-extras
 # decode32k: the resident-page launch of a layer (64 pages x 4 kv heads, 27.26 MB algorithmic):
 # 27.33 MB read, 0 written (the 1.5 MB of partials stay in L2), the same in every layer, captured on
 # a 2-layer copy of the workload with
@@ -97,7 +98,7 @@ GEOM = dict(Hq=24, Hk=4, D=256, P=256)
 #   ncu --set full --clock-control none -k regex:prefill_kernel -s 1 -c 1 -o <report> \
 #       python bench.py --workload prefill131k --layers 1 --steps 1 --warmup 3 --no-cpu --no-timeline --no-extras
 TRAFFIC = {
-    "resident131k": (227.35e6, "ncu capture of one decode_kernel launch (resident131k, 1 layer)"),
+    "resident131k": (226.82e6, "ncu capture of one decode_kernel launch (resident131k, 1 layer)"),
     "decode32k": (27.33e6, "ncu capture of the resident decode_kernel launches (decode32k, 2 layers)"),
     "prefill131k": (327.30e6, "ncu capture of one prefill_kernel launch (prefill131k, 1 layer, 24-page splits)"),
 }
