@@ -406,6 +406,27 @@ def test_prefill_scheduling_fences_and_split_coverage(seed):
     check_trace(st, 6 * Hk)
 
 
+@pytest.mark.parametrize("ring,chunk", [(8, 2), (24, 2), (32, 5)])
+def test_prefill_default_split_scheduling_and_coverage(ring, chunk):
+    """The default prefill split (24 pages, at most the ring) over a 60-page
+    context with a random 40% resident: every page of every split is read once
+    and each split's ring chunks are ready before its launch."""
+    rng = np.random.default_rng(ring)
+    P, L, Hk, R = 64, 1, 1, 40
+    T0 = 60 * P - R
+    st = kvs.KVStream(page_tokens=P, n_layers=L, n_kv_head=Hk, head_dim=256, max_q_head=6 * Hk, max_rows=R,
+                      max_tokens=T0 + R, ring_slots=ring, chunk_pages=chunk, arena_slots=2 * L + ring + 64,
+                      plan_only=True, lanes=2)
+    kvs.kvs_append(st.ctx, 0, None, None, T0 + R)
+    st.set_residency(0, (rng.random(60) < 0.4).astype(np.uint8))
+    st.prefetch(0)
+    n0 = len(st.trace())
+    kvs.kvs_attend(st.ctx, 0, None, kvs.KVS_F16, R, 6 * Hk, T0, 1.0, None, None)
+    reads = sorted(p for p, g in _reads_of_attend(st.trace()[n0:], 0))
+    assert reads == list(range(60))
+    check_trace(st, 6 * Hk)
+
+
 def test_load_host_pages_installs_pages_and_streams_them():
     """Encoded pages written into the host history are attended like any streamed page."""
     P, Hk, D, maxp = 64, 1, 128, 12
